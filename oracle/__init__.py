@@ -1,0 +1,147 @@
+"""fp64 CPU oracle for the selective scan and the Mamba-2 SSD scan.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+library never loads it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, one
+sequential loop per independent unit).  This module only compiles it with
+gcc, loads it with ctypes and converts numpy arrays to contiguous float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile a C source of the oracle's form into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-add, so every product and sum is
+    # rounded exactly as written.
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-std=c99",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP over units)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_source(_SRC, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    i64, dp, ip = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.oracle_selective_scan.argtypes = [i64, i64, i64, i64] + [dp] * 8 + [ip, dp, dp, dp, ip]
+    lib.oracle_selective_scan.restype = ip
+    lib.oracle_ssd.argtypes = [i64] * 6 + [dp] * 6 + [dp, dp, dp, ip]
+    lib.oracle_ssd.restype = ip
+    lib.oracle_threads.restype = ip
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(_LIB)
+    return _lib
+
+
+class _Bound:
+    """The two oracle functions bound to one compiled library (used by the
+    planted-mistake tests to run the pins against a mutated copy)."""
+
+    def __init__(self, lib):
+        self._lib = lib
+
+    def selective_scan(self, *a, **k):
+        return selective_scan(*a, _lib=self._lib, **k)
+
+    def ssd(self, *a, **k):
+        return ssd(*a, _lib=self._lib, **k)
+
+
+def load_library(path: str) -> _Bound:
+    return _Bound(_bind(path))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_threads())
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor: exact upcast of bf16 / fp32 values
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                   softplus=True, h0=None, nthreads=1, _lib=None):
+    """Oracle of the selective scan.
+
+    Shapes: u, delta, z (Bsz, Dch, L); A (Dch, N); B, C (Bsz, N, L);
+    D, delta_bias (Dch,); h0 (Bsz, Dch, N).  Returns (y, last_state), both
+    float64 numpy arrays of shapes (Bsz, Dch, L) and (Bsz, Dch, N).
+    """
+    u, delta, A, B, C = (_f64(t) for t in (u, delta, A, B, C))
+    D, z, delta_bias, h0 = (_f64(t) for t in (D, z, delta_bias, h0))
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and A.shape == (Dch, N)
+    assert B.shape == (Bsz, N, L) and C.shape == (Bsz, N, L)
+    assert z is None or z.shape == u.shape
+    assert D is None or D.shape == (Dch,)
+    assert delta_bias is None or delta_bias.shape == (Dch,)
+    assert h0 is None or h0.shape == (Bsz, Dch, N)
+    y = np.empty((Bsz, Dch, L), np.float64)
+    last = np.empty((Bsz, Dch, N), np.float64)
+    rc = (_lib or _load()).oracle_selective_scan(Bsz, Dch, N, L, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                                       _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                                       int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(last),
+                                       int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_selective_scan rejected its arguments (rc={rc})")
+    return y, last
+
+
+def ssd(x, dt, A_head, B, C, D=None, h0=None, nthreads=1, _lib=None):
+    """Oracle of the Mamba-2 SSD scan (recurrent form).
+
+    Shapes: x (Bsz, L, H, P); dt (Bsz, L, H); A_head (H,); B, C (Bsz, L, G, N);
+    D (H,); h0 (Bsz, H, P, N).  Returns (y, last_state) as float64 arrays of
+    shapes (Bsz, L, H, P) and (Bsz, H, P, N).
+    """
+    x, dt, A_head, B, C = (_f64(t) for t in (x, dt, A_head, B, C))
+    D, h0 = _f64(D), _f64(h0)
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    assert dt.shape == (Bsz, L, H) and A_head.shape == (H,)
+    assert B.shape == (Bsz, L, G, N) and C.shape == B.shape and H % G == 0
+    assert D is None or D.shape == (H,)
+    assert h0 is None or h0.shape == (Bsz, H, P, N)
+    y = np.empty((Bsz, L, H, P), np.float64)
+    last = np.empty((Bsz, H, P, N), np.float64)
+    rc = (_lib or _load()).oracle_ssd(Bsz, L, H, P, G, N, _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B),
+                            _ptr(C), _ptr(D), _ptr(h0), _ptr(y), _ptr(last), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd rejected its arguments (rc={rc})")
+    return y, last

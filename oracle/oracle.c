@@ -1,0 +1,181 @@
+/*
+ * oracle.c -- plain, slow, sequential fp64 reference of the selective scan
+ * and of the Mamba-2 SSD scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or constant with the
+ * CUDA library: it is the plain definition written out, one time step at a
+ * time, in double precision, so that a reader can check it against the
+ * equations by eye.
+ *
+ * Sources (page titles and sections):
+ *  - "Mamba模型笔记" (sunyzhi55 study notes) §2.2: the discrete recurrence
+ *    h_t = Abar h_{t-1} + Bbar x_t,  y_t = C h_t + D x_t.
+ *  - same page §4.1 and §4.4: B, C and Delta depend on the input; one SSM per
+ *    channel (diagonal A, one row of d_state values per channel).
+ *  - same page §4.3: the gate branch; the gate is y * silu(z).
+ *  - 0539edu paper talk §2.3: Abar = exp(Delta A), Bbar = Delta B, Cbar = C,
+ *    Delta made positive by softplus.
+ *  - 0539edu paper talk §4.1: the state is batch x d_inner x d_state and its
+ *    size does not depend on the sequence length.
+ *  - state-spaces/mamba README §4.3 and the study notes §5: Mamba-2 / SSD,
+ *    multi-head with a scalar A per head and d_state 64..128.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes): softplus(x) = log(1 + e^x); A is given already negative and used as
+ * is; the initial state is zero unless h0 is given; B and C are shared by all
+ * channels of one batch row; the SSD dt is already positive.
+ *
+ * Parallelism: the optional OpenMP loop runs over independent (batch,
+ * channel) or (batch, head) units only; every unit is computed by the same
+ * sequential loop, so the result does not depend on the thread count.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <stddef.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + exp(x)).  For x > 0 the identity
+ * log(1 + e^x) = x + log(1 + e^-x) avoids overflowing exp; both branches are
+ * the same real function. */
+static double softplus_d(double x) {
+    if (x > 0.0) return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Selective scan (Mamba-1), one sequential loop per (batch row b, channel d).
+ *
+ *   u, delta, z, y : (Bsz, D, L), t fastest
+ *   A              : (D, N)
+ *   Bm, Cm         : (Bsz, N, L)   (shared by all channels of a batch row)
+ *   Dv, delta_bias : (D)           (nullable: no skip / no bias)
+ *   z              : nullable (no gate)
+ *   h0             : (Bsz, D, N)   nullable (zero initial state)
+ *   last_state     : (Bsz, D, N)   nullable (not written)
+ *
+ * For every t:
+ *   dlt  = delta + delta_bias[d];  if softplus: dlt = softplus(dlt)
+ *   h[n] = exp(dlt * A[d,n]) * h[n] + dlt * B[b,n,t] * u[b,d,t]
+ *   out  = sum_n C[b,n,t] * h[n] + D[d] * u[b,d,t]
+ *   if z: out = out * z / (1 + exp(-z))
+ */
+int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
+                          const double* u, const double* delta, const double* A,
+                          const double* Bm, const double* Cm, const double* Dv,
+                          const double* z, const double* delta_bias, int softplus,
+                          const double* h0, double* y, double* last_state,
+                          int nthreads) {
+    if (Bsz < 0 || D < 0 || N < 1 || L < 0) return -1;
+    int64_t units = Bsz * D;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t unit = 0; unit < units; ++unit) {
+        int64_t b = unit / D, d = unit % D;
+        double* hp = (double*)malloc((size_t)N * sizeof(double));
+        if (!hp) continue;
+        for (int64_t n = 0; n < N; ++n)
+            hp[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+        const double* ur = u + (b * D + d) * L;
+        const double* dr = delta + (b * D + d) * L;
+        const double* zr = z ? z + (b * D + d) * L : NULL;
+        double* yr = y + (b * D + d) * L;
+        for (int64_t t = 0; t < L; ++t) {
+            double dlt = dr[t] + (delta_bias ? delta_bias[d] : 0.0);
+            if (softplus) dlt = softplus_d(dlt);
+            double out = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double abar = exp(dlt * A[d * N + n]);
+                double bbar = dlt * Bm[(b * N + n) * L + t];
+                hp[n] = abar * hp[n] + bbar * ur[t];
+                out += Cm[(b * N + n) * L + t] * hp[n];
+            }
+            if (Dv) out += Dv[d] * ur[t];
+            if (zr) out = out * zr[t] / (1.0 + exp(-zr[t]));
+            yr[t] = out;
+        }
+        if (last_state)
+            for (int64_t n = 0; n < N; ++n) last_state[(b * D + d) * N + n] = hp[n];
+        free(hp);
+    }
+    return 0;
+}
+
+/*
+ * Mamba-2 SSD scan, written as its recurrence, one sequential loop per
+ * (batch row b, head h).  The chunk size of the fast algorithm does not enter
+ * the definition, so it is not a parameter here.
+ *
+ *   x, y       : (Bsz, L, H, P)
+ *   dt         : (Bsz, L, H)      already positive
+ *   A_head     : (H)              scalar A per head
+ *   Bm, Cm     : (Bsz, L, G, N)   head h reads group h / (H / G)
+ *   Dv         : (H)              nullable
+ *   h0         : (Bsz, H, P, N)   nullable (zero initial state)
+ *   last_state : (Bsz, H, P, N)   nullable
+ *
+ * For every t:
+ *   a          = exp(dt * A_h)
+ *   S[p][n]    = a * S[p][n] + dt * x[p] * B[n]
+ *   y[p]       = sum_n C[n] * S[p][n] + D_h * x[p]
+ */
+int oracle_ssd(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+               const double* x, const double* dt, const double* A_head,
+               const double* Bm, const double* Cm, const double* Dv,
+               const double* h0, double* y, double* last_state, int nthreads) {
+    if (Bsz < 0 || L < 0 || H < 1 || P < 1 || G < 1 || N < 1 || H % G != 0) return -1;
+    int64_t units = Bsz * H;
+    int64_t heads_per_group = H / G;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t unit = 0; unit < units; ++unit) {
+        int64_t b = unit / H, hh = unit % H;
+        int64_t g = hh / heads_per_group;
+        double* S = (double*)malloc((size_t)(P * N) * sizeof(double));
+        if (!S) continue;
+        for (int64_t i = 0; i < P * N; ++i)
+            S[i] = h0 ? h0[((b * H + hh) * P) * N + i] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double dtv = dt[(b * L + t) * H + hh];
+            double a = exp(dtv * A_head[hh]);
+            const double* xr = x + ((b * L + t) * H + hh) * P;
+            const double* br = Bm + ((b * L + t) * G + g) * N;
+            const double* cr = Cm + ((b * L + t) * G + g) * N;
+            double* yr = y + ((b * L + t) * H + hh) * P;
+            for (int64_t p = 0; p < P; ++p) {
+                double out = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    S[p * N + n] = a * S[p * N + n] + dtv * xr[p] * br[n];
+                    out += cr[n] * S[p * N + n];
+                }
+                if (Dv) out += Dv[hh] * xr[p];
+                yr[p] = out;
+            }
+        }
+        if (last_state)
+            for (int64_t i = 0; i < P * N; ++i)
+                last_state[((b * H + hh) * P) * N + i] = S[i];
+        free(S);
+    }
+    return 0;
+}
