@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective scan (and the Mamba-2 SSD scan).
+
+One step = one full selective-scan call (discretise, recurrence, readout,
+skip, gate, final state) over the Mamba-130M-shaped layer workload: batch 8,
+d_inner 1536, d_state 16, L 2048, bf16 inputs, fp32 state.  Inputs are
+resident in HBM when the timed region starts; L2 is flushed (a 256 MB write)
+before every timed step, outside the step's events.
+
+Prints ONE JSON line (rank 0): channel-steps/s, the HBM roofline of the scan
+kernel, the end-to-end number through the C ABI with host buffers, the fp64
+oracle timed on the host cores, clocks seen during the timed region, and
+secondary rows for the other workloads (timed only; parity is in tests/).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own replica of the workload (weak
+scaling); value = all ranks' channel-steps / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan channel-steps/s (B·D·L/s) and achieved HBM GB/s vs B300 peak"
+UNIT = "channel-steps/s"
+HEADLINE = "mamba130m_layer"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary workload rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per call.
+
+
+def selective_bytes(cfg):
+    es = 2 if cfg.dtype == "bf16" else 4
+    steps = cfg.batch * cfg.d_inner * cfg.seqlen
+    per_step = es * (3 + (1 if cfg.gate else 0))           # u, delta, (z) in; y out
+    bc = 2 * cfg.batch * cfg.d_state * cfg.seqlen * es       # B and C, read once
+    params = 4 * cfg.d_inner * (cfg.d_state + 2)             # A, D, delta_bias
+    state = 4 * cfg.batch * cfg.d_inner * cfg.d_state if cfg.last_state else 0
+    return steps * per_step + bc + params + state
+
+
+def ssd_bytes(cfg):
+    es = 2 if cfg.dtype == "bf16" else 4
+    xy = 2 * cfg.batch * cfg.seqlen * cfg.nheads * cfg.headdim * es
+    dt = cfg.batch * cfg.seqlen * cfg.nheads * es
+    bc = 2 * cfg.batch * cfg.seqlen * cfg.ngroups * cfg.d_state * es
+    state = 4 * cfg.batch * cfg.nheads * cfg.headdim * cfg.d_state if cfg.last_state else 0
+    return xy + dt + bc + 8 * cfg.nheads + state
+
+
+def ssd_flops(cfg):
+    """Dense-contraction flops of the chunked form (C B^T once per group)."""
+    Q, nch = cfg.chunk, -(-cfg.seqlen // cfg.chunk)
+    per_head_chunk = 2 * Q * Q * cfg.headdim + 4 * Q * cfg.headdim * cfg.d_state
+    cb = 2 * Q * Q * cfg.d_state * cfg.ngroups
+    return cfg.batch * nch * (cfg.nheads * per_head_chunk + cb)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(
+            m.get("bf16_tflops_sustained", m["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "selective_state_space_146_b300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel_key]
+        return e["bytes_per_launch"] if e.get("source_hash") == source_hash() else None
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=3)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+                power.append(float(p[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# GPU timing.
+
+
+def time_device(fn, flush, steps, warmup, torch, counter=None):
+    """Per-step CUDA-event times (ms) of fn() on the current stream, with an
+    L2 flush before every step outside the events.  With `counter`, also
+    returns how many library kernels the timed steps launched."""
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    n0 = counter() if counter else 0
+    for a, b in evs:
+        flush.zero_()
+        a.record(st)
+        fn()
+        b.record(st)
+    n1 = counter() if counter else 0
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    return (times, n1 - n0) if counter else times
+
+
+def run_selective_call(g, torch, abi, y, last):
+    abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                           g["delta_bias"], softplus=True, y=y, last_state=last)
+
+
+def headline(args, dev, rank, world, torch, abi, inputs, dist_helpers):
+    cfg = inputs.WORKLOADS[HEADLINE]
+    host = inputs.workload_selective_inputs(cfg, seed=rank)
+    g = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    y = torch.empty_like(g["u"])
+    last = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        run_selective_call(g, torch, abi, y, last)
+
+    # device-resident timing
+    dist_helpers.barrier(dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        times, launches = time_device(step, flush, args.steps, args.warmup, torch,
+                                      counter=abi.launch_count)
+    torch.cuda.synchronize()
+    dist_helpers.barrier(dev)
+    ms = statistics.mean(times)
+    ms_max = dist_helpers.max_over_ranks(ms, dev)
+
+    # end to end through the C ABI with pinned host buffers
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    last_h = torch.empty(last.shape, dtype=last.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = y_h.numel() * y_h.element_size() + last_h.numel() * last_h.element_size()
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                g[k].copy_(v, non_blocking=True)
+        run_selective_call(g, torch, abi, y, last)
+        y_h.copy_(y, non_blocking=True)
+        last_h.copy_(last, non_blocking=True)
+
+    e2e_times = time_device(e2e_step, flush, max(3, args.steps // 2), 2, torch)
+    e2e_ms = dist_helpers.max_over_ranks(statistics.mean(e2e_times), dev)
+
+    units = cfg.channel_steps
+    total_units = dist_helpers.sum_over_ranks(units, dev)
+    return dict(cfg=cfg, host=host, ms=ms, ms_max=ms_max, times=times, launches=launches,
+                clocks=clk.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, units=units,
+                total_units=total_units)
+
+
+def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
+    """Timing of the other workloads (inputs drawn on the GPU with the same
+    recipe; parity for these shapes is covered by tests/)."""
+    rows = {}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for name in ("tiny_f32", "mamba2p8b_layer", "long_context", "mamba2_ssd"):
+        cfg = inputs.WORKLOADS[name]
+        try:
+            with inputs.on_device(dev):
+                if name == "mamba2_ssd":
+                    g = inputs.workload_ssd_inputs(cfg)
+                else:
+                    g = inputs.workload_selective_inputs(cfg)
+            if name == "mamba2_ssd":
+                yb = torch.empty_like(g["x"])
+                ls = torch.empty(cfg.batch, cfg.nheads, cfg.headdim, cfg.d_state, device=dev)
+
+                def fn():
+                    abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
+                                           chunk=cfg.chunk, y=yb, last_state=ls)
+                nbytes = ssd_bytes(cfg)
+            else:
+                yb = torch.empty_like(g["u"])
+                ls = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+
+                def fn():
+                    run_selective_call(g, torch, abi, yb, ls)
+                nbytes = selective_bytes(cfg)
+            times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+            launches_per_call = nl / 5
+            ms = statistics.mean(times)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            row = {"ms_per_call": round(ms, 4), "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+                   "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                   "launches_per_call": launches_per_call}
+            if name == "mamba2_ssd":
+                tf = ssd_flops(cfg) / (ms * 1e-3) / 1e12
+                row["tensor_tflops"] = round(tf, 1)
+                row["tensor_frac"] = round(tf / tf_peak, 4)
+            rows[name] = row
+            del g, yb, ls
+            torch.cuda.empty_cache()
+        except Exception as e:  # a row failing must not hide the headline
+            rows[name] = {"error": str(e)[:200]}
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing.
+
+
+def oracle_throughput(host, cfg, seconds, oracle):
+    """Time the fp64 oracle on a bounded sample of the workload: whole
+    channels (full length) in blocks, until `seconds` have passed."""
+    import numpy as np
+    nth = oracle.max_threads()
+    Dch = cfg.d_inner
+    block = max(nth * 4, 64)
+    f64 = {k: (None if v is None else v.double().numpy()) for k, v in host.items()}
+    done, t_used, rounds = 0, 0.0, 0
+    b = 0
+    while t_used < seconds and rounds < 1000:
+        d0 = (rounds * block) % Dch
+        d1 = min(Dch, d0 + block)
+        sub = dict(u=f64["u"][b:b + 1, d0:d1], delta=f64["delta"][b:b + 1, d0:d1],
+                   z=None if f64["z"] is None else f64["z"][b:b + 1, d0:d1],
+                   A=f64["A"][d0:d1], B=f64["B"][b:b + 1], C=f64["C"][b:b + 1],
+                   D=None if f64["D"] is None else f64["D"][d0:d1],
+                   delta_bias=None if f64["delta_bias"] is None else f64["delta_bias"][d0:d1])
+        sub = {k: (None if v is None else np.ascontiguousarray(v)) for k, v in sub.items()}
+        t0 = time.perf_counter()
+        oracle.selective_scan(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"],
+                              sub["z"], sub["delta_bias"], softplus=True, nthreads=nth)
+        t_used += time.perf_counter() - t0
+        done += (d1 - d0) * cfg.seqlen
+        rounds += 1
+        b = (b + 1) % cfg.batch
+    return done / t_used, nth, done, t_used
+
+
+def cpu_model():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def config_dict(cfg):
+    return {"workload": f"{cfg.name}: Mamba-130M-shaped layer scan, batch {cfg.batch}, d_inner "
+                        f"{cfg.d_inner}, d_state {cfg.d_state}, L {cfg.seqlen}, {cfg.dtype} inputs, "
+                        f"fp32 state, z gate on, delta softplus with bias, final state returned",
+            "batch": cfg.batch, "d_inner": cfg.d_inner, "d_state": cfg.d_state,
+            "seq_len": cfg.seqlen, "io_dtype": cfg.dtype, "parallelism": "replica per GPU",
+            "l2": "flushed (256 MB write) before every timed step, outside the step's events"}
+
+
+# ---------------------------------------------------------------------------
+
+
+def main_reference(args):
+    from selective_state_space_146_b300 import dist as dh
+    rank, _, world = dh.env_world()
+    if rank != 0:
+        return 0
+    import oracle
+    from selective_state_space_146_b300 import inputs
+    cfg = inputs.WORKLOADS[HEADLINE]
+    host = inputs.workload_selective_inputs(cfg)
+    per_step = max(0.5, min(3.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_throughput(host, cfg, per_step, oracle)
+    vals = []
+    for _ in range(args.steps):
+        v, nth, done, used = oracle_throughput(host, cfg, per_step, oracle)
+        vals.append((v, done, used))
+    value = sum(d for _, d, _ in vals) / sum(u for _, _, u in vals)
+    ms = 1e3 * statistics.mean(u for _, _, u in vals)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
+                             "sample": f"per step, whole channels of the workload (full length "
+                                       f"{cfg.seqlen}) for ~{per_step:.1f} s on {cpu_model()}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    from selective_state_space_146_b300 import _abi as abi
+    from selective_state_space_146_b300 import dist as dh
+    from selective_state_space_146_b300 import inputs
+
+    rank, local_rank, world = dh.env_world()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1 and not tdist.is_initialized():
+        tdist.init_process_group("nccl", device_id=dev)
+    abi.load()
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+
+    h = headline(args, dev, rank, world, torch, abi, inputs, dh)
+    cfg = h["cfg"]
+    nbytes = selective_bytes(cfg)
+    kernel_ms = h["ms"]  # one kernel launch per call for this workload
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    value = h["total_units"] / (h["ms_max"] * 1e-3)
+    e2e_value = h["total_units"] / (h["e2e_ms"] * 1e-3)
+
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_sust)
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        import oracle
+        v, nth, done, used = oracle_throughput(h["host"], cfg, args.cpu_seconds, oracle)
+        cpu = {"value": v, "unit": UNIT, "cores": nth, "kind": "oracle",
+               "sample": f"{done} channel-steps (whole channels of the workload, full length "
+                         f"{cfg.seqlen}) in {used:.1f} s on {cpu_model()}"}
+    if world > 1:
+        dh.barrier(dev)
+    if rank == 0:
+        key = "scan_fast.bf16.split2"
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": h["ms_max"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(cfg),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                         "traffic": measured_traffic(key), "peak_source": f"{peak_src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": nbytes, "kernel": key},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h["h2d"],
+                    "d2h_bytes_per_step": h["d2h"]},
+            "gpu_launches": h["launches"],
+            "clocks": h["clocks"],
+            "step_ms": {"median": statistics.median(h["times"]), "min": min(h["times"]),
+                        "max": max(h["times"])},
+            "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    a = parse()
+    sys.exit(main_reference(a) if a.impl == "reference" else main_ours(a))

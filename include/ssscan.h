@@ -1,0 +1,146 @@
+/*
+ * ssscan.h -- C ABI of the B300 (sm_103a) selective-scan library.
+ *
+ * Two operations, both forward only, both asynchronous on the caller's CUDA
+ * stream:
+ *
+ *   ss_selective_scan_fwd   the Mamba (Mamba-1) selective scan
+ *   ss_ssd_chunk_scan_fwd   the Mamba-2 SSD scan in chunked form
+ *
+ * Every buffer is caller-owned device memory described by an ss_tensor
+ * (pointer, dtype, shape, strides in elements).  The library keeps no pointer
+ * after a call returns, never synchronises the stream, and allocates only the
+ * stream-ordered scratch documented per call.  Optional inputs are passed as
+ * NULL.  Calls return SS_OK (0) or a negative status; ss_status_string()
+ * names it.  An argument error is detected on the host before anything is
+ * launched.  Errors found on the device (a bounded wait that ran out) are
+ * recorded in a per-device error word that ss_get_device_error() reads.
+ */
+#ifndef SSSCAN_H
+#define SSSCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define SS_OK 0
+#define SS_ERR_INVALID_ARG (-1)  /* NULL where required, bad flag, bad chunk  */
+#define SS_ERR_SHAPE (-2)        /* shapes disagree with each other           */
+#define SS_ERR_DTYPE (-3)        /* unsupported or mixed dtypes               */
+#define SS_ERR_ALIGNMENT (-4)    /* pointer not aligned to its element size   */
+#define SS_ERR_UNSUPPORTED (-5)  /* valid but outside what is compiled (N)    */
+#define SS_ERR_ALLOC (-6)        /* stream-ordered scratch allocation failed  */
+#define SS_ERR_LAUNCH (-7)       /* kernel launch failed                      */
+#define SS_ERR_TIMEOUT (-8)      /* a device-side bounded wait ran out        */
+#define SS_ERR_CUDA (-9)         /* other CUDA runtime error                  */
+
+/* ---- tensors ----------------------------------------------------------- */
+#define SS_F32 0
+#define SS_BF16 1
+
+typedef struct ss_tensor {
+    void* data;         /* device pointer (caller-owned)                 */
+    int32_t dtype;      /* SS_F32 or SS_BF16                             */
+    int32_t ndim;       /* number of used entries in shape / stride       */
+    int64_t shape[4];
+    int64_t stride[4];  /* in elements; any non-negative values           */
+} ss_tensor;
+
+/*
+ * Selective scan, forward.
+ *
+ * Defines (page "Mamba模型笔记", §2.2 discrete recurrence, §4.1 input-dependent
+ * B, C and Delta, §4.3 gate branch, §4.4 one SSM per channel; page 0539edu
+ * paper talk §2.3 discretisation Abar = exp(Delta A), Bbar = Delta B,
+ * Delta > 0 through softplus), for every batch row b, channel d and step t:
+ *
+ *   dl        = delta[b,d,t] + delta_bias[d]        (bias optional)
+ *   dl        = softplus(dl) = log(1 + e^dl)        (if softplus != 0)
+ *   h[n]      = exp(dl * A[d,n]) * h[n] + dl * B[b,n,t] * u[b,d,t],  h = 0 at t = 0
+ *   out       = sum_n C[b,n,t] * h[n] + D[d] * u[b,d,t]               (D optional)
+ *   y[b,d,t]  = out * z * sigmoid(z),  z = z[b,d,t]                   (z optional)
+ *   last_state[b,d,n] = h[n] after the last step                      (optional)
+ *
+ * Shapes (element strides free unless noted):
+ *   u, delta, z, y : (Bsz, D, L)        dtype T (all four the same)
+ *   A              : (D, N)             f32
+ *   B, C           : (Bsz, N, L)        dtype T; shared by all channels of row b
+ *   D, delta_bias  : (D)                f32
+ *   last_state     : (Bsz, D, N)        f32
+ * T is SS_F32 or SS_BF16.  N <= 256; the fast path is compiled for N = 16
+ * (other N run a slower general kernel).  The fast path needs unit stride in
+ * t and 16-byte aligned rows for u/delta/z/y; other layouts take the general
+ * kernel (same results up to rounding order).  y may not alias an input.
+ * Arithmetic: fp32 state and accumulation for both dtypes.
+ *
+ * Scratch: when the channel count is too small to fill the GPU, the
+ * sequence is split into segments scanned in parallel (a summary pass, then
+ * the main pass seeded with each segment's incoming state); the summaries
+ * live in stream-ordered memory (cudaMallocAsync / cudaFreeAsync on
+ * `stream`), at most 2 * Bsz * D * N * 64 floats.
+ *
+ * Zero-size inputs (Bsz, D or L = 0) return SS_OK without a launch.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).
+ */
+int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          ss_tensor* y, ss_tensor* last_state, void* stream);
+
+/*
+ * Mamba-2 SSD scan, forward, chunked.
+ *
+ * Defines (page "Mamba模型笔记" §5, SSD; state-spaces/mamba README §4.3,
+ * Mamba-2 with d_state 64 or 128 and a scalar A per head; skill card, Mamba-2
+ * config headdim / ngroups), for every batch row b and head h, with group
+ * g = h / (H / G):
+ *
+ *   a         = exp(dt[b,t,h] * A_head[h])
+ *   S[p][n]   = a * S[p][n] + dt[b,t,h] * x[b,t,h,p] * B[b,t,g,n],  S = 0 at t = 0
+ *   y[b,t,h,p]= sum_n C[b,t,g,n] * S[p][n] + D[h] * x[b,t,h,p]       (D optional)
+ *   last_state[b,h,p,n] = S[p][n] after the last step                 (optional)
+ *
+ * computed chunk by chunk: within a chunk of `chunk` steps through the
+ * quadratic (attention-like) form (C B^T masked by the decays) times x, and
+ * across chunks through the carried state.  The result does not depend on
+ * `chunk` beyond rounding.
+ *
+ * Shapes:
+ *   x, y       : (Bsz, L, H, P)    dtype T
+ *   dt         : (Bsz, L, H)       dtype T, already positive (no bias, no softplus)
+ *   A_head, D  : (H)               f32
+ *   B, C       : (Bsz, L, G, N)    dtype T, H % G == 0
+ *   last_state : (Bsz, H, P, N)    f32
+ * chunk must be one of 64, 128, 256.  N <= 256, P <= 256.  The tensor-core
+ * path is compiled for bf16 with P = 64, N = 128, unit inner strides and
+ * 16-byte aligned rows; everything else runs a general CUDA-core kernel.
+ * Zero-size inputs return SS_OK without a launch.
+ */
+int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
+                          ss_tensor* y, ss_tensor* last_state, void* stream);
+
+/* Name of a status code (static string, never NULL). */
+const char* ss_status_string(int status);
+
+/*
+ * Device-side error word of the current device: synchronises `stream`, then
+ * returns SS_OK or SS_ERR_TIMEOUT if any kernel of this library gave up on a
+ * bounded wait since the last call, and clears the word.
+ */
+int ss_get_device_error(void* stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t ss_launch_count(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSSCAN_H */

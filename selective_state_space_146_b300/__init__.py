@@ -1,0 +1,12 @@
+"""B300-native Mamba selective scan and Mamba-2 SSD scan.
+
+The compute lives in ``libssscan.so`` (hand-written sm_103a CUDA behind the C
+ABI declared in ``include/ssscan.h``); this package only binds it.
+
+    from selective_state_space_146_b300 import selective_scan_fwd, ssd_chunk_scan_fwd
+"""
+from ._abi import (SSError, device_error, launch_count, selective_scan_fwd,  # noqa: F401
+                   ssd_chunk_scan_fwd, status_string)
+
+__all__ = ["selective_scan_fwd", "ssd_chunk_scan_fwd", "SSError", "device_error",
+           "launch_count", "status_string"]

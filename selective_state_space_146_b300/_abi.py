@@ -1,0 +1,148 @@
+"""ctypes binding of libssscan.so (include/ssscan.h).
+
+Argument marshalling only: torch tensors are described as ss_tensor
+(pointer, dtype, shape, strides) and passed with the current CUDA stream.
+Every step of the scan runs in the library's CUDA kernels; there is no other
+implementation behind these functions.  If the library is missing the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssscan.so")
+
+SS_F32, SS_BF16 = 0, 1
+STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_DTYPE",
+          -4: "SS_ERR_ALIGNMENT", -5: "SS_ERR_UNSUPPORTED", -6: "SS_ERR_ALLOC",
+          -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
+EXPORTS = ("ss_selective_scan_fwd", "ss_ssd_chunk_scan_fwd", "ss_status_string",
+           "ss_get_device_error", "ss_launch_count", "ss_version")
+
+
+class SSTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libssscan.so not built at {p}; run "
+                           "`python -m selective_state_space_146_b300.csrc.build`")
+    lib = ctypes.CDLL(p)
+    T = ctypes.POINTER(SSTensor)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.ss_selective_scan_fwd.argtypes = [T, T, T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_selective_scan_fwd.restype = i
+    lib.ss_ssd_chunk_scan_fwd.argtypes = [T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_ssd_chunk_scan_fwd.restype = i
+    lib.ss_status_string.argtypes = [i]
+    lib.ss_status_string.restype = ctypes.c_char_p
+    lib.ss_get_device_error.argtypes = [vp]
+    lib.ss_get_device_error.restype = i
+    lib.ss_launch_count.argtypes = []
+    lib.ss_launch_count.restype = ctypes.c_uint64
+    lib.ss_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().ss_status_string(int(status)).decode()
+
+
+_DT = {torch.float32: SS_F32, torch.bfloat16: SS_BF16}
+
+
+def describe(t: torch.Tensor | None):
+    """ss_tensor for a torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    s = SSTensor()
+    s.data = t.data_ptr() if t.numel() > 0 else 0
+    s.dtype = _DT.get(t.dtype, 99)
+    s.ndim = t.dim()
+    for k in range(t.dim()):
+        s.shape[k] = t.shape[k]
+        s.stride[k] = t.stride(k)
+    return s
+
+
+def _ref(s):
+    return None if s is None else ctypes.byref(s)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                       y=None, last_state=None, return_last_state=False, stream=None):
+    """Selective scan forward (ss_selective_scan_fwd).
+
+    u, delta, z: (batch, d_inner, L); A: (d_inner, N) f32; B, C: (batch, N, L);
+    D, delta_bias: (d_inner,) f32.  Returns y (same dtype as u), or
+    (y, last_state) with last_state (batch, d_inner, N) f32.
+    """
+    if y is None:
+        y = torch.empty_like(u, memory_format=torch.contiguous_format)
+    if last_state is None and return_last_state:
+        last_state = torch.empty(u.shape[0], u.shape[1], A.shape[1], dtype=torch.float32,
+                                 device=u.device)
+    ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    ys, ls = describe(y), describe(last_state)
+    rc = load().ss_selective_scan_fwd(*[_ref(t) for t in ts], int(bool(softplus)), _ref(ys),
+                                      _ref(ls), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_fwd")
+    return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_state=None,
+                       return_last_state=False, stream=None):
+    """Mamba-2 SSD chunked scan forward (ss_ssd_chunk_scan_fwd).
+
+    x: (batch, L, H, P); dt: (batch, L, H) positive; A_head, D: (H,) f32;
+    B, C: (batch, L, G, N).  Returns y, or (y, last_state (batch, H, P, N) f32).
+    """
+    if y is None:
+        y = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if last_state is None and return_last_state:
+        last_state = torch.empty(x.shape[0], x.shape[2], x.shape[3], B.shape[3],
+                                 dtype=torch.float32, device=x.device)
+    ts = [describe(t) for t in (x, dt, A_head, B, C, D)]
+    ys, ls = describe(y), describe(last_state)
+    rc = load().ss_ssd_chunk_scan_fwd(*[_ref(t) for t in ts], int(chunk), _ref(ys), _ref(ls),
+                                      _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_ssd_chunk_scan_fwd")
+    return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def device_error(stream=None) -> int:
+    return int(load().ss_get_device_error(_stream_ptr(stream)))
+
+
+def launch_count() -> int:
+    return int(load().ss_launch_count())

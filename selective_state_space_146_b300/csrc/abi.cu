@@ -1,0 +1,272 @@
+// abi.cu -- the C ABI (include/ssscan.h): argument checks on the host, then
+// dispatch to the kernels on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ssscan.h"
+
+namespace ss {
+
+// ---------------------------------------------------------------------------
+// Per-device state: the device error word and the SM count.
+
+__device__ unsigned g_device_error;
+
+constexpr int kMaxDevices = 64;
+static unsigned* g_err_ptr[kMaxDevices];
+static int g_sms[kMaxDevices];
+static std::mutex g_mu;
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+static unsigned* device_error_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int sm_count_current() {
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sms[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = v > 0 ? v : 148;
+    }
+    return g_sms[dev];
+}
+
+void* tensor_map_encoder() {
+    static void* fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = f;
+    });
+    return fn;
+}
+
+static void* scratch_alloc_async(size_t bytes, cudaStream_t st, void*) {
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+static void scratch_free_async(void* p, cudaStream_t st, void*) { cudaFreeAsync(p, st); }
+
+// ---------------------------------------------------------------------------
+// Argument checks.
+
+static int elem_size(int dtype) { return dtype == SS_BF16 ? 2 : dtype == SS_F32 ? 4 : 0; }
+
+static int check_tensor(const ss_tensor* t, int ndim) {
+    if (!t) return SS_ERR_INVALID_ARG;
+    if (t->ndim != ndim) return SS_ERR_SHAPE;
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (t->shape[i] < 0 || t->stride[i] < 0) return SS_ERR_SHAPE;
+        numel *= t->shape[i];
+    }
+    if (!elem_size(t->dtype)) return SS_ERR_DTYPE;
+    if (numel > 0) {
+        if (!t->data) return SS_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(t->data) % elem_size(t->dtype)) return SS_ERR_ALIGNMENT;
+    }
+    return SS_OK;
+}
+
+static bool same_shape(const ss_tensor* a, const ss_tensor* b) {
+    if (a->ndim != b->ndim) return false;
+    for (int i = 0; i < a->ndim; ++i)
+        if (a->shape[i] != b->shape[i]) return false;
+    return true;
+}
+
+#define SS_TRY(expr)                 \
+    do {                             \
+        int _rc = (expr);            \
+        if (_rc != SS_OK) return _rc; \
+    } while (0)
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+    SS_TRY(check_tensor(u, 3));
+    SS_TRY(check_tensor(delta, 3));
+    SS_TRY(check_tensor(A, 2));
+    SS_TRY(check_tensor(B, 3));
+    SS_TRY(check_tensor(C, 3));
+    SS_TRY(check_tensor(y, 3));
+    if (D) SS_TRY(check_tensor(D, 1));
+    if (z) SS_TRY(check_tensor(z, 3));
+    if (delta_bias) SS_TRY(check_tensor(delta_bias, 1));
+    if (last_state) SS_TRY(check_tensor(last_state, 3));
+    if (softplus != 0 && softplus != 1) return SS_ERR_INVALID_ARG;
+
+    const int dt = u->dtype;
+    if (delta->dtype != dt || B->dtype != dt || C->dtype != dt || y->dtype != dt ||
+        (z && z->dtype != dt))
+        return SS_ERR_DTYPE;
+    if (A->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
+        (delta_bias && delta_bias->dtype != SS_F32) || (last_state && last_state->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+
+    const int64_t Bsz = u->shape[0], Dch = u->shape[1], L = u->shape[2], N = A->shape[1];
+    if (!same_shape(delta, u) || !same_shape(y, u) || (z && !same_shape(z, u)))
+        return SS_ERR_SHAPE;
+    if (A->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (B->shape[0] != Bsz || B->shape[1] != N || B->shape[2] != L) return SS_ERR_SHAPE;
+    if (!same_shape(C, B)) return SS_ERR_SHAPE;
+    if (D && D->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (delta_bias && delta_bias->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != Dch ||
+                       last_state->shape[2] != N))
+        return SS_ERR_SHAPE;
+    if (N < 1) return SS_ERR_SHAPE;
+    if (N > 256) return SS_ERR_UNSUPPORTED;
+    if (Bsz * Dch >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
+    if (Bsz == 0 || Dch == 0) return SS_OK;
+    if (L == 0 && !last_state) return SS_OK;
+
+    ScanArgs a{};
+    a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = dt;
+    a.u = u->data; a.su_b = u->stride[0]; a.su_d = u->stride[1]; a.su_t = u->stride[2];
+    a.dl = delta->data; a.sdl_b = delta->stride[0]; a.sdl_d = delta->stride[1]; a.sdl_t = delta->stride[2];
+    if (z) { a.z = z->data; a.sz_b = z->stride[0]; a.sz_d = z->stride[1]; a.sz_t = z->stride[2]; }
+    a.y = y->data; a.sy_b = y->stride[0]; a.sy_d = y->stride[1]; a.sy_t = y->stride[2];
+    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_n = B->stride[1]; a.sB_t = B->stride[2];
+    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_n = C->stride[1]; a.sC_t = C->stride[2];
+    a.A = static_cast<const float*>(A->data); a.sA_d = A->stride[0]; a.sA_n = A->stride[1];
+    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
+    if (delta_bias) { a.bias = static_cast<const float*>(delta_bias->data); a.sbias = delta_bias->stride[0]; }
+    if (last_state) {
+        a.last = static_cast<float*>(last_state->data);
+        a.sl_b = last_state->stride[0]; a.sl_d = last_state->stride[1]; a.sl_n = last_state->stride[2];
+    }
+    a.softplus = softplus;
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
+                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+    SS_TRY(check_tensor(x, 4));
+    SS_TRY(check_tensor(dt, 3));
+    SS_TRY(check_tensor(A_head, 1));
+    SS_TRY(check_tensor(B, 4));
+    SS_TRY(check_tensor(C, 4));
+    SS_TRY(check_tensor(y, 4));
+    if (D) SS_TRY(check_tensor(D, 1));
+    if (last_state) SS_TRY(check_tensor(last_state, 4));
+    if (chunk != 64 && chunk != 128 && chunk != 256) return SS_ERR_INVALID_ARG;
+    const int ty = x->dtype;
+    if (dt->dtype != ty || B->dtype != ty || C->dtype != ty || y->dtype != ty) return SS_ERR_DTYPE;
+    if (A_head->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
+        (last_state && last_state->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+    const int64_t Bsz = x->shape[0], L = x->shape[1], H = x->shape[2], P = x->shape[3];
+    const int64_t G = B->shape[2], N = B->shape[3];
+    if (!same_shape(y, x)) return SS_ERR_SHAPE;
+    if (dt->shape[0] != Bsz || dt->shape[1] != L || dt->shape[2] != H) return SS_ERR_SHAPE;
+    if (A_head->shape[0] != H || (D && D->shape[0] != H)) return SS_ERR_SHAPE;
+    if (B->shape[0] != Bsz || B->shape[1] != L || !same_shape(C, B)) return SS_ERR_SHAPE;
+    if (G < 1 || N < 1 || H % G != 0) return SS_ERR_SHAPE;
+    if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != H ||
+                       last_state->shape[2] != P || last_state->shape[3] != N))
+        return SS_ERR_SHAPE;
+    if (N > 256 || P > 1024) return SS_ERR_UNSUPPORTED;
+    if (Bsz * H * P >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
+    if (Bsz == 0 || H == 0 || P == 0) return SS_OK;
+    if (L == 0 && !last_state) return SS_OK;
+
+    SSDArgs a{};
+    a.Bsz = (int)Bsz; a.L = (int)L; a.H = (int)H; a.P = (int)P; a.G = (int)G; a.N = (int)N;
+    a.chunk = chunk; a.dtype = ty;
+    a.x = x->data; a.sx_b = x->stride[0]; a.sx_l = x->stride[1]; a.sx_h = x->stride[2]; a.sx_p = x->stride[3];
+    a.dt = dt->data; a.sdt_b = dt->stride[0]; a.sdt_l = dt->stride[1]; a.sdt_h = dt->stride[2];
+    a.A = static_cast<const float*>(A_head->data); a.sA = A_head->stride[0];
+    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_l = B->stride[1]; a.sB_g = B->stride[2]; a.sB_n = B->stride[3];
+    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_l = C->stride[1]; a.sC_g = C->stride[2]; a.sC_n = C->stride[3];
+    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
+    a.y = y->data; a.sy_b = y->stride[0]; a.sy_l = y->stride[1]; a.sy_h = y->stride[2]; a.sy_p = y->stride[3];
+    if (last_state) {
+        a.last = static_cast<float*>(last_state->data);
+        a.sl_b = last_state->stride[0]; a.sl_h = last_state->stride[1];
+        a.sl_p = last_state->stride[2]; a.sl_n = last_state->stride[3];
+    }
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    return launch_ssd(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+const char* ss_status_string(int status) {
+    switch (status) {
+        case SS_OK: return "ok";
+        case SS_ERR_INVALID_ARG: return "invalid argument";
+        case SS_ERR_SHAPE: return "shape mismatch";
+        case SS_ERR_DTYPE: return "unsupported or mixed dtype";
+        case SS_ERR_ALIGNMENT: return "misaligned pointer";
+        case SS_ERR_UNSUPPORTED: return "unsupported size";
+        case SS_ERR_ALLOC: return "scratch allocation failed";
+        case SS_ERR_LAUNCH: return "kernel launch failed";
+        case SS_ERR_TIMEOUT: return "device-side wait timed out";
+        case SS_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+int ss_get_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SS_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return SS_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+        return SS_ERR_TIMEOUT;
+    }
+    return SS_OK;
+}
+
+uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int ss_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ss {
+
+// Host view of one selective-scan call, element strides.
+struct ScanArgs {
+    int Bsz, D, N, L;
+    int dtype;  // SS_F32 / SS_BF16
+    const void* u;  int64_t su_b, su_d, su_t;
+    const void* dl; int64_t sdl_b, sdl_d, sdl_t;
+    const void* z;  int64_t sz_b, sz_d, sz_t;
+    void* y;        int64_t sy_b, sy_d, sy_t;
+    const void* Bm; int64_t sB_b, sB_n, sB_t;
+    const void* Cm; int64_t sC_b, sC_n, sC_t;
+    const float* A; int64_t sA_d, sA_n;
+    const float* Dv; int64_t sD;
+    const float* bias; int64_t sbias;
+    float* last; int64_t sl_b, sl_d, sl_n;
+    int softplus;
+    unsigned* err;  // device error word
+};
+
+// Host view of one SSD call, element strides.
+struct SSDArgs {
+    int Bsz, L, H, P, G, N, chunk;
+    int dtype;
+    const void* x;  int64_t sx_b, sx_l, sx_h, sx_p;
+    const void* dt; int64_t sdt_b, sdt_l, sdt_h;
+    const float* A; int64_t sA;
+    const void* Bm; int64_t sB_b, sB_l, sB_g, sB_n;
+    const void* Cm; int64_t sC_b, sC_l, sC_g, sC_n;
+    const float* Dv; int64_t sD;
+    void* y;        int64_t sy_b, sy_l, sy_h, sy_p;
+    float* last;    int64_t sl_b, sl_h, sl_p, sl_n;
+    unsigned* err;
+};
+
+// Scratch provider: either stream-ordered allocation or a fixed buffer.
+struct Scratch {
+    void* (*alloc)(size_t bytes, cudaStream_t st, void* ctx);
+    void (*release)(void* p, cudaStream_t st, void* ctx);
+    void* ctx;
+};
+
+int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
+int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
+
+// Counts kernels launched by the library.
+void count_launch(int n);
+int sm_count_current();
+// cuTensorMapEncodeTiled resolved through the runtime (no libcuda link).
+void* tensor_map_encoder();
+
+}  // namespace ss

@@ -1,0 +1,688 @@
+// selective_scan.cu -- the Mamba selective scan on sm_103a.
+//
+// What is computed (page "Mamba模型笔记" §2.2 and §4.1-§4.4; 0539edu paper
+// talk §2.3): per batch row b and channel d, with dl = softplus(delta + bias),
+//   h[n] <- exp(dl * A[d,n]) * h[n] + dl * B[b,n,t] * u,
+//   y     = (sum_n C[b,n,t] h[n] + D[d] u) * z * sigmoid(z).
+//
+// Two kernels:
+//
+//  * scan_general: one thread per (b, d), any strides, any N <= 256.  Used for
+//    layouts the fast path does not take (odd lengths, non-unit t strides,
+//    N != 16).
+//
+//  * scan_fast: N = 16, unit t stride, 16-byte aligned rows.  One CTA owns a
+//    tile of channels of one batch row over one time segment:
+//      warp 0      TMA (cp.async.bulk.tensor) of the u / delta / z tiles
+//                  (128 bytes of t per channel row, 128-byte swizzle) and of
+//                  the raw B / C tiles into a ring of stages;
+//      warp 1      converts B and C of each tile to an fp32 table shared by
+//                  all channels of the CTA;
+//      warps 2..   consumers: NSPLIT lanes per channel, each keeping N/NSPLIT
+//                  states in registers and stepping through t sequentially
+//                  with packed f32x2 arithmetic.  delta (softplus) is computed
+//                  once per channel and step and all-gathered in the lane
+//                  group; the partial readouts are reduce-scattered so each
+//                  lane finishes (skip, gate) and stores its own steps of y.
+//    All hand-offs are mbarriers; every wait is bounded (ERR_WAIT_TIMEOUT).
+//    When the channels alone cannot fill the GPU the sequence is split into
+//    segments: a summary pass records, per segment, prod_t exp(dl A) =
+//    exp(A sum_t dl) and the end state from zero; the main pass seeds each
+//    segment with the fold of its predecessors' summaries.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <type_traits>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "ssscan.h"
+
+namespace ss {
+
+// ---------------------------------------------------------------------------
+// General kernel.
+
+template <typename T, int NMAX>
+__global__ void __launch_bounds__(128) scan_general(ScanArgs a) {
+    int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (unit >= (int64_t)a.Bsz * a.D) return;
+    const int b = (int)(unit / a.D), d = (int)(unit % a.D);
+    const int N = a.N;
+    float h[NMAX], A2[NMAX];
+#pragma unroll
+    for (int n = 0; n < NMAX; ++n) {
+        h[n] = 0.f;
+        A2[n] = n < N ? a.A[d * a.sA_d + n * a.sA_n] * kLog2e : 0.f;
+    }
+    const float Dd = a.Dv ? a.Dv[d * a.sD] : 0.f;
+    const float bd = a.bias ? a.bias[d * a.sbias] : 0.f;
+    const T* u = static_cast<const T*>(a.u) + b * a.su_b + d * a.su_d;
+    const T* dl = static_cast<const T*>(a.dl) + b * a.sdl_b + d * a.sdl_d;
+    const T* z = a.z ? static_cast<const T*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
+    T* y = static_cast<T*>(a.y) + b * a.sy_b + d * a.sy_d;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b;
+    for (int t = 0; t < a.L; ++t) {
+        const float uu = Elem<T>::to_f(u[t * a.su_t]);
+        float dd = Elem<T>::to_f(dl[t * a.sdl_t]) + bd;
+        if (a.softplus) dd = softplus_f(dd);
+        const float du = dd * uu;
+        float acc = 0.f;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+            if (n < N) {
+                const float bn = Elem<T>::to_f(Bp[n * a.sB_n + t * a.sB_t]);
+                const float cn = Elem<T>::to_f(Cp[n * a.sC_n + t * a.sC_t]);
+                h[n] = fmaf(ex2_approx(dd * A2[n]), h[n], du * bn);
+                acc = fmaf(cn, h[n], acc);
+            }
+        }
+        acc = fmaf(Dd, uu, acc);
+        if (z) {
+            const float zz = Elem<T>::to_f(z[t * a.sz_t]);
+            acc *= zz * sigmoid_accurate(zz);
+        }
+        y[t * a.sy_t] = Elem<T>::from_f(acc);
+    }
+    if (a.last) {
+        float* ls = a.last + b * a.sl_b + d * a.sl_d;
+        for (int n = 0; n < N; ++n) ls[n * a.sl_n] = h[n];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fast kernel.
+
+struct FastParams {
+    int Bsz, D, L;
+    int dtiles;     // channel tiles per batch row
+    int seg_len;    // multiple of the t tile
+    int nseg;
+    const float* A; int64_t sA_d, sA_n;
+    const float* Dv; int64_t sD;
+    const float* bias; int64_t sbias;
+    float* last; int64_t sl_b, sl_d, sl_n;
+    void* y; int64_t sy_b, sy_d;  // y rows are contiguous in t
+    float* summ;    // [nseg-1][Bsz*D][2][N]: prod of decays, end state from zero
+    int softplus;
+    unsigned* err;
+};
+
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
+struct FastCfg {
+    static constexpr int N = 16;
+    static constexpr int ES = sizeof(T);
+    static constexpr int VEC = 16 / ES;          // elements per 16-byte chunk
+    static constexpr int TT = 128 / ES;          // t per tile (one 128-byte row)
+    static constexpr int CHUNKS = TT / VEC;      // = 8
+    static constexpr int CPW = 32 / NSPLIT;      // channels per consumer warp
+    static constexpr int DT = CWARPS * CPW;      // channels per CTA
+    static constexpr int NS = N / NSPLIT;        // states per thread
+    static constexpr int NCONS = CWARPS * 32;
+    static constexpr int NTHREADS = NCONS + 64;  // + TMA warp + B|C conversion warp
+    static constexpr bool LOAD_Z = HAS_Z && !SUMMARY;
+    static constexpr bool LOAD_C = !SUMMARY;
+    static constexpr int TILE_BYTES = DT * 128;  // one [DT][TT] tile of u, delta, z or y
+    static constexpr int RAW_BYTES = N * 128;    // one [N][TT] tile of B or C as loaded
+    static constexpr int BC_BYTES = TT * 2 * N * 4;
+    // stage: u, delta, [z], raw B, [raw C], fp32 B|C table
+    static constexpr int OFF_DL = TILE_BYTES;
+    static constexpr int OFF_Z = 2 * TILE_BYTES;
+    static constexpr int OFF_RAWB = (LOAD_Z ? 3 : 2) * TILE_BYTES;
+    static constexpr int OFF_RAWC = OFF_RAWB + RAW_BYTES;
+    static constexpr int OFF_BC = OFF_RAWC + (LOAD_C ? RAW_BYTES : 0);
+    static constexpr int STAGE_BYTES = OFF_BC + BC_BYTES;
+    static constexpr int TILE_TX = TILE_BYTES * (LOAD_Z ? 3 : 2);
+    static constexpr int RAW_TX = RAW_BYTES * (LOAD_C ? 2 : 1);
+    static constexpr int SMEM_BYTES = STAGE_BYTES * STAGES + 256 /*barriers*/ + 1024 /*align*/;
+    static_assert(TILE_BYTES % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(NS % 4 == 0, "states per thread must be a multiple of 4");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 7)) << 4); }
+
+template <typename T>
+__device__ __forceinline__ float gate_sigmoid(float z) {
+    if constexpr (sizeof(T) == 2) return sigmoid_fast(z);
+    else return sigmoid_accurate(z);
+}
+
+// Conversion of one tile's raw B / C ([n][t] as loaded by TMA) into the fp32
+// table bc[t][32]: 16-byte chunk 2q holds B[4q..4q+3], chunk 2q+1 holds
+// C[4q..4q+3].  A lane group that owns states [4j, 4j+4m) reads m chunk pairs
+// that sit next to each other, at offsets known at compile time.  Lane l
+// writes rows 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by
+// lane so that the lanes of one store hit distinct banks.
+template <typename T, bool WITH_C>
+__device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int q = (it + lane) & 7;
+        const bool isC = q & 1;
+        if (!WITH_C && isC) continue;
+        const uint32_t src = isC ? rawC : rawB;
+        const int n0 = (q >> 1) * 4;
+        if constexpr (sizeof(T) == 2) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = lds32(src + ((n0 + i) * 32 + lane) * 4);  // (t, t+1)
+            const float4 lo = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[1] << 16),
+                                          __uint_as_float(w[2] << 16), __uint_as_float(w[3] << 16));
+            const float4 hi = make_float4(
+                __uint_as_float(w[0] & 0xffff0000u), __uint_as_float(w[1] & 0xffff0000u),
+                __uint_as_float(w[2] & 0xffff0000u), __uint_as_float(w[3] & 0xffff0000u));
+            sts128f(bc + (2 * lane) * 128 + q * 16, lo);
+            sts128f(bc + (2 * lane + 1) * 128 + q * 16, hi);
+        } else {
+            float4 v;
+            v.x = __uint_as_float(lds32(src + ((n0 + 0) * 32 + lane) * 4));
+            v.y = __uint_as_float(lds32(src + ((n0 + 1) * 32 + lane) * 4));
+            v.z = __uint_as_float(lds32(src + ((n0 + 2) * 32 + lane) * 4));
+            v.w = __uint_as_float(lds32(src + ((n0 + 3) * 32 + lane) * 4));
+            sts128f(bc + lane * 128 + q * 16, v);
+        }
+    }
+}
+
+// K consecutive elements of T (K * sizeof(T) in {4, 8, 16} bytes) from
+// shared memory, widened to float.
+template <typename T, int K>
+__device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
+    constexpr int BYTES = K * (int)sizeof(T);
+    uint32_t w[4];
+    if constexpr (BYTES == 16) {
+        const uint4 v = lds128(a);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BYTES == 8) {
+        const uint2 v = lds64(a);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        w[0] = lds32(a);
+    }
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < K / 2; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i) out[i] = __uint_as_float(w[i]);
+    }
+}
+
+// Store K floats as T to global memory: one aligned vector store, or (in the
+// last chunk of the sequence) element by element up to `limit` elements.
+template <typename T, int K>
+__device__ __forceinline__ void stg_elems(T* p, const float* v, int limit) {
+    constexpr int BYTES = K * (int)sizeof(T);
+    if (limit >= K) {
+        uint32_t w[4];
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < K / 2; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < K; ++i) w[i] = __float_as_uint(v[i]);
+        }
+        if constexpr (BYTES == 16) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        else if constexpr (BYTES == 8) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        else *reinterpret_cast<uint32_t*>(p) = w[0];
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            if (i < limit) p[i] = Elem<T>::from_f(v[i]);
+    }
+}
+
+// One round of the readout reduce-scatter across the lanes of a channel:
+// keep one half of v (the upper half if `upper`), send the other half to the
+// partner lane (lane ^ m) and add what the partner sends back.
+template <int LEN>
+__device__ __forceinline__ void reduce_half(const float* v, float* out, bool upper, int m) {
+#pragma unroll
+    for (int e = 0; e < LEN / 2; ++e) {
+        const float lo = v[e], hi = v[LEN / 2 + e];
+        const float send = upper ? lo : hi;
+        const float keep = upper ? hi : lo;
+        out[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+}
+
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
+__global__ void __launch_bounds__(FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>::NTHREADS, 3)
+scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+          const __grid_constant__ CUtensorMap tm_C, const FastParams p) {
+    using Cfg = FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
+    constexpr int N = Cfg::N, TT = Cfg::TT, VEC = Cfg::VEC, NS = Cfg::NS, DT = Cfg::DT;
+    constexpr int ES = Cfg::ES;
+    constexpr int K = VEC / NSPLIT;  // t per chunk whose delta and y this lane owns
+
+    // Align to 1024 bytes (128-byte swizzle atoms) by pointer arithmetic on the
+    // shared array itself, so every access below stays a shared-memory access.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::STAGE_BYTES * STAGES);
+    uint64_t* full = bars;             // u / delta / z landed (TMA bytes)
+    uint64_t* raw = bars + STAGES;     // raw B / C landed (TMA bytes)
+    uint64_t* table = bars + 2 * STAGES;  // fp32 B|C table written
+    uint64_t* empty = bars + 3 * STAGES;  // consumers done; the stage may be refilled
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x / p.dtiles;
+    const int d0 = (blockIdx.x % p.dtiles) * DT;
+    const int seg = blockIdx.y;
+    const int tbeg = seg * p.seg_len;
+    const int tend = min(p.L, tbeg + p.seg_len);
+    const int ntiles = (tend - tbeg + TT - 1) / TT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&raw[s], 1);
+            mbar_init(&table[s], 32);
+            mbar_init(&empty[s], Cfg::NCONS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto stage = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
+
+    if (warp == 0) {
+        // ---------------- TMA loads ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_u);
+            tma_prefetch_desc(&tm_dl);
+            tma_prefetch_desc(&tm_B);
+            if (Cfg::LOAD_Z) tma_prefetch_desc(&tm_z);
+            if (Cfg::LOAD_C) tma_prefetch_desc(&tm_C);
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % STAGES;
+                if (k >= STAGES && !mbar_wait(&empty[s], ((k / STAGES) - 1) & 1, p.err)) break;
+                const int t0 = tbeg + k * TT;
+                uint8_t* st = stage(s);
+                mbar_arrive_expect_tx(&raw[s], Cfg::RAW_TX);
+                tma_load_3d(st + Cfg::OFF_RAWB, &tm_B, &raw[s], t0, 0, b);
+                if (Cfg::LOAD_C) tma_load_3d(st + Cfg::OFF_RAWC, &tm_C, &raw[s], t0, 0, b);
+                mbar_arrive_expect_tx(&full[s], Cfg::TILE_TX);
+                tma_load_3d(st, &tm_u, &full[s], t0, d0, b);
+                tma_load_3d(st + Cfg::OFF_DL, &tm_dl, &full[s], t0, d0, b);
+                if (Cfg::LOAD_Z) tma_load_3d(st + Cfg::OFF_Z, &tm_z, &full[s], t0, d0, b);
+            }
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // ---------------- B|C table ----------------
+        for (int k = 0; k < ntiles; ++k) {
+            const int s = k % STAGES;
+            if (!mbar_wait(&raw[s], (k / STAGES) & 1, p.err)) break;
+            const uint32_t st = smem_u32(stage(s));
+            convert_bc<T, Cfg::LOAD_C>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC,
+                                       lane);
+            mbar_arrive(&table[s]);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    // NSPLIT consecutive lanes share one channel; lane `part` of the group keeps
+    // states [part*NS, part*NS + NS), computes delta for t in its K-slot of
+    // every chunk, and owns the outputs of that slot.
+    const int cw = warp - 2;
+    const int ci = cw * Cfg::CPW + lane / NSPLIT;  // channel row within the tile
+    const int part = lane % NSPLIT;
+    const int gbase = lane - part;
+    const int d = d0 + ci;
+    const bool valid = d < p.D;
+    const int64_t bd = (int64_t)b * p.D + d;
+
+    float2 A2[NS / 2], h2[NS / 2];
+#pragma unroll
+    for (int j = 0; j < NS / 2; ++j) {
+        const int n = part * NS + 2 * j;
+        A2[j] = valid ? make_float2(p.A[d * p.sA_d + n * p.sA_n] * kLog2e,
+                                    p.A[d * p.sA_d + (n + 1) * p.sA_n] * kLog2e)
+                      : make_float2(0.f, 0.f);
+        h2[j] = make_float2(0.f, 0.f);
+    }
+    const float Dd = (valid && p.Dv) ? p.Dv[d * p.sD] : 0.f;
+    const float biasd = (valid && p.bias) ? p.bias[d * p.sbias] : 0.f;
+    const bool sp = p.softplus != 0;
+
+    if (!SUMMARY && seg > 0 && valid) {
+        // state entering this segment: fold the summaries of segments 0..seg-1
+        const int64_t per = (int64_t)p.Bsz * p.D * 2 * N;
+        for (int j = 0; j < seg; ++j) {
+            const float* sm = p.summ + j * per + bd * 2 * N;
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+                const int n = part * NS + 2 * q;
+                h2[q] = __ffma2_rn(make_float2(sm[n], sm[n + 1]), h2[q],
+                                   make_float2(sm[N + n], sm[N + n + 1]));
+            }
+        }
+    }
+
+    float dsum = 0.f;  // sum of delta over the segment (summary pass)
+
+    // One 16-byte chunk (VEC steps) of this lane's channel.
+    T* yrow = static_cast<T*>(p.y) + (int64_t)b * p.sy_b + (int64_t)(valid ? d : 0) * p.sy_d;
+    auto chunk = [&](uint32_t su, uint32_t bcp, int tile_t0, int c, int tcount, auto tail) {
+        constexpr bool TAIL = decltype(tail)::value;
+        const int off = swz(ci, c);
+        const int own = off + part * K * ES;  // this lane's K-slot of the chunk
+        float uf[VEC];
+        lds_elems<T, VEC>(su + off, uf);
+        // delta for the own slot, then all-gathered across the group
+        float dv[K];
+        lds_elems<T, K>(su + Cfg::OFF_DL + own, dv);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float x = dv[k] + biasd;
+            x = sp ? softplus_f(x) : x;
+            if (TAIL && c * VEC + part * K + k >= tcount) x = 0.f;  // past the end: no update
+            dv[k] = x;
+        }
+        float dd[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            dd[j] = NSPLIT == 1 ? dv[j % K] : __shfl_sync(0xffffffffu, dv[j % K], gbase + j / K);
+
+        float yv[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            if (SUMMARY) dsum += dd[i];
+            const float2 d2 = make_float2(dd[i], dd[i]);
+            const float du = dd[i] * uf[i];
+            const float2 du2 = make_float2(du, du);
+            const uint32_t row = bcp + (c * VEC + i) * 128;
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NS / 4; ++q) {
+                const float4 bq = lds128f(row + q * 32);
+                const float2 ar0 = __fmul2_rn(d2, A2[2 * q]);
+                const float2 ar1 = __fmul2_rn(d2, A2[2 * q + 1]);
+                const float2 a0 = make_float2(ex2_approx(ar0.x), ex2_approx(ar0.y));
+                const float2 a1 = make_float2(ex2_approx(ar1.x), ex2_approx(ar1.y));
+                h2[2 * q] = __ffma2_rn(a0, h2[2 * q], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
+                h2[2 * q + 1] =
+                    __ffma2_rn(a1, h2[2 * q + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
+                if constexpr (!SUMMARY) {
+                    const float4 cq = lds128f(row + q * 32 + 16);
+                    acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h2[2 * q], acc0);
+                    acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h2[2 * q + 1], acc1);
+                }
+            }
+            yv[i] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        }
+        if constexpr (!SUMMARY) {
+            // reduce-scatter the partial readouts: lane `part` ends with the
+            // full sum for its own K steps
+            float yo[K];
+            if constexpr (NSPLIT == 1) {
+#pragma unroll
+                for (int k = 0; k < K; ++k) yo[k] = yv[k];
+            } else if constexpr (NSPLIT == 2) {
+                reduce_half<VEC>(yv, yo, part & 1, 1);
+            } else {
+                float w[VEC / 2];
+                reduce_half<VEC>(yv, w, (part >> 1) & 1, 2);
+                reduce_half<VEC / 2>(w, yo, part & 1, 1);
+            }
+            float uo[K];
+            [[maybe_unused]] float zo[K];
+            lds_elems<T, K>(su + own, uo);
+            if constexpr (HAS_Z) lds_elems<T, K>(su + Cfg::OFF_Z + own, zo);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float o = fmaf(Dd, uo[k], yo[k]);
+                if constexpr (HAS_Z) o *= zo[k] * gate_sigmoid<T>(zo[k]);
+                yo[k] = o;
+            }
+            if (valid) {
+                const int tg = tile_t0 + c * VEC + part * K;
+                stg_elems<T, K>(yrow + tg, yo, TAIL ? tend - tg : K);
+            }
+        }
+    };
+
+    bool ok = true;
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % STAGES;
+        if (!mbar_wait(&full[s], (k / STAGES) & 1, p.err) ||
+            !mbar_wait(&table[s], (k / STAGES) & 1, p.err)) {
+            ok = false;
+            break;
+        }
+        const int tile_t0 = tbeg + k * TT;
+        const int tcount = min(TT, tend - tile_t0);
+        const uint32_t su = smem_u32(stage(s));
+        const uint32_t bcp = su + Cfg::OFF_BC + part * NS * 2 * 4;
+        const int full_chunks = tcount / VEC;
+#pragma unroll 1
+        for (int c = 0; c < full_chunks; ++c) chunk(su, bcp, tile_t0, c, tcount, std::false_type{});
+        if (full_chunks < Cfg::CHUNKS && full_chunks * VEC < tcount)
+            chunk(su, bcp, tile_t0, full_chunks, tcount, std::true_type{});
+        mbar_arrive(&empty[s]);
+    }
+    if (!ok || !valid) return;
+
+    if constexpr (SUMMARY) {
+        const int64_t per = (int64_t)p.Bsz * p.D * 2 * N;
+        float* sm = p.summ + seg * per + bd * 2 * N;
+#pragma unroll
+        for (int q = 0; q < NS / 2; ++q) {
+            const int n = part * NS + 2 * q;
+            sm[n] = ex2_approx(A2[q].x * dsum);
+            sm[n + 1] = ex2_approx(A2[q].y * dsum);
+            sm[N + n] = h2[q].x;
+            sm[N + n + 1] = h2[q].y;
+        }
+    } else {
+        if (p.last && seg == p.nseg - 1) {
+            float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)d * p.sl_d;
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+                const int n = part * NS + 2 * q;
+                ls[n * p.sl_n] = h2[q].x;
+                ls[(n + 1) * p.sl_n] = h2[q].y;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+static bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
+                        int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle = true) {
+    auto enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
+    if (!enc) return false;
+    const int es = dtype == SS_BF16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)L, (cuuint64_t)D, (cuuint64_t)Bsz};
+    cuuint64_t strides[2] = {(cuuint64_t)(sd * es), (cuuint64_t)(sb * es)};
+    cuuint32_t box[3] = {(cuuint32_t)box_t, (cuuint32_t)box_d, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dtype == SS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static bool fast_layout_ok(const ScanArgs& a) {
+    if (a.N != 16) return false;
+    const int es = a.dtype == SS_BF16 ? 2 : 4;
+    auto row_ok = [&](const void* ptr, int64_t sb, int64_t sd, int64_t st) {
+        if (!ptr) return true;
+        if (st != 1 && a.L > 1) return false;
+        if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+        if ((sd * es) % 16 || (sb * es) % 16) return false;
+        if (sd * es >= (int64_t(1) << 40) || sb * es >= (int64_t(1) << 40)) return false;
+        return true;
+    };
+    if (a.D > 1 && a.su_d == 0) return false;
+    return row_ok(a.u, a.su_b, a.su_d, a.su_t) && row_ok(a.dl, a.sdl_b, a.sdl_d, a.sdl_t) &&
+           row_ok(a.z, a.sz_b, a.sz_d, a.sz_t) && row_ok(a.y, a.sy_b, a.sy_d, a.sy_t) &&
+           row_ok(a.Bm, a.sB_b, a.sB_n, a.sB_t) && row_ok(a.Cm, a.sC_b, a.sC_n, a.sC_t) &&
+           a.L < (1 << 30);
+}
+
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
+static cudaError_t launch_fast_kernel(const CUtensorMap* maps, const FastParams& fp, dim3 grid,
+                                      cudaStream_t st) {
+    using Cfg = FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
+    auto kern = scan_fast<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
+    static bool attr_set[64] = {};  // the attribute is set once per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        // all of the unified L1 / shared storage as shared memory: 3 CTAs per SM
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    kern<<<grid, Cfg::NTHREADS, Cfg::SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                       fp);
+    count_launch(1);
+    return cudaGetLastError();
+}
+
+// Tuning of the fast path: lanes per channel (NSPLIT) and consumer warps per
+// CTA are paired so a CTA always holds 32 (NSPLIT = 2, 4) or 64 (NSPLIT = 1)
+// channels; three stages fit three CTAs in one SM's shared memory.
+constexpr int kStages = 3;
+
+template <typename T, int NSPLIT, int kCWarps>
+static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
+    using CfgM = FastCfg<T, NSPLIT, kCWarps, kStages, true, false>;
+    constexpr int TT = CfgM::TT, DT = CfgM::DT;
+    FastParams fp{};
+    fp.Bsz = a.Bsz; fp.D = a.D; fp.L = a.L;
+    fp.dtiles = (a.D + DT - 1) / DT;
+    fp.A = a.A; fp.sA_d = a.sA_d; fp.sA_n = a.sA_n;
+    fp.Dv = a.Dv; fp.sD = a.sD; fp.bias = a.bias; fp.sbias = a.sbias;
+    fp.last = a.last; fp.sl_b = a.sl_b; fp.sl_d = a.sl_d; fp.sl_n = a.sl_n;
+    fp.y = a.y; fp.sy_b = a.sy_b; fp.sy_d = a.sy_d;
+    fp.softplus = a.softplus; fp.err = a.err;
+
+    // Segments: enough CTAs to give every SM several consumer warps.
+    const int sms = sm_count_current();
+    const int64_t ctas = (int64_t)a.Bsz * fp.dtiles;
+    const int64_t want = (int64_t)sms * 2;
+    int nseg = 1;
+    if (ctas < want) nseg = (int)std::min<int64_t>(64, (want + ctas - 1) / ctas);
+    int64_t tiles = (a.L + TT - 1) / TT;
+    nseg = (int)std::min<int64_t>(nseg, tiles);
+    if (nseg < 1) nseg = 1;
+    int64_t seg_tiles = (tiles + nseg - 1) / nseg;
+    nseg = (int)((tiles + seg_tiles - 1) / seg_tiles);
+    fp.seg_len = (int)(seg_tiles * TT);
+    fp.nseg = nseg;
+
+    // maps: 0 u, 1 delta, 2 z, 3 B, 4 C
+    CUtensorMap maps[5];
+    if (!make_map_3d(&maps[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, TT, DT) ||
+        !make_map_3d(&maps[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, TT, DT) ||
+        !make_map_3d(&maps[3], a.Bm, a.dtype, a.L, a.N, a.Bsz, a.sB_n, a.sB_b, TT, 16, false) ||
+        !make_map_3d(&maps[4], a.Cm, a.dtype, a.L, a.N, a.Bsz, a.sC_n, a.sC_b, TT, 16, false))
+        return SS_ERR_CUDA;
+    if (a.z) {
+        if (!make_map_3d(&maps[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, TT, DT))
+            return SS_ERR_CUDA;
+    } else {
+        maps[2] = maps[0];
+    }
+
+    void* summ = nullptr;
+    if (nseg > 1) {
+        size_t bytes = (size_t)(nseg - 1) * a.Bsz * a.D * 2 * 16 * sizeof(float);
+        summ = scratch.alloc(bytes, st, scratch.ctx);
+        if (!summ) return SS_ERR_ALLOC;
+        fp.summ = static_cast<float*>(summ);
+        cudaError_t e = launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, true>(
+            maps, fp, dim3((unsigned)ctas, nseg - 1), st);
+        if (e != cudaSuccess) {
+            scratch.release(summ, st, scratch.ctx);
+            return SS_ERR_LAUNCH;
+        }
+    }
+    cudaError_t e = a.z ? launch_fast_kernel<T, NSPLIT, kCWarps, kStages, true, false>(
+                              maps, fp, dim3((unsigned)ctas, nseg), st)
+                        : launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, false>(
+                              maps, fp, dim3((unsigned)ctas, nseg), st);
+    if (summ) scratch.release(summ, st, scratch.ctx);
+    return e == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
+}
+
+template <typename T>
+static int run_general(const ScanArgs& a, cudaStream_t st) {
+    const int64_t units = (int64_t)a.Bsz * a.D;
+    const int threads = 128;
+    const unsigned blocks = (unsigned)((units + threads - 1) / threads);
+    if (a.N <= 16) scan_general<T, 16><<<blocks, threads, 0, st>>>(a);
+    else if (a.N <= 64) scan_general<T, 64><<<blocks, threads, 0, st>>>(a);
+    else scan_general<T, 256><<<blocks, threads, 0, st>>>(a);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
+}
+
+// Path selection for tests: SS_SCAN_PATH=general forces the general kernel;
+// split1 / split2 / split4 force the fast kernel with 1, 2 or 4 lanes per channel.
+static int forced_path() {
+    const char* s = getenv("SS_SCAN_PATH");
+    if (!s) return -1;
+    if (!strcmp(s, "general")) return 0;
+    if (!strcmp(s, "split1")) return 1;
+    if (!strcmp(s, "split2")) return 2;
+    if (!strcmp(s, "split4")) return 4;
+    return -1;
+}
+
+int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
+    const int force = forced_path();
+    const bool bf = a.dtype == SS_BF16;
+    if (force != 0 && a.L > 0 && fast_layout_ok(a)) {
+        // the fewest lanes per channel that still give every SM 8 consumer warps
+        const int sms = sm_count_current();
+        const int64_t ch = (int64_t)a.Bsz * a.D, want = (int64_t)sms * 256;
+        int split = ch >= want ? 1 : (2 * ch >= want ? 2 : 4);
+        if (force == 1 || force == 2 || force == 4) split = force;
+        if (bf) {
+            if (split == 1) return run_fast<__nv_bfloat16, 1, 2>(a, st, scratch);
+            if (split == 2) return run_fast<__nv_bfloat16, 2, 2>(a, st, scratch);
+            return run_fast<__nv_bfloat16, 4, 4>(a, st, scratch);
+        }
+        if (split == 1) return run_fast<float, 1, 2>(a, st, scratch);
+        if (split == 2) return run_fast<float, 2, 2>(a, st, scratch);
+        return run_fast<float, 4, 4>(a, st, scratch);
+    }
+    return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
+}
+
+}  // namespace ss

@@ -1,0 +1,91 @@
+// ssd.cu -- the Mamba-2 SSD scan on sm_103a.
+//
+// What is computed (page "Mamba模型笔记" §5; state-spaces/mamba README §4.3):
+// per batch row b and head h (group g = h / (H/G)), with a = exp(dt A_h),
+//   S[p][n] <- a S[p][n] + dt x[p] B[g][n],   y[p] = sum_n C[g][n] S[p][n] + D_h x[p].
+//
+// This file holds the general CUDA-core kernel (one thread per (b, h, p),
+// state row in registers, sequential over t): any strides, dtypes, P and
+// N <= 256.  The chunked tensor-core kernel lives in ssd_tc.cu.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "ssscan.h"
+
+namespace ss {
+
+template <typename T, int NMAX>
+__global__ void __launch_bounds__(128) ssd_general(SSDArgs a) {
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t units = (int64_t)a.Bsz * a.H * a.P;
+    if (unit >= units) return;
+    const int p = (int)(unit % a.P);
+    const int h = (int)((unit / a.P) % a.H);
+    const int b = (int)(unit / ((int64_t)a.P * a.H));
+    const int g = h / (a.H / a.G);
+    const int N = a.N;
+    float S[NMAX];
+#pragma unroll
+    for (int n = 0; n < NMAX; ++n) S[n] = 0.f;
+    const float A2 = a.A[h * a.sA] * kLog2e;
+    const float Dh = a.Dv ? a.Dv[h * a.sD] : 0.f;
+    const T* x = static_cast<const T*>(a.x) + b * a.sx_b + h * a.sx_h + p * a.sx_p;
+    const T* dt = static_cast<const T*>(a.dt) + b * a.sdt_b + h * a.sdt_h;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b + g * a.sB_g;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b + g * a.sC_g;
+    T* y = static_cast<T*>(a.y) + b * a.sy_b + h * a.sy_h + p * a.sy_p;
+    for (int t = 0; t < a.L; ++t) {
+        const float dtv = Elem<T>::to_f(dt[t * a.sdt_l]);
+        const float xv = Elem<T>::to_f(x[t * a.sx_l]);
+        const float decay = ex2_approx(dtv * A2);
+        const float dx = dtv * xv;
+        const T* br = Bp + t * a.sB_l;
+        const T* cr = Cp + t * a.sC_l;
+        float acc = 0.f;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+            if (n < N) {
+                S[n] = fmaf(decay, S[n], dx * Elem<T>::to_f(br[n * a.sB_n]));
+                acc = fmaf(Elem<T>::to_f(cr[n * a.sC_n]), S[n], acc);
+            }
+        }
+        y[t * a.sy_l] = Elem<T>::from_f(fmaf(Dh, xv, acc));
+    }
+    if (a.last) {
+        float* ls = a.last + b * a.sl_b + h * a.sl_h + p * a.sl_p;
+        for (int n = 0; n < N; ++n) ls[n * a.sl_n] = S[n];
+    }
+}
+
+template <typename T>
+static int run_ssd_general(const SSDArgs& a, cudaStream_t st) {
+    const int64_t units = (int64_t)a.Bsz * a.H * a.P;
+    const int threads = 128;
+    const unsigned blocks = (unsigned)((units + threads - 1) / threads);
+    if (a.N <= 16) ssd_general<T, 16><<<blocks, threads, 0, st>>>(a);
+    else if (a.N <= 64) ssd_general<T, 64><<<blocks, threads, 0, st>>>(a);
+    else if (a.N <= 128) ssd_general<T, 128><<<blocks, threads, 0, st>>>(a);
+    else ssd_general<T, 256><<<blocks, threads, 0, st>>>(a);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
+}
+
+int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken);
+
+int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch) {
+    const char* force = getenv("SS_SSD_PATH");
+    const bool general_only = force && !strcmp(force, "general");
+    if (!general_only) {
+        bool taken = false;
+        int rc = launch_ssd_tc(a, st, scratch, &taken);
+        if (taken) return rc;
+    }
+    return a.dtype == SS_BF16 ? run_ssd_general<__nv_bfloat16>(a, st) : run_ssd_general<float>(a, st);
+}
+
+}  // namespace ss

@@ -85,8 +85,31 @@ WORKLOADS = {
 }
 
 
+_DEVICE = "cpu"  # where the generators draw; see on_device()
+
+
 def _gen(seed: int, k: str) -> torch.Generator:
-    return torch.Generator(device="cpu").manual_seed(seed * 1000 + _IDX[k])
+    return torch.Generator(device=_DEVICE).manual_seed(seed * 1000 + _IDX[k])
+
+
+class on_device:
+    """Draw with generators on another device (e.g. "cuda") inside this block.
+
+    The recipe is the same; the values differ from the CPU draws, so this is
+    for timing runs only -- parity tests use the CPU draws the oracle reads.
+    """
+
+    def __init__(self, device):
+        self.device = str(device)
+
+    def __enter__(self):
+        global _DEVICE
+        self._old, _DEVICE = _DEVICE, self.device
+        return self
+
+    def __exit__(self, *exc):
+        global _DEVICE
+        _DEVICE = self._old
 
 
 def _tdtype(dtype: str):
@@ -94,14 +117,14 @@ def _tdtype(dtype: str):
 
 
 def _normal(shape, seed, k, std=1.0):
-    t = torch.randn(*shape, generator=_gen(seed, k), dtype=torch.float32)
+    t = torch.randn(*shape, generator=_gen(seed, k), dtype=torch.float32, device=_DEVICE)
     if std != 1.0:
         t.mul_(std)
     return t
 
 
 def _log_uniform(n, lo, hi, seed, k):
-    r = torch.rand(n, generator=_gen(seed, k), dtype=torch.float64)
+    r = torch.rand(n, generator=_gen(seed, k), dtype=torch.float64, device=_DEVICE)
     return torch.exp(math.log(lo) + r * (math.log(hi) - math.log(lo)))
 
 
@@ -123,7 +146,8 @@ def selective_inputs(batch, d_inner, d_state, seqlen, dtype="bf16", *, gate=True
         "B": _normal((batch, d_state, seqlen), seed, "B").to(td),
         "C": _normal((batch, d_state, seqlen), seed, "C").to(td),
         "D": _normal((d_inner,), seed, "D") if skip else None,
-        "A": -(torch.arange(d_state, dtype=torch.float32) + 1.0).expand(d_inner, d_state).contiguous(),
+        "A": -(torch.arange(d_state, dtype=torch.float32, device=_DEVICE) + 1.0)
+        .expand(d_inner, d_state).contiguous(),
     }
     if bias:
         dt = _log_uniform(d_inner, dt_min, dt_max, seed, "dt")
@@ -151,7 +175,7 @@ def ssd_inputs(batch, seqlen, nheads, headdim, d_state, ngroups=1, dtype="bf16",
     bias = torch.log(torch.expm1(dt0))
     raw = _normal((batch, seqlen, nheads), seed, "dt", 0.1).double() + bias
     dt = torch.nn.functional.softplus(raw)  # the recipe's positive step, fp64
-    r = torch.rand(nheads, generator=_gen(seed, "A"), dtype=torch.float64)
+    r = torch.rand(nheads, generator=_gen(seed, "A"), dtype=torch.float64, device=_DEVICE)
     A_head = -torch.exp(r * math.log(16.0))
     return {
         "x": _normal((batch, seqlen, nheads, headdim), seed, "x").to(td),

@@ -1,0 +1,88 @@
+"""Shared helpers of the GPU parity tests: the tolerances and the comparison
+against the fp64 oracle.
+
+Tolerances (the stated bar for this scan): fp32 inputs -> max |err| <=
+1e-4 * max |ref|; bf16 inputs -> relative L2 error <= 3e-3, against the
+oracle run on the same bf16-rounded inputs (fp32 state and accumulation on
+the GPU).
+"""
+import numpy as np
+import torch
+
+import oracle
+
+TOL_F32_MAXABS = 1e-4
+TOL_BF16_RELL2 = 3e-3
+
+
+def to_np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def check_close(got, want, dtype, what=""):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    scale = np.abs(want).max()
+    if dtype == torch.float32:
+        err = np.abs(got - want).max()
+        assert err <= TOL_F32_MAXABS * max(scale, 1e-30), \
+            f"{what}: max|err| {err:.3e} > 1e-4 * max|ref| ({scale:.3e})"
+        return err / max(scale, 1e-30)
+    num = np.linalg.norm((got - want).ravel())
+    den = np.linalg.norm(want.ravel())
+    rel = num / max(den, 1e-30)
+    assert rel <= TOL_BF16_RELL2, f"{what}: rel L2 {rel:.3e} > 3e-3"
+    return rel
+
+
+def cuda_inputs(d, device):
+    return {k: (None if v is None else v.to(device)) for k, v in d.items()}
+
+
+def oracle_selective(inp, softplus=True, nthreads=8):
+    return oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["z"], inp["delta_bias"], softplus=softplus, nthreads=nthreads)
+
+
+def oracle_selective_channels(inp, chans, softplus=True, nthreads=8):
+    """Oracle on a subset of (b, d) channels: each channel only needs its own
+    row of u / delta / z, its row of A, D, bias and its batch row's B, C."""
+    Dch = inp["u"].shape[1]
+    ys, ss = [], []
+    for c in chans:
+        b, d = divmod(int(c), Dch)
+        sub = {
+            "u": inp["u"][b:b + 1, d:d + 1], "delta": inp["delta"][b:b + 1, d:d + 1],
+            "z": None if inp["z"] is None else inp["z"][b:b + 1, d:d + 1],
+            "A": inp["A"][d:d + 1], "B": inp["B"][b:b + 1], "C": inp["C"][b:b + 1],
+            "D": None if inp["D"] is None else inp["D"][d:d + 1],
+            "delta_bias": None if inp["delta_bias"] is None else inp["delta_bias"][d:d + 1],
+        }
+        y, s = oracle_selective(sub, softplus, nthreads=1)
+        ys.append(y[0, 0])
+        ss.append(s[0, 0])
+    return np.stack(ys), np.stack(ss)
+
+
+def oracle_ssd(inp, nthreads=8):
+    return oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"],
+                      nthreads=nthreads)
+
+
+def oracle_ssd_units(inp, units, nthreads=8):
+    """Oracle on a subset of (b, h) units."""
+    H = inp["x"].shape[2]
+    G = inp["B"].shape[2]
+    ys, ss = [], []
+    for un in units:
+        b, h = divmod(int(un), H)
+        g = h // (H // G)
+        y, s = oracle.ssd(inp["x"][b:b + 1, :, h:h + 1], inp["dt"][b:b + 1, :, h:h + 1],
+                          inp["A_head"][h:h + 1], inp["B"][b:b + 1, :, g:g + 1],
+                          inp["C"][b:b + 1, :, g:g + 1],
+                          None if inp["D"] is None else inp["D"][h:h + 1], nthreads=1)
+        ys.append(y[0, :, 0])
+        ss.append(s[0, 0])
+    return np.stack(ys), np.stack(ss)

@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/ssscan.h declares, and rejects bad arguments before touching a GPU.
+No compute call is made here (this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_146_b300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssscan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        from selective_state_space_146_b300.csrc import build
+        build.build()
+    return _abi.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert "ss_selective_scan_fwd" in names and "ss_ssd_chunk_scan_fwd" in names
+    assert set(names) == set(_abi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(0, -10, -1):
+        s = _abi.status_string(code)
+        assert s and s != "unknown status"
+    assert _abi.status_string(-99) == "unknown status"
+    assert lib.ss_version() >= 100
+
+
+class FakeT:
+    """Shape/stride/dtype description with a fake, aligned device address."""
+
+    addr = 0x10000
+
+    def __init__(self, shape, dtype=_abi.SS_BF16, stride=None, data=None):
+        self.s = _abi.SSTensor()
+        FakeT.addr += 0x100000
+        self.s.data = FakeT.addr if data is None else data
+        self.s.dtype = dtype
+        self.s.ndim = len(shape)
+        st = stride or [int(__import__("numpy").prod(shape[i + 1:])) for i in range(len(shape))]
+        for i, (n, k) in enumerate(zip(shape, st)):
+            self.s.shape[i] = n
+            self.s.stride[i] = k
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.s)
+
+
+def _sel_args(Bsz=2, D=8, N=16, L=64, dt=_abi.SS_BF16):
+    u = FakeT((Bsz, D, L), dt)
+    return dict(u=u, delta=FakeT((Bsz, D, L), dt), A=FakeT((D, N), _abi.SS_F32),
+                B=FakeT((Bsz, N, L), dt), C=FakeT((Bsz, N, L), dt), D=FakeT((D,), _abi.SS_F32),
+                z=FakeT((Bsz, D, L), dt), bias=FakeT((D,), _abi.SS_F32), y=FakeT((Bsz, D, L), dt),
+                last=FakeT((Bsz, D, N), _abi.SS_F32))
+
+
+def _call_sel(lib, a, softplus=1, drop=()):
+    r = {k: (None if k in drop else v.ref) for k, v in a.items()}
+    return lib.ss_selective_scan_fwd(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"], r["z"],
+                                     r["bias"], softplus, r["y"], r["last"], None)
+
+
+def test_selective_argument_errors(lib):
+    a = _sel_args()
+    assert _call_sel(lib, a, drop=("u",)) == -1
+    assert _call_sel(lib, a, drop=("y",)) == -1
+    assert _call_sel(lib, a, softplus=2) == -1
+    b = _sel_args()
+    b["delta"] = FakeT((2, 8, 63))
+    assert _call_sel(lib, b) == -2
+    b = _sel_args()
+    b["B"] = FakeT((2, 15, 64))
+    assert _call_sel(lib, b) == -2
+    b = _sel_args()
+    b["last"] = FakeT((2, 8, 8), _abi.SS_F32)
+    assert _call_sel(lib, b) == -2
+    b = _sel_args()
+    b["z"] = FakeT((2, 8, 64), _abi.SS_F32)
+    assert _call_sel(lib, b) == -3
+    b = _sel_args()
+    b["A"] = FakeT((8, 16), _abi.SS_BF16)
+    assert _call_sel(lib, b) == -3
+    b = _sel_args()
+    b["u"] = FakeT((2, 8, 64), 7)
+    assert _call_sel(lib, b) == -3
+    b = _sel_args()
+    b["u"] = FakeT((2, 8, 64), data=0x10001)  # odd address for a 2-byte element
+    assert _call_sel(lib, b) == -4
+    b = _sel_args(N=300)
+    assert _call_sel(lib, b) == -5
+    b = _sel_args()
+    b["u"] = FakeT((2, 8, 64), stride=[512, 64, -1])
+    assert _call_sel(lib, b) == -2
+
+
+def test_selective_zero_size_is_a_no_op(lib):
+    for shp in ((0, 8, 64), (2, 0, 64)):
+        Bsz, D, L = shp
+        a = _sel_args(Bsz, D, 16, L)
+        assert _call_sel(lib, a) == 0
+    a = _sel_args(2, 8, 16, 0)
+    assert _call_sel(lib, a, drop=("last",)) == 0
+
+
+def _ssd_args(Bsz=2, L=64, H=4, P=8, G=1, N=16, dt=_abi.SS_BF16):
+    return dict(x=FakeT((Bsz, L, H, P), dt), dt=FakeT((Bsz, L, H), dt),
+                A=FakeT((H,), _abi.SS_F32), B=FakeT((Bsz, L, G, N), dt),
+                C=FakeT((Bsz, L, G, N), dt), D=FakeT((H,), _abi.SS_F32),
+                y=FakeT((Bsz, L, H, P), dt), last=FakeT((Bsz, H, P, N), _abi.SS_F32))
+
+
+def _call_ssd(lib, a, chunk=64, drop=()):
+    r = {k: (None if k in drop else v.ref) for k, v in a.items()}
+    return lib.ss_ssd_chunk_scan_fwd(r["x"], r["dt"], r["A"], r["B"], r["C"], r["D"], chunk,
+                                     r["y"], r["last"], None)
+
+
+def test_ssd_argument_errors(lib):
+    assert _call_ssd(lib, _ssd_args(), chunk=100) == -1
+    assert _call_ssd(lib, _ssd_args(), drop=("x",)) == -1
+    a = _ssd_args(H=4, G=3)
+    assert _call_ssd(lib, a) == -2
+    a = _ssd_args()
+    a["dt"] = FakeT((2, 64, 5))
+    assert _call_ssd(lib, a) == -2
+    a = _ssd_args()
+    a["B"] = FakeT((2, 64, 1, 16), _abi.SS_F32)
+    assert _call_ssd(lib, a) == -3
+    a = _ssd_args(N=512)
+    assert _call_ssd(lib, a) == -5
+    a = _ssd_args(Bsz=0)
+    assert _call_ssd(lib, a) == 0
