@@ -143,7 +143,8 @@ struct FastCfg {
     static constexpr int SMEM_BYTES = STAGE_BYTES * STAGES + 256 /*barriers*/ + 1024 /*align*/;
     static_assert(TILE_BYTES % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-    static_assert(NS % 4 == 0, "states per thread must be a multiple of 4");
+    static_assert(NS % 2 == 0, "states per lane come in pairs");
+    static_assert(VEC % NSPLIT == 0, "each lane owns whole steps of a chunk");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -157,38 +158,38 @@ __device__ __forceinline__ float gate_sigmoid(float z) {
 }
 
 // Conversion of one tile's raw B / C ([n][t] as loaded by TMA) into the fp32
-// table bc[t][32]: 16-byte chunk 2q holds B[4q..4q+3], chunk 2q+1 holds
-// C[4q..4q+3].  A lane group that owns states [4j, 4j+4m) reads m chunk pairs
-// that sit next to each other, at offsets known at compile time.  Lane l
-// writes rows 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by
-// lane so that the lanes of one store hit distinct banks.
+// table bc[t][32]: 16-byte chunk j holds (B[2j], B[2j+1], C[2j], C[2j+1]), so
+// a lane keeping the state pairs [j0, j0 + m) reads m consecutive chunks, one
+// ld.shared.v4 per pair, at offsets known at compile time.  Lane l writes rows
+// 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by lane so the
+// lanes of one store hit distinct banks.  Without C (summary pass) the C slots
+// hold zeros.
 template <typename T, bool WITH_C>
 __device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
-        const int q = (it + lane) & 7;
-        const bool isC = q & 1;
-        if (!WITH_C && isC) continue;
-        const uint32_t src = isC ? rawC : rawB;
-        const int n0 = (q >> 1) * 4;
+        const int j = (it + lane) & 7;
+        const uint32_t rb = rawB + (2 * j) * 128, rc = rawC + (2 * j) * 128;
         if constexpr (sizeof(T) == 2) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = lds32(src + ((n0 + i) * 32 + lane) * 4);  // (t, t+1)
-            const float4 lo = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[1] << 16),
-                                          __uint_as_float(w[2] << 16), __uint_as_float(w[3] << 16));
-            const float4 hi = make_float4(
-                __uint_as_float(w[0] & 0xffff0000u), __uint_as_float(w[1] & 0xffff0000u),
-                __uint_as_float(w[2] & 0xffff0000u), __uint_as_float(w[3] & 0xffff0000u));
-            sts128f(bc + (2 * lane) * 128 + q * 16, lo);
-            sts128f(bc + (2 * lane + 1) * 128 + q * 16, hi);
+            // word `lane` of a 128-byte row holds the bf16 pair (t = 2 lane, 2 lane + 1)
+            const uint32_t b0 = lds32(rb + lane * 4), b1 = lds32(rb + 128 + lane * 4);
+            const uint32_t c0 = WITH_C ? lds32(rc + lane * 4) : 0u;
+            const uint32_t c1 = WITH_C ? lds32(rc + 128 + lane * 4) : 0u;
+            const float4 lo = make_float4(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16),
+                                          __uint_as_float(c0 << 16), __uint_as_float(c1 << 16));
+            const float4 hi = make_float4(__uint_as_float(b0 & 0xffff0000u),
+                                          __uint_as_float(b1 & 0xffff0000u),
+                                          __uint_as_float(c0 & 0xffff0000u),
+                                          __uint_as_float(c1 & 0xffff0000u));
+            sts128f(bc + (2 * lane) * 128 + j * 16, lo);
+            sts128f(bc + (2 * lane + 1) * 128 + j * 16, hi);
         } else {
             float4 v;
-            v.x = __uint_as_float(lds32(src + ((n0 + 0) * 32 + lane) * 4));
-            v.y = __uint_as_float(lds32(src + ((n0 + 1) * 32 + lane) * 4));
-            v.z = __uint_as_float(lds32(src + ((n0 + 2) * 32 + lane) * 4));
-            v.w = __uint_as_float(lds32(src + ((n0 + 3) * 32 + lane) * 4));
-            sts128f(bc + lane * 128 + q * 16, v);
+            v.x = __uint_as_float(lds32(rb + lane * 4));
+            v.y = __uint_as_float(lds32(rb + 128 + lane * 4));
+            v.z = WITH_C ? __uint_as_float(lds32(rc + lane * 4)) : 0.f;
+            v.w = WITH_C ? __uint_as_float(lds32(rc + 128 + lane * 4)) : 0.f;
+            sts128f(bc + lane * 128 + j * 16, v);
         }
     }
 }
@@ -205,8 +206,11 @@ __device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
     } else if constexpr (BYTES == 8) {
         const uint2 v = lds64(a);
         w[0] = v.x; w[1] = v.y;
-    } else {
+    } else if constexpr (BYTES == 4) {
         w[0] = lds32(a);
+    } else {
+        out[0] = __uint_as_float(lds16(a) << 16);  // one bf16
+        return;
     }
     if constexpr (sizeof(T) == 2) {
 #pragma unroll
@@ -225,6 +229,10 @@ __device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
 template <typename T, int K>
 __device__ __forceinline__ void stg_elems(T* p, const float* v, int limit) {
     constexpr int BYTES = K * (int)sizeof(T);
+    if constexpr (BYTES == 2) {
+        if (limit >= 1) p[0] = Elem<T>::from_f(v[0]);
+        return;
+    }
     if (limit >= K) {
         uint32_t w[4];
         if constexpr (sizeof(T) == 2) {
@@ -380,18 +388,21 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     }
 
     float dsum = 0.f;  // sum of delta over the segment (summary pass)
-
-    // One 16-byte chunk (VEC steps) of this lane's channel.
     T* yrow = static_cast<T*>(p.y) + (int64_t)b * p.sy_b + (int64_t)(valid ? d : 0) * p.sy_d;
-    auto chunk = [&](uint32_t su, uint32_t bcp, int tile_t0, int c, int tcount, auto tail) {
+
+    // The three parts of one 16-byte chunk (VEC steps) of this lane's channel:
+    //   prep:   delta of the own K-slot (softplus), all-gathered in the group,
+    //           and u of the whole chunk;
+    //   core:   the recurrence over the chunk's steps (partial readouts);
+    //   finish: reduce-scatter of the readouts, skip and gate, store of y.
+    // Tiles are processed as prep(c+1) | core(c) | finish(c-1) so the three
+    // independent streams interleave.
+    auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* uf, auto tail) {
         constexpr bool TAIL = decltype(tail)::value;
         const int off = swz(ci, c);
-        const int own = off + part * K * ES;  // this lane's K-slot of the chunk
-        float uf[VEC];
         lds_elems<T, VEC>(su + off, uf);
-        // delta for the own slot, then all-gathered across the group
         float dv[K];
-        lds_elems<T, K>(su + Cfg::OFF_DL + own, dv);
+        lds_elems<T, K>(su + Cfg::OFF_DL + off + part * K * ES, dv);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             float x = dv[k] + biasd;
@@ -399,12 +410,11 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
             if (TAIL && c * VEC + part * K + k >= tcount) x = 0.f;  // past the end: no update
             dv[k] = x;
         }
-        float dd[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
             dd[j] = NSPLIT == 1 ? dv[j % K] : __shfl_sync(0xffffffffu, dv[j % K], gbase + j / K);
-
-        float yv[VEC];
+    };
+    auto core = [&](uint32_t bcp, int c, const float* dd, const float* uf, float* yv) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
             if (SUMMARY) dsum += dd[i];
@@ -412,39 +422,39 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
             const float du = dd[i] * uf[i];
             const float2 du2 = make_float2(du, du);
             const uint32_t row = bcp + (c * VEC + i) * 128;
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-                const float4 bq = lds128f(row + q * 32);
-                const float2 ar0 = __fmul2_rn(d2, A2[2 * q]);
-                const float2 ar1 = __fmul2_rn(d2, A2[2 * q + 1]);
-                const float2 a0 = make_float2(ex2_approx(ar0.x), ex2_approx(ar0.y));
-                const float2 a1 = make_float2(ex2_approx(ar1.x), ex2_approx(ar1.y));
-                h2[2 * q] = __ffma2_rn(a0, h2[2 * q], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
-                h2[2 * q + 1] =
-                    __ffma2_rn(a1, h2[2 * q + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
-                if constexpr (!SUMMARY) {
-                    const float4 cq = lds128f(row + q * 32 + 16);
-                    acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h2[2 * q], acc0);
-                    acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h2[2 * q + 1], acc1);
-                }
+            for (int j = 0; j < NS / 2; ++j) {
+                const float4 bc = lds128f(row + j * 16);  // B pair, C pair
+                const float2 ar = __fmul2_rn(d2, A2[j]);
+                const float2 a = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                h2[j] = __ffma2_rn(a, h2[j], __fmul2_rn(du2, make_float2(bc.x, bc.y)));
+                if constexpr (!SUMMARY) acc = __ffma2_rn(make_float2(bc.z, bc.w), h2[j], acc);
             }
-            yv[i] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            yv[i] = acc.x + acc.y;
         }
+    };
+    auto finish = [&](uint32_t su, int tile_t0, int c, const float* yv, auto tail) {
+        constexpr bool TAIL = decltype(tail)::value;
         if constexpr (!SUMMARY) {
-            // reduce-scatter the partial readouts: lane `part` ends with the
-            // full sum for its own K steps
+            // reduce-scatter: lane `part` ends with the full sums of its K steps
             float yo[K];
             if constexpr (NSPLIT == 1) {
 #pragma unroll
                 for (int k = 0; k < K; ++k) yo[k] = yv[k];
             } else if constexpr (NSPLIT == 2) {
                 reduce_half<VEC>(yv, yo, part & 1, 1);
-            } else {
+            } else if constexpr (NSPLIT == 4) {
                 float w[VEC / 2];
                 reduce_half<VEC>(yv, w, (part >> 1) & 1, 2);
                 reduce_half<VEC / 2>(w, yo, part & 1, 1);
+            } else {
+                float w[VEC / 2], x[VEC / 4];
+                reduce_half<VEC>(yv, w, (part >> 2) & 1, 4);
+                reduce_half<VEC / 2>(w, x, (part >> 1) & 1, 2);
+                reduce_half<VEC / 4>(x, yo, part & 1, 1);
             }
+            const int own = swz(ci, c) + part * K * ES;
             float uo[K];
             [[maybe_unused]] float zo[K];
             lds_elems<T, K>(su + own, uo);
@@ -461,6 +471,40 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
             }
         }
     };
+    // A full tile: 8 chunks, software-pipelined so that every trip holds
+    // core(c) | prep(c+1) | finish(c-1) in one branch-free block.
+    auto full_tile = [&](uint32_t su, int tile_t0) {
+        static_assert(Cfg::CHUNKS == 8, "pipeline below assumes 8 chunks per tile");
+        const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
+        float ddA[VEC], ufA[VEC], ddB[VEC], ufB[VEC], yA[VEC], yB[VEC];
+        prep(su, 0, TT, ddA, ufA, std::false_type{});
+        core(bcp, 0, ddA, ufA, yA);
+        prep(su, 1, TT, ddB, ufB, std::false_type{});
+#pragma unroll 1
+        for (int c = 1; c < 7; c += 2) {
+            core(bcp, c, ddB, ufB, yB);
+            prep(su, c + 1, TT, ddA, ufA, std::false_type{});
+            finish(su, tile_t0, c - 1, yA, std::false_type{});
+            core(bcp, c + 1, ddA, ufA, yA);
+            prep(su, c + 2, TT, ddB, ufB, std::false_type{});
+            finish(su, tile_t0, c, yB, std::false_type{});
+        }
+        core(bcp, 7, ddB, ufB, yB);
+        finish(su, tile_t0, 6, yA, std::false_type{});
+        finish(su, tile_t0, 7, yB, std::false_type{});
+    };
+    // The last, partial tile of a sequence: one chunk at a time, with checks.
+    auto tail_tile = [&](uint32_t su, int tile_t0, int tcount) {
+        const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
+        const int nch = (tcount + VEC - 1) / VEC;
+        float dd[VEC], uf[VEC], yv[VEC];
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            prep(su, c, tcount, dd, uf, std::true_type{});
+            core(bcp, c, dd, uf, yv);
+            finish(su, tile_t0, c, yv, std::true_type{});
+        }
+    };
 
     bool ok = true;
     for (int k = 0; k < ntiles; ++k) {
@@ -473,12 +517,8 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
         const int tile_t0 = tbeg + k * TT;
         const int tcount = min(TT, tend - tile_t0);
         const uint32_t su = smem_u32(stage(s));
-        const uint32_t bcp = su + Cfg::OFF_BC + part * NS * 2 * 4;
-        const int full_chunks = tcount / VEC;
-#pragma unroll 1
-        for (int c = 0; c < full_chunks; ++c) chunk(su, bcp, tile_t0, c, tcount, std::false_type{});
-        if (full_chunks < Cfg::CHUNKS && full_chunks * VEC < tcount)
-            chunk(su, bcp, tile_t0, full_chunks, tcount, std::true_type{});
+        if (tcount == TT) full_tile(su, tile_t0);
+        else tail_tile(su, tile_t0, tcount);
         mbar_arrive(&empty[s]);
     }
     if (!ok || !valid) return;
@@ -653,7 +693,8 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
 }
 
 // Path selection for tests: SS_SCAN_PATH=general forces the general kernel;
-// split1 / split2 / split4 force the fast kernel with 1, 2 or 4 lanes per channel.
+// split1 / split2 / split4 / split8 force the fast kernel with 1, 2, 4 or 8
+// lanes per channel (8 only for bf16; fp32 chunks hold 4 steps).
 static int forced_path() {
     const char* s = getenv("SS_SCAN_PATH");
     if (!s) return -1;
@@ -661,6 +702,7 @@ static int forced_path() {
     if (!strcmp(s, "split1")) return 1;
     if (!strcmp(s, "split2")) return 2;
     if (!strcmp(s, "split4")) return 4;
+    if (!strcmp(s, "split8")) return 8;
     return -1;
 }
 
@@ -668,15 +710,20 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
     const int force = forced_path();
     const bool bf = a.dtype == SS_BF16;
     if (force != 0 && a.L > 0 && fast_layout_ok(a)) {
-        // the fewest lanes per channel that still give every SM 8 consumer warps
+        // The fewest lanes per channel (at most 4) that give every SM 16
+        // consumer warps.  Eight lanes per channel gives more warps but costs
+        // more instructions per step than it recovers in latency (measured on
+        // the Mamba-130M and -2.8B layer shapes); it stays available for tests.
         const int sms = sm_count_current();
-        const int64_t ch = (int64_t)a.Bsz * a.D, want = (int64_t)sms * 256;
-        int split = ch >= want ? 1 : (2 * ch >= want ? 2 : 4);
-        if (force == 1 || force == 2 || force == 4) split = force;
+        const int64_t ch = (int64_t)a.Bsz * a.D, want = (int64_t)sms * 512;
+        int split = 1;
+        while (split < 4 && ch * split < want) split *= 2;
+        if (force == 1 || force == 2 || force == 4 || (force == 8 && bf)) split = force;
         if (bf) {
             if (split == 1) return run_fast<__nv_bfloat16, 1, 2>(a, st, scratch);
             if (split == 2) return run_fast<__nv_bfloat16, 2, 2>(a, st, scratch);
-            return run_fast<__nv_bfloat16, 4, 4>(a, st, scratch);
+            if (split == 4) return run_fast<__nv_bfloat16, 4, 4>(a, st, scratch);
+            return run_fast<__nv_bfloat16, 8, 8>(a, st, scratch);
         }
         if (split == 1) return run_fast<float, 1, 2>(a, st, scratch);
         if (split == 2) return run_fast<float, 2, 2>(a, st, scratch);

@@ -43,7 +43,7 @@ def _run(inp, dev, softplus=True, want_state=True):
     return out
 
 
-@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4"],
+@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4", "split8"],
                          indirect=True)
 def test_tiny_f32_workload(cuda_device, scan_path):
     cfg = inputs.WORKLOADS["tiny_f32"]
@@ -72,7 +72,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])))
-@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4"],
+@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4", "split8"],
                          indirect=True)
 def test_small_shapes(cuda_device, scan_path, case):
     Bsz, D, N, L, dt, gate, skip, bias, softplus = case
@@ -90,7 +90,7 @@ def test_small_shapes(cuda_device, scan_path, case):
 def test_paths_agree_with_each_other(cuda_device, scan_path):
     inp = inputs.selective_inputs(2, 48, 16, 520, "bf16", seed=3)
     outs = []
-    for path in ("general", "split1", "split2", "split4"):
+    for path in ("general", "split1", "split2", "split4", "split8"):
         os.environ["SS_SCAN_PATH"] = path
         outs.append([to_np(t) for t in _run(inp, cuda_device)])
     os.environ.pop("SS_SCAN_PATH", None)
