@@ -91,6 +91,35 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
                           ss_tensor* y, ss_tensor* last_state, void* stream);
 
 /*
+ * Allocation-free selective scan.  The pages have no counterpart to this
+ * call: it is a deployment variant of ss_selective_scan_fwd for callers that
+ * cannot allocate device memory while a call runs -- code whose allocator is
+ * owned by another runtime or arena, loops that must not enter the CUDA
+ * allocator (its locks and its implicit synchronisation), or processes that
+ * have handed all free device memory to a pool.
+ *
+ * Same arguments, checks, results and status codes as ss_selective_scan_fwd,
+ * except where the segment summaries live: instead of stream-ordered memory
+ * they use one fixed 4 MiB array in device memory, defined in the library and
+ * held by every GPU that loads it until the process exits.  The call makes no
+ * cudaMalloc / cudaMallocAsync / cudaFree and no allocating library call.
+ *   - A problem whose summaries need more than 4 MiB is rejected with
+ *     SS_ERR_UNSUPPORTED before anything is launched.  (With the built-in
+ *     tiling on a 148-SM B300 the summaries stay under about 2.5 MiB.)
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; the summary pass writes every entry the main pass reads, so
+ *     nothing needs clearing.  Calls whose kernels overlap on the GPU (other
+ *     streams, other threads) race on the array: serialise them.
+ */
+int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                                  const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                                  const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                                  ss_tensor* y, ss_tensor* last_state, void* stream);
+
+/*
  * Mamba-2 SSD scan, forward, chunked.
  *
  * Defines (page "Mamba模型笔记" §5, SSD; state-spaces/mamba README §4.3,

@@ -20,7 +20,8 @@ SS_F32, SS_BF16 = 0, 1
 STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_DTYPE",
           -4: "SS_ERR_ALIGNMENT", -5: "SS_ERR_UNSUPPORTED", -6: "SS_ERR_ALLOC",
           -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
-EXPORTS = ("ss_selective_scan_fwd", "ss_ssd_chunk_scan_fwd", "ss_status_string",
+EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chunk_scan_fwd",
+           "ss_status_string",
            "ss_get_device_error", "ss_launch_count", "ss_version")
 
 
@@ -52,6 +53,8 @@ def load(path: str | None = None):
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.ss_selective_scan_fwd.argtypes = [T, T, T, T, T, T, T, T, i, T, T, vp]
     lib.ss_selective_scan_fwd.restype = i
+    lib.ss_selective_scan_fwd_noalloc.argtypes = [T, T, T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_selective_scan_fwd_noalloc.restype = i
     lib.ss_ssd_chunk_scan_fwd.argtypes = [T, T, T, T, T, T, i, T, T, vp]
     lib.ss_ssd_chunk_scan_fwd.restype = i
     lib.ss_status_string.argtypes = [i]
@@ -117,6 +120,24 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
     if rc != 0:
         raise SSError(rc, "ss_selective_scan_fwd")
     return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def selective_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                               y=None, last_state=None, stream=None):
+    """ss_selective_scan_fwd_noalloc: the selective scan for callers that
+    cannot allocate device memory during a call.  The library allocates
+    nothing; the caller passes every input and output, here y and (optionally)
+    last_state already allocated.  See include/ssscan.h for the fixed 4 MiB
+    scratch array it uses and for the rule that overlapping calls race."""
+    if y is None:
+        raise ValueError("selective_scan_fwd_noalloc needs a caller-allocated y")
+    ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    ys, ls = describe(y), describe(last_state)
+    rc = load().ss_selective_scan_fwd_noalloc(*[_ref(t) for t in ts], int(bool(softplus)),
+                                              _ref(ys), _ref(ls), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_fwd_noalloc")
+    return (y, last_state) if last_state is not None else y
 
 
 def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_state=None,

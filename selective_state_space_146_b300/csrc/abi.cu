@@ -115,6 +115,115 @@ static bool same_shape(const ss_tensor* a, const ss_tensor* b) {
         if (_rc != SS_OK) return _rc; \
     } while (0)
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for ss_selective_scan_fwd_noalloc.
+//
+// The segment summaries of the selective scan come from this array instead of
+// cudaMallocAsync.  It is a file-scope device array, so every GPU that loads
+// the library holds it until the process exits.  In host code its name is
+// only a stand-in: the device address is taken once per device with
+// cudaGetSymbolAddress (first call on that device, with the device current)
+// and passed to the kernels as a plain pointer.
+constexpr size_t kFixedScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+static void* g_fixed_scratch_ptr[kMaxDevices];
+
+static void* fixed_scratch_address() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_fixed_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fixed_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_fixed_scratch_ptr[dev] = p;
+    }
+    return g_fixed_scratch_ptr[dev];
+}
+
+struct FixedScratch {
+    void* base;
+    bool too_large;  // a request exceeded kFixedScratchBytes
+};
+
+static void* fixed_scratch_alloc(size_t bytes, cudaStream_t, void* ctx) {
+    auto* fs = static_cast<FixedScratch*>(ctx);
+    if (bytes > kFixedScratchBytes) {
+        fs->too_large = true;
+        return nullptr;
+    }
+    return fs->base;
+}
+
+static void fixed_scratch_release(void*, cudaStream_t, void*) {}
+
+// Argument checks and ScanArgs assembly of the allocation-free entry point
+// (the same checks, in the same order, as ss_selective_scan_fwd).  Sets
+// *nothing_to_do for inputs with no work.
+static int noalloc_selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                                  const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                                  const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                                  ss_tensor* y, ss_tensor* last_state, ScanArgs* out,
+                                  bool* nothing_to_do) {
+    *nothing_to_do = false;
+    SS_TRY(check_tensor(u, 3));
+    SS_TRY(check_tensor(delta, 3));
+    SS_TRY(check_tensor(A, 2));
+    SS_TRY(check_tensor(B, 3));
+    SS_TRY(check_tensor(C, 3));
+    SS_TRY(check_tensor(y, 3));
+    if (D) SS_TRY(check_tensor(D, 1));
+    if (z) SS_TRY(check_tensor(z, 3));
+    if (delta_bias) SS_TRY(check_tensor(delta_bias, 1));
+    if (last_state) SS_TRY(check_tensor(last_state, 3));
+    if (softplus != 0 && softplus != 1) return SS_ERR_INVALID_ARG;
+    const int dt = u->dtype;
+    if (delta->dtype != dt || B->dtype != dt || C->dtype != dt || y->dtype != dt ||
+        (z && z->dtype != dt))
+        return SS_ERR_DTYPE;
+    if (A->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
+        (delta_bias && delta_bias->dtype != SS_F32) || (last_state && last_state->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+    const int64_t Bsz = u->shape[0], Dch = u->shape[1], L = u->shape[2], N = A->shape[1];
+    if (!same_shape(delta, u) || !same_shape(y, u) || (z && !same_shape(z, u)))
+        return SS_ERR_SHAPE;
+    if (A->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (B->shape[0] != Bsz || B->shape[1] != N || B->shape[2] != L) return SS_ERR_SHAPE;
+    if (!same_shape(C, B)) return SS_ERR_SHAPE;
+    if (D && D->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (delta_bias && delta_bias->shape[0] != Dch) return SS_ERR_SHAPE;
+    if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != Dch ||
+                       last_state->shape[2] != N))
+        return SS_ERR_SHAPE;
+    if (N < 1) return SS_ERR_SHAPE;
+    if (N > 256) return SS_ERR_UNSUPPORTED;
+    if (Bsz * Dch >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
+    if (Bsz == 0 || Dch == 0 || (L == 0 && !last_state)) {
+        *nothing_to_do = true;
+        return SS_OK;
+    }
+    ScanArgs a{};
+    a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = dt;
+    a.u = u->data; a.su_b = u->stride[0]; a.su_d = u->stride[1]; a.su_t = u->stride[2];
+    a.dl = delta->data; a.sdl_b = delta->stride[0]; a.sdl_d = delta->stride[1]; a.sdl_t = delta->stride[2];
+    if (z) { a.z = z->data; a.sz_b = z->stride[0]; a.sz_d = z->stride[1]; a.sz_t = z->stride[2]; }
+    a.y = y->data; a.sy_b = y->stride[0]; a.sy_d = y->stride[1]; a.sy_t = y->stride[2];
+    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_n = B->stride[1]; a.sB_t = B->stride[2];
+    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_n = C->stride[1]; a.sC_t = C->stride[2];
+    a.A = static_cast<const float*>(A->data); a.sA_d = A->stride[0]; a.sA_n = A->stride[1];
+    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
+    if (delta_bias) { a.bias = static_cast<const float*>(delta_bias->data); a.sbias = delta_bias->stride[0]; }
+    if (last_state) {
+        a.last = static_cast<float*>(last_state->data);
+        a.sl_b = last_state->stride[0]; a.sl_d = last_state->stride[1]; a.sl_n = last_state->stride[2];
+    }
+    a.softplus = softplus;
+    *out = a;
+    return SS_OK;
+}
+
 }  // namespace ss
 
 using namespace ss;
@@ -182,6 +291,26 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                                  const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                                  const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                                  ss_tensor* y, ss_tensor* last_state, void* stream) {
+    ScanArgs a{};
+    bool nothing = false;
+    SS_TRY(noalloc_selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                                  &a, &nothing));
+    if (nothing) return SS_OK;
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    FixedScratch fs{fixed_scratch_address(), false};
+    if (!fs.base) return SS_ERR_CUDA;
+    Scratch sc{fixed_scratch_alloc, fixed_scratch_release, &fs};
+    const int rc = launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+    // the summaries would not fit the fixed buffer: nothing was launched
+    if (rc == SS_ERR_ALLOC && fs.too_large) return SS_ERR_UNSUPPORTED;
+    return rc;
 }
 
 int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
