@@ -1,15 +1,433 @@
 // ssd_tc.cu -- chunked Mamba-2 SSD scan on the tcgen05 tensor cores.
+//
+// What is computed (page "Mamba模型笔记" §5, the SSM / attention duality;
+// state-spaces/mamba README §4.3): per batch row b and head h, steps are
+// taken in blocks of QB = 128.  With cum_t = sum_{r <= t} dt_r A_h inside the
+// block (log2 units below), S the state entering the block and w_t =
+// exp(cum_last - cum_t) dt_t:
+//
+//   CB     = C B^T                                   (QB x QB, K = N)
+//   M_ij   = CB_ij exp(cum_i - cum_j) dt_j  (j <= i), 0 above the diagonal
+//   y      = M X  +  diag(exp(cum)) C S^T  +  D_h x   (the dual form inside the
+//                                                     block, the carried state
+//                                                     for everything before it)
+//   S     <- exp(cum_last) S + (diag(w) X)^T B        (state passed on)
+//
+// The dual form of a longer chunk splits into these 128-step diagonal blocks
+// plus low-rank off-diagonal blocks, and the off-diagonal part is exactly the
+// state term above, so every chunk length that is a multiple of 128 gives the
+// same result; the blocks are always 128 steps here.
+//
+// One CTA (4 warps) per (b, h), blocks in sequence.  Thread 0 issues the TMA
+// loads (x, B, C tiles with 128-byte swizzle; dt) and the MMAs
+// (tcgen05.mma kind::f16, bf16 operands from shared memory, fp32
+// accumulators in tensor memory, M = 128):
+//   CB   = C . B^T      A = C  (K-major)   B = B  (K-major)      TMEM [0, 128)
+//   Yoff = C . S^T      A = C  (K-major)   B = S  (MN-major)     TMEM [192, 256)
+//   Ydg  = M . X        A = M  (K-major)   B = X  (MN-major)     TMEM [128, 192)
+//   dS^T = B^T . X~     A = B  (MN-major)  B = X~ (MN-major)     TMEM [0, 64)
+// Thread t owns row t of every accumulator (TMEM lane t): it builds row t of
+// M, finishes row t of y, scales row t of x into X~, and keeps row n = t of
+// the fp32 state S^T in registers (a bf16 copy in shared memory feeds the
+// next block's Yoff).
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "internal.h"
+#include "ptx.cuh"
 #include "ssscan.h"
+#include "tc.cuh"
 
 namespace ss {
 
+namespace ssdtc {
+
+constexpr int QB = 128;  // steps per block
+constexpr int P = 64;    // head dimension
+constexpr int N = 128;   // state size
+constexpr int NTHREADS = 128;
+
+// shared-memory layout (bytes from a 1024-aligned base)
+constexpr int OFF_X = 0;                 // [128 t][64 p] bf16, swizzled   16 KB
+constexpr int OFF_B = OFF_X + 16384;     // 2 x [128 t][64 n]               32 KB
+constexpr int OFF_C = OFF_B + 32768;     // 2 x [128 t][64 n], later M      32 KB
+constexpr int OFF_S = OFF_C + 32768;     // [128 n][64 p] bf16 state copy   16 KB
+constexpr int OFF_DT = OFF_S + 16384;    // [128 t][8 h] bf16                2 KB
+constexpr int OFF_CUM = OFF_DT + 2048;   // cum (log2 units) [128] f32
+constexpr int OFF_DTF = OFF_CUM + 512;   // dt [128] f32
+constexpr int OFF_WS = OFF_DTF + 512;    // warp partial sums [4] f32
+constexpr int OFF_BAR = OFF_WS + 64;     // mbarriers + TMEM address
+constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
+constexpr uint32_t TMEM_COLS = 256;
+
+struct Params {
+    int Bsz, L, H, G;
+    const float* A; int64_t sA;
+    const float* Dv; int64_t sD;
+    __nv_bfloat16* y; int64_t sy_b, sy_l, sy_h;
+    float* last; int64_t sl_b, sl_h, sl_p, sl_n;
+    unsigned* err;
+};
+
+__device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 2)
+ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+             const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_dt,
+             const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_mma = bar_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+    float* cum = reinterpret_cast<float*>(sm + OFF_CUM);
+    float* dtf = reinterpret_cast<float*>(sm + OFF_DTF);
+    float* wsum = reinterpret_cast<float*>(sm + OFF_WS);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int g = h / (p.H / p.G);
+    const float A2 = p.A[h * p.sA] * kLog2e;
+    const float Dh = p.Dv ? p.Dv[h * p.sD] : 0.f;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (tid == 0) {
+        mbar_init(bar_full, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_B);
+        tma_prefetch_desc(&tm_C);
+        tma_prefetch_desc(&tm_dt);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    // zero state: fp32 rows in registers, bf16 copy in shared memory
+    float S[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) S[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+
+    constexpr uint32_t ID_CB = tc::idesc_bf16(QB, QB, false, false);
+    constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, P, false, true);
+    constexpr uint32_t ID_YDG = tc::idesc_bf16(QB, P, false, true);
+    constexpr uint32_t ID_DS = tc::idesc_bf16(N, P, true, true);
+
+    uint32_t mma_phase = 0;
+    bool ok = true;
+    const int nblk = (p.L + QB - 1) / QB;
+    for (int blk = 0; blk < nblk && ok; ++blk) {
+        const int t0 = blk * QB;
+        // ---- loads
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_full, 16384 + 32768 + 32768 + 2048);
+            tma_load_4d(sm + OFF_X, &tm_x, bar_full, 0, h, t0, b);
+            tma_load_4d(sm + OFF_B, &tm_B, bar_full, 0, g, t0, b);
+            tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_full, 64, g, t0, b);
+            tma_load_4d(sm + OFF_C, &tm_C, bar_full, 0, g, t0, b);
+            tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_full, 64, g, t0, b);
+            tma_load_3d(sm + OFF_DT, &tm_dt, bar_full, (h / 8) * 8, t0, b);
+        }
+        // every wait ends in a block-wide agreement so all threads leave together
+        if (!__syncthreads_and(mbar_wait(bar_full, blk & 1, p.err))) { ok = false; break; }
+
+        // ---- issue C B^T and C S^T while the decays are being summed
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t dc = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
+                const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024);
+                const uint64_t ds = tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024);
+                tc::mma_bf16(tmem + 0, dc, db, ID_CB, kk > 0);
+                tc::mma_bf16(tmem + 192, dc, ds, ID_YOFF, kk > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+
+        // ---- cumulative decay (log2 units) over the block
+        {
+            const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + tid * 16 + (h & 7) * 2);
+            const float dtv = __uint_as_float((uint32_t)raw << 16);
+            float v = dtv * A2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane == 31) wsum[warp] = v;
+            __syncthreads();
+            for (int w = 0; w < warp; ++w) v += wsum[w];
+            cum[tid] = v;
+            dtf[tid] = dtv;
+            __syncthreads();
+        }
+        const float cum_t = cum[tid];
+        const float cum_last = cum[QB - 1];
+
+        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
+        ++mma_phase;
+        tc::fence_after_sync();
+
+        // ---- row tid of M = CB o decay o dt (lower triangle), bf16, K-major
+        //      over the C tiles (C is no longer needed)
+#pragma unroll 1
+        for (int jc = 0; jc < 4; ++jc) {
+            const int tile = jc >> 1;
+            uint8_t* mt = sm + OFF_C + tile * 16384;
+            if (jc <= warp) {
+                float v[32];
+                tc::tmem_ld32(trow + jc * 32, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float m2[2];
+#pragma unroll
+                        for (int s = 0; s < 2; ++s) {
+                            const int j = jc * 32 + q * 8 + e * 2 + s;
+                            const float dec = ex2_approx(cum_t - cum[j]);  // j > i: discarded
+                            m2[s] = j <= tid ? v[q * 8 + e * 2 + s] * dec * dtf[j] : 0.f;
+                        }
+                        w4[e] = pack_bf16(m2[0], m2[1]);
+                    }
+                    const int c = ((jc & 1) * 32 + q * 8) >> 3;  // 16-byte chunk within the row
+                    *reinterpret_cast<uint4*>(mt + swz(tid, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = ((jc & 1) * 32 + q * 8) >> 3;
+                    *reinterpret_cast<uint4*>(mt + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+
+        // ---- Ydiag = M X
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t dm = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
+                const uint64_t dx = tc::smem_desc_sw128(sbase + OFF_X + kk * 2048, 16384, 1024);
+                tc::mma_bf16(tmem + 128, dm, dx, ID_YDG, kk > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
+        ++mma_phase;
+        tc::fence_after_sync();
+
+        // ---- y row tid, then X~ row tid in place
+        {
+            float x[P];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 r = *reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c));
+                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[c * 8 + 2 * i] = __uint_as_float(w[i] << 16);
+                    x[c * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+            }
+            const float eoff = ex2_approx(cum_t);
+            const int t = t0 + tid;
+            __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float yd[32], yo[32];
+                tc::tmem_ld32(trow + 128 + half * 32, yd);
+                tc::tmem_ld32(trow + 192 + half * 32, yo);
+                tc::tmem_wait_ld();
+                uint32_t out[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int pp = half * 32 + 2 * i;
+                    const float a0 = fmaf(Dh, x[pp], fmaf(eoff, yo[2 * i], yd[2 * i]));
+                    const float a1 = fmaf(Dh, x[pp + 1], fmaf(eoff, yo[2 * i + 1], yd[2 * i + 1]));
+                    out[i] = pack_bf16(a0, a1);
+                }
+                if (t < p.L) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
+                            make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                }
+            }
+            const float wt = ex2_approx(cum_last - cum_t) * dtf[tid];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[i] = pack_bf16(wt * x[c * 8 + 2 * i], wt * x[c * 8 + 2 * i + 1]);
+                *reinterpret_cast<uint4*>(sm + OFF_X + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+
+        // ---- dS^T = B^T X~
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024);
+                const uint64_t dx = tc::smem_desc_sw128(sbase + OFF_X + kk * 2048, 16384, 1024);
+                tc::mma_bf16(tmem + 0, db, dx, ID_DS, kk > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
+        ++mma_phase;
+        tc::fence_after_sync();
+
+        // ---- S^T row tid <- exp(cum_last) S^T + dS^T; bf16 copy for the next block
+        {
+            const float ablk = ex2_approx(cum_last);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float ds[32];
+                tc::tmem_ld32(trow + half * 32, ds);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[i] = pack_bf16(S[c * 8 + 2 * i], S[c * 8 + 2 * i + 1]);
+                *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+
+    if (ok && p.last) {
+        float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)h * p.sl_h + (int64_t)tid * p.sl_n;
+#pragma unroll
+        for (int i = 0; i < P; ++i) ls[i * p.sl_p] = S[i];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace ssdtc
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+static bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box, bool swizzle) {
+    auto enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
+    if (!enc) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool tc_layout_ok(const SSDArgs& a) {
+    if (a.dtype != SS_BF16 || a.P != ssdtc::P || a.N != ssdtc::N) return false;
+    auto al16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+    auto m8 = [](int64_t s) { return s % 8 == 0 && s * 2 < (int64_t(1) << 40); };
+    if (a.sx_p != 1 || !al16(a.x) || !m8(a.sx_l) || !m8(a.sx_h) || !m8(a.sx_b)) return false;
+    if (a.sB_n != 1 || !al16(a.Bm) || !m8(a.sB_l) || !m8(a.sB_g) || !m8(a.sB_b)) return false;
+    if (a.sC_n != 1 || !al16(a.Cm) || !m8(a.sC_l) || !m8(a.sC_g) || !m8(a.sC_b)) return false;
+    if (a.sdt_h != 1 || !al16(a.dt) || !m8(a.sdt_l) || !m8(a.sdt_b)) return false;
+    if (a.sy_p != 1 || !al16(a.y) || !m8(a.sy_l) || !m8(a.sy_h) || !m8(a.sy_b)) return false;
+    return true;
+}
+
+// Path selection for tests: SS_SSD_PATH=general forces the CUDA-core kernel.
 int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
-    (void)a; (void)st; (void)scratch;
+    (void)scratch;
     *taken = false;
-    return SS_OK;
+    const char* force = getenv("SS_SSD_PATH");
+    if (force && !strcmp(force, "general")) return SS_OK;
+    if (!tc_layout_ok(a) || a.L < 1) return SS_OK;
+    *taken = true;
+
+    CUtensorMap mx, mb, mc, mdt;
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)a.P, (cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.Bsz};
+        cuuint64_t str[3] = {(cuuint64_t)(a.sx_h * 2), (cuuint64_t)(a.sx_l * 2), (cuuint64_t)(a.sx_b * 2)};
+        cuuint32_t box[4] = {64, 1, ssdtc::QB, 1};
+        if (!encode(&mx, a.x, 4, dims, str, box, true)) return SS_ERR_CUDA;
+    }
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)a.N, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.Bsz};
+        cuuint64_t sb[3] = {(cuuint64_t)(a.sB_g * 2), (cuuint64_t)(a.sB_l * 2), (cuuint64_t)(a.sB_b * 2)};
+        cuuint64_t sc[3] = {(cuuint64_t)(a.sC_g * 2), (cuuint64_t)(a.sC_l * 2), (cuuint64_t)(a.sC_b * 2)};
+        cuuint32_t box[4] = {64, 1, ssdtc::QB, 1};
+        if (!encode(&mb, a.Bm, 4, dims, sb, box, true)) return SS_ERR_CUDA;
+        if (!encode(&mc, a.Cm, 4, dims, sc, box, true)) return SS_ERR_CUDA;
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.Bsz};
+        cuuint64_t str[2] = {(cuuint64_t)(a.sdt_l * 2), (cuuint64_t)(a.sdt_b * 2)};
+        cuuint32_t box[3] = {8, ssdtc::QB, 1};
+        if (!encode(&mdt, a.dt, 3, dims, str, box, false)) return SS_ERR_CUDA;
+    }
+    ssdtc::Params p{};
+    p.Bsz = a.Bsz; p.L = a.L; p.H = a.H; p.G = a.G;
+    p.A = a.A; p.sA = a.sA; p.Dv = a.Dv; p.sD = a.sD;
+    p.y = static_cast<__nv_bfloat16*>(a.y); p.sy_b = a.sy_b; p.sy_l = a.sy_l; p.sy_h = a.sy_h;
+    p.last = a.last; p.sl_b = a.sl_b; p.sl_h = a.sl_h; p.sl_p = a.sl_p; p.sl_n = a.sl_n;
+    p.err = a.err;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if (cudaFuncSetAttribute(ssdtc::ssd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ssdtc::SMEM_BYTES) != cudaSuccess)
+            return SS_ERR_LAUNCH;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    ssdtc::ssd_chunk_tc<<<(unsigned)(a.Bsz * a.H), ssdtc::NTHREADS, ssdtc::SMEM_BYTES, st>>>(
+        mx, mb, mc, mdt, p);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
 }  // namespace ss
