@@ -37,6 +37,17 @@ HEADLINE = "mamba130m_layer"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
+# ALU roof of the selective scan.  Per channel-step the method needs N = 16
+# exponentials exp(delta*A) plus softplus (one ex2, one lg2) and the gate (one
+# tanh): 17 ex2-class and 2 half-rate MUFU operations, i.e. 21 ex2-equivalents.
+# The MUFU pipe bounds the scan before the FP32 pipe does (64 + ~8 fp32
+# lane-operations per channel-step at 128 lanes/SM/clock).  ex2.approx.f32
+# throughput measured on this machine's B300: 29.2 per SM per clock (lg2 and tanh
+# 14.7); 148 SMs at 2032 MHz.
+MUFU_EQ_PER_CHANNEL_STEP = 21
+MUFU_EX2_PER_SM_CLK = 29.2
+N_SM = 148
+SM_MHZ_MAX = 2032.0
 
 
 def parse():
@@ -47,7 +58,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary workload rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="run WORKLOAD's call warmup+steps times with no timing or output "
+                         "(for ncu captures)")
     return ap.parse_args()
 
 
@@ -290,8 +304,14 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
                    "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
                    "launches_per_call": launches_per_call}
             if name == "mamba2_ssd":
-                tf = ssd_flops(cfg) / (ms * 1e-3) / 1e12
-                row["tensor_tflops"] = round(tf, 1)
+                # executed MMA flops of the 128-step block form (C B^T per head)
+                nblk = -(-cfg.seqlen // 128)
+                P, N, Q = cfg.headdim, cfg.d_state, 128
+                ex = cfg.batch * cfg.nheads * nblk * 2 * Q * (Q * N + P * N + Q * P + N * P)
+                tf = ex / (ms * 1e-3) / 1e12
+                row["tensor_tflops_executed"] = round(tf, 1)
+                row["tensor_tflops_algorithmic"] = round(ssd_flops(cfg) / (ms * 1e-3) / 1e12, 1)
+                row["tensor_peak_tflops"] = tf_peak
                 row["tensor_frac"] = round(tf / tf_peak, 4)
             rows[name] = row
             del g, yb, ls
@@ -311,11 +331,11 @@ def oracle_throughput(host, cfg, seconds, oracle):
     import numpy as np
     nth = oracle.max_threads()
     Dch = cfg.d_inner
-    block = max(nth * 4, 64)
+    block = min(Dch, max(nth * 32, 64))
     f64 = {k: (None if v is None else v.double().numpy()) for k, v in host.items()}
     done, t_used, rounds = 0, 0.0, 0
     b = 0
-    while t_used < seconds and rounds < 1000:
+    while t_used < seconds and rounds < 100000:
         d0 = (rounds * block) % Dch
         d1 = min(Dch, d0 + block)
         sub = dict(u=f64["u"][b:b + 1, d0:d1], delta=f64["delta"][b:b + 1, d0:d1],
@@ -386,6 +406,28 @@ def main_reference(args):
     return 0
 
 
+def main_profile(args):
+    """Run one workload's call `warmup + steps` times (inputs drawn on the GPU)."""
+    import torch
+
+    from selective_state_space_146_b300 import _abi as abi
+    from selective_state_space_146_b300 import inputs
+    dev = torch.device("cuda", 0)
+    cfg = inputs.WORKLOADS[args.profile]
+    with inputs.on_device(dev):
+        g = (inputs.workload_ssd_inputs(cfg) if args.profile == "mamba2_ssd"
+             else inputs.workload_selective_inputs(cfg))
+    for _ in range(args.warmup + args.steps):
+        if args.profile == "mamba2_ssd":
+            abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
+                                   chunk=cfg.chunk, return_last_state=True)
+        else:
+            abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    return 0 if abi.device_error() == 0 else 1
+
+
 def main_ours(args):
     import torch
     import torch.distributed as tdist
@@ -425,16 +467,26 @@ def main_ours(args):
     if world > 1:
         dh.barrier(dev)
     if rank == 0:
-        key = "scan_fast.bf16.split2"
+        key = "scan_fast<bf16, 4 lanes/channel>"
+        mufu_peak = MUFU_EX2_PER_SM_CLK * N_SM * SM_MHZ_MAX * 1e6
+        kernel_steps_per_s = cfg.channel_steps / (kernel_ms * 1e-3)
+        mufu_achieved = kernel_steps_per_s * MUFU_EQ_PER_CHANNEL_STEP
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": h["ms_max"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(cfg),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                         "traffic": measured_traffic(key), "peak_source": f"{peak_src} hbm_gbs",
-                         "algorithmic_bytes_per_launch": nbytes, "kernel": key},
+            "roofline": {"bound": "alu", "achieved": round(mufu_achieved / 1e9, 1),
+                         "peak": round(mufu_peak / 1e9, 1),
+                         "unit": "Gop/s (MUFU ex2-equivalent)",
+                         "frac": round(mufu_achieved / mufu_peak, 4),
+                         "traffic": measured_traffic(key), "kernel": key,
+                         "ops_per_channel_step": MUFU_EQ_PER_CHANNEL_STEP,
+                         "peak_source": "measured ex2.approx rate x 148 SMs x 2032 MHz",
+                         "hbm_achieved_gbs": round(achieved, 1), "hbm_peak_gbs": hbm_peak,
+                         "hbm_frac": round(achieved / hbm_peak, 4),
+                         "hbm_peak_source": f"{peak_src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h["h2d"],
                     "d2h_bytes_per_step": h["d2h"]},
@@ -452,4 +504,6 @@ def main_ours(args):
 
 if __name__ == "__main__":
     a = parse()
+    if a.profile:
+        sys.exit(main_profile(a))
     sys.exit(main_reference(a) if a.impl == "reference" else main_ours(a))
