@@ -18,18 +18,23 @@
 // state term above, so every chunk length that is a multiple of 128 gives the
 // same result; the blocks are always 128 steps here.
 //
-// One CTA (4 warps) per (b, h), blocks in sequence.  Thread 0 issues the TMA
-// loads (x, B, C tiles with 128-byte swizzle; dt) and the MMAs
-// (tcgen05.mma kind::f16, bf16 operands from shared memory, fp32
-// accumulators in tensor memory, M = 128):
-//   CB   = C . B^T      A = C  (K-major)   B = B  (K-major)      TMEM [0, 128)
-//   Yoff = C . S^T      A = C  (K-major)   B = S  (MN-major)     TMEM [192, 256)
-//   Ydg  = M . X        A = M  (K-major)   B = X  (MN-major)     TMEM [128, 192)
-//   dS^T = B^T . X~     A = B  (MN-major)  B = X~ (MN-major)     TMEM [0, 64)
-// Thread t owns row t of every accumulator (TMEM lane t): it builds row t of
-// M, finishes row t of y, scales row t of x into X~, and keeps row n = t of
-// the fp32 state S^T in registers (a bf16 copy in shared memory feeds the
-// next block's Yoff).
+// One CTA per (b, h), blocks in sequence, warp-specialised:
+//  * a control warp issues the TMA loads (x, B, C tiles with 128-byte swizzle;
+//    dt) and the MMAs (tcgen05.mma kind::f16, bf16 operands from shared
+//    memory, fp32 accumulators in tensor memory, M = 128), and prefetches the
+//    next block's B, C, dt as soon as this block's MMAs are done:
+//      CB   = C . B^T      A = C  (K-major)   B = B  (K-major)      TMEM [0, 128)
+//      Yoff = C . S^T      A = C  (K-major)   B = S  (MN-major)     TMEM [192, 256)
+//      Ydg  = M . X        A = M  (K-major)   B = X  (MN-major)     TMEM [128, 192)
+//      dS^T = B^T . X~     A = B  (MN-major)  B = X~ (MN-major)     TMEM [0, 64)
+//  * four compute warps: thread t owns row t of every accumulator (TMEM lane
+//    t): it builds row t of M (over the C tiles), writes row t of X~ (over
+//    the state copy, free once C S^T is done), finishes row t of y and keeps
+//    row n = t of the fp32 state S^T in registers (a bf16 copy in shared
+//    memory feeds the next block's Yoff).
+// Off the diagonal 32-step chunk, exp(cum_i - cum_j) = exp(cum_i - cum_e) *
+// exp(cum_e - cum_j) with e the chunk's last step: one exponential per row
+// and chunk plus a column factor shared by all rows, both <= 1 for A <= 0.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,20 +54,23 @@ namespace ssdtc {
 constexpr int QB = 128;  // steps per block
 constexpr int P = 64;    // head dimension
 constexpr int N = 128;   // state size
-constexpr int NTHREADS = 128;
+constexpr int NCOMP = 128;           // compute threads (4 warps, one TMEM lane each)
+constexpr int NTHREADS = NCOMP + 32;  // + control warp (TMA and MMA issue)
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr int OFF_X = 0;                 // [128 t][64 p] bf16, swizzled   16 KB
-constexpr int OFF_B = OFF_X + 16384;     // 2 x [128 t][64 n]               32 KB
-constexpr int OFF_C = OFF_B + 32768;     // 2 x [128 t][64 n], later M      32 KB
-constexpr int OFF_S = OFF_C + 32768;     // [128 n][64 p] bf16 state copy   16 KB
-constexpr int OFF_DT = OFF_S + 16384;    // [128 t][8 h] bf16                2 KB
+constexpr int OFF_X = 0;                 // [128 t][64 p] bf16, swizzled          16 KB
+constexpr int OFF_B = OFF_X + 16384;     // 2 x [128 t][64 n]                      32 KB
+constexpr int OFF_C = OFF_B + 32768;     // 2 x [128 t][64 n]; then M (K-major)    32 KB
+constexpr int OFF_S = OFF_C + 32768;     // X~ [128 t][64 p]; then S^T copy [128 n][64 p]  16 KB
+constexpr int OFF_DT = OFF_S + 16384;    // [128 t][8 h] bf16                       2 KB
 constexpr int OFF_CUM = OFF_DT + 2048;   // cum (log2 units) [128] f32
 constexpr int OFF_DTF = OFF_CUM + 512;   // dt [128] f32
-constexpr int OFF_WS = OFF_DTF + 512;    // warp partial sums [4] f32
+constexpr int OFF_GF = OFF_DTF + 512;    // column factors of the decay matrix [128] f32
+constexpr int OFF_WS = OFF_GF + 512;     // warp partial sums [4] f32
 constexpr int OFF_BAR = OFF_WS + 64;     // mbarriers + TMEM address
-constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
+constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;
 constexpr uint32_t TMEM_COLS = 256;
+constexpr int BAR_COMP = 1;  // named barrier of the compute warps
 
 struct Params {
     int Bsz, L, H, G;
@@ -80,17 +88,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ void unpack8(const uint4& r, float* o) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 2)
 ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_dt,
              const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* bar_mma = bar_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_bc = bar + 0;     // B, C, dt of the block landed
+    uint64_t* bar_x = bar + 1;      // x of the block landed
+    uint64_t* bar_mma1 = bar + 2;   // C B^T and C S^T done
+    uint64_t* bar_mma23 = bar + 3;  // M X and B^T X~ done
+    uint64_t* bar_m = bar + 4;      // M and X~ written (compute -> control)
+    uint64_t* bar_s = bar + 5;      // state copy written, x consumed (compute -> control)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 64);
     float* cum = reinterpret_cast<float*>(sm + OFF_CUM);
     float* dtf = reinterpret_cast<float*>(sm + OFF_DTF);
+    float* gf = reinterpret_cast<float*>(sm + OFF_GF);
     float* wsum = reinterpret_cast<float*>(sm + OFF_WS);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,75 +121,110 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     const int g = h / (p.H / p.G);
     const float A2 = p.A[h * p.sA] * kLog2e;
     const float Dh = p.Dv ? p.Dv[h * p.sD] : 0.f;
+    // off-diagonal decay factorisation needs non-increasing cum (A <= 0)
+    const bool factor = A2 <= 0.f;
     const uint32_t sbase = smem_u32(sm);
+    const int nblk = (p.L + QB - 1) / QB;
 
     if (tid == 0) {
-        mbar_init(bar_full, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_bc, 1);
+        mbar_init(bar_x, 1);
+        mbar_init(bar_mma1, 1);
+        mbar_init(bar_mma23, 1);
+        mbar_init(bar_m, NCOMP);
+        mbar_init(bar_s, NCOMP);
         fence_mbar_init();
-        tma_prefetch_desc(&tm_x);
-        tma_prefetch_desc(&tm_B);
-        tma_prefetch_desc(&tm_C);
-        tma_prefetch_desc(&tm_dt);
     }
     if (warp == 0) {
         tc::tmem_alloc(tmem_slot, TMEM_COLS);
         tc::tmem_relinquish();
     }
-    // zero state: fp32 rows in registers, bf16 copy in shared memory
-    float S[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) S[i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
 
-    constexpr uint32_t ID_CB = tc::idesc_bf16(QB, QB, false, false);
-    constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, P, false, true);
-    constexpr uint32_t ID_YDG = tc::idesc_bf16(QB, P, false, true);
-    constexpr uint32_t ID_DS = tc::idesc_bf16(N, P, true, true);
-
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    const int nblk = (p.L + QB - 1) / QB;
-    for (int blk = 0; blk < nblk && ok; ++blk) {
-        const int t0 = blk * QB;
-        // ---- loads
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_full, 16384 + 32768 + 32768 + 2048);
-            tma_load_4d(sm + OFF_X, &tm_x, bar_full, 0, h, t0, b);
-            tma_load_4d(sm + OFF_B, &tm_B, bar_full, 0, g, t0, b);
-            tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_full, 64, g, t0, b);
-            tma_load_4d(sm + OFF_C, &tm_C, bar_full, 0, g, t0, b);
-            tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_full, 64, g, t0, b);
-            tma_load_3d(sm + OFF_DT, &tm_dt, bar_full, (h / 8) * 8, t0, b);
-        }
-        // every wait ends in a block-wide agreement so all threads leave together
-        if (!__syncthreads_and(mbar_wait(bar_full, blk & 1, p.err))) { ok = false; break; }
-
-        // ---- issue C B^T and C S^T while the decays are being summed
-        if (tid == 0) {
-            tc::fence_after_sync();
+    if (warp == 4) {
+        // ================= control: TMA loads and MMA issue =================
+        if (lane == 0) {
+            constexpr uint32_t ID_CB = tc::idesc_bf16(QB, QB, false, false);
+            constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, P, false, true);
+            constexpr uint32_t ID_YDG = tc::idesc_bf16(QB, P, false, true);
+            constexpr uint32_t ID_DS = tc::idesc_bf16(N, P, true, true);
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(&tm_B);
+            tma_prefetch_desc(&tm_C);
+            tma_prefetch_desc(&tm_dt);
+            auto load_bc = [&](int k) {
+                const int t0 = k * QB;
+                mbar_arrive_expect_tx(bar_bc, 32768 + 32768 + 2048);
+                tma_load_4d(sm + OFF_B, &tm_B, bar_bc, 0, g, t0, b);
+                tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_bc, 64, g, t0, b);
+                tma_load_4d(sm + OFF_C, &tm_C, bar_bc, 0, g, t0, b);
+                tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_bc, 64, g, t0, b);
+                tma_load_3d(sm + OFF_DT, &tm_dt, bar_bc, (h / 8) * 8, k * QB, b);
+            };
+            auto load_x = [&](int k) {
+                mbar_arrive_expect_tx(bar_x, 16384);
+                tma_load_4d(sm + OFF_X, &tm_x, bar_x, 0, h, k * QB, b);
+            };
+            load_bc(0);
+            load_x(0);
+            for (int k = 0; k < nblk; ++k) {
+                // C B^T and C S^T: needs B, C of block k and the state copy S(k)
+                if (!mbar_wait(bar_bc, k & 1, p.err) || !mbar_wait(bar_s, k & 1, p.err)) break;
+                tc::fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint64_t dc = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
-                const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024);
-                const uint64_t ds = tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024);
-                tc::mma_bf16(tmem + 0, dc, db, ID_CB, kk > 0);
-                tc::mma_bf16(tmem + 192, dc, ds, ID_YOFF, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t dc = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
+                    const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024);
+                    const uint64_t ds = tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024);
+                    tc::mma_bf16(tmem + 0, dc, db, ID_CB, kk > 0);
+                    tc::mma_bf16(tmem + 192, dc, ds, ID_YOFF, kk > 0);
+                }
+                tc::mma_commit(bar_mma1);
+                // M X and B^T X~: needs M (over C) and X~ (over the state copy)
+                if (!mbar_wait(bar_m, k & 1, p.err)) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t dm = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
+                    const uint64_t dx = tc::smem_desc_sw128(sbase + OFF_X + kk * 2048, 16384, 1024);
+                    const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024);
+                    const uint64_t dxt = tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024);
+                    tc::mma_bf16(tmem + 128, dm, dx, ID_YDG, kk > 0);
+                    tc::mma_bf16(tmem + 0, db, dxt, ID_DS, kk > 0);
+                }
+                tc::mma_commit(bar_mma23);
+                if (k + 1 < nblk) {
+                    // B, C, dt free once both MMA groups are done
+                    if (!mbar_wait(bar_mma23, k & 1, p.err)) break;
+                    load_bc(k + 1);
+                    // x free once the compute warps have finished block k
+                    if (!mbar_wait(bar_s, (k + 1) & 1, p.err)) break;
+                    load_x(k + 1);
+                }
             }
-            tc::mma_commit(bar_mma);
         }
+    } else {
+        // ================= compute warps: one TMEM lane / row each =================
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        float S[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) S[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        mbar_arrive(bar_s);  // S(0) = 0 is ready
 
-        // ---- cumulative decay (log2 units) over the block
-        {
+        bool ok = true;
+        for (int k = 0; k < nblk; ++k) {
+            const int t0 = k * QB;
+            if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_bc, k & 1, p.err))) { ok = false; break; }
+            // ---- cumulative decay (log2 units) and the column factors
             const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + tid * 16 + (h & 7) * 2);
             const float dtv = __uint_as_float((uint32_t)raw << 16);
             float v = dtv * A2;
@@ -176,172 +234,135 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                 if (lane >= o) v += u;
             }
             if (lane == 31) wsum[warp] = v;
-            __syncthreads();
+            named_sync(BAR_COMP, NCOMP);
             for (int w = 0; w < warp; ++w) v += wsum[w];
-            cum[tid] = v;
+            const float cum_t = v;
+            cum[tid] = cum_t;
             dtf[tid] = dtv;
-            __syncthreads();
-        }
-        const float cum_t = cum[tid];
-        const float cum_last = cum[QB - 1];
+            // end of this thread's 32-step chunk: lane 31 of the same warp
+            const float cum_end = __shfl_sync(0xffffffffu, cum_t, 31);
+            gf[tid] = ex2_approx(cum_end - cum_t) * dtv;  // <= dt when A <= 0
+            named_sync(BAR_COMP, NCOMP);
+            const float cum_last = cum[QB - 1];
 
-        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
-        ++mma_phase;
-        tc::fence_after_sync();
-
-        // ---- row tid of M = CB o decay o dt (lower triangle), bf16, K-major
-        //      over the C tiles (C is no longer needed)
-#pragma unroll 1
-        for (int jc = 0; jc < 4; ++jc) {
-            const int tile = jc >> 1;
-            uint8_t* mt = sm + OFF_C + tile * 16384;
-            if (jc <= warp) {
-                float v[32];
-                tc::tmem_ld32(trow + jc * 32, v);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float m2[2];
-#pragma unroll
-                        for (int s = 0; s < 2; ++s) {
-                            const int j = jc * 32 + q * 8 + e * 2 + s;
-                            const float dec = ex2_approx(cum_t - cum[j]);  // j > i: discarded
-                            m2[s] = j <= tid ? v[q * 8 + e * 2 + s] * dec * dtf[j] : 0.f;
-                        }
-                        w4[e] = pack_bf16(m2[0], m2[1]);
-                    }
-                    const int c = ((jc & 1) * 32 + q * 8) >> 3;  // 16-byte chunk within the row
-                    *reinterpret_cast<uint4*>(mt + swz(tid, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int c = ((jc & 1) * 32 + q * 8) >> 3;
-                    *reinterpret_cast<uint4*>(mt + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-
-        // ---- Ydiag = M X
-        if (tid == 0) {
+            if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_mma1, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint64_t dm = tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024);
-                const uint64_t dx = tc::smem_desc_sw128(sbase + OFF_X + kk * 2048, 16384, 1024);
-                tc::mma_bf16(tmem + 128, dm, dx, ID_YDG, kk > 0);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
-        ++mma_phase;
-        tc::fence_after_sync();
 
-        // ---- y row tid, then X~ row tid in place
-        {
-            float x[P];
+            // ---- row tid of M = C B^T o decay o dt (lower triangle), bf16,
+            //      K-major over the C tiles
+#pragma unroll 1
+            for (int jc = 0; jc < 4; ++jc) {
+                uint8_t* mt = sm + OFF_C + (jc >> 1) * 16384;
+                if (jc <= warp) {
+                    float cb[32];
+                    tc::tmem_ld32(trow + jc * 32, cb);
+                    tc::tmem_wait_ld();
+                    float m[32];
+                    if (jc < warp && factor) {
+                        // rows after this chunk: exp(cum_i - cum_j) = f1 * exp(cum_end - cum_j)
+                        const float f1 = ex2_approx(cum_t - cum[jc * 32 + 31]);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 r = *reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c));
-                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+                        for (int e = 0; e < 32; ++e) m[e] = cb[e] * (f1 * gf[jc * 32 + e]);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    x[c * 8 + 2 * i] = __uint_as_float(w[i] << 16);
-                    x[c * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-                }
-            }
-            const float eoff = ex2_approx(cum_t);
-            const int t = t0 + tid;
-            __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
+                        for (int e = 0; e < 32; ++e) {
+                            const int j = jc * 32 + e;
+                            const float dec = ex2_approx(cum_t - cum[j]);  // j > i: discarded
+                            m[e] = j <= tid ? cb[e] * dec * dtf[j] : 0.f;
+                        }
+                    }
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float yd[32], yo[32];
-                tc::tmem_ld32(trow + 128 + half * 32, yd);
-                tc::tmem_ld32(trow + 192 + half * 32, yo);
-                tc::tmem_wait_ld();
-                uint32_t out[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int pp = half * 32 + 2 * i;
-                    const float a0 = fmaf(Dh, x[pp], fmaf(eoff, yo[2 * i], yd[2 * i]));
-                    const float a1 = fmaf(Dh, x[pp + 1], fmaf(eoff, yo[2 * i + 1], yd[2 * i + 1]));
-                    out[i] = pack_bf16(a0, a1);
-                }
-                if (t < p.L) {
+                    for (int q = 0; q < 4; ++q) {
+                        const int c = (jc & 1) * 4 + q;
+                        *reinterpret_cast<uint4*>(mt + swz(tid, c)) =
+                            make_uint4(pack_bf16(m[q * 8 + 0], m[q * 8 + 1]), pack_bf16(m[q * 8 + 2], m[q * 8 + 3]),
+                                       pack_bf16(m[q * 8 + 4], m[q * 8 + 5]), pack_bf16(m[q * 8 + 6], m[q * 8 + 7]));
+                    }
+                } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
-                            make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(mt + swz(tid, (jc & 1) * 4 + q)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            const float wt = ex2_approx(cum_last - cum_t) * dtf[tid];
+            // ---- X~ row tid = w_t x_t into the state-copy buffer
+            if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_x, k & 1, p.err))) { ok = false; break; }
+            {
+                const float wt = ex2_approx(cum_last - cum_t) * dtv;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) w[i] = pack_bf16(wt * x[c * 8 + 2 * i], wt * x[c * 8 + 2 * i + 1]);
-                *reinterpret_cast<uint4*>(sm + OFF_X + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int c = 0; c < 8; ++c) {
+                    float x8[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c)), x8);
+                    *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) =
+                        make_uint4(pack_bf16(wt * x8[0], wt * x8[1]), pack_bf16(wt * x8[2], wt * x8[3]),
+                                   pack_bf16(wt * x8[4], wt * x8[5]), pack_bf16(wt * x8[6], wt * x8[7]));
+                }
             }
-        }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(bar_m);
 
-        // ---- dS^T = B^T X~
-        if (tid == 0) {
+            if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_mma23, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t db = tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024);
-                const uint64_t dx = tc::smem_desc_sw128(sbase + OFF_X + kk * 2048, 16384, 1024);
-                tc::mma_bf16(tmem + 0, db, dx, ID_DS, kk > 0);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        if (!__syncthreads_and(mbar_wait(bar_mma, mma_phase & 1, p.err))) { ok = false; break; }
-        ++mma_phase;
-        tc::fence_after_sync();
 
-        // ---- S^T row tid <- exp(cum_last) S^T + dS^T; bf16 copy for the next block
-        {
-            const float ablk = ex2_approx(cum_last);
+            // ---- y row tid = Ydiag + exp(cum) Yoff + D x
+            {
+                const float eoff = ex2_approx(cum_t);
+                const int t = t0 + tid;
+                __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float ds[32];
-                tc::tmem_ld32(trow + half * 32, ds);
-                tc::tmem_wait_ld();
+                for (int half = 0; half < 2; ++half) {
+                    float yd[32], yo[32];
+                    tc::tmem_ld32(trow + 128 + half * 32, yd);
+                    tc::tmem_ld32(trow + 192 + half * 32, yo);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
+                    for (int q = 0; q < 4; ++q) {
+                        float x8[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, half * 4 + q)), x8);
+                        float o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = fmaf(Dh, x8[i], fmaf(eoff, yo[q * 8 + i], yd[q * 8 + i]));
+                        if (t < p.L)
+                            *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
+                                make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                           pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+                    }
+                }
             }
+            // ---- S^T row tid <- exp(cum_last) S^T + dS^T; bf16 copy for block k+1
+            {
+                const float ablk = ex2_approx(cum_last);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
+                for (int half = 0; half < 2; ++half) {
+                    float ds[32];
+                    tc::tmem_ld32(trow + half * 32, ds);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 4; ++i) w[i] = pack_bf16(S[c * 8 + 2 * i], S[c * 8 + 2 * i + 1]);
-                *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) =
+                        make_uint4(pack_bf16(S[c * 8 + 0], S[c * 8 + 1]), pack_bf16(S[c * 8 + 2], S[c * 8 + 3]),
+                                   pack_bf16(S[c * 8 + 4], S[c * 8 + 5]), pack_bf16(S[c * 8 + 6], S[c * 8 + 7]));
             }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(bar_s);
         }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-    }
-
-    if (ok && p.last) {
-        float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)h * p.sl_h + (int64_t)tid * p.sl_n;
+        if (ok && p.last) {
+            float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)h * p.sl_h + (int64_t)tid * p.sl_n;
 #pragma unroll
-        for (int i = 0; i < P; ++i) ls[i * p.sl_p] = S[i];
+            for (int i = 0; i < P; ++i) ls[i * p.sl_p] = S[i];
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
 
 }  // namespace ssdtc
