@@ -318,6 +318,74 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
             torch.cuda.empty_cache()
         except Exception as e:  # a row failing must not hide the headline
             rows[name] = {"error": str(e)[:200]}
+    rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
+    return rows
+
+
+def decode_rows(dev, torch, abi, inputs, hbm_peak):
+    """One-token decode steps (the recurrent form): time per step and the
+    state bytes read + written per step against HBM."""
+    rows = {}
+    steps = 200
+    try:
+        cfg = inputs.WORKLOADS["mamba130m_layer"]
+        with inputs.on_device(dev):
+            g = inputs.selective_inputs(cfg.batch, cfg.d_inner, cfg.d_state, 1, "bf16")
+        state = torch.zeros(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+        u, dl, z = (g[k][..., 0].contiguous() for k in ("u", "delta", "z"))
+        Bt, Ct = g["B"][..., 0].contiguous(), g["C"][..., 0].contiguous()
+        y = torch.empty_like(u)
+
+        def step():
+            abi.selective_state_update(state, u, dl, g["A"], Bt, Ct, g["D"], z, g["delta_bias"],
+                                       y=y)
+        for _ in range(10):
+            step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / steps
+        nbytes = 2 * state.numel() * 4
+        rows["decode_step_mamba130m_layer"] = {
+            "us_per_token": round(us, 3), "state_bytes": nbytes,
+            "hbm_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "note": "one launch per token, back to back on one stream"}
+    except Exception as e:
+        rows["decode_step_mamba130m_layer"] = {"error": str(e)[:200]}
+    try:
+        cfg = inputs.WORKLOADS["mamba2_ssd"]
+        with inputs.on_device(dev):
+            g = inputs.ssd_inputs(cfg.batch, 1, cfg.nheads, cfg.headdim, cfg.d_state, cfg.ngroups)
+        state = torch.zeros(cfg.batch, cfg.nheads, cfg.headdim, cfg.d_state, device=dev)
+        x, dt = g["x"][:, 0].contiguous(), g["dt"][:, 0].contiguous()
+        Bt, Ct = g["B"][:, 0].contiguous(), g["C"][:, 0].contiguous()
+        y = torch.empty_like(x)
+
+        def step2():
+            abi.ssd_state_update(state, x, dt, g["A_head"], Bt, Ct, g["D"], y=y)
+        for _ in range(10):
+            step2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            step2()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / steps
+        nbytes = 2 * state.numel() * 4
+        rows["decode_step_mamba2_ssd"] = {
+            "us_per_token": round(us, 3), "state_bytes": nbytes,
+            "hbm_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "note": "one launch per token, back to back on one stream"}
+    except Exception as e:
+        rows["decode_step_mamba2_ssd"] = {"error": str(e)[:200]}
     return rows
 
 

@@ -152,6 +152,56 @@ int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tens
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
                           ss_tensor* y, ss_tensor* last_state, void* stream);
 
+/*
+ * Scans that continue from a given state (page 0539edu paper talk §5.3: split
+ * a long text into chunks and pass the state across; §4.3: generation keeps
+ * only the fixed-size state).  Same arguments and results as the calls above
+ * plus `initial_state`, the state entering step 0 (NULL = zero):
+ *   ss_selective_scan_fwd_init : initial_state (Bsz, D, N) f32
+ *   ss_ssd_chunk_scan_fwd_init : initial_state (Bsz, H, P, N) f32
+ * Running [0, L1) and then [L1, L) from the first call's last_state gives the
+ * result of one call over [0, L) up to rounding.  initial_state and
+ * last_state must not overlap.
+ */
+int ss_selective_scan_fwd_init(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               const ss_tensor* initial_state, ss_tensor* y,
+                               ss_tensor* last_state, void* stream);
+int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               int chunk, const ss_tensor* initial_state, ss_tensor* y,
+                               ss_tensor* last_state, void* stream);
+
+/*
+ * One recurrent step (decoding one token), updating the state in place
+ * (0539edu paper talk §4.3: the step function of the recurrent form; the
+ * state is the only thing carried between tokens).
+ *
+ * ss_selective_state_update, per batch row b and channel d:
+ *   dl = softplus?(delta[b,d] + delta_bias[d]);
+ *   state[b,d,n] = exp(dl A[d,n]) state[b,d,n] + dl B[b,n] u[b,d];
+ *   y[b,d] = (sum_n C[b,n] state[b,d,n] + D[d] u[b,d]) * z * sigmoid(z)
+ *   state (Bsz, D, N) f32 in/out; u, delta, z, y (Bsz, D) dtype T;
+ *   B, C (Bsz, N) dtype T; A (D, N), D, delta_bias (D) f32.  N <= 256.
+ *
+ * ss_ssd_state_update, per batch row b, head h (group g = h / (H/G)), p:
+ *   a = exp(dt[b,h] A_head[h]);
+ *   state[b,h,p,n] = a state[b,h,p,n] + dt[b,h] x[b,h,p] B[b,g,n];
+ *   y[b,h,p] = sum_n C[b,g,n] state[b,h,p,n] + D[h] x[b,h,p]
+ *   state (Bsz, H, P, N) f32 in/out; x, y (Bsz, H, P) dtype T; dt (Bsz, H)
+ *   dtype T (positive); B, C (Bsz, G, N) dtype T; A_head, D (H) f32.
+ *
+ * Applying the step to t = 0 .. L-1 in turn gives the scans' y and final state.
+ */
+int ss_selective_state_update(ss_tensor* state, const ss_tensor* u, const ss_tensor* delta,
+                              const ss_tensor* A, const ss_tensor* B, const ss_tensor* C,
+                              const ss_tensor* D, const ss_tensor* z, const ss_tensor* delta_bias,
+                              int softplus, ss_tensor* y, void* stream);
+int ss_ssd_state_update(ss_tensor* state, const ss_tensor* x, const ss_tensor* dt,
+                        const ss_tensor* A_head, const ss_tensor* B, const ss_tensor* C,
+                        const ss_tensor* D, ss_tensor* y, void* stream);
+
 /* Name of a status code (static string, never NULL). */
 const char* ss_status_string(int status);
 

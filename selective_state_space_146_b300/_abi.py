@@ -21,8 +21,9 @@ STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_
           -4: "SS_ERR_ALIGNMENT", -5: "SS_ERR_UNSUPPORTED", -6: "SS_ERR_ALLOC",
           -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
 EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chunk_scan_fwd",
-           "ss_status_string",
-           "ss_get_device_error", "ss_launch_count", "ss_version")
+           "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
+           "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
+           "ss_version")
 
 
 class SSTensor(ctypes.Structure):
@@ -57,6 +58,14 @@ def load(path: str | None = None):
     lib.ss_selective_scan_fwd_noalloc.restype = i
     lib.ss_ssd_chunk_scan_fwd.argtypes = [T, T, T, T, T, T, i, T, T, vp]
     lib.ss_ssd_chunk_scan_fwd.restype = i
+    lib.ss_selective_scan_fwd_init.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, vp]
+    lib.ss_selective_scan_fwd_init.restype = i
+    lib.ss_ssd_chunk_scan_fwd_init.argtypes = [T, T, T, T, T, T, i, T, T, T, vp]
+    lib.ss_ssd_chunk_scan_fwd_init.restype = i
+    lib.ss_selective_state_update.argtypes = [T, T, T, T, T, T, T, T, T, i, T, vp]
+    lib.ss_selective_state_update.restype = i
+    lib.ss_ssd_state_update.argtypes = [T, T, T, T, T, T, T, T, vp]
+    lib.ss_ssd_state_update.restype = i
     lib.ss_status_string.argtypes = [i]
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_get_device_error.argtypes = [vp]
@@ -101,12 +110,15 @@ def _stream_ptr(stream) -> int:
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                       y=None, last_state=None, return_last_state=False, stream=None):
-    """Selective scan forward (ss_selective_scan_fwd).
+                       y=None, last_state=None, return_last_state=False, initial_state=None,
+                       stream=None):
+    """Selective scan forward (ss_selective_scan_fwd; ss_selective_scan_fwd_init
+    when an initial state is given).
 
     u, delta, z: (batch, d_inner, L); A: (d_inner, N) f32; B, C: (batch, N, L);
-    D, delta_bias: (d_inner,) f32.  Returns y (same dtype as u), or
-    (y, last_state) with last_state (batch, d_inner, N) f32.
+    D, delta_bias: (d_inner,) f32; initial_state (batch, d_inner, N) f32.
+    Returns y (same dtype as u), or (y, last_state) with last_state
+    (batch, d_inner, N) f32.
     """
     if y is None:
         y = torch.empty_like(u, memory_format=torch.contiguous_format)
@@ -115,10 +127,17 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
                                  device=u.device)
     ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
     ys, ls = describe(y), describe(last_state)
-    rc = load().ss_selective_scan_fwd(*[_ref(t) for t in ts], int(bool(softplus)), _ref(ys),
-                                      _ref(ls), _stream_ptr(stream))
+    if initial_state is None:
+        rc = load().ss_selective_scan_fwd(*[_ref(t) for t in ts], int(bool(softplus)), _ref(ys),
+                                          _ref(ls), _stream_ptr(stream))
+        what = "ss_selective_scan_fwd"
+    else:
+        rc = load().ss_selective_scan_fwd_init(*[_ref(t) for t in ts], int(bool(softplus)),
+                                               _ref(describe(initial_state)), _ref(ys), _ref(ls),
+                                               _stream_ptr(stream))
+        what = "ss_selective_scan_fwd_init"
     if rc != 0:
-        raise SSError(rc, "ss_selective_scan_fwd")
+        raise SSError(rc, what)
     return (y, last_state) if (return_last_state or last_state is not None) else y
 
 
@@ -141,11 +160,13 @@ def selective_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=Non
 
 
 def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_state=None,
-                       return_last_state=False, stream=None):
-    """Mamba-2 SSD chunked scan forward (ss_ssd_chunk_scan_fwd).
+                       return_last_state=False, initial_state=None, stream=None):
+    """Mamba-2 SSD chunked scan forward (ss_ssd_chunk_scan_fwd; the _init
+    variant when an initial state is given).
 
     x: (batch, L, H, P); dt: (batch, L, H) positive; A_head, D: (H,) f32;
-    B, C: (batch, L, G, N).  Returns y, or (y, last_state (batch, H, P, N) f32).
+    B, C: (batch, L, G, N); initial_state (batch, H, P, N) f32.  Returns y, or
+    (y, last_state (batch, H, P, N) f32).
     """
     if y is None:
         y = torch.empty_like(x, memory_format=torch.contiguous_format)
@@ -154,11 +175,44 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_stat
                                  dtype=torch.float32, device=x.device)
     ts = [describe(t) for t in (x, dt, A_head, B, C, D)]
     ys, ls = describe(y), describe(last_state)
-    rc = load().ss_ssd_chunk_scan_fwd(*[_ref(t) for t in ts], int(chunk), _ref(ys), _ref(ls),
-                                      _stream_ptr(stream))
+    if initial_state is None:
+        rc = load().ss_ssd_chunk_scan_fwd(*[_ref(t) for t in ts], int(chunk), _ref(ys), _ref(ls),
+                                          _stream_ptr(stream))
+    else:
+        rc = load().ss_ssd_chunk_scan_fwd_init(*[_ref(t) for t in ts], int(chunk),
+                                               _ref(describe(initial_state)), _ref(ys), _ref(ls),
+                                               _stream_ptr(stream))
     if rc != 0:
         raise SSError(rc, "ss_ssd_chunk_scan_fwd")
     return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def selective_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           softplus=True, y=None, stream=None):
+    """One decode step (ss_selective_state_update); state (batch, d_inner, N)
+    f32 is updated in place.  u, delta, z: (batch, d_inner); B, C: (batch, N)."""
+    if y is None:
+        y = torch.empty_like(u, memory_format=torch.contiguous_format)
+    ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    rc = load().ss_selective_state_update(_ref(describe(state)), *[_ref(t) for t in ts],
+                                          int(bool(softplus)), _ref(describe(y)),
+                                          _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_state_update")
+    return y
+
+
+def ssd_state_update(state, x, dt, A_head, B, C, D=None, y=None, stream=None):
+    """One Mamba-2 decode step (ss_ssd_state_update); state (batch, H, P, N) f32
+    is updated in place.  x: (batch, H, P); dt: (batch, H); B, C: (batch, G, N)."""
+    if y is None:
+        y = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ts = [describe(t) for t in (x, dt, A_head, B, C, D)]
+    rc = load().ss_ssd_state_update(_ref(describe(state)), *[_ref(t) for t in ts],
+                                    _ref(describe(y)), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_ssd_state_update")
+    return y
 
 
 def device_error(stream=None) -> int:

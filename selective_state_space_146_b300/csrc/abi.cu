@@ -230,10 +230,14 @@ using namespace ss;
 
 extern "C" {
 
-int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+// Checks and ScanArgs assembly shared by the scans with and without an
+// initial state.
+static int selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                           const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
-                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+                          const ss_tensor* h0, ss_tensor* y, ss_tensor* last_state,
+                          ScanArgs* out, bool* nothing_to_do) {
+    *nothing_to_do = false;
     SS_TRY(check_tensor(u, 3));
     SS_TRY(check_tensor(delta, 3));
     SS_TRY(check_tensor(A, 2));
@@ -244,6 +248,7 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (z) SS_TRY(check_tensor(z, 3));
     if (delta_bias) SS_TRY(check_tensor(delta_bias, 1));
     if (last_state) SS_TRY(check_tensor(last_state, 3));
+    if (h0) SS_TRY(check_tensor(h0, 3));
     if (softplus != 0 && softplus != 1) return SS_ERR_INVALID_ARG;
 
     const int dt = u->dtype;
@@ -251,7 +256,8 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
         (z && z->dtype != dt))
         return SS_ERR_DTYPE;
     if (A->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
-        (delta_bias && delta_bias->dtype != SS_F32) || (last_state && last_state->dtype != SS_F32))
+        (delta_bias && delta_bias->dtype != SS_F32) || (last_state && last_state->dtype != SS_F32) ||
+        (h0 && h0->dtype != SS_F32))
         return SS_ERR_DTYPE;
 
     const int64_t Bsz = u->shape[0], Dch = u->shape[1], L = u->shape[2], N = A->shape[1];
@@ -265,11 +271,14 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != Dch ||
                        last_state->shape[2] != N))
         return SS_ERR_SHAPE;
+    if (h0 && (h0->shape[0] != Bsz || h0->shape[1] != Dch || h0->shape[2] != N)) return SS_ERR_SHAPE;
     if (N < 1) return SS_ERR_SHAPE;
     if (N > 256) return SS_ERR_UNSUPPORTED;
     if (Bsz * Dch >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
-    if (Bsz == 0 || Dch == 0) return SS_OK;
-    if (L == 0 && !last_state) return SS_OK;
+    if (Bsz == 0 || Dch == 0 || (L == 0 && !last_state)) {
+        *nothing_to_do = true;
+        return SS_OK;
+    }
 
     ScanArgs a{};
     a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = dt;
@@ -286,11 +295,37 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
         a.last = static_cast<float*>(last_state->data);
         a.sl_b = last_state->stride[0]; a.sl_d = last_state->stride[1]; a.sl_n = last_state->stride[2];
     }
+    if (h0) {
+        a.h0 = static_cast<const float*>(h0->data);
+        a.sh_b = h0->stride[0]; a.sh_d = h0->stride[1]; a.sh_n = h0->stride[2];
+    }
     a.softplus = softplus;
+    *out = a;
+    return SS_OK;
+}
+
+int ss_selective_scan_fwd_init(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               const ss_tensor* initial_state, ss_tensor* y,
+                               ss_tensor* last_state, void* stream) {
+    ScanArgs a{};
+    bool nothing = false;
+    SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, initial_state, y,
+                          last_state, &a, &nothing));
+    if (nothing) return SS_OK;
     a.err = device_error_ptr();
     if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+    return ss_selective_scan_fwd_init(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, y,
+                                      last_state, stream);
 }
 
 int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
@@ -313,9 +348,11 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
     return rc;
 }
 
-int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
-                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
-                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               int chunk, const ss_tensor* initial_state, ss_tensor* y,
+                               ss_tensor* last_state, void* stream) {
+    const ss_tensor* h0 = initial_state;
     SS_TRY(check_tensor(x, 4));
     SS_TRY(check_tensor(dt, 3));
     SS_TRY(check_tensor(A_head, 1));
@@ -324,11 +361,12 @@ int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tens
     SS_TRY(check_tensor(y, 4));
     if (D) SS_TRY(check_tensor(D, 1));
     if (last_state) SS_TRY(check_tensor(last_state, 4));
+    if (h0) SS_TRY(check_tensor(h0, 4));
     if (chunk != 64 && chunk != 128 && chunk != 256) return SS_ERR_INVALID_ARG;
     const int ty = x->dtype;
     if (dt->dtype != ty || B->dtype != ty || C->dtype != ty || y->dtype != ty) return SS_ERR_DTYPE;
     if (A_head->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
-        (last_state && last_state->dtype != SS_F32))
+        (last_state && last_state->dtype != SS_F32) || (h0 && h0->dtype != SS_F32))
         return SS_ERR_DTYPE;
     const int64_t Bsz = x->shape[0], L = x->shape[1], H = x->shape[2], P = x->shape[3];
     const int64_t G = B->shape[2], N = B->shape[3];
@@ -339,6 +377,8 @@ int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tens
     if (G < 1 || N < 1 || H % G != 0) return SS_ERR_SHAPE;
     if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != H ||
                        last_state->shape[2] != P || last_state->shape[3] != N))
+        return SS_ERR_SHAPE;
+    if (h0 && (h0->shape[0] != Bsz || h0->shape[1] != H || h0->shape[2] != P || h0->shape[3] != N))
         return SS_ERR_SHAPE;
     if (N > 256 || P > 1024) return SS_ERR_UNSUPPORTED;
     if (Bsz * H * P >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
@@ -360,10 +400,110 @@ int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tens
         a.sl_b = last_state->stride[0]; a.sl_h = last_state->stride[1];
         a.sl_p = last_state->stride[2]; a.sl_n = last_state->stride[3];
     }
+    if (h0) {
+        a.h0 = static_cast<const float*>(h0->data);
+        a.sh_b = h0->stride[0]; a.sh_h = h0->stride[1]; a.sh_p = h0->stride[2]; a.sh_n = h0->stride[3];
+    }
     a.err = device_error_ptr();
     if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_ssd(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
+                          ss_tensor* y, ss_tensor* last_state, void* stream) {
+    return ss_ssd_chunk_scan_fwd_init(x, dt, A_head, B, C, D, chunk, nullptr, y, last_state,
+                                      stream);
+}
+
+int ss_selective_state_update(ss_tensor* state, const ss_tensor* u, const ss_tensor* delta,
+                              const ss_tensor* A, const ss_tensor* B, const ss_tensor* C,
+                              const ss_tensor* D, const ss_tensor* z, const ss_tensor* delta_bias,
+                              int softplus, ss_tensor* y, void* stream) {
+    SS_TRY(check_tensor(state, 3));
+    SS_TRY(check_tensor(u, 2));
+    SS_TRY(check_tensor(delta, 2));
+    SS_TRY(check_tensor(A, 2));
+    SS_TRY(check_tensor(B, 2));
+    SS_TRY(check_tensor(C, 2));
+    SS_TRY(check_tensor(y, 2));
+    if (D) SS_TRY(check_tensor(D, 1));
+    if (z) SS_TRY(check_tensor(z, 2));
+    if (delta_bias) SS_TRY(check_tensor(delta_bias, 1));
+    if (softplus != 0 && softplus != 1) return SS_ERR_INVALID_ARG;
+    const int ty = u->dtype;
+    if (delta->dtype != ty || B->dtype != ty || C->dtype != ty || y->dtype != ty ||
+        (z && z->dtype != ty))
+        return SS_ERR_DTYPE;
+    if (state->dtype != SS_F32 || A->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
+        (delta_bias && delta_bias->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+    const int64_t Bsz = u->shape[0], Dch = u->shape[1], N = A->shape[1];
+    if (!same_shape(delta, u) || !same_shape(y, u) || (z && !same_shape(z, u))) return SS_ERR_SHAPE;
+    if (A->shape[0] != Dch || B->shape[0] != Bsz || B->shape[1] != N || !same_shape(C, B))
+        return SS_ERR_SHAPE;
+    if (state->shape[0] != Bsz || state->shape[1] != Dch || state->shape[2] != N) return SS_ERR_SHAPE;
+    if ((D && D->shape[0] != Dch) || (delta_bias && delta_bias->shape[0] != Dch)) return SS_ERR_SHAPE;
+    if (N < 1) return SS_ERR_SHAPE;
+    if (N > 256) return SS_ERR_UNSUPPORTED;
+    if (Bsz * Dch >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
+    if (Bsz == 0 || Dch == 0) return SS_OK;
+    StepArgs a{};
+    a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.dtype = ty;
+    a.state = static_cast<float*>(state->data);
+    a.ss_b = state->stride[0]; a.ss_d = state->stride[1]; a.ss_n = state->stride[2];
+    a.u = u->data; a.su_b = u->stride[0]; a.su_d = u->stride[1];
+    a.dl = delta->data; a.sdl_b = delta->stride[0]; a.sdl_d = delta->stride[1];
+    if (z) { a.z = z->data; a.sz_b = z->stride[0]; a.sz_d = z->stride[1]; }
+    a.y = y->data; a.sy_b = y->stride[0]; a.sy_d = y->stride[1];
+    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_n = B->stride[1];
+    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_n = C->stride[1];
+    a.A = static_cast<const float*>(A->data); a.sA_d = A->stride[0]; a.sA_n = A->stride[1];
+    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
+    if (delta_bias) { a.bias = static_cast<const float*>(delta_bias->data); a.sbias = delta_bias->stride[0]; }
+    a.softplus = softplus;
+    return launch_selective_step(a, static_cast<cudaStream_t>(stream));
+}
+
+int ss_ssd_state_update(ss_tensor* state, const ss_tensor* x, const ss_tensor* dt,
+                        const ss_tensor* A_head, const ss_tensor* B, const ss_tensor* C,
+                        const ss_tensor* D, ss_tensor* y, void* stream) {
+    SS_TRY(check_tensor(state, 4));
+    SS_TRY(check_tensor(x, 3));
+    SS_TRY(check_tensor(dt, 2));
+    SS_TRY(check_tensor(A_head, 1));
+    SS_TRY(check_tensor(B, 3));
+    SS_TRY(check_tensor(C, 3));
+    SS_TRY(check_tensor(y, 3));
+    if (D) SS_TRY(check_tensor(D, 1));
+    const int ty = x->dtype;
+    if (dt->dtype != ty || B->dtype != ty || C->dtype != ty || y->dtype != ty) return SS_ERR_DTYPE;
+    if (state->dtype != SS_F32 || A_head->dtype != SS_F32 || (D && D->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+    const int64_t Bsz = x->shape[0], H = x->shape[1], P = x->shape[2];
+    const int64_t G = B->shape[1], N = B->shape[2];
+    if (!same_shape(y, x) || dt->shape[0] != Bsz || dt->shape[1] != H) return SS_ERR_SHAPE;
+    if (A_head->shape[0] != H || (D && D->shape[0] != H)) return SS_ERR_SHAPE;
+    if (B->shape[0] != Bsz || !same_shape(C, B) || G < 1 || N < 1 || H % G != 0) return SS_ERR_SHAPE;
+    if (state->shape[0] != Bsz || state->shape[1] != H || state->shape[2] != P ||
+        state->shape[3] != N)
+        return SS_ERR_SHAPE;
+    if (N > 256 || P > 1024) return SS_ERR_UNSUPPORTED;
+    if (Bsz * H * P >= (int64_t(1) << 26)) return SS_ERR_UNSUPPORTED;
+    if (Bsz == 0 || H == 0 || P == 0) return SS_OK;
+    SSDStepArgs a{};
+    a.Bsz = (int)Bsz; a.H = (int)H; a.P = (int)P; a.G = (int)G; a.N = (int)N; a.dtype = ty;
+    a.state = static_cast<float*>(state->data);
+    a.ss_b = state->stride[0]; a.ss_h = state->stride[1]; a.ss_p = state->stride[2]; a.ss_n = state->stride[3];
+    a.x = x->data; a.sx_b = x->stride[0]; a.sx_h = x->stride[1]; a.sx_p = x->stride[2];
+    a.dt = dt->data; a.sdt_b = dt->stride[0]; a.sdt_h = dt->stride[1];
+    a.A = static_cast<const float*>(A_head->data); a.sA = A_head->stride[0];
+    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_g = B->stride[1]; a.sB_n = B->stride[2];
+    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_g = C->stride[1]; a.sC_n = C->stride[2];
+    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
+    a.y = y->data; a.sy_b = y->stride[0]; a.sy_h = y->stride[1]; a.sy_p = y->stride[2];
+    return launch_ssd_step(a, static_cast<cudaStream_t>(stream));
 }
 
 const char* ss_status_string(int status) {
@@ -396,6 +536,6 @@ int ss_get_device_error(void* stream) {
 
 uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int ss_version(void) { return 100; }
+int ss_version(void) { return 200; }
 
 }  // extern "C"

@@ -20,6 +20,7 @@ struct ScanArgs {
     const float* Dv; int64_t sD;
     const float* bias; int64_t sbias;
     float* last; int64_t sl_b, sl_d, sl_n;
+    const float* h0; int64_t sh_b, sh_d, sh_n;  // initial state, may be null
     int softplus;
     unsigned* err;  // device error word
 };
@@ -36,7 +37,37 @@ struct SSDArgs {
     const float* Dv; int64_t sD;
     void* y;        int64_t sy_b, sy_l, sy_h, sy_p;
     float* last;    int64_t sl_b, sl_h, sl_p, sl_n;
+    const float* h0; int64_t sh_b, sh_h, sh_p, sh_n;  // initial state, may be null
     unsigned* err;
+};
+
+// One recurrent step of the selective scan (decode), element strides.
+struct StepArgs {
+    int Bsz, D, N, dtype;
+    float* state; int64_t ss_b, ss_d, ss_n;
+    const void* u; int64_t su_b, su_d;
+    const void* dl; int64_t sdl_b, sdl_d;
+    const void* z; int64_t sz_b, sz_d;
+    void* y; int64_t sy_b, sy_d;
+    const void* Bm; int64_t sB_b, sB_n;
+    const void* Cm; int64_t sC_b, sC_n;
+    const float* A; int64_t sA_d, sA_n;
+    const float* Dv; int64_t sD;
+    const float* bias; int64_t sbias;
+    int softplus;
+};
+
+// One recurrent step of the SSD scan (decode), element strides.
+struct SSDStepArgs {
+    int Bsz, H, P, G, N, dtype;
+    float* state; int64_t ss_b, ss_h, ss_p, ss_n;
+    const void* x; int64_t sx_b, sx_h, sx_p;
+    const void* dt; int64_t sdt_b, sdt_h;
+    const float* A; int64_t sA;
+    const void* Bm; int64_t sB_b, sB_g, sB_n;
+    const void* Cm; int64_t sC_b, sC_g, sC_n;
+    const float* Dv; int64_t sD;
+    void* y; int64_t sy_b, sy_h, sy_p;
 };
 
 // Scratch provider: either stream-ordered allocation or a fixed buffer.
@@ -48,6 +79,8 @@ struct Scratch {
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
+int launch_selective_step(const StepArgs& a, cudaStream_t st);
+int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);
 
 // Counts kernels launched by the library.
 void count_launch(int n);

@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(128) scan_general(ScanArgs a) {
     float h[NMAX], A2[NMAX];
 #pragma unroll
     for (int n = 0; n < NMAX; ++n) {
-        h[n] = 0.f;
+        h[n] = (a.h0 && n < N) ? a.h0[b * a.sh_b + d * a.sh_d + n * a.sh_n] : 0.f;
         A2[n] = n < N ? a.A[d * a.sA_d + n * a.sA_n] * kLog2e : 0.f;
     }
     const float Dd = a.Dv ? a.Dv[d * a.sD] : 0.f;
@@ -108,6 +108,7 @@ struct FastParams {
     const float* Dv; int64_t sD;
     const float* bias; int64_t sbias;
     float* last; int64_t sl_b, sl_d, sl_n;
+    const float* h0; int64_t sh_b, sh_d, sh_n;  // initial state, may be null
     void* y; int64_t sy_b, sy_d;  // y rows are contiguous in t
     float* summ;    // [nseg-1][Bsz*D][2][N]: prod of decays, end state from zero
     int softplus;
@@ -361,13 +362,18 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     const int64_t bd = (int64_t)b * p.D + d;
 
     float2 A2[NS / 2], h2[NS / 2];
+    // the summary pass always starts from zero; the main pass from the
+    // caller's initial state (if any)
+    const bool from_h0 = !SUMMARY && valid && p.h0;
 #pragma unroll
     for (int j = 0; j < NS / 2; ++j) {
         const int n = part * NS + 2 * j;
         A2[j] = valid ? make_float2(p.A[d * p.sA_d + n * p.sA_n] * kLog2e,
                                     p.A[d * p.sA_d + (n + 1) * p.sA_n] * kLog2e)
                       : make_float2(0.f, 0.f);
-        h2[j] = make_float2(0.f, 0.f);
+        h2[j] = from_h0 ? make_float2(p.h0[b * p.sh_b + d * p.sh_d + n * p.sh_n],
+                                      p.h0[b * p.sh_b + d * p.sh_d + (n + 1) * p.sh_n])
+                        : make_float2(0.f, 0.f);
     }
     const float Dd = (valid && p.Dv) ? p.Dv[d * p.sD] : 0.f;
     const float biasd = (valid && p.bias) ? p.bias[d * p.sbias] : 0.f;
@@ -629,6 +635,7 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     fp.Dv = a.Dv; fp.sD = a.sD; fp.bias = a.bias; fp.sbias = a.sbias;
     fp.last = a.last; fp.sl_b = a.sl_b; fp.sl_d = a.sl_d; fp.sl_n = a.sl_n;
     fp.y = a.y; fp.sy_b = a.sy_b; fp.sy_d = a.sy_d;
+    fp.h0 = a.h0; fp.sh_b = a.sh_b; fp.sh_d = a.sh_d; fp.sh_n = a.sh_n;
     fp.softplus = a.softplus; fp.err = a.err;
 
     // Segments: enough CTAs to give every SM several consumer warps.
@@ -730,6 +737,48 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
         return run_fast<float, 4, 4>(a, st, scratch);
     }
     return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
+}
+
+// ---------------------------------------------------------------------------
+// One recurrent step (decode): one thread per (b, d), the channel's state
+// row read and written once.
+
+template <typename T>
+__global__ void __launch_bounds__(128) scan_step(StepArgs a) {
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (unit >= (int64_t)a.Bsz * a.D) return;
+    const int b = (int)(unit / a.D), d = (int)(unit % a.D);
+    const float uu = Elem<T>::to_f(static_cast<const T*>(a.u)[b * a.su_b + d * a.su_d]);
+    float dd = Elem<T>::to_f(static_cast<const T*>(a.dl)[b * a.sdl_b + d * a.sdl_d]) +
+               (a.bias ? a.bias[d * a.sbias] : 0.f);
+    if (a.softplus) dd = softplus_f(dd);
+    const float du = dd * uu;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b;
+    float* st = a.state + b * a.ss_b + d * a.ss_d;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int n = 0; n < a.N; ++n) {
+        const float hn = fmaf(ex2_approx(dd * a.A[d * a.sA_d + n * a.sA_n] * kLog2e),
+                              st[n * a.ss_n], du * Elem<T>::to_f(Bp[n * a.sB_n]));
+        st[n * a.ss_n] = hn;
+        acc = fmaf(Elem<T>::to_f(Cp[n * a.sC_n]), hn, acc);
+    }
+    acc = fmaf(a.Dv ? a.Dv[d * a.sD] : 0.f, uu, acc);
+    if (a.z) {
+        const float zz = Elem<T>::to_f(static_cast<const T*>(a.z)[b * a.sz_b + d * a.sz_d]);
+        acc *= zz * sigmoid_accurate(zz);
+    }
+    static_cast<T*>(a.y)[b * a.sy_b + d * a.sy_d] = Elem<T>::from_f(acc);
+}
+
+int launch_selective_step(const StepArgs& a, cudaStream_t st) {
+    const int64_t units = (int64_t)a.Bsz * a.D;
+    const unsigned blocks = (unsigned)((units + 127) / 128);
+    if (a.dtype == SS_BF16) scan_step<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
+    else scan_step<float><<<blocks, 128, 0, st>>>(a);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
 }  // namespace ss

@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(128) ssd_general(SSDArgs a) {
     const int N = a.N;
     float S[NMAX];
 #pragma unroll
-    for (int n = 0; n < NMAX; ++n) S[n] = 0.f;
+    for (int n = 0; n < NMAX; ++n)
+        S[n] = (a.h0 && n < N) ? a.h0[b * a.sh_b + h * a.sh_h + p * a.sh_p + n * a.sh_n] : 0.f;
     const float A2 = a.A[h * a.sA] * kLog2e;
     const float Dh = a.Dv ? a.Dv[h * a.sD] : 0.f;
     const T* x = static_cast<const T*>(a.x) + b * a.sx_b + h * a.sx_h + p * a.sx_p;
@@ -86,6 +87,46 @@ int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch) {
         if (taken) return rc;
     }
     return a.dtype == SS_BF16 ? run_ssd_general<__nv_bfloat16>(a, st) : run_ssd_general<float>(a, st);
+}
+
+// One recurrent step (decode): one warp per (b, h, p) state row; lanes split
+// the N states and the readout is a warp sum.
+template <typename T>
+__global__ void __launch_bounds__(128) ssd_step(SSDStepArgs a) {
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= (int64_t)a.Bsz * a.H * a.P) return;
+    const int p = (int)(row % a.P);
+    const int h = (int)((row / a.P) % a.H);
+    const int b = (int)(row / ((int64_t)a.P * a.H));
+    const int g = h / (a.H / a.G);
+    const float dtv = Elem<T>::to_f(static_cast<const T*>(a.dt)[b * a.sdt_b + h * a.sdt_h]);
+    const float xv = Elem<T>::to_f(static_cast<const T*>(a.x)[b * a.sx_b + h * a.sx_h + p * a.sx_p]);
+    const float decay = ex2_approx(dtv * a.A[h * a.sA] * kLog2e);
+    const float dx = dtv * xv;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b + g * a.sB_g;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b + g * a.sC_g;
+    float* st = a.state + b * a.ss_b + h * a.ss_h + p * a.ss_p;
+    float acc = 0.f;
+    for (int n = lane; n < a.N; n += 32) {
+        const float sn = fmaf(decay, st[n * a.ss_n], dx * Elem<T>::to_f(Bp[n * a.sB_n]));
+        st[n * a.ss_n] = sn;
+        acc = fmaf(Elem<T>::to_f(Cp[n * a.sC_n]), sn, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0)
+        static_cast<T*>(a.y)[b * a.sy_b + h * a.sy_h + p * a.sy_p] =
+            Elem<T>::from_f(fmaf(a.Dv ? a.Dv[h * a.sD] : 0.f, xv, acc));
+}
+
+int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st) {
+    const int64_t threads = (int64_t)a.Bsz * a.H * a.P * 32;
+    const unsigned blocks = (unsigned)((threads + 127) / 128);
+    if (a.dtype == SS_BF16) ssd_step<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
+    else ssd_step<float><<<blocks, 128, 0, st>>>(a);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
 }  // namespace ss

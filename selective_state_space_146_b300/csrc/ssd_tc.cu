@@ -78,6 +78,7 @@ struct Params {
     const float* Dv; int64_t sD;
     __nv_bfloat16* y; int64_t sy_b, sy_l, sy_h;
     float* last; int64_t sl_b, sl_h, sl_p, sl_n;
+    const float* h0; int64_t sh_b, sh_h, sh_p, sh_n;  // initial state, may be null
     unsigned* err;
 };
 
@@ -211,14 +212,20 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     } else {
         // ================= compute warps: one TMEM lane / row each =================
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        // state entering block 0 (row n = tid of S^T): the caller's or zero
         float S[P];
+        const float* h0row = p.h0 ? p.h0 + (int64_t)b * p.sh_b + (int64_t)h * p.sh_h +
+                                        (int64_t)tid * p.sh_n
+                                  : nullptr;
 #pragma unroll
-        for (int i = 0; i < P; ++i) S[i] = 0.f;
+        for (int i = 0; i < P; ++i) S[i] = h0row ? h0row[i * p.sh_p] : 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) =
+                make_uint4(pack_bf16(S[c * 8 + 0], S[c * 8 + 1]), pack_bf16(S[c * 8 + 2], S[c * 8 + 3]),
+                           pack_bf16(S[c * 8 + 4], S[c * 8 + 5]), pack_bf16(S[c * 8 + 6], S[c * 8 + 7]));
         fence_proxy_async_smem();
-        mbar_arrive(bar_s);  // S(0) = 0 is ready
+        mbar_arrive(bar_s);  // S(0) is ready
 
         bool ok = true;
         for (int k = 0; k < nblk; ++k) {
@@ -434,6 +441,7 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
     p.A = a.A; p.sA = a.sA; p.Dv = a.Dv; p.sD = a.sD;
     p.y = static_cast<__nv_bfloat16*>(a.y); p.sy_b = a.sy_b; p.sy_l = a.sy_l; p.sy_h = a.sy_h;
     p.last = a.last; p.sl_b = a.sl_b; p.sl_h = a.sl_h; p.sl_p = a.sl_p; p.sl_n = a.sl_n;
+    p.h0 = a.h0; p.sh_b = a.sh_b; p.sh_h = a.sh_h; p.sh_p = a.sh_p; p.sh_n = a.sh_n;
     p.err = a.err;
 
     static bool attr_set[64] = {};

@@ -151,3 +151,37 @@ def test_ssd_argument_errors(lib):
     assert _call_ssd(lib, a) == -5
     a = _ssd_args(Bsz=0)
     assert _call_ssd(lib, a) == 0
+
+
+def test_initial_state_and_step_argument_errors(lib):
+    a = _sel_args()
+    bad_h0 = FakeT((2, 8, 15), _abi.SS_F32)
+    r = {k: v.ref for k, v in a.items()}
+    assert lib.ss_selective_scan_fwd_init(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 1, bad_h0.ref, r["y"], r["last"],
+                                          None) == -2
+    bf_h0 = FakeT((2, 8, 16), _abi.SS_BF16)
+    assert lib.ss_selective_scan_fwd_init(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 1, bf_h0.ref, r["y"], r["last"],
+                                          None) == -3
+    # one decode step: (batch, d_inner) activations, (batch, N) B / C
+    st = FakeT((2, 8, 16), _abi.SS_F32)
+    u, dl, z, y = (FakeT((2, 8)) for _ in range(4))
+    Bm, Cm = FakeT((2, 16)), FakeT((2, 16))
+    A, D, bias = FakeT((8, 16), _abi.SS_F32), FakeT((8,), _abi.SS_F32), FakeT((8,), _abi.SS_F32)
+    assert lib.ss_selective_state_update(FakeT((2, 8, 8), _abi.SS_F32).ref, u.ref, dl.ref, A.ref,
+                                         Bm.ref, Cm.ref, D.ref, z.ref, bias.ref, 1, y.ref,
+                                         None) == -2
+    assert lib.ss_selective_state_update(FakeT((2, 8, 16), _abi.SS_BF16).ref, u.ref, dl.ref,
+                                         A.ref, Bm.ref, Cm.ref, D.ref, z.ref, bias.ref, 1, y.ref,
+                                         None) == -3
+    assert lib.ss_selective_state_update(st.ref, u.ref, dl.ref, A.ref, Bm.ref, Cm.ref, D.ref,
+                                         z.ref, bias.ref, 5, y.ref, None) == -1
+    # SSD step: groups must divide heads
+    sst = FakeT((2, 4, 8, 16), _abi.SS_F32)
+    x, yy = FakeT((2, 4, 8)), FakeT((2, 4, 8))
+    dt = FakeT((2, 4))
+    Ah, Dh = FakeT((4,), _abi.SS_F32), FakeT((4,), _abi.SS_F32)
+    Bg, Cg = FakeT((2, 3, 16)), FakeT((2, 3, 16))
+    assert lib.ss_ssd_state_update(sst.ref, x.ref, dt.ref, Ah.ref, Bg.ref, Cg.ref, Dh.ref, yy.ref,
+                                   None) == -2

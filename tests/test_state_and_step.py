@@ -1,0 +1,146 @@
+"""Initial states and the recurrent decode step, against the fp64 oracle (GPU).
+
+The oracle already takes an initial state h0 (its split-invariance pin fixes
+what continuing from a state means); the decode step is one iteration of the
+oracle's time loop, so L steps in turn must reproduce the oracle's scan.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_146_b300 import _abi, inputs
+from tests.parity_util import check_close, cuda_inputs, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def scan_path(request):
+    old = os.environ.get("SS_SCAN_PATH")
+    val = getattr(request, "param", None)
+    if val:
+        os.environ["SS_SCAN_PATH"] = val
+    else:
+        os.environ.pop("SS_SCAN_PATH", None)
+    yield val
+    if old is None:
+        os.environ.pop("SS_SCAN_PATH", None)
+    else:
+        os.environ["SS_SCAN_PATH"] = old
+
+
+def _tdt(dt):
+    return torch.float32 if dt == "f32" else torch.bfloat16
+
+
+def _h0(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g, dtype=torch.float32)
+
+
+@pytest.mark.parametrize("case", [(2, 40, 16, 200, "bf16"), (1, 16, 16, 1000, "f32"),
+                                  (1, 32, 16, 4096, "bf16"), (2, 6, 16, 33, "f32"),
+                                  (1, 4, 64, 50, "f32")],
+                         ids=lambda c: "x".join(map(str, c)))
+@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split4"], indirect=True)
+def test_selective_scan_with_initial_state(cuda_device, scan_path, case):
+    Bsz, D, N, L, dt = case
+    inp = inputs.selective_inputs(Bsz, D, N, L, dt, seed=L + 3)
+    h0 = _h0((Bsz, D, N), 11)
+    g = cuda_inputs(inp, cuda_device)
+    y, s = _abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], return_last_state=True,
+                                   initial_state=h0.to(cuda_device))
+    torch.cuda.synchronize()
+    yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], h0=h0, nthreads=8)
+    check_close(to_np(y), yo, _tdt(dt), "y with initial state")
+    check_close(to_np(s), so, _tdt(dt), "last_state with initial state")
+
+
+def test_selective_scan_continues_across_calls(cuda_device):
+    """[0, L1) then [L1, L) from the first call's final state == one call."""
+    inp = inputs.selective_inputs(2, 48, 16, 1536, "bf16", seed=21)
+    g = cuda_inputs(inp, cuda_device)
+    y, s = _abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], return_last_state=True)
+    L1 = 1024
+
+    def part(sl, h0=None):
+        return _abi.selective_scan_fwd(g["u"][..., sl].contiguous(), g["delta"][..., sl].contiguous(),
+                                       g["A"], g["B"][..., sl].contiguous(),
+                                       g["C"][..., sl].contiguous(), g["D"],
+                                       g["z"][..., sl].contiguous(), g["delta_bias"],
+                                       return_last_state=True, initial_state=h0)
+
+    y1, s1 = part(slice(0, L1))
+    y2, s2 = part(slice(L1, None), s1)
+    torch.cuda.synchronize()
+    check_close(to_np(torch.cat([y1, y2], -1)), to_np(y), torch.bfloat16, "y split vs whole")
+    check_close(to_np(s2), to_np(s), torch.bfloat16, "state split vs whole")
+
+
+@pytest.mark.parametrize("case", [(2, 24, 16, 12, "f32"), (3, 40, 16, 10, "bf16"),
+                                  (1, 8, 64, 6, "f32")], ids=lambda c: "x".join(map(str, c)))
+def test_decode_steps_reproduce_the_scan(cuda_device, case):
+    Bsz, D, N, L, dt = case
+    inp = inputs.selective_inputs(Bsz, D, N, L, dt, seed=L * 7 + D)
+    g = cuda_inputs(inp, cuda_device)
+    h0 = _h0((Bsz, D, N), 5)
+    state = h0.to(cuda_device).clone()
+    ys = []
+    for t in range(L):
+        ys.append(_abi.selective_state_update(
+            state, g["u"][..., t].contiguous(), g["delta"][..., t].contiguous(), g["A"],
+            g["B"][..., t].contiguous(), g["C"][..., t].contiguous(), g["D"],
+            g["z"][..., t].contiguous(), g["delta_bias"]))
+    torch.cuda.synchronize()
+    yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], h0=h0)
+    check_close(to_np(torch.stack(ys, -1)), yo, _tdt(dt), "decode y")
+    check_close(to_np(state), so, _tdt(dt), "decode state")
+
+
+@pytest.mark.parametrize("case", [(1, 384, 4, 64, 128, 1, "bf16"), (2, 300, 4, 16, 32, 2, "f32"),
+                                  (1, 1000, 8, 64, 128, 2, "bf16")],
+                         ids=lambda c: "x".join(map(str, c)))
+@pytest.mark.parametrize("ssd_path", [None, "general"])
+def test_ssd_with_initial_state(cuda_device, case, ssd_path, monkeypatch):
+    if ssd_path:
+        monkeypatch.setenv("SS_SSD_PATH", ssd_path)
+    else:
+        monkeypatch.delenv("SS_SSD_PATH", raising=False)
+    Bsz, L, H, P, N, G, dt = case
+    inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, seed=L + 1)
+    h0 = _h0((Bsz, H, P, N), 13)
+    g = cuda_inputs(inp, cuda_device)
+    y, s = _abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
+                                   chunk=128, return_last_state=True,
+                                   initial_state=h0.to(cuda_device))
+    torch.cuda.synchronize()
+    yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0,
+                        nthreads=8)
+    check_close(to_np(y), yo, _tdt(dt), "ssd y with initial state")
+    check_close(to_np(s), so, _tdt(dt), "ssd state with initial state")
+
+
+@pytest.mark.parametrize("case", [(2, 10, 4, 16, 32, 2, "f32"), (1, 8, 8, 64, 128, 1, "bf16")],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_ssd_decode_steps_reproduce_the_scan(cuda_device, case):
+    Bsz, L, H, P, N, G, dt = case
+    inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, seed=L + H)
+    g = cuda_inputs(inp, cuda_device)
+    h0 = _h0((Bsz, H, P, N), 17)
+    state = h0.to(cuda_device).clone()
+    ys = []
+    for t in range(L):
+        ys.append(_abi.ssd_state_update(state, g["x"][:, t].contiguous(), g["dt"][:, t].contiguous(),
+                                        g["A_head"], g["B"][:, t].contiguous(),
+                                        g["C"][:, t].contiguous(), g["D"]))
+    torch.cuda.synchronize()
+    yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0)
+    check_close(to_np(torch.stack(ys, 1)), yo, _tdt(dt), "ssd decode y")
+    check_close(to_np(state), so, _tdt(dt), "ssd decode state")
