@@ -49,6 +49,8 @@ def _bind(path):
     lib.oracle_ssd.argtypes = [i64] * 6 + [dp] * 6 + [dp, dp, dp, ip]
     lib.oracle_ssd.restype = ip
     lib.oracle_threads.restype = ip
+    lib.oracle_causal_conv1d_silu.argtypes = [i64] * 4 + [dp] * 4 + [ip]
+    lib.oracle_causal_conv1d_silu.restype = ip
     return lib
 
 
@@ -72,6 +74,9 @@ class _Bound:
 
     def ssd(self, *a, **k):
         return ssd(*a, _lib=self._lib, **k)
+
+    def causal_conv1d_silu(self, *a, **k):
+        return causal_conv1d_silu(*a, _lib=self._lib, **k)
 
 
 def load_library(path: str) -> _Bound:
@@ -145,3 +150,27 @@ def ssd(x, dt, A_head, B, C, D=None, h0=None, nthreads=1, _lib=None):
     if rc != 0:
         raise ValueError(f"oracle_ssd rejected its arguments (rc={rc})")
     return y, last
+
+
+def causal_conv1d_silu(x, w, bias=None, nthreads=1, _lib=None):
+    """Oracle of the causal depthwise conv1d + SiLU.  x (Bsz, D, L); w (D, W);
+    bias (D,).  Returns u (Bsz, D, L) float64."""
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    Bsz, D, L = x.shape
+    W = w.shape[1]
+    assert w.shape == (D, W) and (bias is None or bias.shape == (D,))
+    u = np.empty_like(x)
+    rc = (_lib or _load()).oracle_causal_conv1d_silu(Bsz, D, L, W, _ptr(x), _ptr(w), _ptr(bias),
+                                                     _ptr(u), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_causal_conv1d_silu rejected its arguments (rc={rc})")
+    return u
+
+
+def conv_selective_scan(x, conv_w, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None,
+                        softplus=True, h0=None, nthreads=1):
+    """The conv branch feeding the scan: u = silu(causal_conv1d(x)), then the
+    selective scan of u (the two oracle functions composed)."""
+    u = causal_conv1d_silu(x, conv_w, conv_bias, nthreads=nthreads)
+    return selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus=softplus, h0=h0,
+                          nthreads=nthreads)

@@ -22,6 +22,10 @@
  *  - state-spaces/mamba README §4.3 and the study notes §5: Mamba-2 / SSD,
  *    multi-head with a scalar A per head and d_state 64..128.
  *
+ *  - study notes §4.3 and the paper talk §3.1: the branch that feeds the SSM
+ *    passes a short causal depthwise convolution (kernel width d_conv = 4)
+ *    first; followed here by SiLU.
+ *
  * Readings where the pages are silent (each is also listed in the design
  * notes): softplus(x) = log(1 + e^x); A is given already negative and used as
  * is; the initial state is zero unless h0 is given; B and C are shared by all
@@ -176,6 +180,40 @@ int oracle_ssd(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t G, int64_t 
             for (int64_t i = 0; i < P * N; ++i)
                 last_state[((b * H + hh) * P) * N + i] = S[i];
         free(S);
+    }
+    return 0;
+}
+
+/*
+ * Causal depthwise convolution over t followed by SiLU, one sequential loop per
+ * (batch row b, channel d):
+ *
+ *   x, u : (Bsz, D, L), t fastest;  w : (D, W);  bias : (D) nullable
+ *   pre  = bias[d] + sum_{k=0}^{W-1} w[d,k] * x[b,d,t - (W-1) + k]   (x = 0 before t = 0)
+ *   u    = pre / (1 + exp(-pre))
+ */
+int oracle_causal_conv1d_silu(int64_t Bsz, int64_t D, int64_t L, int64_t W, const double* x,
+                              const double* w, const double* bias, double* u, int nthreads) {
+    if (Bsz < 0 || D < 0 || L < 0 || W < 1) return -1;
+    int64_t units = Bsz * D;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t unit = 0; unit < units; ++unit) {
+        int64_t d = unit % D;
+        const double* xr = x + unit * L;
+        double* ur = u + unit * L;
+        for (int64_t t = 0; t < L; ++t) {
+            double pre = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < W; ++k) {
+                int64_t s = t - (W - 1) + k;
+                if (s >= 0) pre += w[d * W + k] * xr[s];
+            }
+            ur[t] = pre / (1.0 + exp(-pre));
+        }
     }
     return 0;
 }

@@ -302,6 +302,66 @@ def test_ssd_quadratic_dual_form():
 
 
 # --------------------------------------------------------------------------
+# The causal depthwise conv1d + SiLU in front of the scan (study notes §4.3,
+# paper talk §3.1).
+
+
+def _conv_silu_by_numpy(x, w, bias):
+    """The same map through numpy's convolution (a different algorithm):
+    left-pad by W-1 zeros, correlate with the taps, add the bias, SiLU."""
+    Bsz, D, L = x.shape
+    W = w.shape[1]
+    out = np.empty_like(x)
+    for b in range(Bsz):
+        for d in range(D):
+            pad = np.concatenate([np.zeros(W - 1), x[b, d]])
+            pre = np.convolve(pad, w[d][::-1], mode="valid") + (bias[d] if bias is not None else 0)
+            out[b, d] = pre / (1 + np.exp(-pre))
+    return out
+
+
+def test_conv_identity_and_delay_kernels():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((2, 5, 40))
+    ident = np.zeros((5, 4))
+    ident[:, 3] = 1.0
+    u = oracle.causal_conv1d_silu(x, ident)
+    np.testing.assert_allclose(u, x / (1 + np.exp(-x)), rtol=1e-15, atol=1e-15)
+    delay = np.zeros((5, 4))
+    delay[:, 0] = 1.0
+    u = oracle.causal_conv1d_silu(x, delay)
+    np.testing.assert_array_equal(u[..., :3], 0.0)
+    np.testing.assert_allclose(u[..., 3:], x[..., :-3] / (1 + np.exp(-x[..., :-3])), rtol=1e-15)
+    bias = rng.standard_normal(5)
+    u = oracle.causal_conv1d_silu(x, np.zeros((5, 4)), bias)
+    np.testing.assert_allclose(u, np.broadcast_to((bias / (1 + np.exp(-bias)))[None, :, None],
+                                                  u.shape), rtol=1e-15)
+
+
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_conv_matches_numpy_convolution(W):
+    rng = np.random.default_rng(40 + W)
+    x = rng.standard_normal((2, 6, 33))
+    w = rng.standard_normal((6, W))
+    bias = rng.standard_normal(6)
+    np.testing.assert_allclose(oracle.causal_conv1d_silu(x, w, bias), _conv_silu_by_numpy(x, w, bias),
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_conv_then_scan_composes():
+    rng = np.random.default_rng(45)
+    x = rng.standard_normal((1, 4, 30))
+    w = rng.standard_normal((4, 4))
+    cb = rng.standard_normal(4)
+    _, delta, A, Bm, Cm, D, z, db = _rand_case(rng, 1, 4, 5, 30)
+    y, s = oracle.conv_selective_scan(x, w, cb, delta, A, Bm, Cm, D, z, db)
+    u = _conv_silu_by_numpy(x, w, cb)
+    y2, s2 = oracle.selective_scan(u, delta, A, Bm, Cm, D, z, db)
+    np.testing.assert_allclose(y, y2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(s, s2, rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # Planted mistakes: a copy of the oracle with one plausible bug (made in a
 # temporary copy of the C source, compiled on the CPU) must fail at least one
 # of the pins above.
@@ -320,6 +380,9 @@ _MUTANTS = {
     "ssd_B_C_swapped": ("out += cr[n] * S[p * N + n];", "out += br[n] * S[p * N + n];"),
     "ssd_no_dt_on_input": ("a * S[p * N + n] + dtv * xr[p] * br[n]", "a * S[p * N + n] + xr[p] * br[n]"),
     "ssd_group_index": ("int64_t g = hh / heads_per_group;", "int64_t g = hh % G;"),
+    "conv_taps_reversed": ("int64_t s = t - (W - 1) + k;", "int64_t s = t - k;"),
+    "conv_bias_dropped": ("double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
+    "conv_no_silu": ("ur[t] = pre / (1.0 + exp(-pre));", "ur[t] = pre;"),
 }
 
 
@@ -350,6 +413,12 @@ def _pins_pass(lib):
             want = (Lm * (Cs[0, :, g] @ Bs[0, :, g].T)) @ x[0, :, h] + Dh[h] * x[0, :, h]
             if not np.allclose(ys[0, :, h], want, rtol=1e-10, atol=1e-11):
                 return False
+        xc = rng.standard_normal((2, 3, 17))
+        wc = rng.standard_normal((3, 4))
+        bc = rng.standard_normal(3)
+        uc = lib.causal_conv1d_silu(xc, wc, bc)
+        if not np.allclose(uc, _conv_silu_by_numpy(xc, wc, bc), rtol=1e-12, atol=1e-13):
+            return False
         return True
     except ValueError:
         return False
