@@ -318,6 +318,29 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
             torch.cuda.empty_cache()
         except Exception as e:  # a row failing must not hide the headline
             rows[name] = {"error": str(e)[:200]}
+    try:
+        cfg = inputs.WORKLOADS["mamba130m_layer"]
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(cfg)
+        gen = torch.Generator(device=dev).manual_seed(7)
+        cw = torch.randn(cfg.d_inner, 4, generator=gen, device=dev) * 0.5
+        cb = torch.randn(cfg.d_inner, generator=gen, device=dev) * 0.1
+        yb = torch.empty_like(g["u"])
+        ls = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+
+        def fn():
+            abi.conv_selective_scan_fwd(g["u"], cw, cb, g["delta"], g["A"], g["B"], g["C"],
+                                        g["D"], g["z"], g["delta_bias"], y=yb, last_state=ls)
+        times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+        ms = statistics.mean(times)
+        nbytes = selective_bytes(cfg)  # x replaces u; the conv taps are negligible
+        rows["conv_scan_mamba130m_layer"] = {
+            "ms_per_call": round(ms, 4), "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+            "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_call": nl / 5,
+            "note": "causal conv1d (width 4) + SiLU fused in front of the scan"}
+        del g, yb
+    except Exception as e:
+        rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
     return rows
 

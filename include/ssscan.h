@@ -174,6 +174,25 @@ int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss
                                ss_tensor* last_state, void* stream);
 
 /*
+ * The conv branch feeding the scan, fused: u = silu(causal_conv1d(x)) is
+ * computed on chip and never written to memory, then scanned as in
+ * ss_selective_scan_fwd (page "Mamba模型笔记" §4.3: the SSM branch passes a
+ * local convolution first; 0539edu paper talk §3.1: causal-conv1d, width
+ * d_conv = 4).  For every b, d, t:
+ *   u[b,d,t] = silu(conv_bias[d] + sum_{k<W} conv_weight[d,k] * x[b,d,t-W+1+k])
+ * with x = 0 before t = 0.  x (Bsz, D, L) has the dtype and layout rules of u;
+ * conv_weight (D, W) f32 with 1 <= W <= 4; conv_bias (D) f32 or NULL.  The
+ * other arguments are those of ss_selective_scan_fwd; the D skip and the gate
+ * use u.  Starts from a zero state and zero conv history.
+ */
+int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
+                               const ss_tensor* conv_bias, const ss_tensor* delta,
+                               const ss_tensor* A, const ss_tensor* B, const ss_tensor* C,
+                               const ss_tensor* D, const ss_tensor* z,
+                               const ss_tensor* delta_bias, int softplus, ss_tensor* y,
+                               ss_tensor* last_state, void* stream);
+
+/*
  * One recurrent step (decoding one token), updating the state in place
  * (0539edu paper talk §4.3: the step function of the recurrent form; the
  * state is the only thing carried between tokens).

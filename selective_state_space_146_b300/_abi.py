@@ -22,6 +22,7 @@ STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_
           -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
 EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chunk_scan_fwd",
            "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
+           "ss_conv_selective_scan_fwd",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version")
 
@@ -64,6 +65,8 @@ def load(path: str | None = None):
     lib.ss_ssd_chunk_scan_fwd_init.restype = i
     lib.ss_selective_state_update.argtypes = [T, T, T, T, T, T, T, T, T, i, T, vp]
     lib.ss_selective_state_update.restype = i
+    lib.ss_conv_selective_scan_fwd.argtypes = [T, T, T, T, T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_conv_selective_scan_fwd.restype = i
     lib.ss_ssd_state_update.argtypes = [T, T, T, T, T, T, T, T, vp]
     lib.ss_ssd_state_update.restype = i
     lib.ss_status_string.argtypes = [i]
@@ -184,6 +187,25 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_stat
                                                _stream_ptr(stream))
     if rc != 0:
         raise SSError(rc, "ss_ssd_chunk_scan_fwd")
+    return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def conv_selective_scan_fwd(x, conv_weight, conv_bias, delta, A, B, C, D=None, z=None,
+                            delta_bias=None, softplus=True, y=None, last_state=None,
+                            return_last_state=False, stream=None):
+    """Fused causal conv1d + SiLU + selective scan (ss_conv_selective_scan_fwd).
+    x: (batch, d_inner, L); conv_weight: (d_inner, W <= 4) f32; conv_bias (d_inner,)."""
+    if y is None:
+        y = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if last_state is None and return_last_state:
+        last_state = torch.empty(x.shape[0], x.shape[1], A.shape[1], dtype=torch.float32,
+                                 device=x.device)
+    ts = [describe(t) for t in (x, conv_weight, conv_bias, delta, A, B, C, D, z, delta_bias)]
+    rc = load().ss_conv_selective_scan_fwd(*[_ref(t) for t in ts], int(bool(softplus)),
+                                           _ref(describe(y)), _ref(describe(last_state)),
+                                           _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_conv_selective_scan_fwd")
     return (y, last_state) if (return_last_state or last_state is not None) else y
 
 

@@ -320,6 +320,36 @@ int ss_selective_scan_fwd_init(const ss_tensor* u, const ss_tensor* delta, const
     return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
 }
 
+int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
+                               const ss_tensor* conv_bias, const ss_tensor* delta,
+                               const ss_tensor* A, const ss_tensor* B, const ss_tensor* C,
+                               const ss_tensor* D, const ss_tensor* z,
+                               const ss_tensor* delta_bias, int softplus, ss_tensor* y,
+                               ss_tensor* last_state, void* stream) {
+    SS_TRY(check_tensor(conv_weight, 2));
+    if (conv_bias) SS_TRY(check_tensor(conv_bias, 1));
+    if (conv_weight->dtype != SS_F32 || (conv_bias && conv_bias->dtype != SS_F32))
+        return SS_ERR_DTYPE;
+    ScanArgs a{};
+    bool nothing = false;
+    SS_TRY(selective_args(x, delta, A, B, C, D, z, delta_bias, softplus, nullptr, y, last_state,
+                          &a, &nothing));
+    const int64_t W = conv_weight->shape[1];
+    if (conv_weight->shape[0] != x->shape[1] || (conv_bias && conv_bias->shape[0] != x->shape[1]))
+        return SS_ERR_SHAPE;
+    if (W < 1) return SS_ERR_SHAPE;
+    if (W > 4) return SS_ERR_UNSUPPORTED;
+    if (nothing) return SS_OK;
+    a.cw = static_cast<const float*>(conv_weight->data);
+    a.scw_d = conv_weight->stride[0]; a.scw_k = conv_weight->stride[1];
+    if (conv_bias) { a.cb = static_cast<const float*>(conv_bias->data); a.scb = conv_bias->stride[0]; }
+    a.cwidth = (int)W;
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+}
+
 int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                           const ss_tensor* z, const ss_tensor* delta_bias, int softplus,

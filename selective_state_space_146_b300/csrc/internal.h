@@ -21,6 +21,10 @@ struct ScanArgs {
     const float* bias; int64_t sbias;
     float* last; int64_t sl_b, sl_d, sl_n;
     const float* h0; int64_t sh_b, sh_d, sh_n;  // initial state, may be null
+    // causal conv1d + SiLU in front of the scan (u holds its input x); cw null = off
+    const float* cw; int64_t scw_d, scw_k;
+    const float* cb; int64_t scb;
+    int cwidth;
     int softplus;
     unsigned* err;  // device error word
 };

@@ -68,8 +68,20 @@ __global__ void __launch_bounds__(128) scan_general(ScanArgs a) {
     T* y = static_cast<T*>(a.y) + b * a.sy_b + d * a.sy_d;
     const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b;
     const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b;
+    // conv in front (optional): u = silu(bias + sum_k w[k] x[t - W + 1 + k])
+    float wk[4] = {0.f, 0.f, 0.f, 0.f}, xh[3] = {0.f, 0.f, 0.f}, cbias = 0.f;
+    if (a.cw) {
+        for (int k = 0; k < a.cwidth; ++k) wk[4 - a.cwidth + k] = a.cw[d * a.scw_d + k * a.scw_k];
+        cbias = a.cb ? a.cb[d * a.scb] : 0.f;
+    }
     for (int t = 0; t < a.L; ++t) {
-        const float uu = Elem<T>::to_f(u[t * a.su_t]);
+        float uu = Elem<T>::to_f(u[t * a.su_t]);
+        if (a.cw) {
+            const float pre = fmaf(wk[0], xh[0], fmaf(wk[1], xh[1], fmaf(wk[2], xh[2],
+                                   fmaf(wk[3], uu, cbias))));
+            xh[0] = xh[1]; xh[1] = xh[2]; xh[2] = uu;
+            uu = pre * sigmoid_accurate(pre);
+        }
         float dd = Elem<T>::to_f(dl[t * a.sdl_t]) + bd;
         if (a.softplus) dd = softplus_f(dd);
         const float du = dd * uu;
@@ -110,6 +122,11 @@ struct FastParams {
     float* last; int64_t sl_b, sl_d, sl_n;
     const float* h0; int64_t sh_b, sh_d, sh_n;  // initial state, may be null
     void* y; int64_t sy_b, sy_d;  // y rows are contiguous in t
+    // causal conv1d + SiLU in front of the scan (CONV kernels): u = silu(conv(x))
+    const void* x; int64_t sx_b, sx_d;  // x rows contiguous in t (the "u" tensor map)
+    const float* cw; int64_t scw_d, scw_k;  // taps (D, W), W <= 4
+    const float* cb; int64_t scb;           // bias (D), may be null
+    int cwidth;
     float* summ;    // [nseg-1][Bsz*D][2][N]: prod of decays, end state from zero
     int softplus;
     unsigned* err;
@@ -225,6 +242,30 @@ __device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
     }
 }
 
+// Store K floats as T (K * sizeof(T) in {4, 8, 16} bytes) to shared memory.
+template <typename T, int K>
+__device__ __forceinline__ void sts_elems(uint32_t a, const float* v) {
+    constexpr int BYTES = K * (int)sizeof(T);
+    uint32_t w[4];
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < K / 2; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i) w[i] = __float_as_uint(v[i]);
+    }
+    if constexpr (BYTES == 16)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]) : "memory");
+    else if constexpr (BYTES == 8)
+        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(w[0]), "r"(w[1]) : "memory");
+    else
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(w[0]) : "memory");
+}
+
 // Store K floats as T to global memory: one aligned vector store, or (in the
 // last chunk of the sequence) element by element up to `limit` elements.
 template <typename T, int K>
@@ -270,7 +311,7 @@ __device__ __forceinline__ void reduce_half(const float* v, float* out, bool upp
     }
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV>
 __global__ void __launch_bounds__(FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>::NTHREADS, 3)
 scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -337,13 +378,54 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     }
 
     if (warp == 1) {
-        // ---------------- B|C table ----------------
+        // ---------------- B|C table (and, for CONV, u = silu(conv(x))) ----------------
+        // CONV: lane c owns channel row c of the tile and slides the causal
+        // window along t, carrying the last W-1 inputs across tiles.
+        [[maybe_unused]] float xh[3] = {0.f, 0.f, 0.f};  // x[t-3], x[t-2], x[t-1]
+        [[maybe_unused]] float wk[4] = {0.f, 0.f, 0.f, 0.f};
+        [[maybe_unused]] float cbias = 0.f;
+        if constexpr (CONV) {
+            static_assert(DT <= 32, "one conv lane per channel row");
+            const int dc = d0 + lane;
+            if (lane < DT && dc < p.D) {
+                // taps right-aligned: wk[3] multiplies x[t], wk[4-W] x[t-W+1]
+                for (int k = 0; k < p.cwidth; ++k)
+                    wk[4 - p.cwidth + k] = p.cw[(int64_t)dc * p.scw_d + k * p.scw_k];
+                cbias = p.cb ? p.cb[(int64_t)dc * p.scb] : 0.f;
+                const T* xr = static_cast<const T*>(p.x) + (int64_t)b * p.sx_b + (int64_t)dc * p.sx_d;
+                for (int j = 0; j < 3; ++j) {
+                    const int t = tbeg - 3 + j;
+                    xh[j] = t >= 0 ? Elem<T>::to_f(xr[t]) : 0.f;
+                }
+            }
+        }
         for (int k = 0; k < ntiles; ++k) {
             const int s = k % STAGES;
             if (!mbar_wait(&raw[s], (k / STAGES) & 1, p.err)) break;
             const uint32_t st = smem_u32(stage(s));
             convert_bc<T, Cfg::LOAD_C>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC,
                                        lane);
+            if constexpr (CONV) {
+                if (!mbar_wait(&full[s], (k / STAGES) & 1, p.err)) break;
+                if (lane < DT) {
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::CHUNKS; ++c) {
+                        const uint32_t a = st + swz(lane, c);
+                        float xv[VEC];
+                        lds_elems<T, VEC>(a, xv);
+                        float uv[VEC];
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) {
+                            float pre = fmaf(wk[0], xh[0], fmaf(wk[1], xh[1], fmaf(wk[2], xh[2],
+                                             fmaf(wk[3], xv[i], cbias))));
+                            uv[i] = pre * sigmoid_accurate(pre);
+                            xh[0] = xh[1]; xh[1] = xh[2]; xh[2] = xv[i];
+                        }
+                        sts_elems<T, VEC>(a, uv);
+                    }
+                }
+                fence_proxy_async_smem();  // the stage is later refilled by TMA
+            }
             mbar_arrive(&table[s]);
         }
         return;
@@ -596,11 +678,11 @@ static bool fast_layout_ok(const ScanArgs& a) {
            a.L < (1 << 30);
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV>
 static cudaError_t launch_fast_kernel(const CUtensorMap* maps, const FastParams& fp, dim3 grid,
                                       cudaStream_t st) {
     using Cfg = FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
-    auto kern = scan_fast<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
+    auto kern = scan_fast<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY, CONV>;
     static bool attr_set[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -624,7 +706,7 @@ static cudaError_t launch_fast_kernel(const CUtensorMap* maps, const FastParams&
 // channels; three stages fit three CTAs in one SM's shared memory.
 constexpr int kStages = 3;
 
-template <typename T, int NSPLIT, int kCWarps>
+template <typename T, int NSPLIT, int kCWarps, bool CONV>
 static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
     using CfgM = FastCfg<T, NSPLIT, kCWarps, kStages, true, false>;
     constexpr int TT = CfgM::TT, DT = CfgM::DT;
@@ -636,6 +718,9 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     fp.last = a.last; fp.sl_b = a.sl_b; fp.sl_d = a.sl_d; fp.sl_n = a.sl_n;
     fp.y = a.y; fp.sy_b = a.sy_b; fp.sy_d = a.sy_d;
     fp.h0 = a.h0; fp.sh_b = a.sh_b; fp.sh_d = a.sh_d; fp.sh_n = a.sh_n;
+    fp.x = a.u; fp.sx_b = a.su_b; fp.sx_d = a.su_d;
+    fp.cw = a.cw; fp.scw_d = a.scw_d; fp.scw_k = a.scw_k; fp.cb = a.cb; fp.scb = a.scb;
+    fp.cwidth = a.cwidth;
     fp.softplus = a.softplus; fp.err = a.err;
 
     // Segments: enough CTAs to give every SM several consumer warps.
@@ -672,16 +757,16 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
         summ = scratch.alloc(bytes, st, scratch.ctx);
         if (!summ) return SS_ERR_ALLOC;
         fp.summ = static_cast<float*>(summ);
-        cudaError_t e = launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, true>(
+        cudaError_t e = launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, true, CONV>(
             maps, fp, dim3((unsigned)ctas, nseg - 1), st);
         if (e != cudaSuccess) {
             scratch.release(summ, st, scratch.ctx);
             return SS_ERR_LAUNCH;
         }
     }
-    cudaError_t e = a.z ? launch_fast_kernel<T, NSPLIT, kCWarps, kStages, true, false>(
+    cudaError_t e = a.z ? launch_fast_kernel<T, NSPLIT, kCWarps, kStages, true, false, CONV>(
                               maps, fp, dim3((unsigned)ctas, nseg), st)
-                        : launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, false>(
+                        : launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, false, CONV>(
                               maps, fp, dim3((unsigned)ctas, nseg), st);
     if (summ) scratch.release(summ, st, scratch.ctx);
     return e == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
@@ -726,15 +811,27 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
         int split = 1;
         while (split < 4 && ch * split < want) split *= 2;
         if (force == 1 || force == 2 || force == 4 || (force == 8 && bf)) split = force;
-        if (bf) {
-            if (split == 1) return run_fast<__nv_bfloat16, 1, 2>(a, st, scratch);
-            if (split == 2) return run_fast<__nv_bfloat16, 2, 2>(a, st, scratch);
-            if (split == 4) return run_fast<__nv_bfloat16, 4, 4>(a, st, scratch);
-            return run_fast<__nv_bfloat16, 8, 8>(a, st, scratch);
+        if (a.cw) {
+            // conv in front: the conversion warp owns one channel row per lane
+            if (split == 8) split = 4;
+            if (bf) {
+                if (split == 1) return run_fast<__nv_bfloat16, 1, 1, true>(a, st, scratch);
+                if (split == 2) return run_fast<__nv_bfloat16, 2, 2, true>(a, st, scratch);
+                return run_fast<__nv_bfloat16, 4, 4, true>(a, st, scratch);
+            }
+            if (split == 1) return run_fast<float, 1, 1, true>(a, st, scratch);
+            if (split == 2) return run_fast<float, 2, 2, true>(a, st, scratch);
+            return run_fast<float, 4, 4, true>(a, st, scratch);
         }
-        if (split == 1) return run_fast<float, 1, 2>(a, st, scratch);
-        if (split == 2) return run_fast<float, 2, 2>(a, st, scratch);
-        return run_fast<float, 4, 4>(a, st, scratch);
+        if (bf) {
+            if (split == 1) return run_fast<__nv_bfloat16, 1, 2, false>(a, st, scratch);
+            if (split == 2) return run_fast<__nv_bfloat16, 2, 2, false>(a, st, scratch);
+            if (split == 4) return run_fast<__nv_bfloat16, 4, 4, false>(a, st, scratch);
+            return run_fast<__nv_bfloat16, 8, 8, false>(a, st, scratch);
+        }
+        if (split == 1) return run_fast<float, 1, 2, false>(a, st, scratch);
+        if (split == 2) return run_fast<float, 2, 2, false>(a, st, scratch);
+        return run_fast<float, 4, 4, false>(a, st, scratch);
     }
     return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
 }
