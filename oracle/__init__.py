@@ -51,6 +51,8 @@ def _bind(path):
     lib.oracle_threads.restype = ip
     lib.oracle_causal_conv1d_silu.argtypes = [i64] * 4 + [dp] * 4 + [ip]
     lib.oracle_causal_conv1d_silu.restype = ip
+    lib.oracle_selective_scan_bwd.argtypes = [i64] * 4 + [dp] * 8 + [ip] + [dp] * 9
+    lib.oracle_selective_scan_bwd.restype = ip
     return lib
 
 
@@ -77,6 +79,9 @@ class _Bound:
 
     def causal_conv1d_silu(self, *a, **k):
         return causal_conv1d_silu(*a, _lib=self._lib, **k)
+
+    def selective_scan_bwd(self, *a, **k):
+        return selective_scan_bwd(*a, _lib=self._lib, **k)
 
 
 def load_library(path: str) -> _Bound:
@@ -174,3 +179,26 @@ def conv_selective_scan(x, conv_w, conv_bias, delta, A, B, C, D=None, z=None, de
     u = causal_conv1d_silu(x, conv_w, conv_bias, nthreads=nthreads)
     return selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus=softplus, h0=h0,
                           nthreads=nthreads)
+
+
+def selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, softplus=True, _lib=None):
+    """Oracle of the selective scan's backward pass.  Returns a dict of float64
+    arrays: du, ddelta, dz (like u), dA (like A), dB, dC (like B), dD,
+    ddelta_bias (like D); entries for absent optional inputs are None."""
+    u, delta, A, B, C, dout = (_f64(t) for t in (u, delta, A, B, C, dout))
+    D, z, delta_bias = _f64(D), _f64(z), _f64(delta_bias)
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    out = {"du": np.empty_like(u), "ddelta": np.empty_like(u), "dA": np.empty_like(A),
+           "dB": np.empty_like(B), "dC": np.empty_like(C),
+           "dD": None if D is None else np.empty_like(D),
+           "dz": None if z is None else np.empty_like(z),
+           "ddelta_bias": None if delta_bias is None else np.empty_like(delta_bias)}
+    rc = (_lib or _load()).oracle_selective_scan_bwd(
+        Bsz, Dch, N, L, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(softplus)), _ptr(dout), _ptr(out["du"]), _ptr(out["ddelta"]),
+        _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+        _ptr(out["ddelta_bias"]))
+    if rc != 0:
+        raise ValueError(f"oracle_selective_scan_bwd failed (rc={rc})")
+    return out

@@ -217,3 +217,94 @@ int oracle_causal_conv1d_silu(int64_t Bsz, int64_t D, int64_t L, int64_t W, cons
     }
     return 0;
 }
+
+/*
+ * Backward (reverse-mode derivative) of the selective scan above, one unit
+ * (b, d) at a time, in two sweeps: forward to keep every state h_t, then
+ * backward in t with the adjoint state g_n = dL/dh_t[n].  With out_t the
+ * scan's output and dout_t the incoming gradient:
+ *
+ *   pre_t   = sum_n C[n,t] h_t[n] + D u_t            (output before the gate)
+ *   dz_t    = dout_t * pre_t * silu'(z_t),  dpre_t = dout_t * silu(z_t)
+ *   g_n     = C[n,t] dpre_t + abar_{t+1}[n] g_n      (adjoint, from t = L-1 down)
+ *   dC[n,t] += dpre_t h_t[n]            dD += dpre_t u_t
+ *   dB[n,t] += g_n dl_t u_t             du_t = D dpre_t + sum_n g_n dl_t B[n,t]
+ *   dA[n]   += g_n h_{t-1}[n] abar_t[n] dl_t
+ *   ddl_t   = sum_n g_n (h_{t-1}[n] abar_t[n] A[n] + B[n,t] u_t)
+ *   ddelta_t = ddl_t * sigmoid(delta_t + bias)  (softplus' ; identity if off)
+ *   dbias  += ddelta_t
+ *
+ * dB, dC are summed over all channels of a batch row (B and C are shared),
+ * dA, dD, dbias over batch rows.  All output arrays are overwritten.
+ */
+int oracle_selective_scan_bwd(int64_t Bsz, int64_t D, int64_t N, int64_t L,
+                              const double* u, const double* delta, const double* A,
+                              const double* Bm, const double* Cm, const double* Dv,
+                              const double* z, const double* delta_bias, int softplus,
+                              const double* dout, double* du, double* ddelta, double* dA,
+                              double* dB, double* dC, double* dD, double* dz,
+                              double* ddelta_bias) {
+    if (Bsz < 0 || D < 0 || N < 1 || L < 0) return -1;
+    for (int64_t i = 0; i < D * N; ++i) dA[i] = 0.0;
+    for (int64_t i = 0; i < Bsz * N * L; ++i) { dB[i] = 0.0; dC[i] = 0.0; }
+    if (dD) for (int64_t i = 0; i < D; ++i) dD[i] = 0.0;
+    if (ddelta_bias) for (int64_t i = 0; i < D; ++i) ddelta_bias[i] = 0.0;
+    double* hs = (double*)malloc((size_t)((L + 1) * N) * sizeof(double));
+    double* dls = (double*)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    double* g = (double*)malloc((size_t)N * sizeof(double));
+    if (!hs || !dls || !g) { free(hs); free(dls); free(g); return -2; }
+    for (int64_t b = 0; b < Bsz; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            const double* ur = u + (b * D + d) * L;
+            const double* dr = delta + (b * D + d) * L;
+            const double* zr = z ? z + (b * D + d) * L : NULL;
+            const double* gr = dout + (b * D + d) * L;
+            /* forward sweep: h_0 .. h_L (hs[t+1] is the state after step t) */
+            for (int64_t n = 0; n < N; ++n) hs[n] = 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                double dl = dr[t] + (delta_bias ? delta_bias[d] : 0.0);
+                if (softplus) dl = softplus_d(dl);
+                dls[t] = dl;
+                for (int64_t n = 0; n < N; ++n)
+                    hs[(t + 1) * N + n] = exp(dl * A[d * N + n]) * hs[t * N + n] +
+                                          dl * Bm[(b * N + n) * L + t] * ur[t];
+            }
+            /* backward sweep */
+            for (int64_t n = 0; n < N; ++n) g[n] = 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                double dl = dls[t];
+                double pre = (Dv ? Dv[d] * ur[t] : 0.0);
+                for (int64_t n = 0; n < N; ++n) pre += Cm[(b * N + n) * L + t] * hs[(t + 1) * N + n];
+                double dpre = gr[t];
+                if (zr) {
+                    double sg = 1.0 / (1.0 + exp(-zr[t]));
+                    dpre = gr[t] * zr[t] * sg;
+                    dz[(b * D + d) * L + t] = gr[t] * pre * (sg + zr[t] * sg * (1.0 - sg));
+                }
+                if (Dv) dD[d] += dpre * ur[t];
+                double ddl = 0.0, dut = Dv ? Dv[d] * dpre : 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double c = Cm[(b * N + n) * L + t], bb = Bm[(b * N + n) * L + t];
+                    double abar = exp(dl * A[d * N + n]);
+                    /* g_n currently holds abar_{t+1} g_{t+1}; add this step's readout */
+                    g[n] += c * dpre;
+                    dC[(b * N + n) * L + t] += dpre * hs[(t + 1) * N + n];
+                    dB[(b * N + n) * L + t] += g[n] * dl * ur[t];
+                    dut += g[n] * dl * bb;
+                    dA[d * N + n] += g[n] * hs[t * N + n] * abar * dl;
+                    ddl += g[n] * (hs[t * N + n] * abar * A[d * N + n] + bb * ur[t]);
+                    g[n] *= abar; /* carry to step t-1 */
+                }
+                du[(b * D + d) * L + t] = dut;
+                double x = dr[t] + (delta_bias ? delta_bias[d] : 0.0);
+                double dx = softplus ? ddl / (1.0 + exp(-x)) : ddl;
+                ddelta[(b * D + d) * L + t] = dx;
+                if (ddelta_bias) ddelta_bias[d] += dx;
+            }
+        }
+    }
+    free(hs);
+    free(dls);
+    free(g);
+    return 0;
+}

@@ -383,6 +383,12 @@ _MUTANTS = {
     "conv_taps_reversed": ("int64_t s = t - (W - 1) + k;", "int64_t s = t - k;"),
     "conv_bias_dropped": ("double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
     "conv_no_silu": ("ur[t] = pre / (1.0 + exp(-pre));", "ur[t] = pre;"),
+    "bwd_no_adjoint_carry": ("g[n] *= abar; /* carry to step t-1 */", ""),
+    "bwd_dz_missing_term": ("(sg + zr[t] * sg * (1.0 - sg))", "(sg)"),
+    "bwd_dA_wrong_state": ("dA[d * N + n] += g[n] * hs[t * N + n] * abar * dl;",
+                           "dA[d * N + n] += g[n] * hs[(t + 1) * N + n] * abar * dl;"),
+    "bwd_softplus_chain_dropped": ("double dx = softplus ? ddl / (1.0 + exp(-x)) : ddl;",
+                                   "double dx = ddl;"),
 }
 
 
@@ -419,6 +425,33 @@ def _pins_pass(lib):
         uc = lib.causal_conv1d_silu(xc, wc, bc)
         if not np.allclose(uc, _conv_silu_by_numpy(xc, wc, bc), rtol=1e-12, atol=1e-13):
             return False
+        return _bwd_matches_finite_differences(lib, seed=17)
+    except ValueError:
+        return False
+
+
+def _bwd_matches_finite_differences(lib, seed, Bsz=2, Dch=3, N=4, L=7):
+    """Directional derivatives of sum(dout * out) by central differences of
+    the forward oracle, against the backward oracle, for every input."""
+    try:
+        rng = np.random.default_rng(seed)
+        u, delta, A, Bm, Cm, D, z, db = _rand_case(rng, Bsz, Dch, N, L)
+        dout = rng.standard_normal(u.shape)
+        grads = lib.selective_scan_bwd(u, delta, A, Bm, Cm, D, z, db, dout, softplus=True)
+        args = dict(u=u, delta=delta, A=A, B=Bm, C=Cm, D=D, z=z, delta_bias=db)
+        names = dict(u="du", delta="ddelta", A="dA", B="dB", C="dC", D="dD", z="dz",
+                     delta_bias="ddelta_bias")
+        eps = 1e-6
+        for k, gname in names.items():
+            v = rng.standard_normal(args[k].shape)
+            plus = dict(args); plus[k] = args[k] + eps * v
+            minus = dict(args); minus[k] = args[k] - eps * v
+            yp, _ = lib.selective_scan(**plus, softplus=True)
+            ym, _ = lib.selective_scan(**minus, softplus=True)
+            fd = float(np.sum(dout * (yp - ym)) / (2 * eps))
+            an = float(np.sum(grads[gname] * v))
+            if not abs(fd - an) <= 1e-6 * max(1.0, abs(fd)):
+                return False
         return True
     except ValueError:
         return False
@@ -426,6 +459,32 @@ def _pins_pass(lib):
 
 def test_pins_pass_on_the_oracle():
     assert _pins_pass(oracle)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_backward_matches_finite_differences(seed):
+    assert _bwd_matches_finite_differences(oracle, seed)
+
+
+def test_backward_without_optional_inputs():
+    """No gate, no skip, no bias, softplus off: the remaining gradients still
+    match finite differences."""
+    rng = np.random.default_rng(5)
+    u, delta, A, Bm, Cm, _, _, _ = _rand_case(rng, 1, 2, 3, 6, gate=False, skip=False, bias=False)
+    dout = rng.standard_normal(u.shape)
+    g = oracle.selective_scan_bwd(u, delta, A, Bm, Cm, None, None, None, dout, softplus=False)
+    assert g["dz"] is None and g["dD"] is None and g["ddelta_bias"] is None
+    eps = 1e-6
+    for k, arr, gn in (("u", u, "du"), ("delta", delta, "ddelta"), ("A", A, "dA"),
+                       ("B", Bm, "dB"), ("C", Cm, "dC")):
+        v = rng.standard_normal(arr.shape)
+        args = dict(u=u, delta=delta, A=A, B=Bm, C=Cm)
+        ap = dict(args); ap[k] = arr + eps * v
+        am = dict(args); am[k] = arr - eps * v
+        yp, _ = oracle.selective_scan(**ap, softplus=False)
+        ym, _ = oracle.selective_scan(**am, softplus=False)
+        fd = np.sum(dout * (yp - ym)) / (2 * eps)
+        assert abs(fd - np.sum(g[gn] * v)) <= 1e-6 * max(1.0, abs(fd)), k
 
 
 @pytest.mark.parametrize("name", sorted(_MUTANTS))
