@@ -193,6 +193,41 @@ int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
                                ss_tensor* last_state, void* stream);
 
 /*
+ * Backward of the selective scan (training): given dout, the gradient of a
+ * loss with respect to the y of ss_selective_scan_fwd (same inputs, zero
+ * initial state), writes the gradients with respect to every input
+ * (0539edu paper talk §5.4: training recomputes the states of the scan
+ * instead of keeping one per step; the forward it differentiates is that of
+ * ss_selective_scan_fwd, "Mamba模型笔记" §2.2 and §4.3).
+ *
+ * With pre_t = sum_n C[b,n,t] h_t[n] + D[d] u_t and the adjoint state
+ * g_t[n] = C[b,n,t] dpre_t + abar_{t+1}[n] g_{t+1}[n]:
+ *   dz     = dout * pre * silu'(z);       dpre = dout * silu(z)  (dout if z NULL)
+ *   du     = D dpre + sum_n g dl B;       dD   = sum_{b,t} dpre u
+ *   dA     = sum_{b,t} g h_{t-1} abar dl
+ *   dB     = sum_d g dl u;                dC   = sum_d dpre h_t
+ *   ddelta = softplus'(delta + bias) * sum_n g (h_{t-1} abar A + B u)
+ *   ddelta_bias = sum_{b,t} ddelta
+ *
+ * Inputs: as in ss_selective_scan_fwd; dout (Bsz, D, L) dtype T.
+ * Outputs (all overwritten, none may overlap an input or another output):
+ *   du, ddelta, dz  (Bsz, D, L) dtype T, any strides (dz iff z given)
+ *   dA (D, N), dB, dC (Bsz, N, L), dD (D) iff D given,
+ *   ddelta_bias (D) iff delta_bias given -- f32, contiguous (else
+ *   SS_ERR_UNSUPPORTED).
+ * N <= 16 (else SS_ERR_UNSUPPORTED).  The sums over channels, batch rows and
+ * steps are accumulated in f32 in an order that is not fixed, so results can
+ * differ by rounding from call to call.  Scratch of Bsz*D*(ceil(L/32)+1)*64
+ * bytes is taken stream-ordered from the device's default pool.
+ */
+int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          const ss_tensor* dout, ss_tensor* du, ss_tensor* ddelta, ss_tensor* dA,
+                          ss_tensor* dB, ss_tensor* dC, ss_tensor* dD, ss_tensor* dz,
+                          ss_tensor* ddelta_bias, void* stream);
+
+/*
  * One recurrent step (decoding one token), updating the state in place
  * (0539edu paper talk §4.3: the step function of the recurrent form; the
  * state is the only thing carried between tokens).

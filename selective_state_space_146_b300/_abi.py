@@ -22,7 +22,7 @@ STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_
           -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
 EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chunk_scan_fwd",
            "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
-           "ss_conv_selective_scan_fwd",
+           "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version")
 
@@ -67,6 +67,9 @@ def load(path: str | None = None):
     lib.ss_selective_state_update.restype = i
     lib.ss_conv_selective_scan_fwd.argtypes = [T, T, T, T, T, T, T, T, T, T, i, T, T, vp]
     lib.ss_conv_selective_scan_fwd.restype = i
+    lib.ss_selective_scan_bwd.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, T, T, T, T, T, T,
+                                          vp]
+    lib.ss_selective_scan_bwd.restype = i
     lib.ss_ssd_state_update.argtypes = [T, T, T, T, T, T, T, T, vp]
     lib.ss_ssd_state_update.restype = i
     lib.ss_status_string.argtypes = [i]
@@ -207,6 +210,31 @@ def conv_selective_scan_fwd(x, conv_weight, conv_bias, delta, A, B, C, D=None, z
     if rc != 0:
         raise SSError(rc, "ss_conv_selective_scan_fwd")
     return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, softplus=True, stream=None):
+    """Gradients of the selective scan (ss_selective_scan_bwd) for the
+    incoming gradient dout of y.  Returns a dict with du, ddelta, dz (dtype of
+    u), dA, dB, dC, dD, ddelta_bias (f32); the optional ones are None when the
+    matching input is None."""
+    f32 = dict(dtype=torch.float32, device=u.device)
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    g = dict(du=torch.empty_like(u, memory_format=torch.contiguous_format),
+             ddelta=torch.empty_like(u, memory_format=torch.contiguous_format),
+             dz=None if z is None else torch.empty_like(u, memory_format=torch.contiguous_format),
+             dA=torch.empty(Dch, N, **f32), dB=torch.empty(Bsz, N, L, **f32),
+             dC=torch.empty(Bsz, N, L, **f32),
+             dD=None if D is None else torch.empty(Dch, **f32),
+             ddelta_bias=None if delta_bias is None else torch.empty(Dch, **f32))
+    ins = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    outs = [describe(g[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")]
+    rc = load().ss_selective_scan_bwd(*[_ref(t) for t in ins], int(bool(softplus)),
+                                      _ref(describe(dout)), *[_ref(t) for t in outs],
+                                      _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_bwd")
+    return g
 
 
 def selective_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,

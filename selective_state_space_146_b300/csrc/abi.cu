@@ -378,6 +378,84 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
     return rc;
 }
 
+static bool is_contiguous(const ss_tensor* t) {
+    for (int i = 0; i < t->ndim; ++i)
+        if (t->shape[i] == 0) return true;  // empty: nothing is addressed
+    int64_t expect = 1;
+    for (int i = t->ndim - 1; i >= 0; --i) {
+        if (t->shape[i] != 1 && t->stride[i] != expect) return false;
+        expect *= t->shape[i];
+    }
+    return true;
+}
+
+// An fp32 gradient output: the given shape, contiguous.
+static int check_grad_f32(const ss_tensor* t, int ndim, const int64_t* shape) {
+    SS_TRY(check_tensor(t, ndim));
+    if (t->dtype != SS_F32) return SS_ERR_DTYPE;
+    for (int i = 0; i < ndim; ++i)
+        if (t->shape[i] != shape[i]) return SS_ERR_SHAPE;
+    if (!is_contiguous(t)) return SS_ERR_UNSUPPORTED;
+    return SS_OK;
+}
+
+int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          const ss_tensor* dout, ss_tensor* du, ss_tensor* ddelta, ss_tensor* dA,
+                          ss_tensor* dB, ss_tensor* dC, ss_tensor* dD, ss_tensor* dz,
+                          ss_tensor* ddelta_bias, void* stream) {
+    ScanArgs f{};
+    bool nothing = false;
+    // the forward inputs are checked as for the forward scan, dout in the place of y
+    SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr,
+                          const_cast<ss_tensor*>(dout), nullptr, &f, &nothing));
+    SS_TRY(check_tensor(du, 3));
+    SS_TRY(check_tensor(ddelta, 3));
+    if (!same_shape(du, u) || !same_shape(ddelta, u)) return SS_ERR_SHAPE;
+    if (du->dtype != u->dtype || ddelta->dtype != u->dtype) return SS_ERR_DTYPE;
+    if (!z != !dz || !D != !dD || !delta_bias != !ddelta_bias) return SS_ERR_INVALID_ARG;
+    if (dz) {
+        SS_TRY(check_tensor(dz, 3));
+        if (!same_shape(dz, u)) return SS_ERR_SHAPE;
+        if (dz->dtype != u->dtype) return SS_ERR_DTYPE;
+    }
+    const int64_t Bsz = u->shape[0], Dch = u->shape[1], L = u->shape[2], N = A->shape[1];
+    const int64_t sDN[2] = {Dch, N}, sBNL[3] = {Bsz, N, L}, sD1[1] = {Dch};
+    SS_TRY(check_grad_f32(dA, 2, sDN));
+    SS_TRY(check_grad_f32(dB, 3, sBNL));
+    SS_TRY(check_grad_f32(dC, 3, sBNL));
+    if (dD) SS_TRY(check_grad_f32(dD, 1, sD1));
+    if (ddelta_bias) SS_TRY(check_grad_f32(ddelta_bias, 1, sD1));
+    if (N > 16) return SS_ERR_UNSUPPORTED;
+
+    BwdArgs a{};
+    a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = u->dtype;
+    a.dA = static_cast<float*>(dA->data);
+    a.dB = static_cast<float*>(dB->data);
+    a.dC = static_cast<float*>(dC->data);
+    a.dD = dD ? static_cast<float*>(dD->data) : nullptr;
+    a.dbias = ddelta_bias ? static_cast<float*>(ddelta_bias->data) : nullptr;
+    if (!nothing) {  // else the launcher only zeroes the sums
+        a.u = f.u; a.su_b = f.su_b; a.su_d = f.su_d; a.su_t = f.su_t;
+        a.dl = f.dl; a.sdl_b = f.sdl_b; a.sdl_d = f.sdl_d; a.sdl_t = f.sdl_t;
+        a.z = f.z; a.sz_b = f.sz_b; a.sz_d = f.sz_d; a.sz_t = f.sz_t;
+        a.dout = f.y; a.sg_b = f.sy_b; a.sg_d = f.sy_d; a.sg_t = f.sy_t;
+        a.Bm = f.Bm; a.sB_b = f.sB_b; a.sB_n = f.sB_n; a.sB_t = f.sB_t;
+        a.Cm = f.Cm; a.sC_b = f.sC_b; a.sC_n = f.sC_n; a.sC_t = f.sC_t;
+        a.A = f.A; a.sA_d = f.sA_d; a.sA_n = f.sA_n;
+        a.Dv = f.Dv; a.sD = f.sD;
+        a.bias = f.bias; a.sbias = f.sbias;
+        a.softplus = softplus;
+        a.du = du->data; a.sdu_b = du->stride[0]; a.sdu_d = du->stride[1]; a.sdu_t = du->stride[2];
+        a.ddl = ddelta->data;
+        a.sddl_b = ddelta->stride[0]; a.sddl_d = ddelta->stride[1]; a.sddl_t = ddelta->stride[2];
+        if (dz) { a.dz = dz->data; a.sdz_b = dz->stride[0]; a.sdz_d = dz->stride[1]; a.sdz_t = dz->stride[2]; }
+    }
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    return launch_selective_bwd(a, static_cast<cudaStream_t>(stream), sc);
+}
+
 int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
                                const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                                int chunk, const ss_tensor* initial_state, ss_tensor* y,

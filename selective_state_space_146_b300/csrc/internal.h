@@ -74,6 +74,27 @@ struct SSDStepArgs {
     void* y; int64_t sy_b, sy_h, sy_p;
 };
 
+// Backward of the selective scan, element strides.  The fp32 gradients dA
+// (D, N), dB and dC (Bsz, N, L), dD and dbias (D) are contiguous.
+struct BwdArgs {
+    int Bsz, D, N, L, dtype;
+    const void* u;    int64_t su_b, su_d, su_t;
+    const void* dl;   int64_t sdl_b, sdl_d, sdl_t;
+    const void* z;    int64_t sz_b, sz_d, sz_t;
+    const void* dout; int64_t sg_b, sg_d, sg_t;
+    const void* Bm;   int64_t sB_b, sB_n, sB_t;
+    const void* Cm;   int64_t sC_b, sC_n, sC_t;
+    const float* A;   int64_t sA_d, sA_n;
+    const float* Dv;  int64_t sD;
+    const float* bias; int64_t sbias;
+    int softplus;
+    void* du;  int64_t sdu_b, sdu_d, sdu_t;
+    void* ddl; int64_t sddl_b, sddl_d, sddl_t;
+    void* dz;  int64_t sdz_b, sdz_d, sdz_t;
+    float *dA, *dB, *dC, *dD, *dbias;
+    float* ckpt;  // chunk-start states, filled by the kernel
+};
+
 // Scratch provider: either stream-ordered allocation or a fixed buffer.
 struct Scratch {
     void* (*alloc)(size_t bytes, cudaStream_t st, void* ctx);
@@ -83,6 +104,7 @@ struct Scratch {
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
+int launch_selective_bwd(const BwdArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_selective_step(const StepArgs& a, cudaStream_t st);
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);
 

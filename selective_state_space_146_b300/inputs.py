@@ -7,13 +7,14 @@ CUDA path and the fp64 oracle both take their inputs from here.
 Recipe (every workload):
   * one CPU ``torch.Generator`` per tensor, seeded ``seed * 1000 + k`` with a
     fixed tensor index k (u=0, delta=1, z=2, B=3, C=4, D=5, dt=6, A=7, x=8,
-    dt0=9);
+    dt0=9, dout=10);
   * normal draws are float32, then rounded to bfloat16 (round to nearest
     even) for bfloat16 workloads; the oracle reads the rounded values;
   * selective scan: u, z, B, C ~ N(0, 1); delta_raw ~ N(0, 0.1^2);
     A[d, n] = -(n + 1) (S4D-real); D ~ N(0, 1);
     delta_bias[d] = log(expm1(dt_d)) so that softplus(delta_bias) = dt_d, with
     dt_d log-uniform in [dt_min, dt_max];
+  * backward: the incoming gradient dout of y ~ N(0, 1), shaped like y;
   * SSD: x, B, C ~ N(0, 1); A_h = -exp(U[log 1, log 16]); D_h ~ N(0, 1);
     dt = softplus(N(0, 0.1^2) + log(expm1(dt0_h))), dt0_h log-uniform in
     [1e-3, 1e-1], computed in float64 and then rounded to the input dtype
@@ -30,7 +31,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-_IDX = dict(u=0, delta=1, z=2, B=3, C=4, D=5, dt=6, A=7, x=8, dt0=9)
+_IDX = dict(u=0, delta=1, z=2, B=3, C=4, D=5, dt=6, A=7, x=8, dt0=9, dout=10)
 
 
 @dataclass(frozen=True)
@@ -155,6 +156,12 @@ def selective_inputs(batch, d_inner, d_state, seqlen, dtype="bf16", *, gate=True
     else:
         out["delta_bias"] = None
     return out
+
+
+def grad_output(shape, dtype="bf16", seed=0):
+    """The incoming gradient of a scan's output (stands in for the gradient
+    the layers above would send back), as a CPU tensor."""
+    return _normal(tuple(shape), seed, "dout").to(_tdtype(dtype))
 
 
 def workload_selective_inputs(cfg: SelectiveConfig, seed=0):

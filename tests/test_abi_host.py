@@ -185,3 +185,47 @@ def test_initial_state_and_step_argument_errors(lib):
     Bg, Cg = FakeT((2, 3, 16)), FakeT((2, 3, 16))
     assert lib.ss_ssd_state_update(sst.ref, x.ref, dt.ref, Ah.ref, Bg.ref, Cg.ref, Dh.ref, yy.ref,
                                    None) == -2
+
+
+def _call_bwd(lib, a, g, softplus=1):
+    r = {k: (None if v is None else v.ref) for k, v in a.items()}
+    o = {k: (None if v is None else v.ref) for k, v in g.items()}
+    return lib.ss_selective_scan_bwd(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"], r["z"],
+                                     r["bias"], softplus, r["y"], o["du"], o["ddelta"], o["dA"],
+                                     o["dB"], o["dC"], o["dD"], o["dz"], o["dbias"], None)
+
+
+def _bwd_grads(Bsz=2, D=8, N=16, L=64, dt=_abi.SS_BF16):
+    f = _abi.SS_F32
+    return dict(du=FakeT((Bsz, D, L), dt), ddelta=FakeT((Bsz, D, L), dt), dz=FakeT((Bsz, D, L), dt),
+                dA=FakeT((D, N), f), dB=FakeT((Bsz, N, L), f), dC=FakeT((Bsz, N, L), f),
+                dD=FakeT((D,), f), dbias=FakeT((D,), f))
+
+
+def test_backward_argument_errors(lib):
+    a = _sel_args()  # "y" plays dout
+    assert _call_bwd(lib, a, dict(_bwd_grads(), dz=None)) == -1      # z given, dz missing
+    assert _call_bwd(lib, a, dict(_bwd_grads(), dD=None)) == -1
+    assert _call_bwd(lib, a, dict(_bwd_grads(), dbias=None)) == -1
+    assert _call_bwd(lib, a, dict(_bwd_grads(), du=None)) == -1
+    assert _call_bwd(lib, a, _bwd_grads(), softplus=3) == -1
+    g = _bwd_grads()
+    g["du"] = FakeT((2, 8, 63))
+    assert _call_bwd(lib, a, g) == -2
+    g = _bwd_grads()
+    g["ddelta"] = FakeT((2, 8, 64), _abi.SS_F32)
+    assert _call_bwd(lib, a, g) == -3
+    g = _bwd_grads()
+    g["dA"] = FakeT((8, 16), _abi.SS_BF16)
+    assert _call_bwd(lib, a, g) == -3
+    g = _bwd_grads()
+    g["dB"] = FakeT((2, 16, 65), _abi.SS_F32)
+    assert _call_bwd(lib, a, g) == -2
+    g = _bwd_grads()
+    g["dC"] = FakeT((2, 16, 64), _abi.SS_F32, stride=[1024, 1, 16])  # not contiguous
+    assert _call_bwd(lib, a, g) == -5
+    b = _sel_args(N=32)
+    assert _call_bwd(lib, b, _bwd_grads(N=32)) == -5                  # N > 16
+    b = _sel_args()
+    b["y"] = FakeT((2, 8, 64), _abi.SS_F32)                           # dout dtype
+    assert _call_bwd(lib, b, _bwd_grads()) == -3
