@@ -341,8 +341,92 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
         del g, yb
     except Exception as e:
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
+    rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
     return rows
+
+
+def backward_bytes(cfg):
+    """Algorithmic bytes of one backward call: u, delta, z, dout read and du,
+    ddelta, dz written once per channel-step; B, C read and dB, dC (f32)
+    written once per (batch, state, step); A, D, bias and their gradients."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    per_ch = (4 + 3) * e
+    bnl = cfg.batch * cfg.d_state * cfg.seqlen
+    return (cfg.channel_steps * per_ch + bnl * 2 * (e + 4)
+            + cfg.d_inner * (cfg.d_state + 2) * 8)
+
+
+def backward_rows(dev, torch, abi, inputs, hbm_peak, flush):
+    """The selective scan's backward at the Mamba-130M layer shape."""
+    rows = {}
+    try:
+        cfg = inputs.WORKLOADS["mamba130m_layer"]
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(cfg)
+            dout = inputs.grad_output((cfg.batch, cfg.d_inner, cfg.seqlen), cfg.dtype)
+
+        def fn():
+            abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], dout)
+        times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+        ms = statistics.mean(times)
+        nbytes = backward_bytes(cfg)
+        rows["bwd_mamba130m_layer"] = {
+            "ms_per_call": round(ms, 4), "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+            "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "launches_per_call": nl / 5, "algorithmic_bytes": nbytes,
+            "note": "all eight gradients; includes the memsets of the f32 sums and the "
+                    "checkpoint scratch (stream-ordered)"}
+        del g, dout
+        torch.cuda.empty_cache()
+    except Exception as e:
+        rows["bwd_mamba130m_layer"] = {"error": str(e)[:200]}
+    return rows
+
+
+def time_decode(step, steps, torch):
+    """Microseconds per token, (eager, CUDA-graph replay).  Eager calls from
+    Python are bound by the host-side marshalling; the graph holds `steps`
+    launches captured on a side stream and shows the device time per step."""
+    for _ in range(10):
+        step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    us_eager = a.elapsed_time(b) * 1e3 / steps
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # any one-time setup happens outside the capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(steps):
+                step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return us_eager, a.elapsed_time(b) * 1e3 / (steps * reps)
+
+
+def decode_row(us_eager, us, nbytes, hbm_peak):
+    return {"us_per_token": round(us, 3), "us_per_token_eager": round(us_eager, 3),
+            "state_bytes": nbytes, "hbm_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "note": "one launch per token; us_per_token from a CUDA graph of 200 steps "
+                    "(device time), us_per_token_eager from Python calls (host-bound)"}
 
 
 def decode_rows(dev, torch, abi, inputs, hbm_peak):
@@ -362,22 +446,9 @@ def decode_rows(dev, torch, abi, inputs, hbm_peak):
         def step():
             abi.selective_state_update(state, u, dl, g["A"], Bt, Ct, g["D"], z, g["delta_bias"],
                                        y=y)
-        for _ in range(10):
-            step()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record()
-        for _ in range(steps):
-            step()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / steps
+        us_eager, us = time_decode(step, steps, torch)
         nbytes = 2 * state.numel() * 4
-        rows["decode_step_mamba130m_layer"] = {
-            "us_per_token": round(us, 3), "state_bytes": nbytes,
-            "hbm_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
-            "note": "one launch per token, back to back on one stream"}
+        rows["decode_step_mamba130m_layer"] = decode_row(us_eager, us, nbytes, hbm_peak)
     except Exception as e:
         rows["decode_step_mamba130m_layer"] = {"error": str(e)[:200]}
     try:
@@ -391,22 +462,9 @@ def decode_rows(dev, torch, abi, inputs, hbm_peak):
 
         def step2():
             abi.ssd_state_update(state, x, dt, g["A_head"], Bt, Ct, g["D"], y=y)
-        for _ in range(10):
-            step2()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record()
-        for _ in range(steps):
-            step2()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / steps
+        us_eager, us = time_decode(step2, steps, torch)
         nbytes = 2 * state.numel() * 4
-        rows["decode_step_mamba2_ssd"] = {
-            "us_per_token": round(us, 3), "state_bytes": nbytes,
-            "hbm_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
-            "note": "one launch per token, back to back on one stream"}
+        rows["decode_step_mamba2_ssd"] = decode_row(us_eager, us, nbytes, hbm_peak)
     except Exception as e:
         rows["decode_step_mamba2_ssd"] = {"error": str(e)[:200]}
     return rows
@@ -504,6 +562,16 @@ def main_profile(args):
     from selective_state_space_146_b300 import _abi as abi
     from selective_state_space_146_b300 import inputs
     dev = torch.device("cuda", 0)
+    if args.profile == "bwd_mamba130m_layer":
+        cfg = inputs.WORKLOADS["mamba130m_layer"]
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(cfg)
+            dout = inputs.grad_output((cfg.batch, cfg.d_inner, cfg.seqlen), cfg.dtype)
+        for _ in range(args.warmup + args.steps):
+            abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], dout)
+        torch.cuda.synchronize()
+        return 0 if abi.device_error() == 0 else 1
     cfg = inputs.WORKLOADS[args.profile]
     with inputs.on_device(dev):
         g = (inputs.workload_ssd_inputs(cfg) if args.profile == "mamba2_ssd"

@@ -452,6 +452,8 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
         a.sddl_b = ddelta->stride[0]; a.sddl_d = ddelta->stride[1]; a.sddl_t = ddelta->stride[2];
         if (dz) { a.dz = dz->data; a.sdz_b = dz->stride[0]; a.sdz_d = dz->stride[1]; a.sdz_t = dz->stride[2]; }
     }
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_selective_bwd(a, static_cast<cudaStream_t>(stream), sc);
 }

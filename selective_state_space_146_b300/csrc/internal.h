@@ -2,6 +2,7 @@
 // units (not part of the public ABI).
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ss {
@@ -93,6 +94,7 @@ struct BwdArgs {
     void* dz;  int64_t sdz_b, sdz_d, sdz_t;
     float *dA, *dB, *dC, *dD, *dbias;
     float* ckpt;  // chunk-start states, filled by the kernel
+    unsigned* err;
 };
 
 // Scratch provider: either stream-ordered allocation or a fixed buffer.
@@ -113,5 +115,9 @@ void count_launch(int n);
 int sm_count_current();
 // cuTensorMapEncodeTiled resolved through the runtime (no libcuda link).
 void* tensor_map_encoder();
+// Tensor map of a (Bsz, D, L) activation (or (Bsz, N, L) B / C) with unit
+// t-stride: box of box_t steps x box_d rows, 128-byte swizzle if `swizzle`.
+bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
+                 int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle = true);
 
 }  // namespace ss

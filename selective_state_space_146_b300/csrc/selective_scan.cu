@@ -643,8 +643,8 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                               CUtensorMapFloatOOBfill);
 
-static bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
-                        int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle = true) {
+bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
+                 int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle) {
     auto enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
     if (!enc) return false;
     const int es = dtype == SS_BF16 ? 2 : 4;
@@ -837,13 +837,19 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
 }
 
 // ---------------------------------------------------------------------------
-// One recurrent step (decode): one thread per (b, d), the channel's state
+// One recurrent step (decode): four threads per (b, d), the channel's state
 // row read and written once.
 
 template <typename T>
 __global__ void __launch_bounds__(128) scan_step(StepArgs a) {
-    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (unit >= (int64_t)a.Bsz * a.D) return;
+    // four lanes per (b, d): lane `sub` updates states sub, sub + 4, ...; the
+    // readout is summed over the four lanes (they sit in one warp)
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t units = (int64_t)a.Bsz * a.D;
+    const int64_t unit_raw = gt >> 2;
+    const int sub = (int)(gt & 3);
+    const bool valid = unit_raw < units;
+    const int64_t unit = valid ? unit_raw : 0;
     const int b = (int)(unit / a.D), d = (int)(unit % a.D);
     const float uu = Elem<T>::to_f(static_cast<const T*>(a.u)[b * a.su_b + d * a.su_d]);
     float dd = Elem<T>::to_f(static_cast<const T*>(a.dl)[b * a.sdl_b + d * a.sdl_d]) +
@@ -854,13 +860,18 @@ __global__ void __launch_bounds__(128) scan_step(StepArgs a) {
     const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b;
     float* st = a.state + b * a.ss_b + d * a.ss_d;
     float acc = 0.f;
+    if (valid) {
 #pragma unroll 4
-    for (int n = 0; n < a.N; ++n) {
-        const float hn = fmaf(ex2_approx(dd * a.A[d * a.sA_d + n * a.sA_n] * kLog2e),
-                              st[n * a.ss_n], du * Elem<T>::to_f(Bp[n * a.sB_n]));
-        st[n * a.ss_n] = hn;
-        acc = fmaf(Elem<T>::to_f(Cp[n * a.sC_n]), hn, acc);
+        for (int n = sub; n < a.N; n += 4) {
+            const float hn = fmaf(ex2_approx(dd * a.A[d * a.sA_d + n * a.sA_n] * kLog2e),
+                                  st[n * a.ss_n], du * Elem<T>::to_f(Bp[n * a.sB_n]));
+            st[n * a.ss_n] = hn;
+            acc = fmaf(Elem<T>::to_f(Cp[n * a.sC_n]), hn, acc);
+        }
     }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (!valid || sub != 0) return;
     acc = fmaf(a.Dv ? a.Dv[d * a.sD] : 0.f, uu, acc);
     if (a.z) {
         const float zz = Elem<T>::to_f(static_cast<const T*>(a.z)[b * a.sz_b + d * a.sz_d]);
@@ -870,8 +881,8 @@ __global__ void __launch_bounds__(128) scan_step(StepArgs a) {
 }
 
 int launch_selective_step(const StepArgs& a, cudaStream_t st) {
-    const int64_t units = (int64_t)a.Bsz * a.D;
-    const unsigned blocks = (unsigned)((units + 127) / 128);
+    const int64_t threads = (int64_t)a.Bsz * a.D * 4;
+    const unsigned blocks = (unsigned)((threads + 127) / 128);
     if (a.dtype == SS_BF16) scan_step<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
     else scan_step<float><<<blocks, 128, 0, st>>>(a);
     count_launch(1);

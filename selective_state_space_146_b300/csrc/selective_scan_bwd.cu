@@ -12,15 +12,28 @@
 //   dA    += g_t h_{t-1} abar_t dl_t
 //   ddl_t  = sum_n g_t (h_{t-1} abar_t A + B_t u_t);  ddelta_t = ddl_t softplus'(.)
 //
-// One CTA = 16 channels of one batch row x 16 lanes (one state each, N <= 16).
-// Sweep 1 runs the recurrence forward and stores the state every K = 32 steps
-// (stream-ordered scratch).  Sweep 2 walks the chunks backwards: it recomputes
-// the chunk's states into registers from the stored one, then steps t down
-// with the adjoint.  Sums over n are 16-lane shuffles; dB and dC are reduced
-// over the CTA's channels in shared memory and added to global memory
-// atomically, dA, dD and ddelta_bias are added atomically over batch rows.
+// Two kernels:
+//  * scan_bwd_fast (N = 16, unit t-stride, 16-byte aligned rows): one CTA per
+//    32 channels of a batch row, four lanes per channel, each lane keeping four
+//    states.  Activations arrive as 128-byte-swizzled TMA tiles (64 bf16 or 32
+//    fp32 steps), double buffered.  Pass 1 runs the recurrence forward over the
+//    tiles and stores the state every 16 steps (stream-ordered scratch).
+//    Pass 2 walks the tiles backwards; for each 16-step sub-chunk it recomputes
+//    the states into registers from the stored one, then steps t down with the
+//    adjoint.  Sums over the four lanes of a channel are two xor-shuffles; dB
+//    and dC are reduce-scattered over the eight channels of a warp, summed over
+//    the CTA's warps in shared memory and written as per-CTA partial sums;
+//    du / ddelta / dz leave through TMA stores.  scan_bwd_finish then adds the
+//    partials of dB, dC (over channel blocks) and of dA, dD, ddelta_bias (over
+//    batch rows) in a fixed order, so the result does not depend on timing.
+//  * scan_bwd (any strides, N <= 16): one lane per state, 16 channels per CTA,
+//    dB / dC reduced in shared memory and added with atomics.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -189,9 +202,524 @@ __global__ void __launch_bounds__(NTHREADS) scan_bwd(BwdArgs a) {
 
 }  // namespace bwd
 
+
+// ---------------------------------------------------------------------------
+// scan_bwd_fast
+
+namespace bwdf {
+
+template <typename T>
+struct Cfg {
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int N = 16;
+    static constexpr int TT = 128 / ES;        // steps per tile: one swizzle row
+    static constexpr int KS = 8;               // steps per recompute sub-chunk
+    static constexpr int NSUB = TT / KS;
+    static constexpr int CH = 32;              // channels per CTA
+    static constexpr int NTHREADS = CH * 4;    // four lanes per channel
+    static constexpr int NWARPS = NTHREADS / 32;
+    static constexpr int ACT = CH * 128;       // one activation tile
+    static constexpr int RAWBC = N * 128;      // one raw B or C tile ([n][t])
+    static constexpr int OFF_U = 0, OFF_DL = ACT, OFF_Z = 2 * ACT, OFF_G = 3 * ACT;
+    static constexpr int OFF_B = 4 * ACT, OFF_C = 4 * ACT + RAWBC;
+    static constexpr int STAGE = 4 * ACT + 2 * RAWBC;
+    static constexpr int OFF_TAB = 2 * STAGE;               // fp32 [t][B 0..15 | C 0..15]
+    static constexpr int OFF_OUT = OFF_TAB + TT * 128;      // du, ddelta, dz tiles
+    static constexpr int OFF_RED = OFF_OUT + 3 * ACT;       // [warp][KS][32] fp32
+    static constexpr int OFF_BAR = OFF_RED + NWARPS * KS * 32 * 4;
+    static constexpr int SMEM = OFF_BAR + 64 + 1024;
+    static constexpr int NV = 2 * N;                        // dB and dC values per step
+    static_assert(STAGE % 1024 == 0 && OFF_OUT % 1024 == 0, "swizzled tiles 1024-aligned");
+    static_assert(3 * SMEM <= 228 * 1024, "three CTAs per SM");
+};
+
+struct Params {
+    int Bsz, D, L, ntiles, dgroups, softplus;
+    const float* A; int64_t sA_d, sA_n;
+    const float* Dv; int64_t sD;
+    const float* bias; int64_t sbias;
+    float* ckpt;      // [b][d][L/16 rounded up][16]: the state before each sub-chunk
+    float* part;      // [dgroup][b][t][32]: dB (n) then dC (n), summed over a CTA
+    float* partA;     // [b][d][16]
+    float* partD;     // [b][d]
+    float* partbias;  // [b][d]
+    unsigned* err;
+};
+
+// Byte offset of element j of row r in a 128-byte-swizzled tile.
+template <int ES>
+__device__ __forceinline__ uint32_t swz_elem(int r, int j) {
+    const int byte = j * ES;
+    return (uint32_t)((r << 7) + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15));
+}
+
+template <typename T>
+__device__ __forceinline__ float lds_elem(uint32_t a) {
+    if constexpr (sizeof(T) == 2) return __uint_as_float(lds16(a) << 16);
+    else return __uint_as_float(lds32(a));
+}
+
+template <typename T>
+__device__ __forceinline__ void sts_elem(uint32_t a, float v) {
+    if constexpr (sizeof(T) == 2) {
+        const unsigned short h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(h) : "memory");
+    } else {
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(v)) : "memory");
+    }
+}
+
+// Raw B (and C) of one tile, [n][t] in T, into the fp32 table [t][32]
+// (B[0..15] then C[0..15]).  Warp w converts rows n = (lane + it) & 15 for
+// it = w, w + NWARPS, ...: a lane reads one 32-bit word of a raw row (distinct
+// banks across the warp) and writes its one or two steps.
+template <typename T, int NWARPS>
+__device__ __forceinline__ void convert_table(uint32_t rawB, uint32_t rawC, uint32_t tab,
+                                              bool with_c, int warp, int lane) {
+    for (int it = warp; it < (with_c ? 32 : 16); it += NWARPS) {
+        const int n = (lane + it) & 15;
+        const uint32_t src = (it < 16 ? rawB : rawC) + n * 128 + lane * 4;
+        const uint32_t col = ((it < 16 ? 0 : 16) + n) * 4;
+        const uint32_t w = lds32(src);
+        if constexpr (sizeof(T) == 2) {
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(tab + (2 * lane) * 128 + col),
+                         "r"(w << 16) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(tab + (2 * lane + 1) * 128 + col),
+                         "r"(w & 0xffff0000u) : "memory");
+        } else {
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(tab + lane * 128 + col), "r"(w)
+                         : "memory");
+        }
+    }
+}
+
+// One round of a reduce-scatter across lanes lane and lane ^ m: keep one half
+// of v (the upper one if `upper`), add the partner's copy of that half.
+template <int LEN>
+__device__ __forceinline__ void rs_half(const float* v, float* out, bool upper, int m) {
+#pragma unroll
+    for (int e = 0; e < LEN / 2; ++e) {
+        const float lo = v[e], hi = v[LEN / 2 + e];
+        out[e] = (upper ? hi : lo) + __shfl_xor_sync(0xffffffffu, upper ? lo : hi, m);
+    }
+}
+
+template <typename T, bool HAS_Z>
+__global__ void __launch_bounds__(Cfg<T>::NTHREADS, 3)
+scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+              const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_g,
+              const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
+              const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_ddl,
+              const __grid_constant__ CUtensorMap tm_dz, const Params p) {
+    using C = Cfg<T>;
+    constexpr int ES = C::ES, TT = C::TT, KS = C::KS, NSUB = C::NSUB, NT = C::NTHREADS;
+    static_assert(NT == 128, "four warps of eight channels");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = lane & 3;                 // states 4 sub .. 4 sub + 3
+    const int ci = warp * 8 + (lane >> 2);    // channel row within the tile
+    const int b = blockIdx.x / p.dgroups, dg = blockIdx.x % p.dgroups;
+    const int d0 = dg * C::CH, d = d0 + ci;
+    const bool valid = d < p.D;
+    const int L = p.L, ntiles = p.ntiles, nkc = (L + KS - 1) / KS;
+
+    float A2[4], An[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        An[s] = valid ? p.A[d * p.sA_d + (4 * sub + s) * p.sA_n] : 0.f;
+        A2[s] = An[s] * kLog2e;
+    }
+    const float Dd = (valid && p.Dv) ? p.Dv[d * p.sD] : 0.f;
+    const float biasd = (valid && p.bias) ? p.bias[d * p.sbias] : 0.f;
+    const bool sp = p.softplus != 0;
+    float* ck = p.ckpt + ((int64_t)b * p.D + (valid ? d : 0)) * nkc * 16 + 4 * sub;
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // load q of 2 ntiles: pass 1 tile q, then pass 2 tile 2 ntiles - 1 - q
+    auto issue = [&](int q) {
+        if (q >= 2 * ntiles) return;
+        const uint32_t st = C::STAGE * (q & 1);
+        uint64_t* bar = &full[q & 1];
+        uint8_t* base = smem + st;
+        if (q < ntiles) {
+            const int t0 = q * TT;
+            mbar_arrive_expect_tx(bar, 2 * C::ACT + C::RAWBC);
+            tma_load_3d(base + C::OFF_U, &tm_u, bar, t0, d0, b);
+            tma_load_3d(base + C::OFF_DL, &tm_dl, bar, t0, d0, b);
+            tma_load_3d(base + C::OFF_B, &tm_B, bar, t0, 0, b);
+        } else {
+            const int t0 = (2 * ntiles - 1 - q) * TT;
+            mbar_arrive_expect_tx(bar, (HAS_Z ? 4 : 3) * C::ACT + 2 * C::RAWBC);
+            tma_load_3d(base + C::OFF_U, &tm_u, bar, t0, d0, b);
+            tma_load_3d(base + C::OFF_DL, &tm_dl, bar, t0, d0, b);
+            if (HAS_Z) tma_load_3d(base + C::OFF_Z, &tm_z, bar, t0, d0, b);
+            tma_load_3d(base + C::OFF_G, &tm_g, bar, t0, d0, b);
+            tma_load_3d(base + C::OFF_B, &tm_B, bar, t0, 0, b);
+            tma_load_3d(base + C::OFF_C, &tm_C, bar, t0, 0, b);
+        }
+    };
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_u);
+        tma_prefetch_desc(&tm_dl);
+        tma_prefetch_desc(&tm_g);
+        tma_prefetch_desc(&tm_B);
+        tma_prefetch_desc(&tm_C);
+        if (HAS_Z) tma_prefetch_desc(&tm_z);
+        issue(0);
+        issue(1);
+    }
+
+    const uint32_t tab = s0 + C::OFF_TAB;
+    const uint32_t red = s0 + C::OFF_RED;
+    const uint32_t out = s0 + C::OFF_OUT;
+    float g[4] = {0.f, 0.f, 0.f, 0.f}, dA[4] = {0.f, 0.f, 0.f, 0.f};
+    float dDacc = 0.f, dbacc = 0.f;
+    // value this lane holds after the reduce-scatter over the warp's channels:
+    // kind (lane bit 4: 0 = dB, 1 = dC) of state 4 sub + (lane bits 3..2)
+    const int vidx = ((lane >> 4) & 1) * 16 + 4 * sub + ((lane >> 2) & 3);
+
+    int consumed = 0;  // loads waited for
+    // start of load q: wait for it (and, in pass 2, for the previous tile's
+    // output stores to have left the out tiles), then build the B|C table
+    auto begin = [&](int q) -> bool {
+        bool ok = true;
+        if (tid == 0) {
+            ok = mbar_wait(&full[q & 1], (q >> 1) & 1, p.err);
+            if (q >= ntiles + 1) bulk_wait_read<0>();
+        }
+        if (!__syncthreads_and(ok)) return false;
+        consumed = q + 1;
+        const uint32_t st = s0 + C::STAGE * (q & 1);
+        convert_table<T, C::NWARPS>(st + C::OFF_B, st + C::OFF_C, tab, q >= ntiles, warp, lane);
+        __syncthreads();
+        return true;
+    };
+    auto finish = [&](int q) {
+        __syncthreads();  // the stage and the table are free
+        if (tid == 0) issue(q + 2);
+    };
+
+    bool ok = true;
+    {
+        // ---- pass 1: forward, store the state before every sub-chunk
+        float h[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = 0; q < ntiles && ok; ++q) {
+            if (!(ok = begin(q))) break;
+            const uint32_t st = s0 + C::STAGE * (q & 1);
+            const int t0 = q * TT, tn = min(TT, L - t0);
+#pragma unroll 1
+            for (int kc = 0; kc < NSUB; ++kc) {
+                if (t0 + kc * KS >= L) break;
+                if (valid)
+                    *reinterpret_cast<float4*>(ck + (int64_t)(t0 / KS + kc) * 16) =
+                        make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+                for (int jj = 0; jj < KS; ++jj) {
+                    const int j = kc * KS + jj;
+                    float x = lds_elem<T>(st + C::OFF_DL + swz_elem<ES>(ci, j)) + biasd;
+                    float dd = sp ? softplus_f(x) : x;
+                    dd = j < tn ? dd : 0.f;  // past the end: no update
+                    const float du = dd * lds_elem<T>(st + C::OFF_U + swz_elem<ES>(ci, j));
+                    const float4 Bv = lds128f(tab + j * 128 + sub * 16);
+                    h[0] = fmaf(ex2_approx(dd * A2[0]), h[0], du * Bv.x);
+                    h[1] = fmaf(ex2_approx(dd * A2[1]), h[1], du * Bv.y);
+                    h[2] = fmaf(ex2_approx(dd * A2[2]), h[2], du * Bv.z);
+                    h[3] = fmaf(ex2_approx(dd * A2[3]), h[3], du * Bv.w);
+                }
+            }
+            finish(q);
+        }
+    }
+    for (int q = ntiles; q < 2 * ntiles && ok; ++q) {
+        if (!(ok = begin(q))) break;
+        const uint32_t st = s0 + C::STAGE * (q & 1);
+        const int tile = 2 * ntiles - 1 - q;
+        const int t0 = tile * TT, tn = min(TT, L - t0);
+        {
+            // ---- pass 2: backward over the tile's sub-chunks, last first
+#pragma unroll 1
+            for (int kc = NSUB - 1; kc >= 0; --kc) {
+                const int tb = kc * KS;
+                if (t0 + tb >= L) continue;
+                float hc[4];
+                {
+                    const float4 v = valid ? *reinterpret_cast<const float4*>(
+                                                 ck + (int64_t)(t0 / KS + kc) * 16)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    hc[0] = v.x; hc[1] = v.y; hc[2] = v.z; hc[3] = v.w;
+                }
+                // recompute the sub-chunk's states
+                float hs[4][KS], ds[KS];
+                {
+                    float hr[4] = {hc[0], hc[1], hc[2], hc[3]};
+#pragma unroll
+                    for (int jj = 0; jj < KS; ++jj) {
+                        const int j = tb + jj;
+                        const float x = lds_elem<T>(st + C::OFF_DL + swz_elem<ES>(ci, j)) + biasd;
+                        float dd = sp ? softplus_f(x) : x;
+                        dd = j < tn ? dd : 0.f;
+                        ds[jj] = dd;
+                        const float du = dd * lds_elem<T>(st + C::OFF_U + swz_elem<ES>(ci, j));
+                        const float4 Bv = lds128f(tab + j * 128 + sub * 16);
+                        hr[0] = fmaf(ex2_approx(dd * A2[0]), hr[0], du * Bv.x);
+                        hr[1] = fmaf(ex2_approx(dd * A2[1]), hr[1], du * Bv.y);
+                        hr[2] = fmaf(ex2_approx(dd * A2[2]), hr[2], du * Bv.z);
+                        hr[3] = fmaf(ex2_approx(dd * A2[3]), hr[3], du * Bv.w);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) hs[s][jj] = hr[s];
+                    }
+                }
+                // adjoint sweep, t descending
+#pragma unroll
+                for (int jj = KS - 1; jj >= 0; --jj) {
+                    const int j = tb + jj;
+                    float vred = 0.f;
+                    if (j < tn) {
+                        const uint32_t eo = swz_elem<ES>(ci, j);
+                        const float dd = ds[jj];
+                        const float uu = lds_elem<T>(st + C::OFF_U + eo);
+                        const float go = lds_elem<T>(st + C::OFF_G + eo);
+                        const float4 Bv = lds128f(tab + j * 128 + sub * 16);
+                        const float4 Cv = lds128f(tab + j * 128 + 64 + sub * 16);
+                        const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+                        const float cv[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
+                        float dpre = go, zz = 0.f, sz = 0.f;
+                        if (HAS_Z) {
+                            zz = lds_elem<T>(st + C::OFF_Z + eo);
+                            sz = sigmoid_accurate(zz);
+                            dpre = go * zz * sz;
+                        }
+                        float pre_p = 0.f, du_p = 0.f, ddl_p = 0.f;
+                        float v[8];
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const float ht = hs[s][jj];
+                            const float hm = jj > 0 ? hs[s][jj > 0 ? jj - 1 : 0] : hc[s];
+                            const float abar = ex2_approx(dd * A2[s]);
+                            pre_p = fmaf(cv[s], ht, pre_p);
+                            g[s] = fmaf(cv[s], dpre, g[s]);
+                            const float t1 = hm * abar;
+                            const float gdd = g[s] * dd;
+                            dA[s] = fmaf(gdd, t1, dA[s]);
+                            du_p = fmaf(gdd, bv[s], du_p);
+                            ddl_p = fmaf(g[s], fmaf(t1, An[s], bv[s] * uu), ddl_p);
+                            v[s] = gdd * uu;       // dB
+                            v[4 + s] = dpre * ht;  // dC
+                            g[s] *= abar;
+                        }
+#pragma unroll
+                        for (int m = 1; m <= 2; m <<= 1) {
+                            pre_p += __shfl_xor_sync(0xffffffffu, pre_p, m);
+                            du_p += __shfl_xor_sync(0xffffffffu, du_p, m);
+                            ddl_p += __shfl_xor_sync(0xffffffffu, ddl_p, m);
+                        }
+                        const float dut = fmaf(Dd, dpre, du_p);
+                        // softplus'(x) = sigmoid(x) = 1 - exp(-softplus(x))
+                        const float ddx = sp ? ddl_p * (1.f - ex2_approx(-dd * kLog2e)) : ddl_p;
+                        dDacc = fmaf(dpre, uu, dDacc);
+                        dbacc += ddx;
+                        if (sub == 0) sts_elem<T>(out + eo, dut);
+                        else if (sub == 1) sts_elem<T>(out + C::ACT + eo, ddx);
+                        else if (HAS_Z && sub == 2) {
+                            const float pre = fmaf(Dd, uu, pre_p);
+                            sts_elem<T>(out + 2 * C::ACT + eo,
+                                        go * pre * (sz + zz * sz * (1.f - sz)));
+                        }
+                        float v4[4], v2[2], v1[1];
+                        rs_half<8>(v, v4, lane & 16, 16);
+                        rs_half<4>(v4, v2, lane & 8, 8);
+                        rs_half<2>(v2, v1, lane & 4, 4);
+                        vred = v1[0];
+                    }
+                    asm volatile("st.shared.b32 [%0], %1;"
+                                 ::"r"(red + ((warp * KS + jj) * 32 + vidx) * 4),
+                                 "r"(__float_as_uint(vred)) : "memory");
+                }
+                __syncthreads();
+                // this sub-chunk's dB / dC, summed over the CTA's warps
+                for (int e = tid; e < KS * 32; e += NT) {
+                    const int jj = e >> 5, vv = e & 31;
+                    const int t = t0 + tb + jj;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < C::NWARPS; ++w)
+                        sum += __uint_as_float(lds32(red + ((w * KS + jj) * 32 + vv) * 4));
+                    if (t < L) p.part[(((int64_t)dg * p.Bsz + b) * L + t) * 32 + vv] = sum;
+                }
+                __syncthreads();
+            }
+            // du / ddelta / dz of the tile leave through TMA stores (clipped at
+            // the tensor's edges)
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_3d(&tm_du, smem + C::OFF_OUT, t0, d0, b);
+                tma_store_3d(&tm_ddl, smem + C::OFF_OUT + C::ACT, t0, d0, b);
+                if (HAS_Z) tma_store_3d(&tm_dz, smem + C::OFF_OUT + 2 * C::ACT, t0, d0, b);
+                bulk_commit();
+            }
+        }
+        finish(q);
+    }
+    if (tid == 0) bulk_wait<0>();
+    if (!ok) {
+        // a load never arrived: wait (bounded) for the ones still in flight
+        if (tid == 0)
+            for (int k = consumed; k < min(consumed + 2, 2 * ntiles); ++k)
+                mbar_wait(&full[k & 1], (k >> 1) & 1, p.err);
+        return;
+    }
+    if (!valid) return;
+    const int64_t bd = (int64_t)b * p.D + d;
+    *reinterpret_cast<float4*>(p.partA + bd * 16 + 4 * sub) = make_float4(dA[0], dA[1], dA[2], dA[3]);
+    if (sub == 0) {
+        p.partD[bd] = dDacc;
+        p.partbias[bd] = dbacc;
+    }
+}
+
+// dB, dC summed over channel blocks; dA, dD, ddelta_bias over batch rows.
+__global__ void __launch_bounds__(256) scan_bwd_finish(Params p, int dgroups, float* dB, float* dC,
+                                                      float* dAo, float* dDo, float* dbo) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nbc = (int64_t)p.Bsz * p.L * 32;
+    const int64_t L = p.L;
+    if (i < nbc) {
+        const int v = (int)(i & 31);
+        const int64_t bt = i >> 5;  // b * L + t
+        float sum = 0.f;
+        for (int k = 0; k < dgroups; ++k) sum += p.part[((int64_t)k * p.Bsz * L) * 32 + i];
+        const int64_t b = bt / L, t = bt % L;
+        float* dst = v < 16 ? dB : dC;
+        dst[(b * 16 + (v & 15)) * L + t] = sum;
+        return;
+    }
+    int64_t r = i - nbc;
+    if (r < (int64_t)p.D * 16) {
+        float sum = 0.f;
+        for (int bb = 0; bb < p.Bsz; ++bb) sum += p.partA[(int64_t)bb * p.D * 16 + r];
+        dAo[r] = sum;
+        return;
+    }
+    r -= (int64_t)p.D * 16;
+    if (r < p.D) {
+        float sd = 0.f, sb = 0.f;
+        for (int bb = 0; bb < p.Bsz; ++bb) {
+            sd += p.partD[(int64_t)bb * p.D + r];
+            sb += p.partbias[(int64_t)bb * p.D + r];
+        }
+        if (dDo) dDo[r] = sd;
+        if (dbo) dbo[r] = sb;
+    }
+}
+
+}  // namespace bwdf
+
+static bool bwd_fast_ok(const BwdArgs& a) {
+    if (a.N != 16 || a.L >= (1 << 30)) return false;
+    const int es = a.dtype == SS_BF16 ? 2 : 4;
+    auto row_ok = [&](const void* ptr, int64_t sb, int64_t sr, int64_t st) {
+        if (!ptr) return true;
+        if (st != 1 && a.L > 1) return false;
+        if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+        if ((sr * es) % 16 || (sb * es) % 16) return false;
+        return sr * es < (int64_t(1) << 40) && sb * es < (int64_t(1) << 40);
+    };
+    return row_ok(a.u, a.su_b, a.su_d, a.su_t) && row_ok(a.dl, a.sdl_b, a.sdl_d, a.sdl_t) &&
+           row_ok(a.z, a.sz_b, a.sz_d, a.sz_t) && row_ok(a.dout, a.sg_b, a.sg_d, a.sg_t) &&
+           row_ok(a.Bm, a.sB_b, a.sB_n, a.sB_t) && row_ok(a.Cm, a.sC_b, a.sC_n, a.sC_t) &&
+           row_ok(a.du, a.sdu_b, a.sdu_d, a.sdu_t) && row_ok(a.ddl, a.sddl_b, a.sddl_d, a.sddl_t) &&
+           row_ok(a.dz, a.sdz_b, a.sdz_d, a.sdz_t);
+}
+
+template <typename T>
+static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratch) {
+    using C = bwdf::Cfg<T>;
+    const int TT = C::TT;
+    CUtensorMap m[9];
+    const bool has_z = a.z != nullptr;
+    if (!make_map_3d(&m[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, TT, C::CH) ||
+        !make_map_3d(&m[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, TT, C::CH) ||
+        !make_map_3d(&m[3], a.dout, a.dtype, a.L, a.D, a.Bsz, a.sg_d, a.sg_b, TT, C::CH) ||
+        !make_map_3d(&m[4], a.Bm, a.dtype, a.L, 16, a.Bsz, a.sB_n, a.sB_b, TT, 16, false) ||
+        !make_map_3d(&m[5], a.Cm, a.dtype, a.L, 16, a.Bsz, a.sC_n, a.sC_b, TT, 16, false) ||
+        !make_map_3d(&m[6], a.du, a.dtype, a.L, a.D, a.Bsz, a.sdu_d, a.sdu_b, TT, C::CH) ||
+        !make_map_3d(&m[7], a.ddl, a.dtype, a.L, a.D, a.Bsz, a.sddl_d, a.sddl_b, TT, C::CH))
+        return -1;
+    if (has_z) {
+        if (!make_map_3d(&m[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, TT, C::CH) ||
+            !make_map_3d(&m[8], a.dz, a.dtype, a.L, a.D, a.Bsz, a.sdz_d, a.sdz_b, TT, C::CH))
+            return -1;
+    } else {
+        m[2] = m[0];
+        m[8] = m[6];  // never used without z
+    }
+    const int dgroups = (a.D + C::CH - 1) / C::CH;
+    const int nkc = (a.L + C::KS - 1) / C::KS;
+    const size_t n_ck = (size_t)a.Bsz * a.D * nkc * 16;
+    const size_t n_part = (size_t)dgroups * a.Bsz * a.L * 32;
+    const size_t n_pa = (size_t)a.Bsz * a.D * 16, n_pd = (size_t)a.Bsz * a.D;
+    const size_t bytes = sizeof(float) * (n_ck + n_part + n_pa + 2 * n_pd);
+    float* base = static_cast<float*>(scratch.alloc(bytes, st, scratch.ctx));
+    if (!base) return SS_ERR_ALLOC;
+    bwdf::Params p{};
+    p.Bsz = a.Bsz; p.D = a.D; p.L = a.L; p.ntiles = (a.L + TT - 1) / TT; p.dgroups = dgroups;
+    p.softplus = a.softplus;
+    p.A = a.A; p.sA_d = a.sA_d; p.sA_n = a.sA_n;
+    p.Dv = a.Dv; p.sD = a.sD;
+    p.bias = a.bias; p.sbias = a.sbias;
+    p.ckpt = base;
+    p.part = base + n_ck;
+    p.partA = p.part + n_part;
+    p.partD = p.partA + n_pa;
+    p.partbias = p.partD + n_pd;
+    p.err = a.err;
+    auto kern = has_z ? bwdf::scan_bwd_fast<T, true> : bwdf::scan_bwd_fast<T, false>;
+    static bool attr_set[2][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int zi = has_z ? 1 : 0;
+    if (dev < 0 || dev >= 64 || !attr_set[zi][dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+                cudaSuccess) {
+            scratch.release(base, st, scratch.ctx);
+            return SS_ERR_LAUNCH;
+        }
+        if (dev >= 0 && dev < 64) attr_set[zi][dev] = true;
+    }
+    kern<<<(unsigned)((int64_t)a.Bsz * dgroups), C::NTHREADS, C::SMEM, st>>>(
+        m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], m[8], p);
+    const int64_t total = (int64_t)a.Bsz * a.L * 32 + (int64_t)a.D * 16 + a.D;
+    bwdf::scan_bwd_finish<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p, dgroups, a.dB, a.dC,
+                                                                          a.dA, a.dD, a.dbias);
+    count_launch(2);
+    const cudaError_t e = cudaGetLastError();
+    scratch.release(base, st, scratch.ctx);
+    return e == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
+}
+
 int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& scratch) {
     BwdArgs a = args;
-    // the fp32 sums start from zero (and stay zero when there is nothing to scan)
+    const bool empty = a.L == 0 || a.Bsz == 0 || a.D == 0;
+    const char* force = getenv("SS_BWD_PATH");
+    if (!empty && !(force && !strcmp(force, "general")) && bwd_fast_ok(a)) {
+        const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
+                                          : run_bwd_fast<float>(a, st, scratch);
+        if (rc != -1) return rc;  // -1: no tensor map for this layout, take the general kernel
+    }
+    // the general kernel adds into the fp32 sums; with nothing to scan they stay zero
     const size_t nA = (size_t)a.D * a.N, nBC = (size_t)a.Bsz * a.N * a.L;
     if ((nA && cudaMemsetAsync(a.dA, 0, sizeof(float) * nA, st) != cudaSuccess) ||
         (nBC && cudaMemsetAsync(a.dB, 0, sizeof(float) * nBC, st) != cudaSuccess) ||
@@ -199,7 +727,7 @@ int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& sc
         (a.dD && a.D && cudaMemsetAsync(a.dD, 0, sizeof(float) * a.D, st) != cudaSuccess) ||
         (a.dbias && a.D && cudaMemsetAsync(a.dbias, 0, sizeof(float) * a.D, st) != cudaSuccess))
         return SS_ERR_CUDA;
-    if (a.L == 0 || a.Bsz == 0 || a.D == 0) return SS_OK;
+    if (empty) return SS_OK;
     const int nchunk = (a.L + bwd::K - 1) / bwd::K;
     const size_t bytes = (size_t)a.Bsz * a.D * (nchunk + 1) * bwd::NL * sizeof(float);
     void* ck = scratch.alloc(bytes, st, scratch.ctx);

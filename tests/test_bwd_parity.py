@@ -41,9 +41,25 @@ def _compare(out, ref, dt, tag):
         check_close(to_np(out[k]), ref[k], _tdt(dt), f"{tag} {k}")
 
 
+@pytest.fixture
+def bwd_path(request, monkeypatch):
+    """None: the library's choice (the TMA kernel where the layout allows);
+    "general": the any-stride kernel."""
+    val = getattr(request, "param", None)
+    if val:
+        monkeypatch.setenv("SS_BWD_PATH", val)
+    else:
+        monkeypatch.delenv("SS_BWD_PATH", raising=False)
+    return val
+
+
 CASES = [
     # Bsz, D, N, L, dtype, gate, skip, bias, softplus
     (2, 24, 16, 100, "f32", True, True, True, True),
+    (2, 70, 16, 200, "bf16", True, True, True, True),
+    (1, 32, 16, 8, "f32", True, True, True, True),
+    (1, 64, 16, 72, "bf16", False, True, True, True),
+    (2, 40, 16, 136, "bf16", True, True, False, False),
     (1, 40, 16, 333, "bf16", True, True, True, True),
     (2, 7, 5, 65, "f32", False, False, False, False),
     (1, 17, 16, 32, "f32", True, False, True, True),
@@ -57,10 +73,13 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])) +
                          ("" if all(c[5:]) else "-" + "".join("gsbp"[i] for i in range(4)
                                                               if not c[5 + i])))
-def test_bwd_matches_oracle(cuda_device, case):
+@pytest.mark.parametrize("bwd_path", [None, "general"], indirect=True)
+def test_bwd_matches_oracle(cuda_device, bwd_path, case):
     Bsz, D, N, L, dt, gate, skip, bias, sp = case
     inp = inputs.selective_inputs(Bsz, D, N, L, dt, gate=gate, skip=skip, bias=bias,
                                   seed=L + D)
+    if not sp:  # without softplus the step must already be positive
+        inp["delta"] = inp["delta"].abs()
     dout = inputs.grad_output((Bsz, D, L), dt, seed=L + D)
     out = _run(inp, dout, sp, cuda_device)
     ref = oracle.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
@@ -107,7 +126,19 @@ def test_bwd_rejects_wide_state(cuda_device):
                                 g["delta_bias"], dout)
 
 
-def test_bwd_headline_layer_shape(cuda_device):
+def test_bwd_fast_path_is_deterministic(cuda_device, bwd_path):
+    """The TMA kernel adds its partial sums in a fixed order: two calls give
+    the same bits."""
+    inp = inputs.selective_inputs(2, 96, 16, 512, "bf16", seed=9)
+    dout = inputs.grad_output((2, 96, 512), "bf16", seed=9)
+    a = _run(inp, dout, True, cuda_device)
+    b = _run(inp, dout, True, cuda_device)
+    for k in GRADS:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("bwd_path", [None, "general"], indirect=True)
+def test_bwd_headline_layer_shape(cuda_device, bwd_path):
     """Every gradient at the Mamba-130M layer shape (8 x 1536 x 2048, N = 16,
     bf16) against the full oracle (single-threaded C, a few seconds)."""
     cfg = inputs.WORKLOADS["mamba130m_layer"]
