@@ -246,29 +246,6 @@ struct Params {
     unsigned* err;
 };
 
-// Byte offset of element j of row r in a 128-byte-swizzled tile.
-template <int ES>
-__device__ __forceinline__ uint32_t swz_elem(int r, int j) {
-    const int byte = j * ES;
-    return (uint32_t)((r << 7) + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15));
-}
-
-template <typename T>
-__device__ __forceinline__ float lds_elem(uint32_t a) {
-    if constexpr (sizeof(T) == 2) return __uint_as_float(lds16(a) << 16);
-    else return __uint_as_float(lds32(a));
-}
-
-template <typename T>
-__device__ __forceinline__ void sts_elem(uint32_t a, float v) {
-    if constexpr (sizeof(T) == 2) {
-        const unsigned short h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(h) : "memory");
-    } else {
-        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(v)) : "memory");
-    }
-}
-
 // Raw B (and C) of one tile, [n][t] in T, into the fp32 table [t][32]
 // (B[0..15] then C[0..15]).  Warp w converts rows n = (lane + it) & 15 for
 // it = w, w + NWARPS, ...: a lane reads one 32-bit word of a raw row (distinct
@@ -382,7 +359,6 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     const uint32_t tab = s0 + C::OFF_TAB;
     const uint32_t red = s0 + C::OFF_RED;
     const uint32_t out = s0 + C::OFF_OUT;
-    float g[4] = {0.f, 0.f, 0.f, 0.f}, dA[4] = {0.f, 0.f, 0.f, 0.f};
     float dDacc = 0.f, dbacc = 0.f;
     // value this lane holds after the reduce-scatter over the warp's channels:
     // kind (lane bit 4: 0 = dB, 1 = dC) of state 4 sub + (lane bits 3..2)
@@ -409,10 +385,64 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         if (tid == 0) issue(q + 2);
     };
 
+    // Per 8-step sub-chunk kc of a tile, lane `sub` computes delta (and the
+    // softplus slope) of steps 2 sub, 2 sub + 1 and the four lanes of the
+    // channel exchange them.  Steps past the end get delta = 0 (no update) and
+    // slope 0 (no gradient).
+    auto deltas = [&](uint32_t st, int kc, int tn, float* dd, float* sg) {
+        float x[2];
+        if constexpr (ES == 2) {
+            const uint32_t w = lds32(st + C::OFF_DL + (ci << 7) + ((kc ^ (ci & 7)) << 4) + sub * 4);
+            x[0] = __uint_as_float(w << 16);
+            x[1] = __uint_as_float(w & 0xffff0000u);
+        } else {
+            const uint2 w = lds64(st + C::OFF_DL + (ci << 7) + (((2 * kc + (sub >> 1)) ^ (ci & 7)) << 4) +
+                                  (sub & 1) * 8);
+            x[0] = __uint_as_float(w.x);
+            x[1] = __uint_as_float(w.y);
+        }
+        float own_d[2], own_s[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float xb = x[e] + biasd;
+            const bool live = kc * KS + 2 * sub + e < tn;
+            const float v = sp ? softplus_f(xb) : xb;
+            own_d[e] = live ? v : 0.f;
+            // softplus'(x) = sigmoid(x) = 1 - exp(-softplus(x))
+            own_s[e] = live ? (sp ? 1.f - ex2_approx(-v * kLog2e) : 1.f) : 0.f;
+        }
+        const int gbase = lane & ~3;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+            dd[j] = __shfl_sync(0xffffffffu, own_d[j & 1], gbase + (j >> 1));
+            if (sg) sg[j] = __shfl_sync(0xffffffffu, own_s[j & 1], gbase + (j >> 1));
+        }
+    };
+    // the KS elements of an activation tile row for sub-chunk kc, widened
+    auto load8 = [&](uint32_t tile, int kc, float* v) {
+        if constexpr (ES == 2) {
+            const uint4 w = lds128(tile + (ci << 7) + ((kc ^ (ci & 7)) << 4));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(ww[i] << 16);
+                v[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const float4 w = lds128f(tile + (ci << 7) + (((2 * kc + h2) ^ (ci & 7)) << 4));
+                v[4 * h2] = w.x; v[4 * h2 + 1] = w.y; v[4 * h2 + 2] = w.z; v[4 * h2 + 3] = w.w;
+            }
+        }
+    };
+    const float2 A2p[2] = {make_float2(A2[0], A2[1]), make_float2(A2[2], A2[3])};
+    const float2 Anp[2] = {make_float2(An[0], An[1]), make_float2(An[2], An[3])};
+
     bool ok = true;
     {
         // ---- pass 1: forward, store the state before every sub-chunk
-        float h[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 h2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         for (int q = 0; q < ntiles && ok; ++q) {
             if (!(ok = begin(q))) break;
             const uint32_t st = s0 + C::STAGE * (q & 1);
@@ -422,155 +452,181 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
                 if (t0 + kc * KS >= L) break;
                 if (valid)
                     *reinterpret_cast<float4*>(ck + (int64_t)(t0 / KS + kc) * 16) =
-                        make_float4(h[0], h[1], h[2], h[3]);
+                        make_float4(h2[0].x, h2[0].y, h2[1].x, h2[1].y);
+                float dd[KS], uf[KS];
+                deltas(st, kc, tn, dd, nullptr);
+                load8(st + C::OFF_U, kc, uf);
 #pragma unroll
                 for (int jj = 0; jj < KS; ++jj) {
                     const int j = kc * KS + jj;
-                    float x = lds_elem<T>(st + C::OFF_DL + swz_elem<ES>(ci, j)) + biasd;
-                    float dd = sp ? softplus_f(x) : x;
-                    dd = j < tn ? dd : 0.f;  // past the end: no update
-                    const float du = dd * lds_elem<T>(st + C::OFF_U + swz_elem<ES>(ci, j));
                     const float4 Bv = lds128f(tab + j * 128 + sub * 16);
-                    h[0] = fmaf(ex2_approx(dd * A2[0]), h[0], du * Bv.x);
-                    h[1] = fmaf(ex2_approx(dd * A2[1]), h[1], du * Bv.y);
-                    h[2] = fmaf(ex2_approx(dd * A2[2]), h[2], du * Bv.z);
-                    h[3] = fmaf(ex2_approx(dd * A2[3]), h[3], du * Bv.w);
+                    const float du = dd[jj] * uf[jj];
+                    const float2 d2 = make_float2(dd[jj], dd[jj]), du2 = make_float2(du, du);
+                    const float2 bv2[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 ar = __fmul2_rn(d2, A2p[k]);
+                        const float2 ab = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                        h2[k] = __ffma2_rn(ab, h2[k], __fmul2_rn(du2, bv2[k]));
+                    }
                 }
             }
             finish(q);
         }
     }
+    float2 g2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 dA2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    // the stored state of the next sub-chunk to process (sub-chunks go from
+    // the last to the first), loaded one sub-chunk ahead
+    auto load_ck = [&](int kcg) {
+        return (valid && kcg >= 0) ? *reinterpret_cast<const float4*>(ck + (int64_t)kcg * 16)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 ck_next = load_ck(nkc - 1);
     for (int q = ntiles; q < 2 * ntiles && ok; ++q) {
         if (!(ok = begin(q))) break;
         const uint32_t st = s0 + C::STAGE * (q & 1);
         const int tile = 2 * ntiles - 1 - q;
         const int t0 = tile * TT, tn = min(TT, L - t0);
-        {
-            // ---- pass 2: backward over the tile's sub-chunks, last first
+        // ---- pass 2: backward over the tile's sub-chunks, last first
 #pragma unroll 1
-            for (int kc = NSUB - 1; kc >= 0; --kc) {
-                const int tb = kc * KS;
-                if (t0 + tb >= L) continue;
-                float hc[4];
-                {
-                    const float4 v = valid ? *reinterpret_cast<const float4*>(
-                                                 ck + (int64_t)(t0 / KS + kc) * 16)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                    hc[0] = v.x; hc[1] = v.y; hc[2] = v.z; hc[3] = v.w;
-                }
-                // recompute the sub-chunk's states
-                float hs[4][KS], ds[KS];
-                {
-                    float hr[4] = {hc[0], hc[1], hc[2], hc[3]};
+        for (int kc = NSUB - 1; kc >= 0; --kc) {
+            const int tb = kc * KS;
+            if (t0 + tb >= L) continue;
+            const float2 hc2[2] = {make_float2(ck_next.x, ck_next.y),
+                                   make_float2(ck_next.z, ck_next.w)};
+            ck_next = load_ck(t0 / KS + kc - 1);
+            float ds[KS], sg[KS], uf[KS], gf[KS], zf[KS];
+            deltas(st, kc, tn, ds, sg);
+            load8(st + C::OFF_U, kc, uf);
+            load8(st + C::OFF_G, kc, gf);
+            if (HAS_Z) load8(st + C::OFF_Z, kc, zf);
+            // recompute the sub-chunk's states
+            float2 hs2[2][KS];
+            {
+                float2 hr[2] = {hc2[0], hc2[1]};
 #pragma unroll
-                    for (int jj = 0; jj < KS; ++jj) {
-                        const int j = tb + jj;
-                        const float x = lds_elem<T>(st + C::OFF_DL + swz_elem<ES>(ci, j)) + biasd;
-                        float dd = sp ? softplus_f(x) : x;
-                        dd = j < tn ? dd : 0.f;
-                        ds[jj] = dd;
-                        const float du = dd * lds_elem<T>(st + C::OFF_U + swz_elem<ES>(ci, j));
-                        const float4 Bv = lds128f(tab + j * 128 + sub * 16);
-                        hr[0] = fmaf(ex2_approx(dd * A2[0]), hr[0], du * Bv.x);
-                        hr[1] = fmaf(ex2_approx(dd * A2[1]), hr[1], du * Bv.y);
-                        hr[2] = fmaf(ex2_approx(dd * A2[2]), hr[2], du * Bv.z);
-                        hr[3] = fmaf(ex2_approx(dd * A2[3]), hr[3], du * Bv.w);
+                for (int jj = 0; jj < KS; ++jj) {
+                    const float4 Bv = lds128f(tab + (tb + jj) * 128 + sub * 16);
+                    const float du = ds[jj] * uf[jj];
+                    const float2 d2 = make_float2(ds[jj], ds[jj]), du2 = make_float2(du, du);
+                    const float2 bv2[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
 #pragma unroll
-                        for (int s = 0; s < 4; ++s) hs[s][jj] = hr[s];
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 ar = __fmul2_rn(d2, A2p[k]);
+                        const float2 ab = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                        hr[k] = __ffma2_rn(ab, hr[k], __fmul2_rn(du2, bv2[k]));
+                        hs2[k][jj] = hr[k];
                     }
                 }
-                // adjoint sweep, t descending
-#pragma unroll
-                for (int jj = KS - 1; jj >= 0; --jj) {
-                    const int j = tb + jj;
-                    float vred = 0.f;
-                    if (j < tn) {
-                        const uint32_t eo = swz_elem<ES>(ci, j);
-                        const float dd = ds[jj];
-                        const float uu = lds_elem<T>(st + C::OFF_U + eo);
-                        const float go = lds_elem<T>(st + C::OFF_G + eo);
-                        const float4 Bv = lds128f(tab + j * 128 + sub * 16);
-                        const float4 Cv = lds128f(tab + j * 128 + 64 + sub * 16);
-                        const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
-                        const float cv[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-                        float dpre = go, zz = 0.f, sz = 0.f;
-                        if (HAS_Z) {
-                            zz = lds_elem<T>(st + C::OFF_Z + eo);
-                            sz = sigmoid_accurate(zz);
-                            dpre = go * zz * sz;
-                        }
-                        float pre_p = 0.f, du_p = 0.f, ddl_p = 0.f;
-                        float v[8];
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const float ht = hs[s][jj];
-                            const float hm = jj > 0 ? hs[s][jj > 0 ? jj - 1 : 0] : hc[s];
-                            const float abar = ex2_approx(dd * A2[s]);
-                            pre_p = fmaf(cv[s], ht, pre_p);
-                            g[s] = fmaf(cv[s], dpre, g[s]);
-                            const float t1 = hm * abar;
-                            const float gdd = g[s] * dd;
-                            dA[s] = fmaf(gdd, t1, dA[s]);
-                            du_p = fmaf(gdd, bv[s], du_p);
-                            ddl_p = fmaf(g[s], fmaf(t1, An[s], bv[s] * uu), ddl_p);
-                            v[s] = gdd * uu;       // dB
-                            v[4 + s] = dpre * ht;  // dC
-                            g[s] *= abar;
-                        }
-#pragma unroll
-                        for (int m = 1; m <= 2; m <<= 1) {
-                            pre_p += __shfl_xor_sync(0xffffffffu, pre_p, m);
-                            du_p += __shfl_xor_sync(0xffffffffu, du_p, m);
-                            ddl_p += __shfl_xor_sync(0xffffffffu, ddl_p, m);
-                        }
-                        const float dut = fmaf(Dd, dpre, du_p);
-                        // softplus'(x) = sigmoid(x) = 1 - exp(-softplus(x))
-                        const float ddx = sp ? ddl_p * (1.f - ex2_approx(-dd * kLog2e)) : ddl_p;
-                        dDacc = fmaf(dpre, uu, dDacc);
-                        dbacc += ddx;
-                        if (sub == 0) sts_elem<T>(out + eo, dut);
-                        else if (sub == 1) sts_elem<T>(out + C::ACT + eo, ddx);
-                        else if (HAS_Z && sub == 2) {
-                            const float pre = fmaf(Dd, uu, pre_p);
-                            sts_elem<T>(out + 2 * C::ACT + eo,
-                                        go * pre * (sz + zz * sz * (1.f - sz)));
-                        }
-                        float v4[4], v2[2], v1[1];
-                        rs_half<8>(v, v4, lane & 16, 16);
-                        rs_half<4>(v4, v2, lane & 8, 8);
-                        rs_half<2>(v2, v1, lane & 4, 4);
-                        vred = v1[0];
-                    }
-                    asm volatile("st.shared.b32 [%0], %1;"
-                                 ::"r"(red + ((warp * KS + jj) * 32 + vidx) * 4),
-                                 "r"(__float_as_uint(vred)) : "memory");
-                }
-                __syncthreads();
-                // this sub-chunk's dB / dC, summed over the CTA's warps
-                for (int e = tid; e < KS * 32; e += NT) {
-                    const int jj = e >> 5, vv = e & 31;
-                    const int t = t0 + tb + jj;
-                    float sum = 0.f;
-#pragma unroll
-                    for (int w = 0; w < C::NWARPS; ++w)
-                        sum += __uint_as_float(lds32(red + ((w * KS + jj) * 32 + vv) * 4));
-                    if (t < L) p.part[(((int64_t)dg * p.Bsz + b) * L + t) * 32 + vv] = sum;
-                }
-                __syncthreads();
             }
-            // du / ddelta / dz of the tile leave through TMA stores (clipped at
-            // the tensor's edges)
-            fence_proxy_async_smem();
+            // adjoint sweep, t descending; lane `sub` keeps output `sub` of each
+            // step (du, ddelta, dz)
+            float outv[KS];
+#pragma unroll
+            for (int jj = KS - 1; jj >= 0; --jj) {
+                const int j = tb + jj;
+                const float dd = ds[jj], uu = uf[jj], go = gf[jj];
+                const float4 Bv = lds128f(tab + j * 128 + sub * 16);
+                const float4 Cv = lds128f(tab + j * 128 + 64 + sub * 16);
+                const float2 bv2[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+                const float2 cv2[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
+                float dpre = go, zz = 0.f, sz = 0.f;
+                if (HAS_Z) {
+                    zz = zf[jj];
+                    sz = sigmoid_accurate(zz);
+                    dpre = go * zz * sz;
+                }
+                const float ddu = dd * uu;
+                const float2 d2 = make_float2(dd, dd), dpre2 = make_float2(dpre, dpre);
+                const float2 ddu2 = make_float2(ddu, ddu);
+                float2 pre2 = make_float2(0.f, 0.f), gb2 = pre2, ga2 = pre2;
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float2 ht = hs2[k][jj];
+                    const float2 hm = jj > 0 ? hs2[k][jj > 0 ? jj - 1 : 0] : hc2[k];
+                    const float2 ar = __fmul2_rn(d2, A2p[k]);
+                    const float2 ab = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                    pre2 = __ffma2_rn(cv2[k], ht, pre2);
+                    g2[k] = __ffma2_rn(cv2[k], dpre2, g2[k]);
+                    const float2 qv = __fmul2_rn(g2[k], __fmul2_rn(hm, ab));  // g h_{t-1} abar
+                    dA2[k] = __ffma2_rn(qv, d2, dA2[k]);
+                    ga2 = __ffma2_rn(qv, Anp[k], ga2);
+                    gb2 = __ffma2_rn(g2[k], bv2[k], gb2);
+                    const float2 vb = __fmul2_rn(g2[k], ddu2);   // dB
+                    const float2 vc = __fmul2_rn(dpre2, ht);      // dC
+                    v[2 * k] = vb.x; v[2 * k + 1] = vb.y;
+                    v[4 + 2 * k] = vc.x; v[4 + 2 * k + 1] = vc.y;
+                    g2[k] = __fmul2_rn(g2[k], ab);
+                }
+                float pre_p = pre2.x + pre2.y, gb = gb2.x + gb2.y, ga = ga2.x + ga2.y;
+#pragma unroll
+                for (int m = 1; m <= 2; m <<= 1) {
+                    pre_p += __shfl_xor_sync(0xffffffffu, pre_p, m);
+                    gb += __shfl_xor_sync(0xffffffffu, gb, m);
+                    ga += __shfl_xor_sync(0xffffffffu, ga, m);
+                }
+                const float dut = fmaf(dd, gb, Dd * dpre);
+                const float ddx = fmaf(uu, gb, ga) * sg[jj];
+                dDacc = fmaf(dpre, uu, dDacc);
+                dbacc += ddx;
+                float dzv = 0.f;
+                if (HAS_Z) dzv = go * fmaf(Dd, uu, pre_p) * (sz + zz * sz * (1.f - sz));
+                outv[jj] = sub == 0 ? dut : (sub == 1 ? ddx : dzv);
+                float v4[4], vv2[2], v1[1];
+                rs_half<8>(v, v4, lane & 16, 16);
+                rs_half<4>(v4, vv2, lane & 8, 8);
+                rs_half<2>(vv2, v1, lane & 4, 4);
+                asm volatile("st.shared.b32 [%0], %1;"
+                             ::"r"(red + ((warp * KS + jj) * 32 + vidx) * 4),
+                             "r"(__float_as_uint(v1[0])) : "memory");
+            }
+            if (sub < (HAS_Z ? 3 : 2)) {
+                const uint32_t row = out + sub * C::ACT + (ci << 7);
+                if constexpr (ES == 2) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(outv[2 * i], outv[2 * i + 1]);
+                        w[i] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(row + ((kc ^ (ci & 7)) << 4)), "r"(w[0]), "r"(w[1]),
+                                 "r"(w[2]), "r"(w[3]) : "memory");
+                } else {
+                    sts128f(row + (((2 * kc) ^ (ci & 7)) << 4),
+                            make_float4(outv[0], outv[1], outv[2], outv[3]));
+                    sts128f(row + (((2 * kc + 1) ^ (ci & 7)) << 4),
+                            make_float4(outv[4], outv[5], outv[6], outv[7]));
+                }
+            }
             __syncthreads();
-            if (tid == 0) {
-                tma_store_3d(&tm_du, smem + C::OFF_OUT, t0, d0, b);
-                tma_store_3d(&tm_ddl, smem + C::OFF_OUT + C::ACT, t0, d0, b);
-                if (HAS_Z) tma_store_3d(&tm_dz, smem + C::OFF_OUT + 2 * C::ACT, t0, d0, b);
-                bulk_commit();
+            // this sub-chunk's dB / dC, summed over the CTA's warps
+            for (int e = tid; e < KS * 32; e += NT) {
+                const int jj = e >> 5, vv = e & 31;
+                const int t = t0 + tb + jj;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::NWARPS; ++w)
+                    sum += __uint_as_float(lds32(red + ((w * KS + jj) * 32 + vv) * 4));
+                if (t < L) p.part[(((int64_t)dg * p.Bsz + b) * L + t) * 32 + vv] = sum;
             }
+            __syncthreads();
+        }
+        // du / ddelta / dz of the tile leave through TMA stores (clipped at
+        // the tensor's edges)
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_3d(&tm_du, smem + C::OFF_OUT, t0, d0, b);
+            tma_store_3d(&tm_ddl, smem + C::OFF_OUT + C::ACT, t0, d0, b);
+            if (HAS_Z) tma_store_3d(&tm_dz, smem + C::OFF_OUT + 2 * C::ACT, t0, d0, b);
+            bulk_commit();
         }
         finish(q);
     }
+    const float dA[4] = {dA2[0].x, dA2[0].y, dA2[1].x, dA2[1].y};
     if (tid == 0) bulk_wait<0>();
     if (!ok) {
         // a load never arrived: wait (bounded) for the ones still in flight
