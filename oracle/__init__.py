@@ -46,6 +46,8 @@ def _bind(path):
     i64, dp, ip = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.oracle_selective_scan.argtypes = [i64, i64, i64, i64] + [dp] * 8 + [ip, dp, dp, dp, ip]
     lib.oracle_selective_scan.restype = ip
+    lib.oracle_selective_scan_grouped.argtypes = [i64] * 5 + [dp] * 8 + [ip, dp, dp, dp, ip]
+    lib.oracle_selective_scan_grouped.restype = ip
     lib.oracle_ssd.argtypes = [i64] * 6 + [dp] * 6 + [dp, dp, dp, ip]
     lib.oracle_ssd.restype = ip
     lib.oracle_threads.restype = ip
@@ -108,7 +110,8 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                    softplus=True, h0=None, nthreads=1, _lib=None):
     """Oracle of the selective scan.
 
-    Shapes: u, delta, z (Bsz, Dch, L); A (Dch, N); B, C (Bsz, N, L);
+    Shapes: u, delta, z (Bsz, Dch, L); A (Dch, N); B, C (Bsz, N, L), or
+    (Bsz, G, N, L) with one B, C per group of Dch / G consecutive channels;
     D, delta_bias (Dch,); h0 (Bsz, Dch, N).  Returns (y, last_state), both
     float64 numpy arrays of shapes (Bsz, Dch, L) and (Bsz, Dch, N).
     """
@@ -116,15 +119,27 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     D, z, delta_bias, h0 = (_f64(t) for t in (D, z, delta_bias, h0))
     Bsz, Dch, L = u.shape
     N = A.shape[1]
+    grouped = B.ndim == 4
+    G = B.shape[1] if grouped else 1
     assert delta.shape == u.shape and A.shape == (Dch, N)
-    assert B.shape == (Bsz, N, L) and C.shape == (Bsz, N, L)
+    if grouped:
+        assert B.shape == (Bsz, G, N, L) and C.shape == B.shape and Dch % G == 0
+    else:
+        assert B.shape == (Bsz, N, L) and C.shape == (Bsz, N, L)
     assert z is None or z.shape == u.shape
     assert D is None or D.shape == (Dch,)
     assert delta_bias is None or delta_bias.shape == (Dch,)
     assert h0 is None or h0.shape == (Bsz, Dch, N)
     y = np.empty((Bsz, Dch, L), np.float64)
     last = np.empty((Bsz, Dch, N), np.float64)
-    rc = (_lib or _load()).oracle_selective_scan(Bsz, Dch, N, L, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+    lib = _lib or _load()
+    if grouped:
+        rc = lib.oracle_selective_scan_grouped(Bsz, Dch, G, N, L, _ptr(u), _ptr(delta), _ptr(A),
+                                               _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                               _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                                               _ptr(y), _ptr(last), int(nthreads))
+    else:
+        rc = lib.oracle_selective_scan(Bsz, Dch, N, L, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
                                        _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
                                        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(last),
                                        int(nthreads))

@@ -29,7 +29,9 @@
  * Readings where the pages are silent (each is also listed in the design
  * notes): softplus(x) = log(1 + e^x); A is given already negative and used as
  * is; the initial state is zero unless h0 is given; B and C are shared by all
- * channels of one batch row; the SSD dt is already positive.
+ * channels of one batch row unless given per channel group (G groups of D/G
+ * consecutive channels; G = D is one B, C per channel); the SSD dt is
+ * already positive.
  *
  * Parallelism: the optional OpenMP loop runs over independent (batch,
  * channel) or (batch, head) units only; every unit is computed by the same
@@ -64,7 +66,9 @@ int oracle_threads(void) {
  *
  *   u, delta, z, y : (Bsz, D, L), t fastest
  *   A              : (D, N)
- *   Bm, Cm         : (Bsz, N, L)   (shared by all channels of a batch row)
+ *   Bm, Cm         : (Bsz, G, N, L)  channel d reads group g = d / (D / G):
+ *                    G = 1 is one B, C per batch row shared by all channels,
+ *                    G = D one per channel
  *   Dv, delta_bias : (D)           (nullable: no skip / no bias)
  *   z              : nullable (no gate)
  *   h0             : (Bsz, D, N)   nullable (zero initial state)
@@ -72,17 +76,17 @@ int oracle_threads(void) {
  *
  * For every t:
  *   dlt  = delta + delta_bias[d];  if softplus: dlt = softplus(dlt)
- *   h[n] = exp(dlt * A[d,n]) * h[n] + dlt * B[b,n,t] * u[b,d,t]
- *   out  = sum_n C[b,n,t] * h[n] + D[d] * u[b,d,t]
+ *   h[n] = exp(dlt * A[d,n]) * h[n] + dlt * B[b,g,n,t] * u[b,d,t]
+ *   out  = sum_n C[b,g,n,t] * h[n] + D[d] * u[b,d,t]
  *   if z: out = out * z / (1 + exp(-z))
  */
-int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
-                          const double* u, const double* delta, const double* A,
-                          const double* Bm, const double* Cm, const double* Dv,
-                          const double* z, const double* delta_bias, int softplus,
-                          const double* h0, double* y, double* last_state,
-                          int nthreads) {
-    if (Bsz < 0 || D < 0 || N < 1 || L < 0) return -1;
+int oracle_selective_scan_grouped(int64_t Bsz, int64_t D, int64_t G, int64_t N, int64_t L,
+                                  const double* u, const double* delta, const double* A,
+                                  const double* Bm, const double* Cm, const double* Dv,
+                                  const double* z, const double* delta_bias, int softplus,
+                                  const double* h0, double* y, double* last_state,
+                                  int nthreads) {
+    if (Bsz < 0 || D < 0 || N < 1 || L < 0 || G < 1 || (D > 0 && D % G != 0)) return -1;
     int64_t units = Bsz * D;
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
@@ -92,6 +96,7 @@ int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
 #endif
     for (int64_t unit = 0; unit < units; ++unit) {
         int64_t b = unit / D, d = unit % D;
+        int64_t g = d / (D / G);
         double* hp = (double*)malloc((size_t)N * sizeof(double));
         if (!hp) continue;
         for (int64_t n = 0; n < N; ++n)
@@ -99,6 +104,8 @@ int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
         const double* ur = u + (b * D + d) * L;
         const double* dr = delta + (b * D + d) * L;
         const double* zr = z ? z + (b * D + d) * L : NULL;
+        const double* Bg = Bm + (b * G + g) * N * L;  /* this channel's group */
+        const double* Cg = Cm + (b * G + g) * N * L;
         double* yr = y + (b * D + d) * L;
         for (int64_t t = 0; t < L; ++t) {
             double dlt = dr[t] + (delta_bias ? delta_bias[d] : 0.0);
@@ -106,9 +113,9 @@ int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
             double out = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 double abar = exp(dlt * A[d * N + n]);
-                double bbar = dlt * Bm[(b * N + n) * L + t];
+                double bbar = dlt * Bg[n * L + t];
                 hp[n] = abar * hp[n] + bbar * ur[t];
-                out += Cm[(b * N + n) * L + t] * hp[n];
+                out += Cg[n * L + t] * hp[n];
             }
             if (Dv) out += Dv[d] * ur[t];
             if (zr) out = out * zr[t] / (1.0 + exp(-zr[t]));
@@ -119,6 +126,17 @@ int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
         free(hp);
     }
     return 0;
+}
+
+/* The common case: one B and one C per batch row, (Bsz, N, L). */
+int oracle_selective_scan(int64_t Bsz, int64_t D, int64_t N, int64_t L,
+                          const double* u, const double* delta, const double* A,
+                          const double* Bm, const double* Cm, const double* Dv,
+                          const double* z, const double* delta_bias, int softplus,
+                          const double* h0, double* y, double* last_state,
+                          int nthreads) {
+    return oracle_selective_scan_grouped(Bsz, D, 1, N, L, u, delta, A, Bm, Cm, Dv, z, delta_bias,
+                                         softplus, h0, y, last_state, nthreads);
 }
 
 /*

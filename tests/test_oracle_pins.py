@@ -135,6 +135,10 @@ def test_delta_zero_limit():
 def _brute_selective(u, delta, A, Bm, Cm, D, z, db, softplus):
     Bsz, Dch, L = u.shape
     N = A.shape[1]
+    if Bm.ndim == 4:  # one B, C per group of Dch / G consecutive channels
+        G = Bm.shape[1]
+        grp = [d // (Dch // G) for d in range(Dch)]
+        return _brute_grouped(u, delta, A, Bm, Cm, D, z, db, softplus, grp)
     y = np.zeros((Bsz, Dch, L))
     last = np.zeros((Bsz, Dch, N))
     for b, d in itertools.product(range(Bsz), range(Dch)):
@@ -163,6 +167,25 @@ def _brute_selective(u, delta, A, Bm, Cm, D, z, db, softplus):
     return y, last
 
 
+def _brute_grouped(u, delta, A, Bm, Cm, D, z, db, softplus, grp):
+    """Channel d of a grouped call, unrolled with its group's B, C written out
+    as a per-channel 3-D copy, one channel at a time."""
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    y = np.zeros((Bsz, Dch, L))
+    last = np.zeros((Bsz, Dch, N))
+    for d in range(Dch):
+        Bd = np.stack([Bm[b, grp[d]] for b in range(Bsz)])  # (Bsz, N, L)
+        Cd = np.stack([Cm[b, grp[d]] for b in range(Bsz)])
+        yd, ld = _brute_selective(u[:, d:d + 1], delta[:, d:d + 1], A[d:d + 1], Bd, Cd,
+                                  None if D is None else D[d:d + 1],
+                                  None if z is None else z[:, d:d + 1],
+                                  None if db is None else db[d:d + 1], softplus)
+        y[:, d] = yd[:, 0]
+        last[:, d] = ld[:, 0]
+    return y, last
+
+
 @pytest.mark.parametrize("L", [1, 2, 5, 8])
 @pytest.mark.parametrize("flags", [(True, True, True, True), (False, False, False, False),
                                    (True, False, True, False)])
@@ -176,6 +199,35 @@ def test_brute_force_unrolling(L, flags):
     np.testing.assert_allclose(last, lb, rtol=1e-12, atol=1e-13)
 
 
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+@pytest.mark.parametrize("L", [1, 3, 6])
+def test_grouped_brute_force_unrolling(G, L):
+    """B, C per channel group (G = Dch: one per channel) against the explicit
+    sums of products, channel by channel with the group's B, C."""
+    rng = np.random.default_rng(100 + 10 * G + L)
+    Bsz, Dch, N = 2, 4, 3
+    u, delta, A, _, _, D, z, db = _rand_case(rng, Bsz, Dch, N, L)
+    Bm = rng.standard_normal((Bsz, G, N, L))
+    Cm = rng.standard_normal((Bsz, G, N, L))
+    y, last = oracle.selective_scan(u, delta, A, Bm, Cm, D, z, db)
+    yb, lb = _brute_selective(u, delta, A, Bm, Cm, D, z, db, True)
+    np.testing.assert_allclose(y, yb, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(last, lb, rtol=1e-12, atol=1e-13)
+
+
+def test_grouped_with_copies_of_one_B_equals_shared():
+    """Every group holding the same B, C gives the shared-B, C scan."""
+    rng = np.random.default_rng(7)
+    Bsz, Dch, N, L, G = 2, 6, 5, 40, 3
+    u, delta, A, Bm, Cm, D, z, db = _rand_case(rng, Bsz, Dch, N, L)
+    Bg = np.repeat(Bm[:, None], G, axis=1)
+    Cg = np.repeat(Cm[:, None], G, axis=1)
+    y1, s1 = oracle.selective_scan(u, delta, A, Bm, Cm, D, z, db)
+    y2, s2 = oracle.selective_scan(u, delta, A, Bg, Cg, D, z, db)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(s1, s2)
 # --------------------------------------------------------------------------
 # P4: the final state is the carry: running [0, L1) and then [L1, L) from
 # that state reproduces y and the final state exactly (paper talk §5.3, §5.4:
@@ -371,8 +423,9 @@ _MUTANTS = {
     "no_decay": ("hp[n] = abar * hp[n] + bbar * ur[t];", "hp[n] = hp[n] + bbar * ur[t];"),
     "input_sign": ("hp[n] = abar * hp[n] + bbar * ur[t];", "hp[n] = abar * hp[n] - bbar * ur[t];"),
     "readout_before_update": (
-        "hp[n] = abar * hp[n] + bbar * ur[t];\n                out += Cm[(b * N + n) * L + t] * hp[n];",
-        "out += Cm[(b * N + n) * L + t] * hp[n];\n                hp[n] = abar * hp[n] + bbar * ur[t];"),
+        "hp[n] = abar * hp[n] + bbar * ur[t];\n                out += Cg[n * L + t] * hp[n];",
+        "out += Cg[n * L + t] * hp[n];\n                hp[n] = abar * hp[n] + bbar * ur[t];"),
+    "group_index": ("int64_t g = d / (D / G);", "int64_t g = d % G;"),
     "A_transposed": ("exp(dlt * A[d * N + n])", "exp(dlt * A[n * D + d])"),
     "gate_sign": ("out * zr[t] / (1.0 + exp(-zr[t]))", "out * zr[t] / (1.0 + exp(zr[t]))"),
     "softplus_dropped": ("if (softplus) dlt = softplus_d(dlt);", ""),
@@ -401,6 +454,17 @@ def _pins_pass(lib):
         yb, lb = _brute_selective(u, delta, A, Bm, Cm, D, z, db, True)
         if not (np.allclose(y, yb, rtol=1e-12, atol=1e-13) and np.allclose(last, lb, rtol=1e-12,
                                                                             atol=1e-13)):
+            return False
+        Bg = rng.standard_normal((1, 3, 4, 6))
+        Cg = rng.standard_normal((1, 3, 4, 6))
+        u6 = np.concatenate([u, u], axis=1)
+        d6 = np.concatenate([delta, delta], axis=1)
+        A6, D6, db6 = np.concatenate([A, A]), np.concatenate([D, D]), np.concatenate([db, db])
+        z6 = np.concatenate([z, z], axis=1)
+        yg, lg = lib.selective_scan(u6, d6, A6, Bg, Cg, D6, z6, db6, softplus=True)
+        ygb, lgb = _brute_selective(u6, d6, A6, Bg, Cg, D6, z6, db6, True)
+        if not (np.allclose(yg, ygb, rtol=1e-12, atol=1e-13) and
+                np.allclose(lg, lgb, rtol=1e-12, atol=1e-13)):
             return False
         Bsz, L, H, P, G, N = 1, 24, 4, 3, 2, 5
         x = rng.standard_normal((Bsz, L, H, P))
