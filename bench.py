@@ -341,8 +341,43 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
         del g, yb
     except Exception as e:
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
+    rows.update(grouped_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
+    return rows
+
+
+def grouped_rows(dev, torch, abi, inputs, hbm_peak, flush):
+    """B, C per channel (G = d_inner) and per group of 64 channels at the
+    Mamba-130M layer shape."""
+    rows = {}
+    cfg = inputs.WORKLOADS["mamba130m_layer"]
+    for name, G in (("per_channel_bc_mamba130m_layer", cfg.d_inner),
+                    ("groups24_bc_mamba130m_layer", cfg.d_inner // 64)):
+        try:
+            with inputs.on_device(dev):
+                g = inputs.selective_inputs(cfg.batch, cfg.d_inner, cfg.d_state, cfg.seqlen,
+                                            cfg.dtype, groups=G)
+            yb = torch.empty_like(g["u"])
+            ls = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+
+            def fn():
+                run_selective_call(g, torch, abi, yb, ls)
+            times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+            ms = statistics.mean(times)
+            e = 2
+            nbytes = (cfg.channel_steps * 4 * e + cfg.batch * G * cfg.d_state * cfg.seqlen * 2 * e
+                      + cfg.batch * cfg.d_inner * cfg.d_state * 4)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            rows[name] = {"ms_per_call": round(ms, 4),
+                          "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+                          "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                          "launches_per_call": nl / 5, "algorithmic_bytes": nbytes,
+                          "groups": G}
+            del g, yb, ls
+            torch.cuda.empty_cache()
+        except Exception as ex:
+            rows[name] = {"error": str(ex)[:200]}
     return rows
 
 
@@ -593,12 +628,13 @@ def keep_pool_memory(dev_index, nbytes=1 << 30):
     every synchronisation (the CUDA default threshold is 0).  Process-local;
     a caller that calls the library repeatedly would do the same."""
     try:
+        from cuda.bindings import driver as drv
         from cuda.bindings import runtime as rt
         err, pool = rt.cudaDeviceGetDefaultMemPool(dev_index)
         if int(err) != 0:
             return False
         (err,) = rt.cudaMemPoolSetAttribute(
-            pool, rt.cudaMemPoolAttr.cudaMemPoolAttrReleaseThreshold, rt.cuuint64_t(nbytes))
+            pool, rt.cudaMemPoolAttr.cudaMemPoolAttrReleaseThreshold, drv.cuuint64_t(nbytes))
         return int(err) == 0
     except Exception:
         return False

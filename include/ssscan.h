@@ -68,12 +68,19 @@ typedef struct ss_tensor {
  *   u, delta, z, y : (Bsz, D, L)        dtype T (all four the same)
  *   A              : (D, N)             f32
  *   B, C           : (Bsz, N, L)        dtype T; shared by all channels of row b
+ *               or   (Bsz, G, N, L)     dtype T; one B, C per group of D/G
+ *                                       consecutive channels (channel d reads
+ *                                       group d / (D/G)); G = D is one B, C
+ *                                       per channel.  D % G must be 0.
  *   D, delta_bias  : (D)                f32
  *   last_state     : (Bsz, D, N)        f32
- * T is SS_F32 or SS_BF16.  N <= 256; the fast path is compiled for N = 16
- * (other N run a slower general kernel).  The fast path needs unit stride in
- * t and 16-byte aligned rows for u/delta/z/y; other layouts take the general
- * kernel (same results up to rounding order).  y may not alias an input.
+ * T is SS_F32 or SS_BF16.  N <= 256; the fast paths are compiled for N = 16
+ * (other N run a slower general kernel).  They need unit stride in t and
+ * 16-byte aligned rows for u/delta/z/y/B/C; grouped B, C with groups of at
+ * least 64 channels (a multiple of 64) share the shared-B, C kernel, smaller
+ * groups run a kernel that streams each channel's own B, C.  Other layouts
+ * take the general kernel (same results up to rounding order).  y may not
+ * alias an input.
  * Arithmetic: fp32 state and accumulation for both dtypes.
  *
  * Scratch: when the channel count is too small to fill the GPU, the

@@ -241,8 +241,11 @@ static int selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_t
     SS_TRY(check_tensor(u, 3));
     SS_TRY(check_tensor(delta, 3));
     SS_TRY(check_tensor(A, 2));
-    SS_TRY(check_tensor(B, 3));
-    SS_TRY(check_tensor(C, 3));
+    // B, C: (Bsz, N, L), or (Bsz, G, N, L) with one B, C per group of channels
+    if (!B || !C) return SS_ERR_INVALID_ARG;
+    const bool grouped = B->ndim == 4;
+    SS_TRY(check_tensor(B, grouped ? 4 : 3));
+    SS_TRY(check_tensor(C, grouped ? 4 : 3));
     SS_TRY(check_tensor(y, 3));
     if (D) SS_TRY(check_tensor(D, 1));
     if (z) SS_TRY(check_tensor(z, 3));
@@ -264,8 +267,11 @@ static int selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (!same_shape(delta, u) || !same_shape(y, u) || (z && !same_shape(z, u)))
         return SS_ERR_SHAPE;
     if (A->shape[0] != Dch) return SS_ERR_SHAPE;
-    if (B->shape[0] != Bsz || B->shape[1] != N || B->shape[2] != L) return SS_ERR_SHAPE;
+    const int nd = grouped ? 1 : 0;  // index shift of the (N, L) dims
+    const int64_t G = grouped ? B->shape[1] : 1;
+    if (B->shape[0] != Bsz || B->shape[1 + nd] != N || B->shape[2 + nd] != L) return SS_ERR_SHAPE;
     if (!same_shape(C, B)) return SS_ERR_SHAPE;
+    if (G < 1 || (Dch > 0 && Dch % G != 0)) return SS_ERR_SHAPE;
     if (D && D->shape[0] != Dch) return SS_ERR_SHAPE;
     if (delta_bias && delta_bias->shape[0] != Dch) return SS_ERR_SHAPE;
     if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != Dch ||
@@ -286,8 +292,13 @@ static int selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_t
     a.dl = delta->data; a.sdl_b = delta->stride[0]; a.sdl_d = delta->stride[1]; a.sdl_t = delta->stride[2];
     if (z) { a.z = z->data; a.sz_b = z->stride[0]; a.sz_d = z->stride[1]; a.sz_t = z->stride[2]; }
     a.y = y->data; a.sy_b = y->stride[0]; a.sy_d = y->stride[1]; a.sy_t = y->stride[2];
-    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_n = B->stride[1]; a.sB_t = B->stride[2];
-    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_n = C->stride[1]; a.sC_t = C->stride[2];
+    a.Bm = B->data; a.sB_b = B->stride[0];
+    a.sB_n = B->stride[1 + nd]; a.sB_t = B->stride[2 + nd];
+    a.Cm = C->data; a.sC_b = C->stride[0];
+    a.sC_n = C->stride[1 + nd]; a.sC_t = C->stride[2 + nd];
+    a.G = (int)G;
+    a.sB_g = grouped ? B->stride[1] : 0;
+    a.sC_g = grouped ? C->stride[1] : 0;
     a.A = static_cast<const float*>(A->data); a.sA_d = A->stride[0]; a.sA_n = A->stride[1];
     if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
     if (delta_bias) { a.bias = static_cast<const float*>(delta_bias->data); a.sbias = delta_bias->stride[0]; }
@@ -407,6 +418,7 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
                           ss_tensor* ddelta_bias, void* stream) {
     ScanArgs f{};
     bool nothing = false;
+    if (B && B->ndim == 4) return SS_ERR_UNSUPPORTED;  // B, C shared per batch row only
     // the forward inputs are checked as for the forward scan, dout in the place of y
     SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr,
                           const_cast<ss_tensor*>(dout), nullptr, &f, &nothing));

@@ -17,6 +17,9 @@ struct ScanArgs {
     void* y;        int64_t sy_b, sy_d, sy_t;
     const void* Bm; int64_t sB_b, sB_n, sB_t;
     const void* Cm; int64_t sC_b, sC_n, sC_t;
+    // B, C per channel group: G groups of D / G consecutive channels, group
+    // stride sB_g / sC_g; G <= 1 is one B, C per batch row
+    int G; int64_t sB_g, sC_g;
     const float* A; int64_t sA_d, sA_n;
     const float* Dv; int64_t sD;
     const float* bias; int64_t sbias;

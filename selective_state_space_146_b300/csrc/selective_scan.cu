@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <type_traits>
 #include <cstdio>
 #include <cstdlib>
@@ -66,8 +67,9 @@ __global__ void __launch_bounds__(128) scan_general(ScanArgs a) {
     const T* dl = static_cast<const T*>(a.dl) + b * a.sdl_b + d * a.sdl_d;
     const T* z = a.z ? static_cast<const T*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     T* y = static_cast<T*>(a.y) + b * a.sy_b + d * a.sy_d;
-    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b;
-    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b;
+    const int g = a.G > 1 ? d / (a.D / a.G) : 0;  // this channel's B, C group
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b + g * a.sB_g;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b + g * a.sC_g;
     // conv in front (optional): u = silu(bias + sum_k w[k] x[t - W + 1 + k])
     float wk[4] = {0.f, 0.f, 0.f, 0.f}, xh[3] = {0.f, 0.f, 0.f}, cbias = 0.f;
     if (a.cw) {
@@ -128,6 +130,8 @@ struct FastParams {
     const float* cb; int64_t scb;           // bias (D), may be null
     int cwidth;
     float* summ;    // [nseg-1][Bsz*D][2][N]: prod of decays, end state from zero
+    int bc_groups;  // B, C groups per batch row (1: shared)
+    int bc_dpg;     // channels per group, a multiple of the channel tile
     int softplus;
     unsigned* err;
 };
@@ -355,6 +359,8 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     if (warp == 0) {
         // ---------------- TMA loads ----------------
         if (lane == 0) {
+            // the CTA's B / C rows: batch row b, group of the tile's channels
+            const int bc_row = b * p.bc_groups + d0 / p.bc_dpg;
             tma_prefetch_desc(&tm_u);
             tma_prefetch_desc(&tm_dl);
             tma_prefetch_desc(&tm_B);
@@ -366,8 +372,8 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
                 const int t0 = tbeg + k * TT;
                 uint8_t* st = stage(s);
                 mbar_arrive_expect_tx(&raw[s], Cfg::RAW_TX);
-                tma_load_3d(st + Cfg::OFF_RAWB, &tm_B, &raw[s], t0, 0, b);
-                if (Cfg::LOAD_C) tma_load_3d(st + Cfg::OFF_RAWC, &tm_C, &raw[s], t0, 0, b);
+                tma_load_3d(st + Cfg::OFF_RAWB, &tm_B, &raw[s], t0, 0, bc_row);
+                if (Cfg::LOAD_C) tma_load_3d(st + Cfg::OFF_RAWC, &tm_C, &raw[s], t0, 0, bc_row);
                 mbar_arrive_expect_tx(&full[s], Cfg::TILE_TX);
                 tma_load_3d(st, &tm_u, &full[s], t0, d0, b);
                 tma_load_3d(st + Cfg::OFF_DL, &tm_dl, &full[s], t0, d0, b);
@@ -672,6 +678,13 @@ static bool fast_layout_ok(const ScanArgs& a) {
         return true;
     };
     if (a.D > 1 && a.su_d == 0) return false;
+    if (a.G > 1) {
+        // every channel tile (32 or 64 channels) inside one group, and the
+        // (batch, group) rows of B / C evenly spaced so one tensor map covers them
+        if ((a.D / a.G) % 64 != 0) return false;
+        if (a.sB_b != a.G * a.sB_g || a.sC_b != a.G * a.sC_g) return false;
+        if ((a.sB_g * es) % 16 || (a.sC_g * es) % 16) return false;
+    }
     return row_ok(a.u, a.su_b, a.su_d, a.su_t) && row_ok(a.dl, a.sdl_b, a.sdl_d, a.sdl_t) &&
            row_ok(a.z, a.sz_b, a.sz_d, a.sz_t) && row_ok(a.y, a.sy_b, a.sy_d, a.sy_t) &&
            row_ok(a.Bm, a.sB_b, a.sB_n, a.sB_t) && row_ok(a.Cm, a.sC_b, a.sC_n, a.sC_t) &&
@@ -722,6 +735,9 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     fp.cw = a.cw; fp.scw_d = a.scw_d; fp.scw_k = a.scw_k; fp.cb = a.cb; fp.scb = a.scb;
     fp.cwidth = a.cwidth;
     fp.softplus = a.softplus; fp.err = a.err;
+    const bool grouped = a.G > 1;
+    fp.bc_groups = grouped ? a.G : 1;
+    fp.bc_dpg = grouped ? a.D / a.G : a.D;
 
     // Segments: enough CTAs to give every SM several consumer warps.
     const int sms = sm_count_current();
@@ -741,8 +757,11 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     CUtensorMap maps[5];
     if (!make_map_3d(&maps[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, TT, DT) ||
         !make_map_3d(&maps[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, TT, DT) ||
-        !make_map_3d(&maps[3], a.Bm, a.dtype, a.L, a.N, a.Bsz, a.sB_n, a.sB_b, TT, 16, false) ||
-        !make_map_3d(&maps[4], a.Cm, a.dtype, a.L, a.N, a.Bsz, a.sC_n, a.sC_b, TT, 16, false))
+        // grouped B / C: (batch, group) rows merged, row stride = group stride
+        !make_map_3d(&maps[3], a.Bm, a.dtype, a.L, a.N, (int64_t)a.Bsz * fp.bc_groups, a.sB_n,
+                     grouped ? a.sB_g : a.sB_b, TT, 16, false) ||
+        !make_map_3d(&maps[4], a.Cm, a.dtype, a.L, a.N, (int64_t)a.Bsz * fp.bc_groups, a.sC_n,
+                     grouped ? a.sC_g : a.sC_b, TT, 16, false))
         return SS_ERR_CUDA;
     if (a.z) {
         if (!make_map_3d(&maps[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, TT, DT))
@@ -780,6 +799,132 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
     if (a.N <= 16) scan_general<T, 16><<<blocks, threads, 0, st>>>(a);
     else if (a.N <= 64) scan_general<T, 64><<<blocks, threads, 0, st>>>(a);
     else scan_general<T, 256><<<blocks, threads, 0, st>>>(a);
+    count_launch(1);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Per-channel B / C (groups smaller than a channel tile, e.g. one B, C per
+// channel): every channel streams its own 2 N rows, 64 bytes per step in bf16,
+// so the kernel is bound by HBM.  Sixteen lanes per channel, lane n keeping
+// state n; rows are read 16 steps (32 or 64 bytes) at a time with vector
+// loads.  delta is computed once per step (lane n takes step n of the chunk)
+// and shared by shuffles; the 16 partial readouts of each lane are
+// reduce-scattered so that lane n ends with y of step n and finishes it.
+
+template <typename T>
+__device__ __forceinline__ void load16_row(const T* p, float* v) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(p) + q);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[8 * q + 2 * i] = __uint_as_float(ww[i] << 16);
+                v[8 * q + 2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(p) + q);
+            v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+        }
+    }
+}
+
+template <typename T, bool HAS_Z>
+__global__ void __launch_bounds__(256) scan_pc(ScanArgs a) {
+    constexpr int TC = 16;
+    const int lane = threadIdx.x & 31, n = lane & 15;
+    const int64_t ch = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+    const bool valid = ch < (int64_t)a.Bsz * a.D;
+    const int64_t chs = valid ? ch : 0;
+    const int b = (int)(chs / a.D), d = (int)(chs % a.D);
+    const int g = a.G > 1 ? d / (a.D / a.G) : 0;
+    const float A2 = a.A[d * a.sA_d + n * a.sA_n] * kLog2e;
+    float h = (valid && a.h0) ? a.h0[b * a.sh_b + d * a.sh_d + n * a.sh_n] : 0.f;
+    const float Dd = a.Dv ? a.Dv[d * a.sD] : 0.f;
+    const float bd = a.bias ? a.bias[d * a.sbias] : 0.f;
+    const bool sp = a.softplus != 0;
+    const T* u = static_cast<const T*>(a.u) + b * a.su_b + d * a.su_d;
+    const T* dl = static_cast<const T*>(a.dl) + b * a.sdl_b + d * a.sdl_d;
+    const T* z = HAS_Z ? static_cast<const T*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
+    T* y = static_cast<T*>(a.y) + b * a.sy_b + d * a.sy_d;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b + g * a.sB_g + n * a.sB_n;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b + g * a.sC_g + n * a.sC_n;
+    const int src = lane & 16;  // first lane of this channel's group
+
+    for (int t0 = 0; t0 < a.L; t0 += TC) {
+        const int tn = min(TC, a.L - t0);
+        float bv[TC], cv[TC], uv[TC];
+        if (tn == TC) {
+            load16_row<T>(Bp + t0, bv);
+            load16_row<T>(Cp + t0, cv);
+            load16_row<T>(u + t0, uv);
+        } else {
+#pragma unroll
+            for (int j = 0; j < TC; ++j) {
+                const bool in = j < tn;
+                bv[j] = in ? Elem<T>::to_f(Bp[t0 + j]) : 0.f;
+                cv[j] = in ? Elem<T>::to_f(Cp[t0 + j]) : 0.f;
+                uv[j] = in ? Elem<T>::to_f(u[t0 + j]) : 0.f;
+            }
+        }
+        float own = 0.f;
+        if (n < tn) {
+            const float x = Elem<T>::to_f(dl[t0 + n]) + bd;
+            own = sp ? softplus_f(x) : x;
+        }
+        float yp[TC];
+#pragma unroll
+        for (int j = 0; j < TC; ++j) {
+            const float dd = __shfl_sync(0xffffffffu, own, src + j);
+            h = fmaf(ex2_approx(dd * A2), h, dd * uv[j] * bv[j]);
+            yp[j] = cv[j] * h;
+        }
+        float y8[8], y4[4], y2[2], y1[1];
+        reduce_half<16>(yp, y8, lane & 8, 8);
+        reduce_half<8>(y8, y4, lane & 4, 4);
+        reduce_half<4>(y4, y2, lane & 2, 2);
+        reduce_half<2>(y2, y1, lane & 1, 1);
+        // lane n now holds the readout of step t0 + n
+        if (valid && n < tn) {
+            const float uu = Elem<T>::to_f(u[t0 + n]);
+            float out = fmaf(Dd, uu, y1[0]);
+            if constexpr (HAS_Z) {
+                const float zz = Elem<T>::to_f(z[t0 + n]);
+                out *= zz * sigmoid_accurate(zz);
+            }
+            y[t0 + n] = Elem<T>::from_f(out);
+        }
+    }
+    if (valid && a.last) a.last[b * a.sl_b + d * a.sl_d + n * a.sl_n] = h;
+}
+
+static bool pc_layout_ok(const ScanArgs& a) {
+    if (a.N != 16 || a.cw) return false;
+    const int es = a.dtype == SS_BF16 ? 2 : 4;
+    auto row_ok = [&](const void* ptr, std::initializer_list<int64_t> outer, int64_t st) {
+        if (!ptr) return true;
+        if (st != 1 && a.L > 1) return false;
+        if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+        for (int64_t o : outer)
+            if ((o * es) % 16) return false;
+        return true;
+    };
+    return row_ok(a.u, {a.su_b, a.su_d}, a.su_t) && row_ok(a.dl, {a.sdl_b, a.sdl_d}, a.sdl_t) &&
+           row_ok(a.z, {a.sz_b, a.sz_d}, a.sz_t) && row_ok(a.y, {a.sy_b, a.sy_d}, a.sy_t) &&
+           row_ok(a.Bm, {a.sB_b, a.sB_g, a.sB_n}, a.sB_t) &&
+           row_ok(a.Cm, {a.sC_b, a.sC_g, a.sC_n}, a.sC_t);
+}
+
+template <typename T>
+static int run_pc(const ScanArgs& a, cudaStream_t st) {
+    const int64_t blocks = ((int64_t)a.Bsz * a.D + 15) / 16;
+    if (a.z) scan_pc<T, true><<<(unsigned)blocks, 256, 0, st>>>(a);
+    else scan_pc<T, false><<<(unsigned)blocks, 256, 0, st>>>(a);
     count_launch(1);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
@@ -833,6 +978,8 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
         if (split == 2) return run_fast<float, 2, 2, false>(a, st, scratch);
         return run_fast<float, 4, 4, false>(a, st, scratch);
     }
+    if (force != 0 && a.L > 0 && a.G > 1 && pc_layout_ok(a))
+        return bf ? run_pc<__nv_bfloat16>(a, st) : run_pc<float>(a, st);
     return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
 }
 

@@ -10,7 +10,9 @@ Recipe (every workload):
     dt0=9, dout=10);
   * normal draws are float32, then rounded to bfloat16 (round to nearest
     even) for bfloat16 workloads; the oracle reads the rounded values;
-  * selective scan: u, z, B, C ~ N(0, 1); delta_raw ~ N(0, 0.1^2);
+  * selective scan: u, z, B, C ~ N(0, 1); delta_raw ~ N(0, 0.1^2); B, C
+    either shared per batch row or one per group of channels (same draws,
+    one more dimension);
     A[d, n] = -(n + 1) (S4D-real); D ~ N(0, 1);
     delta_bias[d] = log(expm1(dt_d)) so that softplus(delta_bias) = dt_d, with
     dt_d log-uniform in [dt_min, dt_max];
@@ -130,22 +132,25 @@ def _log_uniform(n, lo, hi, seed, k):
 
 
 def selective_inputs(batch, d_inner, d_state, seqlen, dtype="bf16", *, gate=True, skip=True,
-                     bias=True, dt_min=1e-3, dt_max=1e-1, seed=0):
+                     bias=True, dt_min=1e-3, dt_max=1e-1, groups=None, seed=0):
     """Inputs of one selective-scan call, as CPU tensors.
 
     Returns a dict with u, delta (raw, before bias and softplus), z, A, B, C,
     D, delta_bias; z / D / delta_bias are None when switched off.
     Layouts: u, delta, z (batch, d_inner, seqlen); A (d_inner, d_state) f32;
-    B, C (batch, d_state, seqlen); D, delta_bias (d_inner,) f32.
+    B, C (batch, d_state, seqlen), or (batch, groups, d_state, seqlen) when
+    `groups` is given (one B, C per group of d_inner / groups channels);
+    D, delta_bias (d_inner,) f32.
     """
     td = _tdtype(dtype)
     shp = (batch, d_inner, seqlen)
+    bc = (batch, d_state, seqlen) if groups is None else (batch, groups, d_state, seqlen)
     out = {
         "u": _normal(shp, seed, "u").to(td),
         "delta": _normal(shp, seed, "delta", 0.1).to(td),
         "z": _normal(shp, seed, "z").to(td) if gate else None,
-        "B": _normal((batch, d_state, seqlen), seed, "B").to(td),
-        "C": _normal((batch, d_state, seqlen), seed, "C").to(td),
+        "B": _normal(bc, seed, "B").to(td),
+        "C": _normal(bc, seed, "C").to(td),
         "D": _normal((d_inner,), seed, "D") if skip else None,
         "A": -(torch.arange(d_state, dtype=torch.float32, device=_DEVICE) + 1.0)
         .expand(d_inner, d_state).contiguous(),

@@ -229,3 +229,18 @@ def test_backward_argument_errors(lib):
     b = _sel_args()
     b["y"] = FakeT((2, 8, 64), _abi.SS_F32)                           # dout dtype
     assert _call_bwd(lib, b, _bwd_grads()) == -3
+
+
+def test_grouped_bc_argument_errors(lib):
+    a = _sel_args(D=12)
+    a["B"] = FakeT((2, 5, 16, 64))                         # 12 channels in 5 groups
+    a["C"] = FakeT((2, 5, 16, 64))
+    assert _call_sel(lib, a) == -2
+    a = _sel_args(D=12)
+    a["B"] = FakeT((2, 4, 16, 64))
+    a["C"] = FakeT((2, 3, 16, 64))                         # B and C disagree
+    assert _call_sel(lib, a) == -2
+    a = _sel_args(D=12)
+    a["B"] = FakeT((2, 4, 16, 64))
+    a["C"] = FakeT((2, 4, 16, 64))
+    assert _call_bwd(lib, a, _bwd_grads(D=12)) == -5       # backward: shared B, C only
