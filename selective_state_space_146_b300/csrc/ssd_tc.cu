@@ -375,6 +375,349 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 }  // namespace ssdtc
 
 // ---------------------------------------------------------------------------
+// Two heads of one group per CTA (one CTA per SM, all 512 TMEM columns).
+//
+// Same algebra as ssd_chunk_tc.  C B^T is shared by the heads of a group, so
+// it is loaded and computed once for the pair; each head has its own Ydiag,
+// Yoff and dS^T columns, so C B^T of the next block can be issued as soon as
+// its B, C have landed, while both heads still finish the current block's
+// epilogue, and C S^T is issued per head as soon as that head's state copy is
+// written.  TMEM: C B^T [0, 128); head hh: Ydiag 128 + 192 hh, Yoff 192 + 192 hh,
+// dS^T 256 + 192 hh.  Warps 0-3 compute head 0, warps 4-7 head 1 (warp w
+// reads TMEM lanes 32 (w % 4) ..), warp 8 issues TMA loads and MMAs.
+namespace ssdtc2 {
+
+using ssdtc::N;
+using ssdtc::P;
+using ssdtc::QB;
+using ssdtc::pack_bf16;
+using ssdtc::swz;
+using ssdtc::unpack8;
+
+constexpr int NHEAD = 2;
+constexpr int NCOMP = 128 * NHEAD;
+constexpr int NTHREADS = NCOMP + 32;
+constexpr int OFF_X = 0;                  // NHEAD x [128 t][64 p] bf16            32 KB
+constexpr int OFF_B = OFF_X + 32768;      // 2 x [128 t][64 n]                     32 KB
+constexpr int OFF_C = OFF_B + 32768;      // 2 x [128 t][64 n]                     32 KB
+constexpr int OFF_M = OFF_C + 32768;      // NHEAD x M (K-major, two 64-col halves) 64 KB
+constexpr int OFF_S = OFF_M + 65536;      // NHEAD x (X~, then the S^T copy)       32 KB
+constexpr int OFF_DT = OFF_S + 32768;     // [128 t][8 h] bf16                      2 KB
+constexpr int OFF_CUM = OFF_DT + 2048;    // [NHEAD][128] f32
+constexpr int OFF_DTF = OFF_CUM + 1024;
+constexpr int OFF_GF = OFF_DTF + 1024;
+constexpr int OFF_WS = OFF_GF + 1024;     // [NHEAD][4] f32
+constexpr int OFF_BAR = OFF_WS + 64;      // 12 mbarriers, then the TMEM address
+constexpr int SMEM_BYTES = OFF_BAR + 128 + 16 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ uint32_t tm_ydg(int hh) { return 128u + 192u * hh; }
+__device__ __forceinline__ uint32_t tm_yoff(int hh) { return 192u + 192u * hh; }
+__device__ __forceinline__ uint32_t tm_ds(int hh) { return 256u + 192u * hh; }
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_dt,
+              const ssdtc::Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_bc = bar + 0;      // B, C, dt of the block landed
+    uint64_t* bar_x = bar + 1;       // [hh] x of the block landed
+    uint64_t* bar_cb = bar + 3;      // C B^T done
+    uint64_t* bar_yoff = bar + 4;    // [hh] C S^T done
+    uint64_t* bar_mma23 = bar + 6;   // [hh] M X and B^T X~ done
+    uint64_t* bar_m = bar + 8;       // [hh] M and X~ written (compute -> control)
+    uint64_t* bar_s = bar + 10;      // [hh] state copy written, x consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 128);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hpairs = p.H / NHEAD;
+    const int b = blockIdx.x / hpairs, h0 = (blockIdx.x % hpairs) * NHEAD;
+    const int g = h0 / (p.H / p.G);
+    const uint32_t sbase = smem_u32(sm);
+    const int nblk = (p.L + QB - 1) / QB;
+
+    if (tid == 0) {
+        mbar_init(bar_bc, 1);
+        mbar_init(bar_cb, 1);
+        for (int hh = 0; hh < NHEAD; ++hh) {
+            mbar_init(&bar_x[hh], 1);
+            mbar_init(&bar_yoff[hh], 1);
+            mbar_init(&bar_mma23[hh], 1);
+            mbar_init(&bar_m[hh], 128);
+            mbar_init(&bar_s[hh], 128);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == NCOMP / 32) {
+        // ================= control: TMA loads and MMA issue =================
+        if (lane == 0) {
+            constexpr uint32_t ID_CB = tc::idesc_bf16(QB, QB, false, false);
+            constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, P, false, true);
+            constexpr uint32_t ID_YDG = tc::idesc_bf16(QB, P, false, true);
+            constexpr uint32_t ID_DS = tc::idesc_bf16(N, P, true, true);
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(&tm_B);
+            tma_prefetch_desc(&tm_C);
+            tma_prefetch_desc(&tm_dt);
+            auto load_bc = [&](int k) {
+                const int t0 = k * QB;
+                mbar_arrive_expect_tx(bar_bc, 32768 + 32768 + 2048);
+                tma_load_4d(sm + OFF_B, &tm_B, bar_bc, 0, g, t0, b);
+                tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_bc, 64, g, t0, b);
+                tma_load_4d(sm + OFF_C, &tm_C, bar_bc, 0, g, t0, b);
+                tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_bc, 64, g, t0, b);
+                tma_load_3d(sm + OFF_DT, &tm_dt, bar_bc, (h0 / 8) * 8, t0, b);
+            };
+            auto load_x = [&](int hh, int k) {
+                mbar_arrive_expect_tx(&bar_x[hh], 16384);
+                tma_load_4d(sm + OFF_X + hh * 16384, &tm_x, &bar_x[hh], 0, h0 + hh, k * QB, b);
+            };
+            load_bc(0);
+            for (int hh = 0; hh < NHEAD; ++hh) load_x(hh, 0);
+            bool go = true;
+            for (int k = 0; k < nblk && go; ++k) {
+                // C B^T: needs B, C of block k (the CB columns were read by
+                // both heads' M of block k-1 before block k's B, C were loaded)
+                if (!mbar_wait(bar_bc, k & 1, p.err)) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + 0, tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024),
+                                 tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024), ID_CB, kk > 0);
+                }
+                tc::mma_commit(bar_cb);
+                // C S^T per head: needs the head's state copy S(k)
+                for (int hh = 0; hh < NHEAD && go; ++hh) {
+                    if (!mbar_wait(&bar_s[hh], k & 1, p.err)) { go = false; break; }
+                    if (k > 0) load_x(hh, k);  // x of block k-1 consumed
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + tm_yoff(hh),
+                                     tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024),
+                                     tc::smem_desc_sw128(sbase + OFF_S + hh * 16384 + kk * 2048,
+                                                         16384, 1024),
+                                     ID_YOFF, kk > 0);
+                    }
+                    tc::mma_commit(&bar_yoff[hh]);
+                }
+                // M X and B^T X~ per head: needs the head's M and X~
+                for (int hh = 0; hh < NHEAD && go; ++hh) {
+                    if (!mbar_wait(&bar_m[hh], k & 1, p.err)) { go = false; break; }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + tm_ydg(hh),
+                                     tc::smem_desc_sw128(sbase + OFF_M + hh * 32768 + koff, 0, 1024),
+                                     tc::smem_desc_sw128(sbase + OFF_X + hh * 16384 + kk * 2048,
+                                                         16384, 1024),
+                                     ID_YDG, kk > 0);
+                        tc::mma_bf16(tmem + tm_ds(hh),
+                                     tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024),
+                                     tc::smem_desc_sw128(sbase + OFF_S + hh * 16384 + kk * 2048,
+                                                         16384, 1024),
+                                     ID_DS, kk > 0);
+                    }
+                    tc::mma_commit(&bar_mma23[hh]);
+                }
+                if (go && k + 1 < nblk) {
+                    // B, C, dt free once every MMA of block k is done
+                    for (int hh = 0; hh < NHEAD && go; ++hh)
+                        if (!mbar_wait(&bar_mma23[hh], k & 1, p.err)) go = false;
+                    if (go) load_bc(k + 1);
+                }
+            }
+        }
+    } else {
+        // ================= compute warps: head hh, one TMEM lane / row each =================
+        const int hh = warp / 4, wq = warp & 3, row = tid & 127;
+        const int h = h0 + hh;
+        const int nb = 1 + hh;  // named barrier of this head's 128 threads
+        const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
+        const float A2 = p.A[h * p.sA] * kLog2e;
+        const float Dh = p.Dv ? p.Dv[h * p.sD] : 0.f;
+        const bool factor = A2 <= 0.f;
+        float* cum = reinterpret_cast<float*>(sm + OFF_CUM) + hh * 128;
+        float* dtf = reinterpret_cast<float*>(sm + OFF_DTF) + hh * 128;
+        float* gf = reinterpret_cast<float*>(sm + OFF_GF) + hh * 128;
+        float* wsum = reinterpret_cast<float*>(sm + OFF_WS) + hh * 4;
+        uint8_t* xs = sm + OFF_X + hh * 16384;
+        uint8_t* ss = sm + OFF_S + hh * 16384;
+        uint8_t* ms = sm + OFF_M + hh * 32768;
+
+        float S[P];
+        const float* h0row = p.h0 ? p.h0 + (int64_t)b * p.sh_b + (int64_t)h * p.sh_h +
+                                        (int64_t)row * p.sh_n
+                                  : nullptr;
+#pragma unroll
+        for (int i = 0; i < P; ++i) S[i] = h0row ? h0row[i * p.sh_p] : 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(ss + swz(row, c)) =
+                make_uint4(pack_bf16(S[c * 8 + 0], S[c * 8 + 1]), pack_bf16(S[c * 8 + 2], S[c * 8 + 3]),
+                           pack_bf16(S[c * 8 + 4], S[c * 8 + 5]), pack_bf16(S[c * 8 + 6], S[c * 8 + 7]));
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_s[hh]);  // S(0) is ready
+
+        bool ok = true;
+        for (int k = 0; k < nblk; ++k) {
+            const int t0 = k * QB;
+            if (!named_sync_and(nb, 128, mbar_wait(bar_bc, k & 1, p.err))) { ok = false; break; }
+            // ---- cumulative decay (log2 units) and the column factors
+            const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + row * 16 + (h & 7) * 2);
+            const float dtv = __uint_as_float((uint32_t)raw << 16);
+            float v = dtv * A2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane == 31) wsum[wq] = v;
+            named_sync(nb, 128);
+            for (int w = 0; w < wq; ++w) v += wsum[w];
+            const float cum_t = v;
+            cum[row] = cum_t;
+            dtf[row] = dtv;
+            const float cum_end = __shfl_sync(0xffffffffu, cum_t, 31);
+            gf[row] = ex2_approx(cum_end - cum_t) * dtv;  // <= dt when A <= 0
+            named_sync(nb, 128);
+            const float cum_last = cum[QB - 1];
+
+            if (!named_sync_and(nb, 128, mbar_wait(bar_cb, k & 1, p.err))) { ok = false; break; }
+            tc::fence_after_sync();
+            // ---- row `row` of M = C B^T o decay o dt (lower triangle), bf16, K-major
+#pragma unroll 1
+            for (int jc = 0; jc < 4; ++jc) {
+                uint8_t* mt = ms + (jc >> 1) * 16384;
+                if (jc <= wq) {
+                    float cb[32];
+                    tc::tmem_ld32(trow + jc * 32, cb);
+                    tc::tmem_wait_ld();
+                    float m[32];
+                    if (jc < wq && factor) {
+                        const float f1 = ex2_approx(cum_t - cum[jc * 32 + 31]);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) m[e] = cb[e] * (f1 * gf[jc * 32 + e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int j = jc * 32 + e;
+                            const float dec = ex2_approx(cum_t - cum[j]);  // j > row: discarded
+                            m[e] = j <= row ? cb[e] * dec * dtf[j] : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int c = (jc & 1) * 4 + q;
+                        *reinterpret_cast<uint4*>(mt + swz(row, c)) =
+                            make_uint4(pack_bf16(m[q * 8 + 0], m[q * 8 + 1]), pack_bf16(m[q * 8 + 2], m[q * 8 + 3]),
+                                       pack_bf16(m[q * 8 + 4], m[q * 8 + 5]), pack_bf16(m[q * 8 + 6], m[q * 8 + 7]));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(mt + swz(row, (jc & 1) * 4 + q)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // ---- X~ row = w_t x_t into the state-copy buffer, once C S^T has read it
+            const bool got = mbar_wait(&bar_x[hh], k & 1, p.err) && mbar_wait(&bar_yoff[hh], k & 1, p.err);
+            if (!named_sync_and(nb, 128, got)) { ok = false; break; }
+            {
+                const float wt = ex2_approx(cum_last - cum_t) * dtv;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float x8[8];
+                    unpack8(*reinterpret_cast<const uint4*>(xs + swz(row, c)), x8);
+                    *reinterpret_cast<uint4*>(ss + swz(row, c)) =
+                        make_uint4(pack_bf16(wt * x8[0], wt * x8[1]), pack_bf16(wt * x8[2], wt * x8[3]),
+                                   pack_bf16(wt * x8[4], wt * x8[5]), pack_bf16(wt * x8[6], wt * x8[7]));
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(&bar_m[hh]);
+
+            if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
+            tc::fence_after_sync();
+            // ---- y row = Ydiag + exp(cum) Yoff + D x
+            {
+                const float eoff = ex2_approx(cum_t);
+                const int t = t0 + row;
+                __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float yd[32], yo[32];
+                    tc::tmem_ld32(trow + tm_ydg(hh) + half * 32, yd);
+                    tc::tmem_ld32(trow + tm_yoff(hh) + half * 32, yo);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float x8[8];
+                        unpack8(*reinterpret_cast<const uint4*>(xs + swz(row, half * 4 + q)), x8);
+                        float o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = fmaf(Dh, x8[i], fmaf(eoff, yo[q * 8 + i], yd[q * 8 + i]));
+                        if (t < p.L)
+                            *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
+                                make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                           pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+                    }
+                }
+            }
+            // ---- S^T row <- exp(cum_last) S^T + dS^T; bf16 copy for block k+1
+            {
+                const float ablk = ex2_approx(cum_last);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float ds[32];
+                    tc::tmem_ld32(trow + tm_ds(hh) + half * 32, ds);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(ss + swz(row, c)) =
+                        make_uint4(pack_bf16(S[c * 8 + 0], S[c * 8 + 1]), pack_bf16(S[c * 8 + 2], S[c * 8 + 3]),
+                                   pack_bf16(S[c * 8 + 4], S[c * 8 + 5]), pack_bf16(S[c * 8 + 6], S[c * 8 + 7]));
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(&bar_s[hh]);
+        }
+        if (ok && p.last) {
+            float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)h * p.sl_h + (int64_t)row * p.sl_n;
+#pragma unroll
+            for (int i = 0; i < P; ++i) ls[i * p.sl_p] = S[i];
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace ssdtc2
+
+// ---------------------------------------------------------------------------
 // Host side.
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -444,17 +787,29 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
     p.h0 = a.h0; p.sh_b = a.sh_b; p.sh_h = a.sh_h; p.sh_p = a.sh_p; p.sh_n = a.sh_n;
     p.err = a.err;
 
-    static bool attr_set[64] = {};
+    // two heads per CTA when every group holds an even number of heads
+    // (SS_SSD_PATH=tc1 keeps one head per CTA, for tests)
+    const bool pair = (a.H / a.G) % 2 == 0 && !(force && !strcmp(force, "tc1"));
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(ssdtc::ssd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ssdtc::SMEM_BYTES) != cudaSuccess)
-            return SS_ERR_LAUNCH;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev < 0 || dev >= 64 || !attr_set[pair][dev]) {
+        const cudaError_t e =
+            pair ? cudaFuncSetAttribute(ssdtc2::ssd_chunk_tc2,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        ssdtc2::SMEM_BYTES)
+                 : cudaFuncSetAttribute(ssdtc::ssd_chunk_tc,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        ssdtc::SMEM_BYTES);
+        if (e != cudaSuccess) return SS_ERR_LAUNCH;
+        if (dev >= 0 && dev < 64) attr_set[pair][dev] = true;
     }
-    ssdtc::ssd_chunk_tc<<<(unsigned)(a.Bsz * a.H), ssdtc::NTHREADS, ssdtc::SMEM_BYTES, st>>>(
-        mx, mb, mc, mdt, p);
+    if (pair)
+        ssdtc2::ssd_chunk_tc2<<<(unsigned)(a.Bsz * (a.H / 2)), ssdtc2::NTHREADS, ssdtc2::SMEM_BYTES,
+                                st>>>(mx, mb, mc, mdt, p);
+    else
+        ssdtc::ssd_chunk_tc<<<(unsigned)(a.Bsz * a.H), ssdtc::NTHREADS, ssdtc::SMEM_BYTES, st>>>(
+            mx, mb, mc, mdt, p);
     count_launch(1);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }

@@ -45,11 +45,13 @@ CASES = [
     (1, 1, 2, 8, 16, 1, "f32", 64, True),            # L = 1
     (1, 130, 3, 5, 7, 3, "f32", 64, True),           # odd sizes
     (1, 384, 2, 64, 256, 1, "bf16", 64, True),       # N = 256
+    (1, 384, 3, 64, 128, 1, "bf16", 128, True),      # odd heads per group: one head per CTA
+    (2, 200, 8, 64, 128, 4, "bf16", 128, True),      # two heads per group, ragged tail
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:8])))
-@pytest.mark.parametrize("ssd_path", [None, "general"], indirect=True)
+@pytest.mark.parametrize("ssd_path", [None, "general", "tc1"], indirect=True)
 def test_small_shapes(cuda_device, ssd_path, case):
     Bsz, L, H, P, N, G, dt, chunk, skip = case
     inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, skip=skip, seed=L + H)
@@ -68,7 +70,8 @@ def test_chunk_size_does_not_change_result(cuda_device):
         check_close(to_np(s), to_np(outs[0][1]), torch.bfloat16, "state across chunk sizes")
 
 
-def test_full_size_workload_sampled(cuda_device):
+@pytest.mark.parametrize("ssd_path", [None, "tc1"], indirect=True)
+def test_full_size_workload_sampled(cuda_device, ssd_path):
     cfg = inputs.WORKLOADS["mamba2_ssd"]
     inp = inputs.workload_ssd_inputs(cfg)
     y, s = _run(inp, cuda_device, cfg.chunk)
