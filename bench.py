@@ -304,10 +304,12 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
                    "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
                    "launches_per_call": launches_per_call}
             if name == "mamba2_ssd":
-                # executed MMA flops of the 128-step block form (C B^T per head)
+                # executed MMA flops of the 128-step block form: C B^T once per
+                # pair of heads of a group (once per head for odd heads per group)
                 nblk = -(-cfg.seqlen // 128)
                 P, N, Q = cfg.headdim, cfg.d_state, 128
-                ex = cfg.batch * cfg.nheads * nblk * 2 * Q * (Q * N + P * N + Q * P + N * P)
+                cb_share = 2 if (cfg.nheads // cfg.ngroups) % 2 == 0 else 1
+                ex = cfg.batch * cfg.nheads * nblk * 2 * Q * (Q * N / cb_share + P * N + Q * P + N * P)
                 tf = ex / (ms * 1e-3) / 1e12
                 row["tensor_tflops_executed"] = round(tf, 1)
                 row["tensor_tflops_algorithmic"] = round(ssd_flops(cfg) / (ms * 1e-3) / 1e12, 1)

@@ -419,7 +419,7 @@ __device__ __forceinline__ uint32_t tm_ds(int hh) { return 256u + 192u * hh; }
 __global__ void __launch_bounds__(NTHREADS, 1)
 ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_dt,
-              const ssdtc::Params p) {
+              const __grid_constant__ CUtensorMap tm_y, const ssdtc::Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -654,11 +654,11 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
 
             if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-            // ---- y row = Ydiag + exp(cum) Yoff + D x
+            // ---- y row = Ydiag + exp(cum) Yoff + D x, written over the row's x in
+            //      shared memory; the tile leaves with one TMA store (rows past
+            //      the end are clipped)
             {
                 const float eoff = ex2_approx(cum_t);
-                const int t = t0 + row;
-                __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float yd[32], yo[32];
@@ -667,30 +667,33 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
+                        uint4* cell = reinterpret_cast<uint4*>(xs + swz(row, half * 4 + q));
                         float x8[8];
-                        unpack8(*reinterpret_cast<const uint4*>(xs + swz(row, half * 4 + q)), x8);
+                        unpack8(*cell, x8);
                         float o[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             o[i] = fmaf(Dh, x8[i], fmaf(eoff, yo[q * 8 + i], yd[q * 8 + i]));
-                        if (t < p.L)
-                            *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
-                                make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                        *cell = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
                                            pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
                     }
+                }
+                fence_proxy_async_smem();
+                named_sync(nb, 128);
+                if (row == 0) {
+                    tma_store_4d(&tm_y, xs, 0, h, t0, b);
+                    bulk_commit();
                 }
             }
             // ---- S^T row <- exp(cum_last) S^T + dS^T; bf16 copy for block k+1
             {
                 const float ablk = ex2_approx(cum_last);
+                float ds[64];
+                tc::tmem_ld32(trow + tm_ds(hh), ds);
+                tc::tmem_ld32(trow + tm_ds(hh) + 32, ds + 32);
+                tc::tmem_wait_ld();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float ds[32];
-                    tc::tmem_ld32(trow + tm_ds(hh) + half * 32, ds);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
-                }
+                for (int i = 0; i < 64; ++i) S[i] = fmaf(ablk, S[i], ds[i]);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<uint4*>(ss + swz(row, c)) =
@@ -699,8 +702,10 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
+            if (row == 0) bulk_wait_read<0>();  // y has left the x tile: it may be refilled
             mbar_arrive(&bar_s[hh]);
         }
+        if (row == 0) bulk_wait<0>();
         if (ok && p.last) {
             float* ls = p.last + (int64_t)b * p.sl_b + (int64_t)h * p.sl_h + (int64_t)row * p.sl_n;
 #pragma unroll
@@ -779,6 +784,13 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
         cuuint32_t box[3] = {8, ssdtc::QB, 1};
         if (!encode(&mdt, a.dt, 3, dims, str, box, false)) return SS_ERR_CUDA;
     }
+    CUtensorMap my;
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)a.P, (cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.Bsz};
+        cuuint64_t str[3] = {(cuuint64_t)(a.sy_h * 2), (cuuint64_t)(a.sy_l * 2), (cuuint64_t)(a.sy_b * 2)};
+        cuuint32_t box[4] = {64, 1, ssdtc::QB, 1};
+        if (!encode(&my, a.y, 4, dims, str, box, true)) return SS_ERR_CUDA;
+    }
     ssdtc::Params p{};
     p.Bsz = a.Bsz; p.L = a.L; p.H = a.H; p.G = a.G;
     p.A = a.A; p.sA = a.sA; p.Dv = a.Dv; p.sD = a.sD;
@@ -806,7 +818,7 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
     }
     if (pair)
         ssdtc2::ssd_chunk_tc2<<<(unsigned)(a.Bsz * (a.H / 2)), ssdtc2::NTHREADS, ssdtc2::SMEM_BYTES,
-                                st>>>(mx, mb, mc, mdt, p);
+                                st>>>(mx, mb, mc, mdt, my, p);
     else
         ssdtc::ssd_chunk_tc<<<(unsigned)(a.Bsz * a.H), ssdtc::NTHREADS, ssdtc::SMEM_BYTES, st>>>(
             mx, mb, mc, mdt, p);
