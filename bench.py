@@ -106,23 +106,32 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
 
 
-def source_hash():
+# The source files each measured kernel is built from.
+KERNEL_SOURCES = {
+    "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "ptx.cuh", "internal.h"],
+    "ssd_chunk_tc2": ["ssd_tc.cu", "tc.cuh", "ptx.cuh", "internal.h"],
+    "scan_bwd_fast<bf16>": ["selective_scan_bwd.cu", "ptx.cuh", "internal.h"],
+}
+
+
+def source_hash(files=None):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "selective_state_space_146_b300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(d, f), "rb").read())
+    names = files or sorted(f for f in os.listdir(d) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on
-    the current kernel sources (else None)."""
+    the kernel's current sources (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t[kernel_key]
-        return e["bytes_per_launch"] if e.get("source_hash") == source_hash() else None
+        cur = source_hash(KERNEL_SOURCES.get(kernel_key))
+        return e["bytes_per_launch"] if e.get("source_hash") == cur else None
     except Exception:
         return None
 
@@ -315,6 +324,7 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
                 row["tensor_tflops_algorithmic"] = round(ssd_flops(cfg) / (ms * 1e-3) / 1e12, 1)
                 row["tensor_peak_tflops"] = tf_peak
                 row["tensor_frac"] = round(tf / tf_peak, 4)
+                row["traffic"] = measured_traffic("ssd_chunk_tc2")
             rows[name] = row
             del g, yb, ls
             torch.cuda.empty_cache()
@@ -414,8 +424,9 @@ def backward_rows(dev, torch, abi, inputs, hbm_peak, flush):
             "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 4),
             "launches_per_call": nl / 5, "algorithmic_bytes": nbytes,
-            "note": "all eight gradients; includes the memsets of the f32 sums and the "
-                    "checkpoint scratch (stream-ordered)"}
+            "traffic": measured_traffic("scan_bwd_fast<bf16>"),
+            "note": "all eight gradients, two launches (scan_bwd_fast + scan_bwd_finish); "
+                    "stored states and partial sums in stream-ordered scratch"}
         del g, dout
         torch.cuda.empty_cache()
     except Exception as e:
