@@ -120,11 +120,58 @@ __global__ void __launch_bounds__(128) ssd_step(SSDStepArgs a) {
             Elem<T>::from_f(fmaf(a.Dv ? a.Dv[h * a.sD] : 0.f, xv, acc));
 }
 
+// N = 128 with contiguous, 16-byte aligned state rows: lane l keeps states
+// 4l .. 4l+3, so each warp moves its 512-byte row with one vector load and
+// one vector store.
+template <typename T>
+__global__ void __launch_bounds__(128) ssd_step128(SSDStepArgs a) {
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= (int64_t)a.Bsz * a.H * a.P) return;
+    const int p = (int)(row % a.P);
+    const int h = (int)((row / a.P) % a.H);
+    const int b = (int)(row / ((int64_t)a.P * a.H));
+    const int g = h / (a.H / a.G);
+    float4* st = reinterpret_cast<float4*>(a.state + b * a.ss_b + h * a.ss_h + p * a.ss_p) + lane;
+    const float4 s4 = *st;
+    const float dtv = Elem<T>::to_f(static_cast<const T*>(a.dt)[b * a.sdt_b + h * a.sdt_h]);
+    const float xv = Elem<T>::to_f(static_cast<const T*>(a.x)[b * a.sx_b + h * a.sx_h + p * a.sx_p]);
+    const float decay = ex2_approx(dtv * a.A[h * a.sA] * kLog2e);
+    const float dx = dtv * xv;
+    const T* Bp = static_cast<const T*>(a.Bm) + b * a.sB_b + g * a.sB_g + 4 * lane * a.sB_n;
+    const T* Cp = static_cast<const T*>(a.Cm) + b * a.sC_b + g * a.sC_g + 4 * lane * a.sC_n;
+    float bv[4], cv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        bv[i] = Elem<T>::to_f(Bp[i * a.sB_n]);
+        cv[i] = Elem<T>::to_f(Cp[i * a.sC_n]);
+    }
+    float4 n4;
+    n4.x = fmaf(decay, s4.x, dx * bv[0]);
+    n4.y = fmaf(decay, s4.y, dx * bv[1]);
+    n4.z = fmaf(decay, s4.z, dx * bv[2]);
+    n4.w = fmaf(decay, s4.w, dx * bv[3]);
+    *st = n4;
+    float acc = fmaf(cv[0], n4.x, fmaf(cv[1], n4.y, fmaf(cv[2], n4.z, cv[3] * n4.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0)
+        static_cast<T*>(a.y)[b * a.sy_b + h * a.sy_h + p * a.sy_p] =
+            Elem<T>::from_f(fmaf(a.Dv ? a.Dv[h * a.sD] : 0.f, xv, acc));
+}
+
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st) {
     const int64_t threads = (int64_t)a.Bsz * a.H * a.P * 32;
     const unsigned blocks = (unsigned)((threads + 127) / 128);
-    if (a.dtype == SS_BF16) ssd_step<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
-    else ssd_step<float><<<blocks, 128, 0, st>>>(a);
+    const bool vec = a.N == 128 && a.ss_n == 1 && reinterpret_cast<uintptr_t>(a.state) % 16 == 0 &&
+                     a.ss_p % 4 == 0 && a.ss_h % 4 == 0 && a.ss_b % 4 == 0;
+    if (vec) {
+        if (a.dtype == SS_BF16) ssd_step128<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
+        else ssd_step128<float><<<blocks, 128, 0, st>>>(a);
+    } else {
+        if (a.dtype == SS_BF16) ssd_step<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
+        else ssd_step<float><<<blocks, 128, 0, st>>>(a);
+    }
     count_launch(1);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }

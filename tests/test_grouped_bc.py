@@ -23,11 +23,15 @@ def _tdt(dt):
 
 @pytest.fixture
 def scan_path(request, monkeypatch):
+    """None: the library's choice; "general": the any-stride kernel; "rows":
+    per-channel B, C read row by row instead of through TMA tiles."""
     val = getattr(request, "param", None)
-    if val:
+    monkeypatch.delenv("SS_SCAN_PATH", raising=False)
+    monkeypatch.delenv("SS_PC_PATH", raising=False)
+    if val == "rows":
+        monkeypatch.setenv("SS_PC_PATH", "rows")
+    elif val:
         monkeypatch.setenv("SS_SCAN_PATH", val)
-    else:
-        monkeypatch.delenv("SS_SCAN_PATH", raising=False)
     return val
 
 
@@ -37,6 +41,8 @@ CASES = [
     (1, 192, 3, 16, 200, "f32", True),
     (1, 64, 64, 16, 500, "f32", True),     # one B, C per channel: streaming kernel
     (2, 48, 48, 16, 1000, "bf16", True),
+    (2, 20, 20, 16, 136, "bf16", True),     # per channel, partial 8-channel tile
+    (1, 24, 24, 16, 100, "f32", False),
     (2, 40, 8, 16, 72, "bf16", False),     # groups of 5 channels, no gate / skip / bias
     (2, 24, 4, 16, 77, "f32", True),       # odd length: general kernel
     (1, 16, 16, 8, 64, "f32", True),       # N = 8: general kernel
@@ -45,7 +51,7 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:6])) +
                          ("" if c[6] else "-nogate"))
-@pytest.mark.parametrize("scan_path", [None, "general"], indirect=True)
+@pytest.mark.parametrize("scan_path", [None, "general", "rows"], indirect=True)
 def test_grouped_bc_matches_oracle(cuda_device, scan_path, case):
     Bsz, D, G, N, L, dt, on = case
     inp = inputs.selective_inputs(Bsz, D, N, L, dt, gate=on, skip=on, bias=on, groups=G,
@@ -97,7 +103,8 @@ def test_grouped_bc_rejects_bad_groups(cuda_device):
                                 g["delta_bias"])
 
 
-def test_per_channel_bc_layer_shape_sampled(cuda_device):
+@pytest.mark.parametrize("scan_path", [None, "rows"], indirect=True)
+def test_per_channel_bc_layer_shape_sampled(cuda_device, scan_path):
     """One B, C per channel at the Mamba-130M layer's d_inner and length
     (batch 2; bf16): sampled channels against the oracle run channel by
     channel on its own B, C rows."""
