@@ -108,7 +108,8 @@ def peaks():
 
 # The source files each measured kernel is built from.
 KERNEL_SOURCES = {
-    "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "ptx.cuh", "internal.h"],
+    "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "scan_common.cuh", "ptx.cuh",
+                                         "internal.h"],
     "ssd_chunk_tc2": ["ssd_tc.cu", "tc.cuh", "ptx.cuh", "internal.h"],
     "scan_bwd_fast<bf16>": ["selective_scan_bwd.cu", "ptx.cuh", "internal.h"],
 }

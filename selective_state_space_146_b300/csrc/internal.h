@@ -109,6 +109,9 @@ struct Scratch {
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
+// B, C per small channel group (scan_pc / scan_pc_tma); *taken is false when
+// the layout suits neither and the caller should run the general kernel.
+int launch_selective_grouped(const ScanArgs& a, cudaStream_t st, bool* taken);
 int launch_selective_bwd(const BwdArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_selective_step(const StepArgs& a, cudaStream_t st);
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);
