@@ -354,10 +354,37 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
         del g, yb
     except Exception as e:
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
+    rows.update(length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(grouped_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
     return rows
+
+
+def length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush):
+    """Scan-only length sweep (batch 1, d_inner 2048 = d_model 1024 x expand
+    2, N 16, bf16, gate on): time per call should grow linearly in L."""
+    out = {}
+    for L in (1024, 2048, 4096, 8192, 16384):
+        try:
+            with inputs.on_device(dev):
+                g = inputs.selective_inputs(1, 2048, 16, L, "bf16", seed=L)
+            yb = torch.empty_like(g["u"])
+            ls = torch.empty(1, 2048, 16, device=dev)
+
+            def fn():
+                run_selective_call(g, torch, abi, yb, ls)
+            times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+            ms = statistics.mean(times)
+            out[str(L)] = {"ms_per_call": round(ms, 4),
+                           "channel_steps_per_s": 2048 * L / (ms * 1e-3),
+                           "launches_per_call": nl / 5}
+            del g, yb, ls
+        except Exception as ex:
+            out[str(L)] = {"error": str(ex)[:200]}
+    return {"length_sweep_d2048": {"by_L": out, "note": "batch 1, d_inner 2048, N 16, bf16; "
+                                   "few channels, so the sequence is split into segments "
+                                   "(summary pass + main pass)"}}
 
 
 def grouped_rows(dev, torch, abi, inputs, hbm_peak, flush):
@@ -523,11 +550,11 @@ def decode_rows(dev, torch, abi, inputs, hbm_peak):
 # CPU oracle timing.
 
 
-def oracle_throughput(host, cfg, seconds, oracle):
+def oracle_throughput(host, cfg, seconds, oracle, threads=None):
     """Time the fp64 oracle on a bounded sample of the workload: whole
     channels (full length) in blocks, until `seconds` have passed."""
     import numpy as np
-    nth = oracle.max_threads()
+    nth = threads or oracle.max_threads()
     Dch = cfg.d_inner
     block = min(Dch, max(nth * 32, 64))
     f64 = {k: (None if v is None else v.double().numpy()) for k, v in host.items()}
@@ -688,9 +715,13 @@ def main_ours(args):
     if rank == 0 and not args.no_cpu:
         import oracle
         v, nth, done, used = oracle_throughput(h["host"], cfg, args.cpu_seconds, oracle)
+        v1, _, done1, used1 = oracle_throughput(h["host"], cfg, max(2.0, args.cpu_seconds / 5),
+                                                oracle, threads=1)
         cpu = {"value": v, "unit": UNIT, "cores": nth, "kind": "oracle",
                "sample": f"{done} channel-steps (whole channels of the workload, full length "
-                         f"{cfg.seqlen}) in {used:.1f} s on {cpu_model()}"}
+                         f"{cfg.seqlen}) in {used:.1f} s on {cpu_model()}",
+               "single_thread_value": v1,
+               "single_thread_sample": f"{done1} channel-steps in {used1:.1f} s on one core"}
     if world > 1:
         dh.barrier(dev)
     if rank == 0:

@@ -138,3 +138,17 @@ def test_full_size_workloads_sampled(cuda_device, name):
     check_close(yg, yo, torch.bfloat16, f"{name} y (sampled channels)")
     check_close(sg, so, torch.bfloat16, f"{name} last_state (sampled channels)")
     assert bool(torch.isfinite(y).all())
+
+
+@pytest.mark.parametrize("L", [1024, 4096, 16384])
+def test_length_sweep_shapes_sampled(cuda_device, L):
+    """The length-sweep shapes of the benchmark (batch 1, d_inner 2048, N 16,
+    bf16): few channels, so the sequence is split into segments; sampled
+    channels against the oracle."""
+    inp = inputs.selective_inputs(1, 2048, 16, L, "bf16", seed=L)
+    y, s = _run(inp, cuda_device)
+    chans = inputs.sample_units(2048, 16, seed=L)
+    yo, so = oracle_selective_channels(inp, chans)
+    idx = torch.as_tensor(chans, device=y.device)
+    check_close(to_np(y[0][idx]), yo, torch.bfloat16, f"L={L} y (sampled channels)")
+    check_close(to_np(s[0][idx]), so, torch.bfloat16, f"L={L} last_state (sampled channels)")
