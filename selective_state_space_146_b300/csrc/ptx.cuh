@@ -245,12 +245,6 @@ __device__ __forceinline__ float sigmoid_accurate(float z) {
     return __fdividef(1.0f, 1.0f + ex2_approx(-z * kLog2e));
 }
 
-// sigmoid(z) = 0.5 + 0.5 tanh(z / 2) on one MUFU op; absolute error about
-// 2.5e-4, used only where the output is rounded to bfloat16.
-__device__ __forceinline__ float sigmoid_fast(float z) {
-    return fmaf(0.5f, tanh_approx(0.5f * z), 0.5f);
-}
-
 // ---- bf16 / f32 element helpers -----------------------------------------------
 
 template <typename T> struct Elem;

@@ -174,12 +174,6 @@ struct FastCfg {
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 7)) << 4); }
 
-template <typename T>
-__device__ __forceinline__ float gate_sigmoid(float z) {
-    if constexpr (sizeof(T) == 2) return sigmoid_fast(z);
-    else return sigmoid_accurate(z);
-}
-
 // Conversion of one tile's raw B / C ([n][t] as loaded by TMA) into the fp32
 // table bc[t][32]: 16-byte chunk j holds (B[2j], B[2j+1], C[2j], C[2j+1]), so
 // a lane keeping the state pairs [j0, j0 + m) reads m consecutive chunks, one
@@ -341,54 +335,13 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     }
 
     if (warp == 1) {
-        // ---------------- B|C table (and, for CONV, u = silu(conv(x))) ----------------
-        // CONV: lane c owns channel row c of the tile and slides the causal
-        // window along t, carrying the last W-1 inputs across tiles.
-        [[maybe_unused]] float xh[3] = {0.f, 0.f, 0.f};  // x[t-3], x[t-2], x[t-1]
-        [[maybe_unused]] float wk[4] = {0.f, 0.f, 0.f, 0.f};
-        [[maybe_unused]] float cbias = 0.f;
-        if constexpr (CONV) {
-            static_assert(DT <= 32, "one conv lane per channel row");
-            const int dc = d0 + lane;
-            if (lane < DT && dc < p.D) {
-                // taps right-aligned: wk[3] multiplies x[t], wk[4-W] x[t-W+1]
-                for (int k = 0; k < p.cwidth; ++k)
-                    wk[4 - p.cwidth + k] = p.cw[(int64_t)dc * p.scw_d + k * p.scw_k];
-                cbias = p.cb ? p.cb[(int64_t)dc * p.scb] : 0.f;
-                const T* xr = static_cast<const T*>(p.x) + (int64_t)b * p.sx_b + (int64_t)dc * p.sx_d;
-                for (int j = 0; j < 3; ++j) {
-                    const int t = tbeg - 3 + j;
-                    xh[j] = t >= 0 ? Elem<T>::to_f(xr[t]) : 0.f;
-                }
-            }
-        }
+        // ---------------- B|C table ----------------
         for (int k = 0; k < ntiles; ++k) {
             const int s = k % STAGES;
             if (!mbar_wait(&raw[s], (k / STAGES) & 1, p.err)) break;
             const uint32_t st = smem_u32(stage(s));
             convert_bc<T, Cfg::LOAD_C>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC,
                                        lane);
-            if constexpr (CONV) {
-                if (!mbar_wait(&full[s], (k / STAGES) & 1, p.err)) break;
-                if (lane < DT) {
-#pragma unroll 1
-                    for (int c = 0; c < Cfg::CHUNKS; ++c) {
-                        const uint32_t a = st + swz(lane, c);
-                        float xv[VEC];
-                        lds_elems<T, VEC>(a, xv);
-                        float uv[VEC];
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            float pre = fmaf(wk[0], xh[0], fmaf(wk[1], xh[1], fmaf(wk[2], xh[2],
-                                             fmaf(wk[3], xv[i], cbias))));
-                            uv[i] = pre * sigmoid_accurate(pre);
-                            xh[0] = xh[1]; xh[1] = xh[2]; xh[2] = xv[i];
-                        }
-                        sts_elems<T, VEC>(a, uv);
-                    }
-                }
-                fence_proxy_async_smem();  // the stage is later refilled by TMA
-            }
             mbar_arrive(&table[s]);
         }
         return;
@@ -438,6 +391,29 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
         }
     }
 
+    // conv in front (CONV): taps right-aligned, wk[3] multiplies x[t] and
+    // wk[4-W] x[t-W+1]; xc holds x at the three steps before the current tile
+    [[maybe_unused]] float wk[4] = {0.f, 0.f, 0.f, 0.f}, xc[3] = {0.f, 0.f, 0.f};
+    [[maybe_unused]] float cbias = 0.f;
+    if constexpr (CONV) {
+        if (valid) {
+            for (int k = 0; k < p.cwidth; ++k)
+                wk[4 - p.cwidth + k] = p.cw[(int64_t)d * p.scw_d + k * p.scw_k];
+            cbias = p.cb ? p.cb[(int64_t)d * p.scb] : 0.f;
+            const T* xr = static_cast<const T*>(p.x) + (int64_t)b * p.sx_b + (int64_t)d * p.sx_d;
+            for (int j = 0; j < 3; ++j) {
+                const int t = tbeg - 3 + j;
+                xc[j] = t >= 0 ? Elem<T>::to_f(xr[t]) : 0.f;
+            }
+        }
+    }
+    // x at tile-local step j of this lane's row (j >= -3; the carry before 0)
+    [[maybe_unused]] auto x_at = [&](uint32_t su, int j) -> float {
+        if (j < 0) return j == -3 ? xc[0] : (j == -2 ? xc[1] : xc[2]);
+        const uint32_t a = su + swz(ci, j / VEC) + (j % VEC) * ES;
+        return ES == 2 ? __uint_as_float(lds16(a) << 16) : __uint_as_float(lds32(a));
+    };
+
     float dsum = 0.f;  // sum of delta over the segment (summary pass)
     T* yrow = static_cast<T*>(p.y) + (int64_t)b * p.sy_b + (int64_t)(valid ? d : 0) * p.sy_d;
 
@@ -448,10 +424,27 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     //   finish: reduce-scatter of the readouts, skip and gate, store of y.
     // Tiles are processed as prep(c+1) | core(c) | finish(c-1) so the three
     // independent streams interleave.
-    auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* uf, auto tail) {
+    auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* uf, float* uo, auto tail) {
         constexpr bool TAIL = decltype(tail)::value;
         const int off = swz(ci, c);
-        lds_elems<T, VEC>(su + off, uf);
+        if constexpr (CONV) {
+            // u = silu(conv(x)) in fp32 for the own K-slot, all-gathered like delta
+            const int j0 = c * VEC + part * K;
+            float xw[K + 3];
+#pragma unroll
+            for (int m = 0; m < K + 3; ++m) xw[m] = x_at(su, j0 - 3 + m);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const float pre = fmaf(wk[0], xw[k], fmaf(wk[1], xw[k + 1],
+                                       fmaf(wk[2], xw[k + 2], fmaf(wk[3], xw[k + 3], cbias))));
+                uo[k] = pre * sigmoid_accurate(pre);
+            }
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                uf[j] = NSPLIT == 1 ? uo[j % K] : __shfl_sync(0xffffffffu, uo[j % K], gbase + j / K);
+        } else {
+            lds_elems<T, VEC>(su + off, uf);
+        }
         float dv[K];
         lds_elems<T, K>(su + Cfg::OFF_DL + off + part * K * ES, dv);
 #pragma unroll
@@ -485,8 +478,9 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
             yv[i] = acc.x + acc.y;
         }
     };
-    auto finish = [&](uint32_t su, int tile_t0, int c, const float* yv, auto tail) {
-        constexpr bool TAIL = decltype(tail)::value;
+    auto finish = [&](uint32_t su, int tile_t0, int c, const float* yv, const float* uo,
+                      auto tail) {
+        [[maybe_unused]] constexpr bool TAIL = decltype(tail)::value;
         if constexpr (!SUMMARY) {
             // reduce-scatter: lane `part` ends with the full sums of its K steps
             float yo[K];
@@ -506,14 +500,21 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
                 reduce_half<VEC / 4>(x, yo, part & 1, 1);
             }
             const int own = swz(ci, c) + part * K * ES;
-            float uo[K];
+            // u of the own K-slot for the skip: still in the tile, or (CONV,
+            // where the tile holds x) computed by prep
+            float us[K];
+            if constexpr (CONV) {
+#pragma unroll
+                for (int k = 0; k < K; ++k) us[k] = uo[k];
+            } else {
+                lds_elems<T, K>(su + own, us);
+            }
             [[maybe_unused]] float zo[K];
-            lds_elems<T, K>(su + own, uo);
             if constexpr (HAS_Z) lds_elems<T, K>(su + Cfg::OFF_Z + own, zo);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                float o = fmaf(Dd, uo[k], yo[k]);
-                if constexpr (HAS_Z) o *= zo[k] * gate_sigmoid<T>(zo[k]);
+                float o = fmaf(Dd, us[k], yo[k]);
+                if constexpr (HAS_Z) o *= zo[k] * sigmoid_accurate(zo[k]);
                 yo[k] = o;
             }
             if (valid) {
@@ -527,33 +528,43 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     auto full_tile = [&](uint32_t su, int tile_t0) {
         static_assert(Cfg::CHUNKS == 8, "pipeline below assumes 8 chunks per tile");
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
-        float ddA[VEC], ufA[VEC], ddB[VEC], ufB[VEC], yA[VEC], yB[VEC];
-        prep(su, 0, TT, ddA, ufA, std::false_type{});
+        float ddA[VEC], ufA[VEC], ddB[VEC], ufB[VEC], yA[VEC], yB[VEC], uoA[K], uoB[K];
+        prep(su, 0, TT, ddA, ufA, uoA, std::false_type{});
         core(bcp, 0, ddA, ufA, yA);
-        prep(su, 1, TT, ddB, ufB, std::false_type{});
+        prep(su, 1, TT, ddB, ufB, uoB, std::false_type{});
 #pragma unroll 1
         for (int c = 1; c < 7; c += 2) {
             core(bcp, c, ddB, ufB, yB);
-            prep(su, c + 1, TT, ddA, ufA, std::false_type{});
-            finish(su, tile_t0, c - 1, yA, std::false_type{});
+            if constexpr (CONV) {
+                finish(su, tile_t0, c - 1, yA, uoA, std::false_type{});  // before uoA is refilled
+                prep(su, c + 1, TT, ddA, ufA, uoA, std::false_type{});
+            } else {
+                prep(su, c + 1, TT, ddA, ufA, uoA, std::false_type{});
+                finish(su, tile_t0, c - 1, yA, uoA, std::false_type{});
+            }
             core(bcp, c + 1, ddA, ufA, yA);
-            prep(su, c + 2, TT, ddB, ufB, std::false_type{});
-            finish(su, tile_t0, c, yB, std::false_type{});
+            if constexpr (CONV) {
+                finish(su, tile_t0, c, yB, uoB, std::false_type{});
+                prep(su, c + 2, TT, ddB, ufB, uoB, std::false_type{});
+            } else {
+                prep(su, c + 2, TT, ddB, ufB, uoB, std::false_type{});
+                finish(su, tile_t0, c, yB, uoB, std::false_type{});
+            }
         }
         core(bcp, 7, ddB, ufB, yB);
-        finish(su, tile_t0, 6, yA, std::false_type{});
-        finish(su, tile_t0, 7, yB, std::false_type{});
+        finish(su, tile_t0, 6, yA, uoA, std::false_type{});
+        finish(su, tile_t0, 7, yB, uoB, std::false_type{});
     };
     // The last, partial tile of a sequence: one chunk at a time, with checks.
     auto tail_tile = [&](uint32_t su, int tile_t0, int tcount) {
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
         const int nch = (tcount + VEC - 1) / VEC;
-        float dd[VEC], uf[VEC], yv[VEC];
+        float dd[VEC], uf[VEC], yv[VEC], uo[K];
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
-            prep(su, c, tcount, dd, uf, std::true_type{});
+            prep(su, c, tcount, dd, uf, uo, std::true_type{});
             core(bcp, c, dd, uf, yv);
-            finish(su, tile_t0, c, yv, std::true_type{});
+            finish(su, tile_t0, c, yv, uo, std::true_type{});
         }
     };
 
@@ -570,6 +581,11 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
         const uint32_t su = smem_u32(stage(s));
         if (tcount == TT) full_tile(su, tile_t0);
         else tail_tile(su, tile_t0, tcount);
+        if constexpr (CONV) {
+            // the next tile's first steps look back at the last three of this one
+            const float x0 = x_at(su, TT - 3), x1 = x_at(su, TT - 2), x2 = x_at(su, TT - 1);
+            xc[0] = x0; xc[1] = x1; xc[2] = x2;
+        }
         mbar_arrive(&empty[s]);
     }
     if (!ok || !valid) return;
