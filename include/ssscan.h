@@ -200,6 +200,29 @@ int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
                                ss_tensor* last_state, void* stream);
 
 /*
+ * The selective scan of ss_selective_scan_fwd with every tensor in HOST
+ * memory (no counterpart on the pages: this is the path a caller whose data
+ * lives on the host takes, copies included).  Same arguments, shapes, dtypes
+ * and results as ss_selective_scan_fwd, except:
+ *   - every ss_tensor.data is a host pointer; page-locked (pinned) memory
+ *     lets the copies run asynchronously, pageable memory works but the
+ *     copies then block the calling thread;
+ *   - every tensor must be contiguous (else SS_ERR_UNSUPPORTED).
+ * The batch is cut into chunks of about 32 MB of inputs; chunks alternate
+ * between `stream` and one library-owned side stream per device, so copies in,
+ * scans and copies out of neighbouring chunks overlap.  All work is joined back
+ * into `stream` before the call returns (asynchronously: y and last_state
+ * are valid once `stream` has completed, and the host buffers must stay
+ * valid until then).  Device memory for the chunks is taken stream-ordered
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).  Calls on different streams
+ * of one device share the side stream and so partly serialise.
+ */
+int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               ss_tensor* y, ss_tensor* last_state, void* stream);
+
+/*
  * Backward of the selective scan (training): given dout, the gradient of a
  * loss with respect to the y of ss_selective_scan_fwd (same inputs, zero
  * initial state), writes the gradients with respect to every input

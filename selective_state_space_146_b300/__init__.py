@@ -7,10 +7,11 @@ ABI declared in ``include/ssscan.h``); this package only binds it.
 """
 from ._abi import (SSError, conv_selective_scan_fwd, device_error,  # noqa: F401
                    launch_count, selective_scan_bwd, selective_scan_fwd,
+                   selective_scan_fwd_host,
                    selective_scan_fwd_noalloc, selective_state_update, ssd_chunk_scan_fwd,
                    ssd_state_update, status_string)
 
-__all__ = ["selective_scan_fwd", "conv_selective_scan_fwd", "selective_scan_fwd_noalloc",
+__all__ = ["selective_scan_fwd", "selective_scan_fwd_host", "conv_selective_scan_fwd", "selective_scan_fwd_noalloc",
            "ssd_chunk_scan_fwd", "selective_scan_bwd",
            "selective_state_update", "ssd_state_update", "SSError", "device_error",
            "launch_count", "status_string"]

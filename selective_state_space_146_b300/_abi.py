@@ -22,7 +22,7 @@ STATUS = {0: "SS_OK", -1: "SS_ERR_INVALID_ARG", -2: "SS_ERR_SHAPE", -3: "SS_ERR_
           -7: "SS_ERR_LAUNCH", -8: "SS_ERR_TIMEOUT", -9: "SS_ERR_CUDA"}
 EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chunk_scan_fwd",
            "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
-           "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd",
+           "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version")
 
@@ -67,6 +67,8 @@ def load(path: str | None = None):
     lib.ss_selective_state_update.restype = i
     lib.ss_conv_selective_scan_fwd.argtypes = [T, T, T, T, T, T, T, T, T, T, i, T, T, vp]
     lib.ss_conv_selective_scan_fwd.restype = i
+    lib.ss_selective_scan_fwd_host.argtypes = [T, T, T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_selective_scan_fwd_host.restype = i
     lib.ss_selective_scan_bwd.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, T, T, T, T, T, T,
                                           vp]
     lib.ss_selective_scan_bwd.restype = i
@@ -144,6 +146,26 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
         what = "ss_selective_scan_fwd_init"
     if rc != 0:
         raise SSError(rc, what)
+    return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                            y=None, last_state=None, return_last_state=False, stream=None):
+    """ss_selective_scan_fwd_host: the selective scan with every tensor in
+    host memory (contiguous CPU tensors, pinned for asynchronous copies).
+    The results are valid once `stream` (default: the current CUDA stream) has
+    completed."""
+    if y is None:
+        y = torch.empty(u.shape, dtype=u.dtype, pin_memory=True)
+    if last_state is None and return_last_state:
+        last_state = torch.empty(u.shape[0], u.shape[1], A.shape[1], dtype=torch.float32,
+                                 pin_memory=True)
+    ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    rc = load().ss_selective_scan_fwd_host(*[_ref(t) for t in ts], int(bool(softplus)),
+                                           _ref(describe(y)), _ref(describe(last_state)),
+                                           _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_fwd_host")
     return (y, last_state) if (return_last_state or last_state is not None) else y
 
 

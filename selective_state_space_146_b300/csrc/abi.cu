@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -468,6 +469,139 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_selective_bwd(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+// ---------------------------------------------------------------------------
+// Host buffers in and out: ss_selective_scan_fwd_host.  The batch is cut into
+// chunks of rows; chunks alternate between the caller's stream and one side
+// stream per device, so the copy in of one chunk overlaps the scan of the one
+// before and the copy out of the one before that.
+
+static cudaStream_t g_side[kMaxDevices];
+
+static cudaStream_t side_stream() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_side[dev]) {
+        cudaStream_t s = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_side[dev] = s;
+    }
+    return g_side[dev];
+}
+
+static size_t numel(const ss_tensor* t) {
+    size_t n = 1;
+    for (int i = 0; i < t->ndim; ++i) n *= (size_t)t->shape[i];
+    return n;
+}
+
+static size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
+int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               ss_tensor* y, ss_tensor* last_state, void* stream) {
+    ScanArgs a{};
+    bool nothing = false;
+    SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, y, last_state,
+                          &a, &nothing));
+    if (nothing) return SS_OK;
+    for (const ss_tensor* t : {u, delta, A, B, C, D, z, delta_bias, static_cast<const ss_tensor*>(y),
+                               static_cast<const ss_tensor*>(last_state)})
+        if (t && !is_contiguous(t)) return SS_ERR_UNSUPPORTED;
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+    cudaStream_t s1 = side_stream();
+    if (!s1) return SS_ERR_CUDA;
+
+    const int es = elem_size(u->dtype);
+    const int64_t Bsz = a.Bsz, Dch = a.D, L = a.L, N = a.N, G = a.G > 1 ? a.G : 1;
+    const size_t act_row = (size_t)Dch * L * es;        // one batch row of u / delta / z / y
+    const size_t bc_row = (size_t)G * N * L * es;       // one batch row of B or C
+    const size_t st_row = (size_t)Dch * N * sizeof(float);
+    const size_t in_row = act_row * (z ? 3 : 2) + 2 * bc_row;
+    // about 32 MB of inputs per chunk, and at least two chunks when there are two rows
+    int64_t rows = std::max<int64_t>(1, (int64_t)((size_t(32) << 20) / std::max<size_t>(in_row, 1)));
+    if (Bsz >= 2) rows = std::min<int64_t>(rows, (Bsz + 1) / 2);
+    rows = std::min<int64_t>(rows, Bsz);
+    const int64_t nchunk = (Bsz + rows - 1) / rows;
+    const int nset = nchunk > 1 ? 2 : 1;
+
+    // device layout: A, D, bias once; then `nset` sets of chunk buffers
+    const size_t szA = round256(numel(A) * sizeof(float));
+    const size_t szD = D ? round256(Dch * sizeof(float)) : 0;
+    const size_t szb = delta_bias ? round256(Dch * sizeof(float)) : 0;
+    const size_t cact = round256(act_row * rows), cbc = round256(bc_row * rows);
+    const size_t cst = last_state ? round256(st_row * rows) : 0;
+    const size_t per_set = cact * (z ? 4 : 3) + 2 * cbc + cst;
+    const size_t total = szA + szD + szb + per_set * nset;
+    uint8_t* base = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&base), total, s0) != cudaSuccess) {
+        cudaGetLastError();
+        return SS_ERR_ALLOC;
+    }
+    int rc = SS_OK;
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    auto H2D = [&](void* dst, const void* src, size_t n, cudaStream_t st) {
+        if (n && rc == SS_OK && cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            rc = SS_ERR_CUDA;
+    };
+    auto D2H = [&](void* dst, const void* src, size_t n, cudaStream_t st) {
+        if (n && rc == SS_OK && cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            rc = SS_ERR_CUDA;
+    };
+    float* dA = reinterpret_cast<float*>(base);
+    float* dD = D ? reinterpret_cast<float*>(base + szA) : nullptr;
+    float* dbias = delta_bias ? reinterpret_cast<float*>(base + szA + szD) : nullptr;
+    H2D(dA, A->data, numel(A) * sizeof(float), s0);
+    if (D) H2D(dD, D->data, Dch * sizeof(float), s0);
+    if (delta_bias) H2D(dbias, delta_bias->data, Dch * sizeof(float), s0);
+    if (rc == SS_OK && (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
+                        cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming) != cudaSuccess ||
+                        cudaEventRecord(ev_start, s0) != cudaSuccess ||
+                        cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess))
+        rc = SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    for (int64_t i = 0; i < nchunk && rc == SS_OK; ++i) {
+        const int64_t b0 = i * rows, nb = std::min(rows, Bsz - b0);
+        cudaStream_t st = (i % 2 == 0) ? s0 : s1;
+        uint8_t* set = base + szA + szD + szb + per_set * (i % nset);
+        uint8_t *du = set, *ddl = set + cact, *dy = set + 2 * cact;
+        uint8_t* dz = z ? set + 3 * cact : nullptr;
+        uint8_t* dB = set + cact * (z ? 4 : 3);
+        uint8_t* dC = dB + cbc;
+        float* dlast = last_state ? reinterpret_cast<float*>(dC + cbc) : nullptr;
+        const size_t off_act = (size_t)b0 * act_row, off_bc = (size_t)b0 * bc_row;
+        H2D(du, static_cast<const uint8_t*>(u->data) + off_act, act_row * nb, st);
+        H2D(ddl, static_cast<const uint8_t*>(delta->data) + off_act, act_row * nb, st);
+        if (z) H2D(dz, static_cast<const uint8_t*>(z->data) + off_act, act_row * nb, st);
+        H2D(dB, static_cast<const uint8_t*>(B->data) + off_bc, bc_row * nb, st);
+        H2D(dC, static_cast<const uint8_t*>(C->data) + off_bc, bc_row * nb, st);
+        if (rc != SS_OK) break;
+        ScanArgs c = a;  // contiguous rows: the strides stay, the pointers move
+        c.Bsz = (int)nb;
+        c.u = du; c.dl = ddl; c.z = dz; c.y = dy; c.Bm = dB; c.Cm = dC;
+        c.A = dA; c.Dv = dD; c.bias = dbias; c.last = dlast;
+        rc = launch_selective(c, st, sc);
+        if (rc != SS_OK) break;
+        D2H(static_cast<uint8_t*>(y->data) + off_act, dy, act_row * nb, st);
+        if (last_state)
+            D2H(static_cast<uint8_t*>(last_state->data) + (size_t)b0 * st_row, dlast, st_row * nb, st);
+    }
+    // join the side stream back into the caller's stream, then free
+    if (ev_end && (cudaEventRecord(ev_end, s1) != cudaSuccess ||
+                   cudaStreamWaitEvent(s0, ev_end, 0) != cudaSuccess) && rc == SS_OK)
+        rc = SS_ERR_CUDA;
+    cudaFreeAsync(base, s0);
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (ev_end) cudaEventDestroy(ev_end);
+    return rc;
 }
 
 int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,

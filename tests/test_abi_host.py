@@ -244,3 +244,15 @@ def test_grouped_bc_argument_errors(lib):
     a["B"] = FakeT((2, 4, 16, 64))
     a["C"] = FakeT((2, 4, 16, 64))
     assert _call_bwd(lib, a, _bwd_grads(D=12)) == -5       # backward: shared B, C only
+
+
+def test_host_buffer_entry_point_rejects_strided_tensors(lib):
+    a = _sel_args()
+    a["u"] = FakeT((2, 8, 64), stride=[1024, 128, 1])  # rows of 128 with 64 used
+    r = {k: v.ref for k, v in a.items()}
+    assert lib.ss_selective_scan_fwd_host(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 1, r["y"], r["last"], None) == -5
+    b = _sel_args()
+    r = {k: v.ref for k, v in b.items()}
+    assert lib.ss_selective_scan_fwd_host(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 3, r["y"], r["last"], None) == -1

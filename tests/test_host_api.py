@@ -1,0 +1,76 @@
+"""ss_selective_scan_fwd_host: host tensors in, host tensors out, the batch
+cut into chunks that overlap on two streams.  Compared with the fp64 oracle
+on the same inputs (GPU)."""
+import pytest
+import torch
+
+import oracle
+from selective_state_space_146_b300 import _abi, inputs
+from tests.parity_util import check_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _tdt(dt):
+    return torch.float32 if dt == "f32" else torch.bfloat16
+
+
+def _pin(d):
+    return {k: (None if v is None else v.pin_memory()) for k, v in d.items()}
+
+
+@pytest.mark.parametrize("case", [(2, 64, 16, 512, "bf16", None), (5, 40, 16, 300, "f32", None),
+                                  (3, 48, 16, 200, "bf16", 48), (4, 24, 8, 77, "f32", None),
+                                  (1, 32, 16, 64, "bf16", None)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_host_api_matches_oracle(cuda_device, case):
+    Bsz, D, N, L, dt, G = case
+    inp = inputs.selective_inputs(Bsz, D, N, L, dt, groups=G, seed=Bsz * 100 + L)
+    h = _pin(inp)
+    y, s = _abi.selective_scan_fwd_host(h["u"], h["delta"], h["A"], h["B"], h["C"], h["D"],
+                                        h["z"], h["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    assert y.device.type == "cpu" and s.device.type == "cpu"
+    yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], nthreads=8)
+    check_close(to_np(y), yo, _tdt(dt), "y")
+    check_close(to_np(s), so, _tdt(dt), "last_state")
+
+
+def test_host_api_pageable_memory_and_no_state(cuda_device):
+    inp = inputs.selective_inputs(3, 32, 16, 128, "f32", seed=4)
+    y = torch.empty(3, 32, 128)
+    _abi.selective_scan_fwd_host(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["z"], inp["delta_bias"], y=y)
+    torch.cuda.synchronize()
+    yo, _ = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["delta_bias"])
+    check_close(to_np(y), yo, torch.float32, "y (pageable host memory)")
+
+
+def test_host_api_zero_length_writes_zero_state(cuda_device):
+    inp = _pin(inputs.selective_inputs(2, 8, 16, 0, "f32", seed=1))
+    last = torch.full((2, 8, 16), 3.0).pin_memory()
+    _abi.selective_scan_fwd_host(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["z"], inp["delta_bias"], y=torch.empty(2, 8, 0),
+                                 last_state=last)
+    torch.cuda.synchronize()
+    assert bool((last == 0).all())
+
+
+def test_host_api_layer_shape_sampled(cuda_device):
+    """The end-to-end call of the benchmark (Mamba-130M layer, 8 x 1536 x 2048
+    bf16): sampled channels against the oracle."""
+    cfg = inputs.WORKLOADS["mamba130m_layer"]
+    inp = inputs.workload_selective_inputs(cfg, seed=0)
+    h = _pin(inp)
+    y, s = _abi.selective_scan_fwd_host(h["u"], h["delta"], h["A"], h["B"], h["C"], h["D"],
+                                        h["z"], h["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    from tests.parity_util import oracle_selective_channels
+    total = cfg.batch * cfg.d_inner
+    chans = inputs.sample_units(total, 24, seed=3)
+    yo, so = oracle_selective_channels(inp, chans)
+    idx = torch.as_tensor(chans)
+    check_close(to_np(y.reshape(total, cfg.seqlen)[idx]), yo, torch.bfloat16, "y (sampled)")
+    check_close(to_np(s.reshape(total, cfg.d_state)[idx]), so, torch.bfloat16, "state (sampled)")
