@@ -80,3 +80,29 @@ def test_conv_scan_full_size_sampled(cuda_device):
     idx = torch.as_tensor(chans, device=y.device)
     check_close(to_np(y.reshape(total, -1)[idx]), np.stack(ys), torch.bfloat16, "conv-scan y")
     check_close(to_np(s.reshape(total, -1)[idx]), np.stack(ss), torch.bfloat16, "conv-scan state")
+
+
+def test_conv_scan_layer_shape_sampled(cuda_device, monkeypatch):
+    """The fused call the benchmark times (8 x 1536 x 2048 bf16, width 4),
+    sampled channels against the oracle run on those channels alone."""
+    monkeypatch.delenv("SS_SCAN_PATH", raising=False)
+    cfg = inputs.WORKLOADS["mamba130m_layer"]
+    inp = inputs.workload_selective_inputs(cfg, seed=0)
+    w, b = _conv_params(cfg.d_inner, 4, seed=7)
+    g = {k: (None if v is None else v.to(cuda_device)) for k, v in inp.items()}
+    y, s = _abi.conv_selective_scan_fwd(g["u"], w.to(cuda_device), b.to(cuda_device), g["delta"],
+                                        g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"],
+                                        return_last_state=True)
+    torch.cuda.synchronize()
+    chans = inputs.sample_units(cfg.batch * cfg.d_inner, 16, seed=5)
+    ys, ss, yo, so = [], [], [], []
+    for c in chans:
+        bb, d = divmod(int(c), cfg.d_inner)
+        y1, s1 = oracle.conv_selective_scan(
+            inp["u"][bb:bb + 1, d:d + 1], w[d:d + 1], b[d:d + 1], inp["delta"][bb:bb + 1, d:d + 1],
+            inp["A"][d:d + 1], inp["B"][bb:bb + 1], inp["C"][bb:bb + 1], inp["D"][d:d + 1],
+            inp["z"][bb:bb + 1, d:d + 1], inp["delta_bias"][d:d + 1])
+        yo.append(y1[0, 0]); so.append(s1[0, 0])
+        ys.append(to_np(y[bb, d])); ss.append(to_np(s[bb, d]))
+    check_close(np.stack(ys), np.stack(yo), torch.bfloat16, "conv y (sampled channels)")
+    check_close(np.stack(ss), np.stack(so), torch.bfloat16, "conv state (sampled channels)")

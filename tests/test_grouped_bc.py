@@ -124,3 +124,26 @@ def test_per_channel_bc_layer_shape_sampled(cuda_device, scan_path):
             inp["z"][b:b + 1, d:d + 1], inp["delta_bias"][d:d + 1])
         check_close(y[b, d], yo[0, 0], torch.bfloat16, f"y channel {c}")
         check_close(s[b, d], so[0, 0], torch.bfloat16, f"state channel {c}")
+
+
+def test_groups_of_64_layer_shape_sampled(cuda_device):
+    """B, C per group of 64 channels at the Mamba-130M layer shape (the
+    benchmark's groups24 row, TMA kernel with group rows): sampled channels."""
+    cfg = inputs.WORKLOADS["mamba130m_layer"]
+    G = cfg.d_inner // 64
+    inp = inputs.selective_inputs(cfg.batch, cfg.d_inner, cfg.d_state, cfg.seqlen, "bf16",
+                                  groups=G, seed=2)
+    g = cuda_inputs(inp, cuda_device)
+    y, s = _abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    y, s = to_np(y), to_np(s)
+    for c in inputs.sample_units(cfg.batch * cfg.d_inner, 24, seed=4):
+        b, d = divmod(int(c), cfg.d_inner)
+        gi = d // 64
+        yo, so = oracle.selective_scan(
+            inp["u"][b:b + 1, d:d + 1], inp["delta"][b:b + 1, d:d + 1], inp["A"][d:d + 1],
+            inp["B"][b:b + 1, gi], inp["C"][b:b + 1, gi], inp["D"][d:d + 1],
+            inp["z"][b:b + 1, d:d + 1], inp["delta_bias"][d:d + 1])
+        check_close(y[b, d], yo[0, 0], torch.bfloat16, f"y channel {c}")
+        check_close(s[b, d], so[0, 0], torch.bfloat16, f"state channel {c}")

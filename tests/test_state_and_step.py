@@ -144,3 +144,37 @@ def test_ssd_decode_steps_reproduce_the_scan(cuda_device, case):
     yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0)
     check_close(to_np(torch.stack(ys, 1)), yo, _tdt(dt), "ssd decode y")
     check_close(to_np(state), so, _tdt(dt), "ssd decode state")
+
+
+def test_decode_steps_at_benchmark_shapes(cuda_device):
+    """One decode step at the shapes the benchmark times: 8 x 1536 channels,
+    N 16 (selective) and 4 x 64 heads x 64, N 128 (SSD), from a random state,
+    against one step of the oracles."""
+    Bsz, D, N = 8, 1536, 16
+    inp = inputs.selective_inputs(Bsz, D, N, 1, "bf16", seed=8)
+    h0 = _h0((Bsz, D, N), 9)
+    state = h0.to(cuda_device).clone()
+    g = cuda_inputs(inp, cuda_device)
+    y = _abi.selective_state_update(state, g["u"][..., 0].contiguous(),
+                                    g["delta"][..., 0].contiguous(), g["A"],
+                                    g["B"][..., 0].contiguous(), g["C"][..., 0].contiguous(),
+                                    g["D"], g["z"][..., 0].contiguous(), g["delta_bias"])
+    torch.cuda.synchronize()
+    yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], h0=h0, nthreads=8)
+    check_close(to_np(y), yo[..., 0], torch.bfloat16, "selective decode y")
+    check_close(to_np(state), so, torch.bfloat16, "selective decode state")
+
+    Bsz, H, P, N = 4, 64, 64, 128
+    inp = inputs.ssd_inputs(Bsz, 1, H, P, N, 1, "bf16", seed=10)
+    h0 = _h0((Bsz, H, P, N), 11)
+    state = h0.to(cuda_device).clone()
+    g = cuda_inputs(inp, cuda_device)
+    y = _abi.ssd_state_update(state, g["x"][:, 0].contiguous(), g["dt"][:, 0].contiguous(),
+                              g["A_head"], g["B"][:, 0].contiguous(), g["C"][:, 0].contiguous(),
+                              g["D"])
+    torch.cuda.synchronize()
+    yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0,
+                        nthreads=8)
+    check_close(to_np(y), yo[:, 0], torch.bfloat16, "ssd decode y")
+    check_close(to_np(state), so, torch.bfloat16, "ssd decode state")
