@@ -148,7 +148,7 @@ struct FastCfg {
     static constexpr int DT = CWARPS * CPW;      // channels per CTA
     static constexpr int NS = N / NSPLIT;        // states per thread
     static constexpr int NCONS = CWARPS * 32;
-    static constexpr int NTHREADS = NCONS + 64;  // + TMA warp + B|C conversion warp
+    static constexpr int NTHREADS = NCONS + 32;  // + one warp: TMA issue and B|C conversion
     static constexpr bool LOAD_Z = HAS_Z && !SUMMARY;
     static constexpr bool LOAD_C = !SUMMARY;
     static constexpr int TILE_BYTES = DT * 128;  // one [DT][TT] tile of u, delta, z or y
@@ -308,41 +308,46 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     auto stage = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
 
     if (warp == 0) {
-        // ---------------- TMA loads ----------------
+        // ---------------- TMA loads (lane 0) and the B|C table (all lanes) ----------------
+        // One warp does both so a CTA has one helper warp: with three CTAs per
+        // SM that keeps four warps per SM sub-partition (the register cap).
+        // Tile k + STAGES - 1 is issued into the stage of tile k - 1 right after
+        // tile k's table is written, once the consumers have released it.
+        const int bc_row = b * p.bc_groups + d0 / p.bc_dpg;  // B / C rows of the tile
+        auto issue = [&](int k) {
+            const int s = k % STAGES;
+            const int t0 = tbeg + k * TT;
+            uint8_t* st = stage(s);
+            mbar_arrive_expect_tx(&raw[s], Cfg::RAW_TX);
+            tma_load_3d(st + Cfg::OFF_RAWB, &tm_B, &raw[s], t0, 0, bc_row);
+            if (Cfg::LOAD_C) tma_load_3d(st + Cfg::OFF_RAWC, &tm_C, &raw[s], t0, 0, bc_row);
+            mbar_arrive_expect_tx(&full[s], Cfg::TILE_TX);
+            tma_load_3d(st, &tm_u, &full[s], t0, d0, b);
+            tma_load_3d(st + Cfg::OFF_DL, &tm_dl, &full[s], t0, d0, b);
+            if (Cfg::LOAD_Z) tma_load_3d(st + Cfg::OFF_Z, &tm_z, &full[s], t0, d0, b);
+        };
         if (lane == 0) {
-            // the CTA's B / C rows: batch row b, group of the tile's channels
-            const int bc_row = b * p.bc_groups + d0 / p.bc_dpg;
             tma_prefetch_desc(&tm_u);
             tma_prefetch_desc(&tm_dl);
             tma_prefetch_desc(&tm_B);
             if (Cfg::LOAD_Z) tma_prefetch_desc(&tm_z);
             if (Cfg::LOAD_C) tma_prefetch_desc(&tm_C);
-            for (int k = 0; k < ntiles; ++k) {
-                const int s = k % STAGES;
-                if (k >= STAGES && !mbar_wait(&empty[s], ((k / STAGES) - 1) & 1, p.err)) break;
-                const int t0 = tbeg + k * TT;
-                uint8_t* st = stage(s);
-                mbar_arrive_expect_tx(&raw[s], Cfg::RAW_TX);
-                tma_load_3d(st + Cfg::OFF_RAWB, &tm_B, &raw[s], t0, 0, bc_row);
-                if (Cfg::LOAD_C) tma_load_3d(st + Cfg::OFF_RAWC, &tm_C, &raw[s], t0, 0, bc_row);
-                mbar_arrive_expect_tx(&full[s], Cfg::TILE_TX);
-                tma_load_3d(st, &tm_u, &full[s], t0, d0, b);
-                tma_load_3d(st + Cfg::OFF_DL, &tm_dl, &full[s], t0, d0, b);
-                if (Cfg::LOAD_Z) tma_load_3d(st + Cfg::OFF_Z, &tm_z, &full[s], t0, d0, b);
-            }
+            for (int k = 0; k < STAGES && k < ntiles; ++k) issue(k);
         }
-        return;
-    }
-
-    if (warp == 1) {
-        // ---------------- B|C table ----------------
         for (int k = 0; k < ntiles; ++k) {
             const int s = k % STAGES;
-            if (!mbar_wait(&raw[s], (k / STAGES) & 1, p.err)) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&raw[s], (k / STAGES) & 1, p.err))) break;
             const uint32_t st = smem_u32(stage(s));
             convert_bc<T, Cfg::LOAD_C>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC,
                                        lane);
             mbar_arrive(&table[s]);
+            const int kn = k - 1 + STAGES;
+            bool ok = true;
+            if (lane == 0 && k >= 1 && kn < ntiles) {
+                ok = mbar_wait(&empty[kn % STAGES], ((kn / STAGES) - 1) & 1, p.err);
+                if (ok) issue(kn);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
         return;
     }
@@ -351,7 +356,7 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
     // NSPLIT consecutive lanes share one channel; lane `part` of the group keeps
     // states [part*NS, part*NS + NS), computes delta for t in its K-slot of
     // every chunk, and owns the outputs of that slot.
-    const int cw = warp - 2;
+    const int cw = warp - 1;
     const int ci = cw * Cfg::CPW + lane / NSPLIT;  // channel row within the tile
     const int part = lane % NSPLIT;
     const int gbase = lane - part;
