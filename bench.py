@@ -355,6 +355,7 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
     rows.update(length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(grouped_rows(dev, torch, abi, inputs, hbm_peak, flush))
+    rows.update(wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
     return rows
@@ -384,6 +385,35 @@ def length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush):
     return {"length_sweep_d2048": {"by_L": out, "note": "batch 1, d_inner 2048, N 16, bf16; "
                                    "few channels, so the sequence is split into segments "
                                    "(summary pass + main pass)"}}
+
+
+def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush):
+    """d_state 64 and 128 at the Mamba-130M layer shape (bf16, gate on)."""
+    rows = {}
+    cfg = inputs.WORKLOADS["mamba130m_layer"]
+    for N in (64, 128):
+        name = f"mamba130m_layer_N{N}"
+        try:
+            with inputs.on_device(dev):
+                g = inputs.selective_inputs(cfg.batch, cfg.d_inner, N, cfg.seqlen, cfg.dtype)
+            yb = torch.empty_like(g["u"])
+            ls = torch.empty(cfg.batch, cfg.d_inner, N, device=dev)
+
+            def fn():
+                run_selective_call(g, torch, abi, yb, ls)
+            times, nl = time_device(fn, flush, 3, 2, torch, counter=abi.launch_count)
+            ms = statistics.mean(times)
+            mufu = cfg.channel_steps * (N + 5) / (ms * 1e-3)
+            rows[name] = {"ms_per_call": round(ms, 4),
+                          "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+                          "state_steps_per_s": cfg.channel_steps * N / (ms * 1e-3),
+                          "mufu_frac": round(mufu / (MUFU_EX2_PER_SM_CLK * N_SM * SM_MHZ_MAX * 1e6), 4),
+                          "launches_per_call": nl / 3}
+            del g, yb, ls
+            torch.cuda.empty_cache()
+        except Exception as ex:
+            rows[name] = {"error": str(ex)[:200]}
+    return rows
 
 
 def grouped_rows(dev, torch, abi, inputs, hbm_peak, flush):

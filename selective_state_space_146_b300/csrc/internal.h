@@ -112,6 +112,9 @@ int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
 // B, C per small channel group (scan_pc / scan_pc_tma); *taken is false when
 // the layout suits neither and the caller should run the general kernel.
 int launch_selective_grouped(const ScanArgs& a, cudaStream_t st, bool* taken);
+// N in {32, 64, 128} with B, C shared per batch row (scan_wide); *taken is
+// false when the shape or layout does not fit and the general kernel runs.
+int launch_selective_wide(const ScanArgs& a, cudaStream_t st, bool* taken);
 int launch_selective_bwd(const BwdArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_selective_step(const StepArgs& a, cudaStream_t st);
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);

@@ -12,11 +12,12 @@
 
 namespace ss {
 
-// K consecutive elements of T (K * sizeof(T) in {4, 8, 16} bytes) from
+// K consecutive elements of T (K * sizeof(T) in {2, 4, 8, 16} bytes) from
 // shared memory, widened to float.
 template <typename T, int K>
 __device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
     constexpr int BYTES = K * (int)sizeof(T);
+    static_assert(BYTES == 2 || BYTES == 4 || BYTES == 8 || BYTES == 16, "one load of 2..16 bytes");
     uint32_t w[4];
     if constexpr (BYTES == 16) {
         const uint4 v = lds128(a);

@@ -830,6 +830,11 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
         const int rc = launch_selective_grouped(a, st, &taken);
         if (taken) return rc;
     }
+    if (force != 0 && a.L > 0) {
+        bool taken = false;
+        const int rc = launch_selective_wide(a, st, &taken);
+        if (taken) return rc;
+    }
     return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
 }
 
