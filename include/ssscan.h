@@ -296,6 +296,21 @@ const char* ss_status_string(int status);
  */
 int ss_get_device_error(void* stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches a
+ * kernel on `stream` whose bounded wait on an mbarrier can never complete and
+ * gives up after `limit_us` microseconds (1 .. 100000, else
+ * SS_ERR_INVALID_ARG), recording the same device error bit as a scan kernel
+ * whose wait ran out.  The next ss_get_device_error on that stream returns
+ * SS_ERR_TIMEOUT and clears it; the CUDA context stays usable.  Nothing
+ * faults, traps or hangs.
+ *
+ * Host-side fault injection for tests: with the environment variable
+ * SS_FAULT_ALLOC=1 every stream-ordered scratch allocation of the library
+ * fails, so calls that need scratch return SS_ERR_ALLOC before launching.
+ */
+int ss_selftest_timeout(unsigned limit_us, void* stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ss_launch_count(void);
 

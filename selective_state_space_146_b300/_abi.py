@@ -24,7 +24,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
            "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
-           "ss_version")
+           "ss_version", "ss_selftest_timeout")
 
 
 class SSTensor(ctypes.Structure):
@@ -78,6 +78,8 @@ def load(path: str | None = None):
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_get_device_error.argtypes = [vp]
     lib.ss_get_device_error.restype = i
+    lib.ss_selftest_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.ss_selftest_timeout.restype = i
     lib.ss_launch_count.argtypes = []
     lib.ss_launch_count.restype = ctypes.c_uint64
     lib.ss_version.restype = i
@@ -289,6 +291,14 @@ def ssd_state_update(state, x, dt, A_head, B, C, D=None, y=None, stream=None):
 
 def device_error(stream=None) -> int:
     return int(load().ss_get_device_error(_stream_ptr(stream)))
+
+
+def selftest_timeout(limit_us=2000, stream=None) -> None:
+    """ss_selftest_timeout: a kernel whose bounded wait runs out; afterwards
+    device_error() returns the SS_ERR_TIMEOUT code."""
+    rc = load().ss_selftest_timeout(int(limit_us), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selftest_timeout")
 
 
 def launch_count() -> int:

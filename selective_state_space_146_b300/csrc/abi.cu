@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -71,7 +72,15 @@ void* tensor_map_encoder() {
     return fn;
 }
 
+// SS_FAULT_ALLOC=1 makes every stream-ordered scratch allocation report
+// failure (a host-side fault injection for the tests of SS_ERR_ALLOC).
+static bool fault_alloc() {
+    const char* f = getenv("SS_FAULT_ALLOC");
+    return f && f[0] == '1';
+}
+
 static void* scratch_alloc_async(size_t bytes, cudaStream_t st, void*) {
+    if (fault_alloc()) return nullptr;
     void* p = nullptr;
     if (cudaMallocAsync(&p, bytes, st) != cudaSuccess) {
         cudaGetLastError();
@@ -542,7 +551,8 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
     const size_t per_set = cact * (z ? 4 : 3) + 2 * cbc + cst;
     const size_t total = szA + szD + szb + per_set * nset;
     uint8_t* base = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&base), total, s0) != cudaSuccess) {
+    if (fault_alloc() ||
+        cudaMallocAsync(reinterpret_cast<void**>(&base), total, s0) != cudaSuccess) {
         cudaGetLastError();
         return SS_ERR_ALLOC;
     }
@@ -788,6 +798,13 @@ int ss_get_device_error(void* stream) {
         return SS_ERR_TIMEOUT;
     }
     return SS_OK;
+}
+
+int ss_selftest_timeout(unsigned limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 100000) return SS_ERR_INVALID_ARG;
+    unsigned* err = device_error_ptr();
+    if (!err) return SS_ERR_CUDA;
+    return launch_selftest_wait(limit_us, err, static_cast<cudaStream_t>(stream));
 }
 
 uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -115,6 +115,8 @@ int launch_selective_grouped(const ScanArgs& a, cudaStream_t st, bool* taken);
 // N in {32, 64, 128} with B, C shared per batch row (scan_wide); *taken is
 // false when the shape or layout does not fit and the general kernel runs.
 int launch_selective_wide(const ScanArgs& a, cudaStream_t st, bool* taken);
+// A kernel whose bounded wait always runs out (ss_selftest_timeout).
+int launch_selftest_wait(unsigned limit_us, unsigned* err, cudaStream_t st);
 int launch_selective_bwd(const BwdArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_selective_step(const StepArgs& a, cudaStream_t st);
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);
