@@ -225,8 +225,9 @@ struct Cfg {
     static constexpr int STAGE = 4 * ACT + 2 * RAWBC;
     static constexpr int OFF_TAB = 2 * STAGE;               // fp32 [t][B 0..15 | C 0..15]
     static constexpr int OFF_OUT = OFF_TAB + TT * 128;      // du, ddelta, dz tiles
-    static constexpr int OFF_RED = OFF_OUT + 3 * ACT;       // [warp][KS][32] fp32
-    static constexpr int OFF_BAR = OFF_RED + NWARPS * KS * 32 * 4;
+    static constexpr int RED = NWARPS * KS * 32 * 4;        // [warp][KS][32] fp32
+    static constexpr int OFF_RED = OFF_OUT + 3 * ACT;       // two of them, alternating
+    static constexpr int OFF_BAR = OFF_RED + 2 * RED;
     static constexpr int SMEM = OFF_BAR + 64 + 1024;
     static constexpr int NV = 2 * N;                        // dB and dC values per step
     static_assert(STAGE % 1024 == 0 && OFF_OUT % 1024 == 0, "swizzled tiles 1024-aligned");
@@ -358,6 +359,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
 
     const uint32_t tab = s0 + C::OFF_TAB;
     const uint32_t red = s0 + C::OFF_RED;
+    int nred = 0;  // sub-chunks flushed so far (selects the reduction buffer)
     const uint32_t out = s0 + C::OFF_OUT;
     float dDacc = 0.f, dbacc = 0.f;
     // value this lane holds after the reduce-scatter over the warp's channels:
@@ -493,6 +495,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         for (int kc = NSUB - 1; kc >= 0; --kc) {
             const int tb = kc * KS;
             if (t0 + tb >= L) continue;
+            const uint32_t redb = red + (nred & 1) * C::RED;
             const float2 hc2[2] = {make_float2(ck_next.x, ck_next.y),
                                    make_float2(ck_next.z, ck_next.w)};
             ck_next = load_ck(t0 / KS + kc - 1);
@@ -579,7 +582,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
                 rs_half<4>(v4, vv2, lane & 8, 8);
                 rs_half<2>(vv2, v1, lane & 4, 4);
                 asm volatile("st.shared.b32 [%0], %1;"
-                             ::"r"(red + ((warp * KS + jj) * 32 + vidx) * 4),
+                             ::"r"(redb + ((warp * KS + jj) * 32 + vidx) * 4),
                              "r"(__float_as_uint(v1[0])) : "memory");
             }
             if (sub < (HAS_Z ? 3 : 2)) {
@@ -609,10 +612,12 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
                 float sum = 0.f;
 #pragma unroll
                 for (int w = 0; w < C::NWARPS; ++w)
-                    sum += __uint_as_float(lds32(red + ((w * KS + jj) * 32 + vv) * 4));
+                    sum += __uint_as_float(lds32(redb + ((w * KS + jj) * 32 + vv) * 4));
                 if (t < L) p.part[(((int64_t)dg * p.Bsz + b) * L + t) * 32 + vv] = sum;
             }
-            __syncthreads();
+            // no barrier here: the next sub-chunk writes the other buffer, and
+            // the barrier after it orders this flush before the one after that
+            ++nred;
         }
         // du / ddelta / dz of the tile leave through TMA stores (clipped at
         // the tensor's edges)
