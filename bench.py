@@ -116,12 +116,37 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C/C++ source without comments and blank lines: edits to comments do
+    not change the kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    lines = ("".join(out)).splitlines()
+    return "\n".join(ln.rstrip() for ln in lines if ln.strip())
+
+
 def source_hash(files=None):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "selective_state_space_146_b300", "csrc")
     names = files or sorted(f for f in os.listdir(d) if f.endswith((".cu", ".cuh", ".h")))
     for f in names:
-        h.update(open(os.path.join(d, f), "rb").read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

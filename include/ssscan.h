@@ -245,10 +245,14 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
  *   dA (D, N), dB, dC (Bsz, N, L), dD (D) iff D given,
  *   ddelta_bias (D) iff delta_bias given -- f32, contiguous (else
  *   SS_ERR_UNSUPPORTED).
- * N <= 16 (else SS_ERR_UNSUPPORTED).  The sums over channels, batch rows and
- * steps are accumulated in f32 in an order that is not fixed, so results can
- * differ by rounding from call to call.  Scratch of Bsz*D*(ceil(L/32)+1)*64
- * bytes is taken stream-ordered from the device's default pool.
+ * N <= 16 (else SS_ERR_UNSUPPORTED).  With N = 16, unit t-stride and 16-byte
+ * aligned rows the sums over channels, batch rows and steps are added in a
+ * fixed order (bitwise reproducible); other layouts use f32 atomics, whose
+ * order, and so the last bits, can differ from call to call.  Scratch is taken
+ * stream-ordered from the device's default pool: the state every 8 steps
+ * (Bsz*D*ceil(L/8)*64 bytes) and per-block partial sums of dB, dC
+ * (ceil(D/32)*Bsz*L*128 bytes) on the fast path; SS_ERR_ALLOC if it cannot
+ * be had.
  */
 int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,

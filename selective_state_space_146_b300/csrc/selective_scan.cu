@@ -5,30 +5,35 @@
 //   h[n] <- exp(dl * A[d,n]) * h[n] + dl * B[b,n,t] * u,
 //   y     = (sum_n C[b,n,t] h[n] + D[d] u) * z * sigmoid(z).
 //
-// Two kernels:
+// Kernels here (the grouped-B/C kernels live in selective_scan_grouped.cu,
+// the N = 32 / 64 / 128 kernel in selective_scan_wide.cu):
 //
 //  * scan_general: one thread per (b, d), any strides, any N <= 256.  Used for
-//    layouts the fast path does not take (odd lengths, non-unit t strides,
-//    N != 16).
+//    what the faster kernels do not take (odd lengths, non-unit t strides,
+//    other N).
 //
 //  * scan_fast: N = 16, unit t stride, 16-byte aligned rows.  One CTA owns a
 //    tile of channels of one batch row over one time segment:
-//      warp 0      TMA (cp.async.bulk.tensor) of the u / delta / z tiles
-//                  (128 bytes of t per channel row, 128-byte swizzle) and of
-//                  the raw B / C tiles into a ring of stages;
-//      warp 1      converts B and C of each tile to an fp32 table shared by
-//                  all channels of the CTA;
-//      warps 2..   consumers: NSPLIT lanes per channel, each keeping N/NSPLIT
+//      warp 0      lane 0 issues the TMA (cp.async.bulk.tensor) loads of the
+//                  u / delta / z tiles (128 bytes of t per channel row,
+//                  128-byte swizzle) and of the raw B / C tiles into a ring of
+//                  stages; all lanes convert B and C of each landed tile to an
+//                  fp32 table shared by all channels of the CTA;
+//      warps 1..   consumers: NSPLIT lanes per channel, each keeping N/NSPLIT
 //                  states in registers and stepping through t sequentially
 //                  with packed f32x2 arithmetic.  delta (softplus) is computed
 //                  once per channel and step and all-gathered in the lane
 //                  group; the partial readouts are reduce-scattered so each
 //                  lane finishes (skip, gate) and stores its own steps of y.
+//                  With the conv in front the tile holds x and the lanes
+//                  compute u = silu(conv(x)) in fp32 the same way as delta.
 //    All hand-offs are mbarriers; every wait is bounded (ERR_WAIT_TIMEOUT).
 //    When the channels alone cannot fill the GPU the sequence is split into
 //    segments: a summary pass records, per segment, prod_t exp(dl A) =
 //    exp(A sum_t dl) and the end state from zero; the main pass seeds each
 //    segment with the fold of its predecessors' summaries.
+//
+//  * scan_step: one recurrent step (decode), four lanes per (b, d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
