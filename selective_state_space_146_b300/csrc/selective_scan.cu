@@ -657,9 +657,10 @@ static bool fast_layout_ok(const ScanArgs& a) {
     };
     if (a.D > 1 && a.su_d == 0) return false;
     if (a.G > 1) {
-        // every channel tile (32 or 64 channels) inside one group, and the
-        // (batch, group) rows of B / C evenly spaced so one tensor map covers them
-        if ((a.D / a.G) % 64 != 0) return false;
+        // every channel tile (32 channels; 64 with one lane per channel, which
+        // is then not used) inside one group, and the (batch, group) rows of
+        // B / C evenly spaced so one tensor map covers them
+        if ((a.D / a.G) % 32 != 0) return false;
         if (a.sB_b != a.G * a.sB_g || a.sC_b != a.G * a.sC_g) return false;
         if ((a.sB_g * es) % 16 || (a.sC_g * es) % 16) return false;
     }
@@ -808,6 +809,8 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
         int split = 1;
         while (split < 4 && ch * split < want) split *= 2;
         if (force == 1 || force == 2 || force == 4 || (force == 8 && bf)) split = force;
+        // one lane per channel makes 64-channel tiles: groups of 32 need two lanes
+        if (a.G > 1 && (a.D / a.G) % 64 != 0 && split == 1) split = 2;
         if (a.cw) {
             // conv in front: the conversion warp owns one channel row per lane
             if (split == 8) split = 4;

@@ -118,13 +118,13 @@ __global__ void __launch_bounds__(256) scan_pc(ScanArgs a) {
     if (valid && a.last) a.last[b * a.sl_b + d * a.sl_d + n * a.sl_n] = h;
 }
 
-// One B, C per channel with TMA staging: the per-lane row loads above make a
-// warp touch 32 rows per instruction, so L1 throughput, not HBM, bounds
-// scan_pc.  Here a CTA takes 8 consecutive channels of one batch row; a
+// Groups of 1, 2, 4 or 8 channels with TMA staging: the per-lane row loads
+// above make a warp touch 32 rows per instruction, so L1 throughput, not HBM,
+// bounds scan_pc.  Here a CTA takes 8 consecutive channels of one batch row; a
 // producer warp streams, per tile of 128 bytes of t, the u / delta / z rows and
-// the 16 B and 16 C rows of each channel ([channel][n][t], 128-byte swizzle)
-// into a 3-stage mbarrier ring, and 16 lanes per channel read their state's
-// row 8 steps at a time from shared memory.
+// the 16 B and 16 C rows of each group the tile's channels read
+// ([group][n][t], 128-byte swizzle) into a 3-stage mbarrier ring, and 16 lanes
+// per channel read their state's row 8 steps at a time from shared memory.
 namespace pc2 {
 
 template <typename T>
@@ -159,6 +159,10 @@ scan_pc_tma(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CU
     const int dtiles = (a.D + C::CH - 1) / C::CH;
     const int b = blockIdx.x / dtiles, d0 = (blockIdx.x % dtiles) * C::CH;
     const int ntiles = (a.L + TT - 1) / TT;
+    // channels per B / C group (1, 2, 4 or 8): the tile's 8 channels read
+    // 8 / gsize group rows of B and C, starting at group d0 / gsize
+    const int gsize = a.D / a.G;
+    const int ngr = C::CH / gsize;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -181,12 +185,12 @@ scan_pc_tma(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CU
                 if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, a.err)) break;
                 uint8_t* st = smem + s * C::STAGE;
                 const int t0 = k * TT;
-                mbar_arrive_expect_tx(&full[s], (HAS_Z ? 3 : 2) * C::ACT + 2 * C::BC);
+                mbar_arrive_expect_tx(&full[s], (HAS_Z ? 3 : 2) * C::ACT + 2 * ngr * 16 * 128);
                 tma_load_3d(st + C::OFF_U, &tm_u, &full[s], t0, d0, b);
                 tma_load_3d(st + C::OFF_DL, &tm_dl, &full[s], t0, d0, b);
                 if (HAS_Z) tma_load_3d(st + C::OFF_Z, &tm_z, &full[s], t0, d0, b);
-                tma_load_4d(st + C::OFF_B, &tm_B, &full[s], t0, 0, d0, b);
-                tma_load_4d(st + C::OFF_C, &tm_C, &full[s], t0, 0, d0, b);
+                tma_load_4d(st + C::OFF_B, &tm_B, &full[s], t0, 0, d0 / gsize, b);
+                tma_load_4d(st + C::OFF_C, &tm_C, &full[s], t0, 0, d0 / gsize, b);
             }
         }
         return;
@@ -203,7 +207,7 @@ scan_pc_tma(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CU
     const bool sp = a.softplus != 0;
     T* y = static_cast<T*>(a.y) + b * a.sy_b + dd_ * a.sy_d;
     const int src = lane & 16;
-    const int brow = (ci * 16 + n);  // this lane's B / C row in the tile
+    const int brow = (ci / gsize) * 16 + n;  // this lane's B / C row in the tile
 
     bool ok = true;
     for (int k = 0; k < ntiles; ++k) {
@@ -270,7 +274,9 @@ scan_pc_tma(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CU
 }  // namespace pc2
 
 static bool pc_tma_ok(const ScanArgs& a) {
-    if (a.G != a.D || a.N != 16 || a.cw || a.L >= (1 << 30)) return false;
+    if (a.G <= 1 || a.N != 16 || a.cw || a.L >= (1 << 30)) return false;
+    const int gsize = a.D / a.G;  // channels per group: the tile's 8 must hold whole groups
+    if (gsize != 1 && gsize != 2 && gsize != 4 && gsize != 8) return false;
     const int es = a.dtype == SS_BF16 ? 2 : 4;
     auto al = [&](const void* ptr, std::initializer_list<int64_t> outer, int64_t st) {
         if (!ptr) return true;
@@ -306,8 +312,10 @@ static int run_pc_tma(const ScanArgs& a, cudaStream_t st) {
     CUtensorMap m[5];
     if (!make_map_3d(&m[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, C::TT, C::CH) ||
         !make_map_3d(&m[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, C::TT, C::CH) ||
-        !make_map_bc4(&m[3], a.Bm, a.dtype, a.L, a.G, a.Bsz, a.sB_n, a.sB_g, a.sB_b, C::TT, C::CH) ||
-        !make_map_bc4(&m[4], a.Cm, a.dtype, a.L, a.G, a.Bsz, a.sC_n, a.sC_g, a.sC_b, C::TT, C::CH))
+        !make_map_bc4(&m[3], a.Bm, a.dtype, a.L, a.G, a.Bsz, a.sB_n, a.sB_g, a.sB_b, C::TT,
+                      C::CH / (a.D / a.G)) ||
+        !make_map_bc4(&m[4], a.Cm, a.dtype, a.L, a.G, a.Bsz, a.sC_n, a.sC_g, a.sC_b, C::TT,
+                      C::CH / (a.D / a.G)))
         return -1;
     if (a.z) {
         if (!make_map_3d(&m[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, C::TT, C::CH)) return -1;
@@ -357,14 +365,14 @@ static int run_pc(const ScanArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
-// One B, C per channel: the TMA kernel (SS_PC_PATH=rows keeps the row-load
-// kernel, for tests); other small groups: the row-load kernel.  *taken says
+// Groups of 1, 2, 4 or 8 channels: the TMA kernel (SS_PC_PATH=rows keeps the
+// row-load kernel, for tests); other small groups: the row-load kernel.  *taken says
 // whether a kernel was launched.
 int launch_selective_grouped(const ScanArgs& a, cudaStream_t st, bool* taken) {
     *taken = false;
     const bool bf = a.dtype == SS_BF16;
     const char* rows = getenv("SS_PC_PATH");
-    if (a.G == a.D && pc_tma_ok(a) && !(rows && !strcmp(rows, "rows"))) {
+    if (pc_tma_ok(a) && !(rows && !strcmp(rows, "rows"))) {
         const int rc = bf ? run_pc_tma<__nv_bfloat16>(a, st) : run_pc_tma<float>(a, st);
         if (rc != -1) {  // -1: no tensor map for this layout
             *taken = true;

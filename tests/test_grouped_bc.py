@@ -44,6 +44,9 @@ CASES = [
     (2, 20, 20, 16, 136, "bf16", True),     # per channel, partial 8-channel tile
     (1, 24, 24, 16, 100, "f32", False),
     (2, 40, 8, 16, 72, "bf16", False),     # groups of 5 channels, no gate / skip / bias
+    (2, 40, 20, 16, 200, "bf16", True),    # groups of 2 channels: TMA kernel, 4 group rows a tile
+    (1, 36, 9, 16, 96, "f32", True),       # groups of 4, partial last tile
+    (2, 96, 3, 16, 128, "bf16", True),     # groups of 32: shared-B, C kernel with group rows
     (2, 24, 4, 16, 77, "f32", True),       # odd length: general kernel
     (1, 16, 16, 8, 64, "f32", True),       # N = 8: general kernel
 ]
