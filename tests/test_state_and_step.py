@@ -146,6 +146,36 @@ def test_ssd_decode_steps_reproduce_the_scan(cuda_device, case):
     check_close(to_np(state), so, _tdt(dt), "ssd decode state")
 
 
+@pytest.mark.parametrize("case", [(3, 3, 6, 5, 128, 3, "f32", False),
+                                  (2, 2, 4, 7, 128, 2, "bf16", True),
+                                  (1, 4, 3, 3, 128, 1, "bf16", False),
+                                  (2, 3, 2, 64, 128, 2, "f32", True)],
+                         ids=lambda c: "x".join(map(str, c[:7])) + ("-strided" if c[7] else ""))
+def test_ssd_decode_n128_rows_cross_heads(cuda_device, case):
+    """The N = 128 step takes several (b, h, p) rows per warp: head dims
+    that are not a multiple of that count make one warp cross heads, groups
+    and batch rows, and B, C with a state stride above one take the
+    element-wise loads."""
+    Bsz, L, H, P, N, G, dt, strided = case
+    inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, seed=3 * L + P)
+    g = cuda_inputs(inp, cuda_device)
+    h0 = _h0((Bsz, H, P, N), 19)
+    state = h0.to(cuda_device).clone()
+
+    def bc(t):
+        return t.transpose(-1, -2).contiguous().transpose(-1, -2) if strided else t.contiguous()
+    ys = []
+    for t in range(L):
+        Bt, Ct = bc(g["B"][:, t]), bc(g["C"][:, t])
+        assert (Bt.stride(-1) == 1) != strided
+        ys.append(_abi.ssd_state_update(state, g["x"][:, t].contiguous(), g["dt"][:, t].contiguous(),
+                                        g["A_head"], Bt, Ct, g["D"]))
+    torch.cuda.synchronize()
+    yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0)
+    check_close(to_np(torch.stack(ys, 1)), yo, _tdt(dt), "ssd decode y")
+    check_close(to_np(state), so, _tdt(dt), "ssd decode state")
+
+
 def test_decode_steps_at_benchmark_shapes(cuda_device):
     """One decode step at the shapes the benchmark times: 8 x 1536 channels,
     N 16 (selective) and 4 x 64 heads x 64, N 128 (SSD), from a random state,
