@@ -1,6 +1,6 @@
 // scan_common.cuh -- device helpers shared by the selective-scan kernels
-// (shared-memory element loads, the lane reduce-scatter) and the signature of
-// cuTensorMapEncodeTiled.
+// (shared-memory element loads, branch-free selects, the lane reduce-scatter)
+// and the signature of cuTensorMapEncodeTiled.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -41,6 +41,19 @@ __device__ __forceinline__ void lds_elems(uint32_t a, float* out) {
 #pragma unroll
         for (int i = 0; i < K; ++i) out[i] = __uint_as_float(w[i]);
     }
+}
+
+// on ? a : b as a select instruction, so that a flag fixed for the whole
+// launch puts no branch into the caller's loop.
+__device__ __forceinline__ float sel_f(bool on, float a, float b) {
+    asm("{ .reg .pred q; setp.ne.s32 q, %2, 0; selp.f32 %0, %1, %0, q; }"
+        : "+f"(b) : "f"(a), "r"((int)on));
+    return b;
+}
+
+// softplus(x) when `on`, else x (both evaluated, then selected).
+__device__ __forceinline__ float softplus_if(float x, bool on) {
+    return sel_f(on, softplus_f(x), x);
 }
 
 // One round of the readout reduce-scatter across the lanes of a channel:

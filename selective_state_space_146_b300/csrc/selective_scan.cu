@@ -460,7 +460,7 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             float x = dv[k] + biasd;
-            x = sp ? softplus_f(x) : x;
+            x = softplus_if(x, sp);
             if (TAIL && c * VEC + part * K + k >= tcount) x = 0.f;  // past the end: no update
             dv[k] = x;
         }

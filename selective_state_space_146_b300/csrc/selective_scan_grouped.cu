@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) scan_pc(ScanArgs a) {
         float own = 0.f;
         if (n < tn) {
             const float x = Elem<T>::to_f(dl[t0 + n]) + bd;
-            own = sp ? softplus_f(x) : x;
+            own = softplus_if(x, sp);
         }
         float yp[TC];
 #pragma unroll
@@ -225,7 +225,7 @@ scan_pc_tma(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CU
                 const uint32_t off = (ci << 7) + ((((j * ES) >> 4) ^ (ci & 7)) << 4) + ((j * ES) & 15);
                 const float x = (ES == 2 ? __uint_as_float(lds16(st + C::OFF_DL + off) << 16)
                                          : __uint_as_float(lds32(st + C::OFF_DL + off))) + bd;
-                own = j < tn ? (sp ? softplus_f(x) : x) : 0.f;
+                own = j < tn ? softplus_if(x, sp) : 0.f;
             }
             // this lane's B and C row, 16 steps, and the channel's u
             float bv[16], cv[16], uv[16];

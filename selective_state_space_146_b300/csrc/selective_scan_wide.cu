@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) scan_wide(ScanArgs a) {
             for (int k = 0; k < K; ++k) {
                 const int t = ts + part * K + k;
                 float x = lds_elem(dr + (jo + k) * ES) + biasd;
-                x = sp ? softplus_f(x) : x;
+                x = softplus_if(x, sp);
                 own[k] = t < L ? x : 0.f;  // past the end: no update
             }
             float dd[VEC], uf[VEC];
