@@ -105,14 +105,19 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
  * allocator (its locks and its implicit synchronisation), or processes that
  * have handed all free device memory to a pool.
  *
- * Same arguments, checks, results and status codes as ss_selective_scan_fwd,
- * except where the segment summaries live: instead of stream-ordered memory
- * they use one fixed 4 MiB array in device memory, defined in the library and
- * held by every GPU that loads it until the process exits.  The call makes no
- * cudaMalloc / cudaMallocAsync / cudaFree and no allocating library call.
- *   - A problem whose summaries need more than 4 MiB is rejected with
- *     SS_ERR_UNSUPPORTED before anything is launched.  (With the built-in
- *     tiling on a 148-SM B300 the summaries stay under about 2.5 MiB.)
+ * Same arguments, checks and status codes as ss_selective_scan_fwd, and the
+ * same results up to rounding, except where the segment summaries live:
+ * instead of stream-ordered memory they use one fixed 4 MiB array in device
+ * memory, defined in the library and held by every GPU that loads it until
+ * the process exits.  The call makes no cudaMalloc / cudaMallocAsync /
+ * cudaFree and no allocating library call.
+ *   - The number of time segments is capped so that the summaries fit the
+ *     array: where ss_selective_scan_fwd would use more (long sequences over
+ *     few channels, e.g. 1 x 2048 x 262144 at N = 16 takes 17 segments here
+ *     instead of 28), the segments are longer and the call can be slower, and
+ *     the summation order (hence the rounding) differs.
+ *   - SS_ERR_UNSUPPORTED is returned, before anything is launched, only if a
+ *     request still exceeded the array.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

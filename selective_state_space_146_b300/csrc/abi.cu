@@ -392,7 +392,7 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
     if (!a.err) return SS_ERR_CUDA;
     FixedScratch fs{fixed_scratch_address(), false};
     if (!fs.base) return SS_ERR_CUDA;
-    Scratch sc{fixed_scratch_alloc, fixed_scratch_release, &fs};
+    Scratch sc{fixed_scratch_alloc, fixed_scratch_release, &fs, kFixedScratchBytes};
     const int rc = launch_selective(a, static_cast<cudaStream_t>(stream), sc);
     // the summaries would not fit the fixed buffer: nothing was launched
     if (rc == SS_ERR_ALLOC && fs.too_large) return SS_ERR_UNSUPPORTED;

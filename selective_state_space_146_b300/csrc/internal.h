@@ -105,6 +105,7 @@ struct Scratch {
     void* (*alloc)(size_t bytes, cudaStream_t st, void* ctx);
     void (*release)(void* p, cudaStream_t st, void* ctx);
     void* ctx;
+    size_t limit = ~size_t(0);  // largest request alloc can meet (kernels size to fit)
 };
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);

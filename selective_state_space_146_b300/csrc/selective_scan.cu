@@ -718,15 +718,33 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     fp.bc_groups = grouped ? a.G : 1;
     fp.bc_dpg = grouped ? a.D / a.G : a.D;
 
-    // Segments: enough CTAs to give every SM several consumer warps.
-    const int sms = sm_count_current();
+    // Segments along t when the channels alone leave the GPU short of CTAs.
+    // Each extra segment adds a summary pass over its predecessors' steps
+    // (about 0.65 of a main step), so the split pays only where the sequence
+    // is long enough; the thresholds below were measured on the B300 over
+    // 48..640 channel tiles and 16..4096 tiles of t (3 CTAs per SM resident):
+    //   >= 2 CTAs per SM already                  -> no split;
+    //   >= 128 tiles of t                         -> about 4 waves of CTAs,
+    //                                                segments >= 8 tiles;
+    //   >= 1 CTA per SM and a shorter sequence    -> no split;
+    //   64..127 tiles                             -> about 2 waves, >= 4 tiles;
+    //   fewer                                     -> about 2 CTAs per SM, >= 4 tiles
+    //                                                (shorter where that leaves SMs idle).
+    const int64_t sms = sm_count_current();
+    const int64_t slots = sms * 3;
     const int64_t ctas = (int64_t)a.Bsz * fp.dtiles;
-    const int64_t want = (int64_t)sms * 2;
-    int nseg = 1;
-    if (ctas < want) nseg = (int)std::min<int64_t>(64, (want + ctas - 1) / ctas);
-    int64_t tiles = (a.L + TT - 1) / TT;
-    nseg = (int)std::min<int64_t>(nseg, tiles);
-    if (nseg < 1) nseg = 1;
+    const int64_t tiles = (a.L + TT - 1) / TT;
+    auto cdiv = [](int64_t x, int64_t y) { return (x + y - 1) / y; };
+    int64_t nseg64 = 1;
+    if (ctas >= 2 * sms) nseg64 = 1;
+    else if (tiles >= 128) nseg64 = std::min(cdiv(4 * slots, ctas), tiles / 8);
+    else if (ctas >= sms) nseg64 = 1;
+    else if (tiles >= 64) nseg64 = std::min(cdiv(2 * slots, ctas), tiles / 4);
+    else nseg64 = std::min(cdiv(2 * sms, ctas), std::max(tiles / 4, cdiv(sms, ctas)));
+    // the summaries ((nseg - 1) x channels x 2N floats) must fit the scratch
+    const size_t per_seg = (size_t)a.Bsz * a.D * 2 * 16 * sizeof(float);
+    nseg64 = std::min<int64_t>(nseg64, 1 + (int64_t)(scratch.limit / per_seg));
+    int nseg = (int)std::max<int64_t>(1, std::min<int64_t>(64, nseg64));
     int64_t seg_tiles = (tiles + nseg - 1) / nseg;
     nseg = (int)((tiles + seg_tiles - 1) / seg_tiles);
     fp.seg_len = (int)(seg_tiles * TT);

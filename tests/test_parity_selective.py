@@ -68,6 +68,8 @@ CASES = [
     (1, 2, 256, 24, "f32", True, True, False, True),      # N = 256
     (1, 32, 16, 4096, "bf16", True, True, True, True),    # few channels: split into segments
     (1, 16, 16, 1000, "f32", True, True, True, True),     # segments with a ragged tail
+    (1, 40, 16, 20000, "bf16", True, True, True, True),   # 39 segments, partial channel tile
+    (1, 8, 16, 70000, "bf16", True, True, True, True),    # the 64-segment cap
 ]
 
 

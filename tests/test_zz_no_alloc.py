@@ -34,9 +34,12 @@ def _call(fn_name, g, y, last):
     assert rc == 0, _abi.status_string(rc)
 
 
-# (batch, d_inner, seqlen, dtype): the first two are split into segments
-# (few channels, long sequence), the last one is not.
-CASES = [(1, 64, 16384, "bf16"), (2, 24, 3000, "f32"), (2, 256, 512, "bf16")]
+# (batch, d_inner, seqlen, dtype): the first three are split into segments
+# (few channels, long sequence); in the third the fixed array holds fewer
+# segments than the regular call uses (16 instead of 26); the last one is
+# not split.
+CASES = [(1, 64, 16384, "bf16"), (2, 24, 3000, "f32"), (1, 2048, 16384, "bf16"),
+         (2, 256, 512, "bf16")]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
