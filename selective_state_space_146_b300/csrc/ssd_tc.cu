@@ -387,6 +387,12 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 // reads TMEM lanes 32 (w % 4) ..), warp 8 issues TMA loads and MMAs.
 namespace ssdtc2 {
 
+// Prefetch a tile of a 4-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
 using ssdtc::N;
 using ssdtc::P;
 using ssdtc::QB;
@@ -402,19 +408,23 @@ constexpr int OFF_B = OFF_X + 32768;      // 2 x [128 t][64 n]                  
 constexpr int OFF_C = OFF_B + 32768;      // 2 x [128 t][64 n]                     32 KB
 constexpr int OFF_M = OFF_C + 32768;      // NHEAD x M (K-major, two 64-col halves) 64 KB
 constexpr int OFF_S = OFF_M + 65536;      // NHEAD x (X~, then the S^T copy)       32 KB
-constexpr int OFF_DT = OFF_S + 32768;     // [128 t][8 h] bf16                      2 KB
-constexpr int OFF_CUM = OFF_DT + 2048;    // [NHEAD][128] f32
+constexpr int OFF_DT = OFF_S + 32768;     // 2 x [128 t][8 h] bf16 (block parity)   4 KB
+constexpr int OFF_CUM = OFF_DT + 4096;    // [NHEAD][128] f32
 constexpr int OFF_DTF = OFF_CUM + 1024;
 constexpr int OFF_GF = OFF_DTF + 1024;
 constexpr int OFF_WS = OFF_GF + 1024;     // [NHEAD][4] f32
-constexpr int OFF_BAR = OFF_WS + 64;      // 12 mbarriers, then the TMEM address
+constexpr int OFF_BAR = OFF_WS + 64;      // 15 mbarriers, then the TMEM address
 constexpr int SMEM_BYTES = OFF_BAR + 128 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ uint32_t tm_ydg(int hh) { return 128u + 192u * hh; }
-__device__ __forceinline__ uint32_t tm_yoff(int hh) { return 192u + 192u * hh; }
-__device__ __forceinline__ uint32_t tm_ds(int hh) { return 256u + 192u * hh; }
+// TMEM columns: C B^T 0..127, then per head pair M X, C S^T and B^T X~ with
+// the two heads side by side (C S^T and B^T X~ of both heads are one MMA of
+// N = 128 each: the heads' S buffers are 16 KB apart, the operand's stride
+// between its two 64-column halves)
+__device__ __forceinline__ uint32_t tm_ydg(int hh) { return 128u + 64u * hh; }
+__device__ __forceinline__ uint32_t tm_yoff(int hh) { return 256u + 64u * hh; }
+__device__ __forceinline__ uint32_t tm_ds(int hh) { return 384u + 64u * hh; }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
@@ -423,13 +433,16 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* bar_bc = bar + 0;      // B, C, dt of the block landed
+    uint64_t* bar_c = bar + 0;       // C and dt of the block landed
     uint64_t* bar_x = bar + 1;       // [hh] x of the block landed
     uint64_t* bar_cb = bar + 3;      // C B^T done
     uint64_t* bar_yoff = bar + 4;    // [hh] C S^T done
     uint64_t* bar_mma23 = bar + 6;   // [hh] M X and B^T X~ done
     uint64_t* bar_m = bar + 8;       // [hh] M and X~ written (compute -> control)
     uint64_t* bar_s = bar + 10;      // [hh] state copy written, x consumed
+    uint64_t* bar_b = bar + 12;      // B of the block landed
+    uint64_t* bar_cfree = bar + 13;  // C S^T of both heads done: C may be refilled
+    uint64_t* bar_bfree = bar + 14;  // B^T X~ of both heads done: B may be refilled
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 128);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -440,8 +453,11 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     const int nblk = (p.L + QB - 1) / QB;
 
     if (tid == 0) {
-        mbar_init(bar_bc, 1);
+        mbar_init(bar_c, 1);
+        mbar_init(bar_b, 1);
         mbar_init(bar_cb, 1);
+        mbar_init(bar_cfree, 1);
+        mbar_init(bar_bfree, 1);
         for (int hh = 0; hh < NHEAD; ++hh) {
             mbar_init(&bar_x[hh], 1);
             mbar_init(&bar_yoff[hh], 1);
@@ -464,33 +480,40 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         // ================= control: TMA loads and MMA issue =================
         if (lane == 0) {
             constexpr uint32_t ID_CB = tc::idesc_bf16(QB, QB, false, false);
-            constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, P, false, true);
+            constexpr uint32_t ID_YOFF = tc::idesc_bf16(QB, NHEAD * P, false, true);
             constexpr uint32_t ID_YDG = tc::idesc_bf16(QB, P, false, true);
-            constexpr uint32_t ID_DS = tc::idesc_bf16(N, P, true, true);
+            constexpr uint32_t ID_DS = tc::idesc_bf16(N, NHEAD * P, true, true);
             tma_prefetch_desc(&tm_x);
             tma_prefetch_desc(&tm_B);
             tma_prefetch_desc(&tm_C);
             tma_prefetch_desc(&tm_dt);
-            auto load_bc = [&](int k) {
+            // C (with dt) and B have their own barriers and reload as soon as
+            // their last reader of block k is done: C after both heads' C S^T,
+            // B after both heads' B^T X~ (issued before M X for that reason),
+            // so block k+1's C B^T is ready when the compute warps reach it
+            auto load_c = [&](int k) {
                 const int t0 = k * QB;
-                mbar_arrive_expect_tx(bar_bc, 32768 + 32768 + 2048);
-                tma_load_4d(sm + OFF_B, &tm_B, bar_bc, 0, g, t0, b);
-                tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_bc, 64, g, t0, b);
-                tma_load_4d(sm + OFF_C, &tm_C, bar_bc, 0, g, t0, b);
-                tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_bc, 64, g, t0, b);
-                tma_load_3d(sm + OFF_DT, &tm_dt, bar_bc, (h0 / 8) * 8, t0, b);
+                mbar_arrive_expect_tx(bar_c, 32768 + 2048);
+                tma_load_4d(sm + OFF_C, &tm_C, bar_c, 0, g, t0, b);
+                tma_load_4d(sm + OFF_C + 16384, &tm_C, bar_c, 64, g, t0, b);
+                tma_load_3d(sm + OFF_DT + (k & 1) * 2048, &tm_dt, bar_c, (h0 / 8) * 8, t0, b);
+            };
+            auto load_b = [&](int k) {
+                const int t0 = k * QB;
+                mbar_arrive_expect_tx(bar_b, 32768);
+                tma_load_4d(sm + OFF_B, &tm_B, bar_b, 0, g, t0, b);
+                tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_b, 64, g, t0, b);
             };
             auto load_x = [&](int hh, int k) {
                 mbar_arrive_expect_tx(&bar_x[hh], 16384);
                 tma_load_4d(sm + OFF_X + hh * 16384, &tm_x, &bar_x[hh], 0, h0 + hh, k * QB, b);
             };
-            load_bc(0);
-            for (int hh = 0; hh < NHEAD; ++hh) load_x(hh, 0);
-            bool go = true;
-            for (int k = 0; k < nblk && go; ++k) {
-                // C B^T: needs B, C of block k (the CB columns were read by
-                // both heads' M of block k-1 before block k's B, C were loaded)
-                if (!mbar_wait(bar_bc, k & 1, p.err)) break;
+            // the last block whose load was issued, per barrier (for draining
+            // loads still in flight if a wait gives up)
+            int c_last = 0, b_last = 0, x_last[NHEAD] = {};
+            // C B^T of block k into TMEM columns 0..127 (read by both heads'
+            // M build of block k)
+            auto issue_cb = [&]() {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -499,26 +522,61 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                                  tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024), ID_CB, kk > 0);
                 }
                 tc::mma_commit(bar_cb);
-                // C S^T per head: needs the head's state copy S(k)
+            };
+            load_c(0);
+            load_b(0);
+            for (int hh = 0; hh < NHEAD; ++hh) load_x(hh, 0);
+            bool go = mbar_wait(bar_c, 0, p.err) && mbar_wait(bar_b, 0, p.err);
+            if (go) issue_cb();
+            for (int k = 0; k < nblk && go; ++k) {
+                // both heads' state copies S(k) written and x tiles free (y of
+                // block k-1 has left them): x of block k first, then C S^T
                 for (int hh = 0; hh < NHEAD && go; ++hh) {
                     if (!mbar_wait(&bar_s[hh], k & 1, p.err)) { go = false; break; }
-                    if (k > 0) load_x(hh, k);  // x of block k-1 consumed
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + tm_yoff(hh),
-                                     tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024),
-                                     tc::smem_desc_sw128(sbase + OFF_S + hh * 16384 + kk * 2048,
-                                                         16384, 1024),
-                                     ID_YOFF, kk > 0);
+                    if (k > 0) {
+                        load_x(hh, k);
+                        x_last[hh] = k;
                     }
-                    tc::mma_commit(&bar_yoff[hh]);
                 }
-                // M X and B^T X~ per head: needs the head's M and X~
+                if (!go) break;
+                // x of block k+1 into L2 now: its copy into shared memory (at
+                // the top of the next block, once y of this block has left the
+                // tile) then comes from L2 instead of DRAM
+                if (k + 1 < nblk)
+                    for (int hh = 0; hh < NHEAD; ++hh)
+                        tma_prefetch_l2_4d(&tm_x, 0, h0 + hh, (k + 1) * QB, b);
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + tm_yoff(0), tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024),
+                                 tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024),
+                                 ID_YOFF, kk > 0);
+                }
+                for (int hh = 0; hh < NHEAD; ++hh) tc::mma_commit(&bar_yoff[hh]);
+                tc::mma_commit(bar_cfree);
+                if (k + 1 < nblk) {
+                    if (!mbar_wait(bar_cfree, k & 1, p.err)) { go = false; break; }
+                    load_c(k + 1);
+                    c_last = k + 1;
+                }
+                // M X per head once the head's M and X~ are written; B^T X~ of
+                // both heads (one MMA of N = 128) once the last head's are,
+                // ahead of that head's M X so that B frees early
                 for (int hh = 0; hh < NHEAD && go; ++hh) {
                     if (!mbar_wait(&bar_m[hh], k & 1, p.err)) { go = false; break; }
                     tc::fence_after_sync();
+                    if (hh == NHEAD - 1) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_bf16(tmem + tm_ds(0),
+                                         tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024),
+                                         tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024),
+                                         ID_DS, kk > 0);
+                        tc::mma_commit(bar_bfree);
+                        // the earlier heads' results are complete with it
+                        for (int h2 = 0; h2 < NHEAD - 1; ++h2) tc::mma_commit(&bar_mma23[h2]);
+                    }
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -527,20 +585,29 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                                      tc::smem_desc_sw128(sbase + OFF_X + hh * 16384 + kk * 2048,
                                                          16384, 1024),
                                      ID_YDG, kk > 0);
-                        tc::mma_bf16(tmem + tm_ds(hh),
-                                     tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024),
-                                     tc::smem_desc_sw128(sbase + OFF_S + hh * 16384 + kk * 2048,
-                                                         16384, 1024),
-                                     ID_DS, kk > 0);
                     }
-                    tc::mma_commit(&bar_mma23[hh]);
+                    if (hh == NHEAD - 1) tc::mma_commit(&bar_mma23[hh]);
                 }
                 if (go && k + 1 < nblk) {
-                    // B, C, dt free once every MMA of block k is done
-                    for (int hh = 0; hh < NHEAD && go; ++hh)
-                        if (!mbar_wait(&bar_mma23[hh], k & 1, p.err)) go = false;
-                    if (go) load_bc(k + 1);
+                    // B of block k+1 once B^T X~ is done, then C B^T of block
+                    // k+1 right away (both heads' M of block k are built, so
+                    // the C B^T columns are free): it runs under the epilogue
+                    if (!mbar_wait(bar_bfree, k & 1, p.err)) { go = false; break; }
+                    load_b(k + 1);
+                    b_last = k + 1;
+                    if (!mbar_wait(bar_c, (k + 1) & 1, p.err) ||
+                        !mbar_wait(bar_b, (k + 1) & 1, p.err)) {
+                        go = false;
+                        break;
+                    }
+                    issue_cb();
                 }
+            }
+            if (!go) {
+                // a wait gave up: let the loads still in flight land (bounded)
+                mbar_wait(bar_c, c_last & 1, p.err);
+                mbar_wait(bar_b, b_last & 1, p.err);
+                for (int hh = 0; hh < NHEAD; ++hh) mbar_wait(&bar_x[hh], x_last[hh] & 1, p.err);
             }
         }
     } else {
@@ -574,13 +641,16 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         fence_proxy_async_smem();
         mbar_arrive(&bar_s[hh]);  // S(0) is ready
 
-        bool ok = true;
-        for (int k = 0; k < nblk; ++k) {
-            const int t0 = k * QB;
-            if (!named_sync_and(nb, 128, mbar_wait(bar_bc, k & 1, p.err))) { ok = false; break; }
-            // ---- cumulative decay (log2 units) and the column factors
-            const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + row * 16 + (h & 7) * 2);
-            const float dtv = __uint_as_float((uint32_t)raw << 16);
+        // ---- cumulative decay of block k (log2 units) and the column factors:
+        //      this row's step, cumulative decay and the block's total in
+        //      registers, the head's columns in shared memory (read by the M
+        //      build only, so the next block's may replace them once every
+        //      thread of the head has built its row of M)
+        auto cumsum = [&](int k, float& cum_t, float& dtv, float& cum_last) -> bool {
+            if (!named_sync_and(nb, 128, mbar_wait(bar_c, k & 1, p.err))) return false;
+            const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + (k & 1) * 2048 +
+                                                                    row * 16 + (h & 7) * 2);
+            dtv = __uint_as_float((uint32_t)raw << 16);
             float v = dtv * A2;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -590,14 +660,20 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             if (lane == 31) wsum[wq] = v;
             named_sync(nb, 128);
             for (int w = 0; w < wq; ++w) v += wsum[w];
-            const float cum_t = v;
+            cum_t = v;
             cum[row] = cum_t;
             dtf[row] = dtv;
             const float cum_end = __shfl_sync(0xffffffffu, cum_t, 31);
             gf[row] = ex2_approx(cum_end - cum_t) * dtv;  // <= dt when A <= 0
             named_sync(nb, 128);
-            const float cum_last = cum[QB - 1];
+            cum_last = cum[QB - 1];
+            return true;
+        };
 
+        float cum_t = 0.f, dtv = 0.f, cum_last = 0.f;
+        bool ok = cumsum(0, cum_t, dtv, cum_last);
+        for (int k = 0; k < nblk && ok; ++k) {
+            const int t0 = k * QB;
             if (!named_sync_and(nb, 128, mbar_wait(bar_cb, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
             // ---- row `row` of M = C B^T o decay o dt (lower triangle), bf16, K-major
@@ -652,6 +728,10 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tc::fence_before_sync();
             mbar_arrive(&bar_m[hh]);
 
+            // ---- the next block's cumulative decay, while this block's MMAs run
+            float n_cum_t = 0.f, n_dtv = 0.f, n_cum_last = 0.f;
+            if (k + 1 < nblk && !cumsum(k + 1, n_cum_t, n_dtv, n_cum_last)) { ok = false; break; }
+
             if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
             // ---- y row = Ydiag + exp(cum) Yoff + D x, written over the row's x in
@@ -704,6 +784,9 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tc::fence_before_sync();
             if (row == 0) bulk_wait_read<0>();  // y has left the x tile: it may be refilled
             mbar_arrive(&bar_s[hh]);
+            cum_t = n_cum_t;
+            dtv = n_dtv;
+            cum_last = n_cum_last;
         }
         if (row == 0) bulk_wait<0>();
         if (ok && p.last) {
