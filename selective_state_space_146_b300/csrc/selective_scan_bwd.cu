@@ -478,13 +478,14 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     }
     float2 g2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 dA2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    // the stored state of the next sub-chunk to process (sub-chunks go from
-    // the last to the first), loaded one sub-chunk ahead
+    // the stored states of the next two sub-chunks to process (sub-chunks go
+    // from the last to the first), loaded two sub-chunks ahead: one ahead
+    // left the load's latency exposed (0.93 -> 0.86 ms at the layer shape)
     auto load_ck = [&](int kcg) {
         return (valid && kcg >= 0) ? *reinterpret_cast<const float4*>(ck + (int64_t)kcg * 16)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    float4 ck_next = load_ck(nkc - 1);
+    float4 ck_next = load_ck(nkc - 1), ck_next2 = load_ck(nkc - 2);
     for (int q = ntiles; q < 2 * ntiles && ok; ++q) {
         if (!(ok = begin(q))) break;
         const uint32_t st = s0 + C::STAGE * (q & 1);
@@ -498,7 +499,8 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
             const uint32_t redb = red + (nred & 1) * C::RED;
             const float2 hc2[2] = {make_float2(ck_next.x, ck_next.y),
                                    make_float2(ck_next.z, ck_next.w)};
-            ck_next = load_ck(t0 / KS + kc - 1);
+            ck_next = ck_next2;
+            ck_next2 = load_ck(t0 / KS + kc - 2);
             float ds[KS], sg[KS], uf[KS], gf[KS], zf[KS];
             deltas(st, kc, tn, ds, sg);
             load8(st + C::OFF_U, kc, uf);

@@ -47,6 +47,9 @@ CASES = [
     (1, 384, 2, 64, 256, 1, "bf16", 64, True),       # N = 256
     (1, 384, 3, 64, 128, 1, "bf16", 128, True),      # odd heads per group: one head per CTA
     (2, 200, 8, 64, 128, 4, "bf16", 128, True),      # two heads per group, ragged tail
+    (1, 100, 2, 64, 128, 1, "bf16", 128, True),      # a single, partial 128-step block
+    (3, 128, 2, 64, 128, 1, "bf16", 64, False),      # exactly one block
+    (1, 129, 4, 64, 128, 2, "bf16", 128, True),      # a second block of one step
 ]
 
 
