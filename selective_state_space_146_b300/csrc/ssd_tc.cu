@@ -687,14 +687,27 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                     float m[32];
                     if (jc < wq && factor) {
                         const float f1 = ex2_approx(cum_t - cum[jc * 32 + 31]);
+                        const float2 f11 = make_float2(f1, f1);
+                        const float2* g2 = reinterpret_cast<const float2*>(gf + jc * 32);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) m[e] = cb[e] * (f1 * gf[jc * 32 + e]);
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 v = __fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]),
+                                                        __fmul2_rn(f11, g2[e]));
+                            m[2 * e] = v.x;
+                            m[2 * e + 1] = v.y;
+                        }
                     } else {
+                        const float2* c2 = reinterpret_cast<const float2*>(cum + jc * 32);
+                        const float2* d2 = reinterpret_cast<const float2*>(dtf + jc * 32);
+                        const float2 ct = make_float2(cum_t, cum_t);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int j = jc * 32 + e;
-                            const float dec = ex2_approx(cum_t - cum[j]);  // j > row: discarded
-                            m[e] = j <= row ? cb[e] * dec * dtf[j] : 0.f;
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = jc * 32 + 2 * e;
+                            const float2 arg = __ffma2_rn(c2[e], make_float2(-1.f, -1.f), ct);  // ct - c, exact negation
+                            const float2 dec = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));  // j > row: discarded
+                            const float2 v = __fmul2_rn(__fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]), dec), d2[e]);
+                            m[2 * e] = j <= row ? v.x : 0.f;
+                            m[2 * e + 1] = j + 1 <= row ? v.y : 0.f;
                         }
                     }
 #pragma unroll
@@ -715,13 +728,18 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             if (!named_sync_and(nb, 128, got)) { ok = false; break; }
             {
                 const float wt = ex2_approx(cum_last - cum_t) * dtv;
+                const float2 wt2 = make_float2(wt, wt);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float x8[8];
                     unpack8(*reinterpret_cast<const uint4*>(xs + swz(row, c)), x8);
-                    *reinterpret_cast<uint4*>(ss + swz(row, c)) =
-                        make_uint4(pack_bf16(wt * x8[0], wt * x8[1]), pack_bf16(wt * x8[2], wt * x8[3]),
-                                   pack_bf16(wt * x8[4], wt * x8[5]), pack_bf16(wt * x8[6], wt * x8[7]));
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 v = __fmul2_rn(wt2, make_float2(x8[2 * i], x8[2 * i + 1]));
+                        w[i] = pack_bf16(v.x, v.y);
+                    }
+                    *reinterpret_cast<uint4*>(ss + swz(row, c)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -750,12 +768,17 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                         uint4* cell = reinterpret_cast<uint4*>(xs + swz(row, half * 4 + q));
                         float x8[8];
                         unpack8(*cell, x8);
-                        float o[8];
+                        uint32_t w[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            o[i] = fmaf(Dh, x8[i], fmaf(eoff, yo[q * 8 + i], yd[q * 8 + i]));
-                        *cell = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                                           pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = q * 8 + 2 * i;
+                            const float2 o = __ffma2_rn(
+                                make_float2(Dh, Dh), make_float2(x8[2 * i], x8[2 * i + 1]),
+                                __ffma2_rn(make_float2(eoff, eoff), make_float2(yo[e], yo[e + 1]),
+                                           make_float2(yd[e], yd[e + 1])));
+                            w[i] = pack_bf16(o.x, o.y);
+                        }
+                        *cell = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
                 fence_proxy_async_smem();
@@ -773,7 +796,12 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 tc::tmem_ld32(trow + tm_ds(hh) + 32, ds + 32);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 64; ++i) S[i] = fmaf(ablk, S[i], ds[i]);
+                for (int i = 0; i < 64; i += 2) {
+                    const float2 v = __ffma2_rn(make_float2(ablk, ablk), make_float2(S[i], S[i + 1]),
+                                                make_float2(ds[i], ds[i + 1]));
+                    S[i] = v.x;
+                    S[i + 1] = v.y;
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<uint4*>(ss + swz(row, c)) =
