@@ -268,14 +268,27 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                     if (jc < warp && factor) {
                         // rows after this chunk: exp(cum_i - cum_j) = f1 * exp(cum_end - cum_j)
                         const float f1 = ex2_approx(cum_t - cum[jc * 32 + 31]);
+                        const float2 f11 = make_float2(f1, f1);
+                        const float2* g2 = reinterpret_cast<const float2*>(gf + jc * 32);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) m[e] = cb[e] * (f1 * gf[jc * 32 + e]);
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 v = __fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]),
+                                                        __fmul2_rn(f11, g2[e]));
+                            m[2 * e] = v.x;
+                            m[2 * e + 1] = v.y;
+                        }
                     } else {
+                        const float2* c2 = reinterpret_cast<const float2*>(cum + jc * 32);
+                        const float2* d2 = reinterpret_cast<const float2*>(dtf + jc * 32);
+                        const float2 ct = make_float2(cum_t, cum_t);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int j = jc * 32 + e;
-                            const float dec = ex2_approx(cum_t - cum[j]);  // j > i: discarded
-                            m[e] = j <= tid ? cb[e] * dec * dtf[j] : 0.f;
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = jc * 32 + 2 * e;
+                            const float2 arg = __ffma2_rn(c2[e], make_float2(-1.f, -1.f), ct);  // ct - c, exact negation
+                            const float2 dec = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));  // j > i: discarded
+                            const float2 v = __fmul2_rn(__fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]), dec), d2[e]);
+                            m[2 * e] = j <= tid ? v.x : 0.f;
+                            m[2 * e + 1] = j + 1 <= tid ? v.y : 0.f;
                         }
                     }
 #pragma unroll
@@ -295,13 +308,18 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_x, k & 1, p.err))) { ok = false; break; }
             {
                 const float wt = ex2_approx(cum_last - cum_t) * dtv;
+                const float2 wt2 = make_float2(wt, wt);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float x8[8];
                     unpack8(*reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c)), x8);
-                    *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) =
-                        make_uint4(pack_bf16(wt * x8[0], wt * x8[1]), pack_bf16(wt * x8[2], wt * x8[3]),
-                                   pack_bf16(wt * x8[4], wt * x8[5]), pack_bf16(wt * x8[6], wt * x8[7]));
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 v = __fmul2_rn(wt2, make_float2(x8[2 * i], x8[2 * i + 1]));
+                        w[i] = pack_bf16(v.x, v.y);
+                    }
+                    *reinterpret_cast<uint4*>(sm + OFF_S + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -326,14 +344,19 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                     for (int q = 0; q < 4; ++q) {
                         float x8[8];
                         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, half * 4 + q)), x8);
-                        float o[8];
+                        uint32_t w[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            o[i] = fmaf(Dh, x8[i], fmaf(eoff, yo[q * 8 + i], yd[q * 8 + i]));
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = q * 8 + 2 * i;
+                            const float2 o = __ffma2_rn(
+                                make_float2(Dh, Dh), make_float2(x8[2 * i], x8[2 * i + 1]),
+                                __ffma2_rn(make_float2(eoff, eoff), make_float2(yo[e], yo[e + 1]),
+                                           make_float2(yd[e], yd[e + 1])));
+                            w[i] = pack_bf16(o.x, o.y);
+                        }
                         if (t < p.L)
                             *reinterpret_cast<uint4*>(yrow + half * 32 + q * 8) =
-                                make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                                           pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+                                make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -346,7 +369,13 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                     tc::tmem_ld32(trow + half * 32, ds);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) S[half * 32 + i] = fmaf(ablk, S[half * 32 + i], ds[i]);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 v = __ffma2_rn(make_float2(ablk, ablk),
+                                                    make_float2(S[half * 32 + i], S[half * 32 + i + 1]),
+                                                    make_float2(ds[i], ds[i + 1]));
+                        S[half * 32 + i] = v.x;
+                        S[half * 32 + i + 1] = v.y;
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
