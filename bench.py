@@ -38,13 +38,16 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 # ALU roof of the selective scan.  Per channel-step the method needs N = 16
-# exponentials exp(delta*A) plus softplus (one ex2, one lg2) and the gate (one
-# tanh): 17 ex2-class and 2 half-rate MUFU operations, i.e. 21 ex2-equivalents.
-# The MUFU pipe bounds the scan before the FP32 pipe does (64 + ~8 fp32
-# lane-operations per channel-step at 128 lanes/SM/clock).  ex2.approx.f32
-# throughput measured on this machine's B300: 29.2 per SM per clock (lg2 and tanh
-# 14.7); 148 SMs at 2032 MHz.
-MUFU_EQ_PER_CHANNEL_STEP = 21
+# exponentials exp(delta*A), softplus log1p(exp(x)) (one ex2, one lg2) and the
+# gate's sigmoid 1/(1 + exp(-z)) (one ex2, one reciprocal): 18 ex2 and 2
+# half-rate MUFU operations, i.e. 22 ex2-equivalents.  The MUFU pipe bounds
+# the scan before the FP32 pipe does (64 + ~8 fp32 lane-operations per
+# channel-step at 128 lanes/SM/clock).  ex2.approx.f32 throughput measured on
+# the B300: 29.2 per SM per clock (lg2 and rcp at half that); 148 SMs at
+# 2032 MHz.
+MUFU_EQ_PER_CHANNEL_STEP = 22
+# nominal B300 HBM3e bandwidth, for the fraction next to the measured one
+NOMINAL_HBM_GBS = 7700.0
 MUFU_EX2_PER_SM_CLK = 29.2
 N_SM = 148
 SM_MHZ_MAX = 2032.0
@@ -800,6 +803,8 @@ def main_ours(args):
                          "hbm_achieved_gbs": round(achieved, 1), "hbm_peak_gbs": hbm_peak,
                          "hbm_frac": round(achieved / hbm_peak, 4),
                          "hbm_peak_source": f"{peak_src} hbm_gbs",
+                         "hbm_frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                         "hbm_nominal_gbs": NOMINAL_HBM_GBS,
                          "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h["h2d"],
