@@ -64,7 +64,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="run WORKLOAD's call warmup+steps times with no timing or output "
-                         "(for ncu captures)")
+                         "(for ncu captures): a workload name, bwd_mamba130m_layer, "
+                         "conv_mamba130m_layer, per_channel_bc_mamba130m_layer, "
+                         "mamba130m_layer_N64 or decode_mamba2_ssd")
     return ap.parse_args()
 
 
@@ -704,6 +706,41 @@ def main_profile(args):
         for _ in range(args.warmup + args.steps):
             abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
                                    g["delta_bias"], dout)
+        torch.cuda.synchronize()
+        return 0 if abi.device_error() == 0 else 1
+    layer = inputs.WORKLOADS["mamba130m_layer"]
+    runs = args.warmup + args.steps
+    if args.profile == "conv_mamba130m_layer":  # causal conv (width 4) + SiLU + scan
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(layer)
+        gen = torch.Generator(device=dev).manual_seed(7)
+        cw = torch.randn(layer.d_inner, 4, generator=gen, device=dev) * 0.5
+        cb = torch.randn(layer.d_inner, generator=gen, device=dev) * 0.1
+        for _ in range(runs):
+            abi.conv_selective_scan_fwd(g["u"], cw, cb, g["delta"], g["A"], g["B"], g["C"],
+                                        g["D"], g["z"], g["delta_bias"], return_last_state=True)
+        torch.cuda.synchronize()
+        return 0 if abi.device_error() == 0 else 1
+    if args.profile in ("per_channel_bc_mamba130m_layer", "mamba130m_layer_N64"):
+        N = 64 if args.profile.endswith("N64") else layer.d_state
+        G = layer.d_inner if args.profile.startswith("per_channel") else None
+        with inputs.on_device(dev):
+            g = inputs.selective_inputs(layer.batch, layer.d_inner, N, layer.seqlen, layer.dtype,
+                                        groups=G)
+        for _ in range(runs):
+            abi.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], return_last_state=True)
+        torch.cuda.synchronize()
+        return 0 if abi.device_error() == 0 else 1
+    if args.profile == "decode_mamba2_ssd":  # one-token SSD state update, 4 x 64 heads x 64, N 128
+        cfg = inputs.WORKLOADS["mamba2_ssd"]
+        with inputs.on_device(dev):
+            g = inputs.ssd_inputs(cfg.batch, 1, cfg.nheads, cfg.headdim, cfg.d_state, cfg.ngroups)
+        state = torch.zeros(cfg.batch, cfg.nheads, cfg.headdim, cfg.d_state, device=dev)
+        x, dt = g["x"][:, 0].contiguous(), g["dt"][:, 0].contiguous()
+        Bt, Ct = g["B"][:, 0].contiguous(), g["C"][:, 0].contiguous()
+        for _ in range(runs):
+            abi.ssd_state_update(state, x, dt, g["A_head"], Bt, Ct, g["D"])
         torch.cuda.synchronize()
         return 0 if abi.device_error() == 0 else 1
     cfg = inputs.WORKLOADS[args.profile]
