@@ -4,8 +4,9 @@
 // longer memory).  Same definition as selective_scan.cu; B, C shared by the
 // channels of a batch row.
 //
-// N / 16 lanes per channel, 16 states per lane in registers.  A CTA of 256
-// threads owns 256 / (N / 16) channels of one batch row.  Time runs in chunks
+// N / 16 lanes per channel, 16 states per lane in registers.  A CTA of T
+// threads (128 for N = 64, else 256) owns T / (N / 16) channels of one batch
+// row.  Time runs in chunks
 // of 32 steps: all threads load the chunk's B and C rows (16-byte loads, the
 // next chunk's while the current one is scanned) and write them as an fp32
 // table [t][state pair: B, B, C, C] in shared memory, double buffered.  Per
@@ -25,20 +26,26 @@ namespace ss {
 
 namespace wide {
 
-constexpr int NTHREADS = 256;
+// Threads per CTA, measured at the Mamba-130M layer shape (8 x 1536 x 2048).
+// N = 64: 256-thread CTAs made 192 CTAs, two on 44 SMs and one on the rest;
+// 128-thread CTAs (four per SM) ran 14% faster.  N = 128: the fp32 B, C tables
+// (64 KB double-buffered) leave room for only three 128-thread CTAs per SM, and
+// 256-thread CTAs ran 13% faster.  N = 32: 256 threads, 1% ahead.
+__host__ __device__ constexpr int threads_for(int N) { return N == 64 ? 128 : 256; }
 constexpr int TC = 32;  // steps per chunk
 constexpr int VEC = 8;  // steps per sub-chunk
 
 template <int N>
 struct Cfg {
+    static constexpr int NT = threads_for(N);     // threads per CTA
     static constexpr int NL = N / 16;             // lanes per channel
-    static constexpr int CPB = NTHREADS / NL;     // channels per CTA
+    static constexpr int CPB = NT / NL;           // channels per CTA
     static constexpr int K = VEC / NL;            // own steps per lane and sub-chunk
     static constexpr int ROW = 8 * N;             // table bytes per step
     static constexpr int TABLE = TC * ROW;        // one table buffer
-    static constexpr int SEGS = 2 * N * (TC / 8) / NTHREADS;  // 8-step row pieces per thread
+    static constexpr int SEGS = 2 * N * (TC / 8) / NT;  // 8-step row pieces per thread
     static_assert(N % 16 == 0 && NL <= VEC, "16 states per lane, at least one own step");
-    static_assert(SEGS >= 1 && 2 * N * (TC / 8) % NTHREADS == 0, "chunk pieces per thread");
+    static_assert(SEGS >= 1 && 2 * N * (TC / 8) % NT == 0, "chunk pieces per thread");
 };
 
 // u, delta and z of the CTA's channels for one chunk: [tensor][channel][TC]
@@ -52,7 +59,7 @@ struct ActCfg {
     static constexpr int BYTES = 3 * TENSOR;                // one buffer
     static constexpr int PIECES_PER_ROW = TC * ES / 16;
     static constexpr int PIECES = 3 * Cfg<N>::CPB * PIECES_PER_ROW;
-    static constexpr int PER_THREAD = (PIECES + NTHREADS - 1) / NTHREADS;
+    static constexpr int PER_THREAD = (PIECES + Cfg<N>::NT - 1) / Cfg<N>::NT;
     static constexpr int SMEM = 2 * Cfg<N>::TABLE + 2 * BYTES;
 };
 
@@ -67,7 +74,7 @@ struct ActLoader {
                                          int tid) {
 #pragma unroll
         for (int q = 0; q < AC::PER_THREAD; ++q) {
-            const int pc = tid + q * NTHREADS;
+            const int pc = tid + q * Cfg<N>::NT;
             w[q] = make_uint4(0u, 0u, 0u, 0u);
             if (pc >= AC::PIECES) continue;
             const int tensor = pc / (Cfg<N>::CPB * AC::PIECES_PER_ROW);
@@ -102,7 +109,7 @@ struct ActLoader {
     __device__ __forceinline__ void store(uint32_t act, int tid) const {
 #pragma unroll
         for (int q = 0; q < AC::PER_THREAD; ++q) {
-            const int pc = tid + q * NTHREADS;
+            const int pc = tid + q * Cfg<N>::NT;
             if (pc >= AC::PIECES) continue;
             const int tensor = pc / (Cfg<N>::CPB * AC::PIECES_PER_ROW);
             const int rem = pc % (Cfg<N>::CPB * AC::PIECES_PER_ROW);
@@ -127,7 +134,7 @@ struct ChunkLoader {
                                          int t0, int L, int tid) {
 #pragma unroll
         for (int q = 0; q < C::SEGS; ++q) {
-            const int s = tid + q * NTHREADS;
+            const int s = tid + q * Cfg<N>::NT;
             const int tensor = s / (4 * N), n = s % N, seg = (s / N) % 4;
             const T* src = (tensor ? Cp + n * sC_n : Bp + n * sB_n) + t0 + seg * 8;
             const int left = L - (t0 + seg * 8);
@@ -155,7 +162,7 @@ struct ChunkLoader {
     __device__ __forceinline__ void store(uint32_t table, int tid) const {
 #pragma unroll
         for (int q = 0; q < C::SEGS; ++q) {
-            const int s = tid + q * NTHREADS;
+            const int s = tid + q * Cfg<N>::NT;
             const int tensor = s / (4 * N), n = s % N, seg = (s / N) % 4;
             float v[8];
             if constexpr (sizeof(T) == 2) {
@@ -189,7 +196,7 @@ struct ChunkLoader {
 };
 
 template <typename T, int N, bool HAS_Z>
-__global__ void __launch_bounds__(NTHREADS, 2) scan_wide(ScanArgs a) {
+__global__ void __launch_bounds__(Cfg<N>::NT, Cfg<N>::NT == 128 ? 4 : 2) scan_wide(ScanArgs a) {
     using C = Cfg<N>;
     using AC = ActCfg<T, N>;
     constexpr int NL = C::NL, K = C::K, ES = (int)sizeof(T);
@@ -355,7 +362,7 @@ static int run(const ScanArgs& a, cudaStream_t st) {
         if (dev >= 0 && dev < 64) attr_set[zi][dev] = true;
     }
     const int64_t ctas = (int64_t)a.Bsz * ((a.D + C::CPB - 1) / C::CPB);
-    kern<<<(unsigned)ctas, NTHREADS, SMEM, st>>>(a);
+    kern<<<(unsigned)ctas, C::NT, SMEM, st>>>(a);
     count_launch(1);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
