@@ -519,6 +519,39 @@ def backward_rows(dev, torch, abi, inputs, hbm_peak, flush):
         torch.cuda.empty_cache()
     except Exception as e:
         rows["bwd_mamba130m_layer"] = {"error": str(e)[:200]}
+    try:
+        # a training step's scan: forward then backward, plain and with the
+        # forward's states kept for the backward
+        cfg = inputs.WORKLOADS["mamba130m_layer"]
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(cfg)
+            dout = inputs.grad_output((cfg.batch, cfg.d_inner, cfg.seqlen), cfg.dtype)
+        args = [g[k] for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")]
+        yb = torch.empty_like(g["u"])
+        ls = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+        ck = torch.empty(cfg.batch, cfg.d_inner, (cfg.seqlen + 7) // 8, 16, device=dev)
+
+        def plain():
+            abi.selective_scan_fwd(*args, y=yb, last_state=ls)
+            abi.selective_scan_bwd(*args, dout)
+
+        def kept():
+            abi.selective_scan_fwd_ckpt(*args, y=yb, last_state=ls, ckpt=ck)
+            abi.selective_scan_bwd_ckpt(*args, dout, ck)
+        ms_plain = statistics.mean(time_device(plain, flush, 5, 3, torch))
+        times, nl = time_device(kept, flush, 5, 3, torch, counter=abi.launch_count)
+        ms = statistics.mean(times)
+        rows["train_step_mamba130m_layer"] = {
+            "ms_per_call": round(ms, 4), "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+            "ms_plain_fwd_then_bwd": round(ms_plain, 4), "launches_per_call": nl / 5,
+            "checkpoint_bytes": ck.numel() * 4,
+            "note": "ss_selective_scan_fwd_ckpt then ss_selective_scan_bwd_ckpt (the backward "
+                    "reads the forward's state every 8 steps); ms_plain_fwd_then_bwd is "
+                    "ss_selective_scan_fwd then ss_selective_scan_bwd"}
+        del g, dout, ck
+        torch.cuda.empty_cache()
+    except Exception as e:
+        rows["train_step_mamba130m_layer"] = {"error": str(e)[:200]}
     return rows
 
 

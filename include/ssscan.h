@@ -267,6 +267,40 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
                           ss_tensor* ddelta_bias, void* stream);
 
 /*
+ * Forward and backward of a training step that share the states (0539edu
+ * paper talk §5.4 weighs keeping the scan's intermediate states for the
+ * backward against recomputing them from the forward; here the forward keeps
+ * the state every 8 steps, 64 bytes per channel and 8 steps, so that the
+ * backward needs no forward pass of its own and recomputes only within 8
+ * steps).
+ *
+ * ss_selective_scan_fwd_ckpt: ss_selective_scan_fwd (same arguments,
+ *   checks, y and last_state) that also writes `ckpt`, f32 (Bsz, D,
+ *   ceil(L/8), 16), contiguous, 16-byte aligned: ckpt[b,d,k,:] = the state
+ *   h before step 8k (h after steps 0 .. 8k-1; zero at k = 0).  N = 16, B, C
+ *   (Bsz, N, L) shared per batch row, unit t-stride and 16-byte aligned rows
+ *   only (the layouts the fast kernels take); else SS_ERR_UNSUPPORTED.
+ * ss_selective_scan_bwd_ckpt: ss_selective_scan_bwd (same arguments, checks
+ *   and gradients) given that checkpoint tensor from the forward of the same
+ *   inputs; it reads the states from it instead of recomputing them (the
+ *   scratch of the states is not taken).  Same layout limits, else
+ *   SS_ERR_UNSUPPORTED; a null ckpt is SS_ERR_INVALID_ARG.  Gradients equal
+ *   ss_selective_scan_bwd's up to rounding (bit for bit when the forward did
+ *   not split the sequence into segments).
+ */
+int ss_selective_scan_fwd_ckpt(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               ss_tensor* y, ss_tensor* last_state, ss_tensor* ckpt,
+                               void* stream);
+int ss_selective_scan_bwd_ckpt(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               const ss_tensor* dout, const ss_tensor* ckpt, ss_tensor* du,
+                               ss_tensor* ddelta, ss_tensor* dA, ss_tensor* dB, ss_tensor* dC,
+                               ss_tensor* dD, ss_tensor* dz, ss_tensor* ddelta_bias, void* stream);
+
+/*
  * One recurrent step (decoding one token), updating the state in place
  * (0539edu paper talk §4.3: the step function of the recurrent form; the
  * state is the only thing carried between tokens).

@@ -24,7 +24,8 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_selective_scan_fwd_init", "ss_ssd_chunk_scan_fwd_init", "ss_selective_state_update",
            "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
-           "ss_version", "ss_selftest_timeout")
+           "ss_version", "ss_selftest_timeout", "ss_selective_scan_fwd_ckpt",
+           "ss_selective_scan_bwd_ckpt")
 
 
 class SSTensor(ctypes.Structure):
@@ -72,6 +73,11 @@ def load(path: str | None = None):
     lib.ss_selective_scan_bwd.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, T, T, T, T, T, T,
                                           vp]
     lib.ss_selective_scan_bwd.restype = i
+    lib.ss_selective_scan_fwd_ckpt.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, vp]
+    lib.ss_selective_scan_fwd_ckpt.restype = i
+    lib.ss_selective_scan_bwd_ckpt.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, T, T, T, T, T,
+                                               T, T, vp]
+    lib.ss_selective_scan_bwd_ckpt.restype = i
     lib.ss_ssd_state_update.argtypes = [T, T, T, T, T, T, T, T, vp]
     lib.ss_ssd_state_update.restype = i
     lib.ss_status_string.argtypes = [i]
@@ -258,6 +264,51 @@ def selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, softplus=True,
                                       _stream_ptr(stream))
     if rc != 0:
         raise SSError(rc, "ss_selective_scan_bwd")
+    return g
+
+
+def selective_scan_fwd_ckpt(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                            y=None, last_state=None, ckpt=None, stream=None):
+    """Forward of a training step (ss_selective_scan_fwd_ckpt): y, the final
+    state and the state every 8 steps for selective_scan_bwd_ckpt.  Returns
+    (y, last_state, ckpt) with ckpt (batch, d_inner, ceil(L / 8), 16) f32."""
+    Bsz, Dch, L = u.shape
+    if y is None:
+        y = torch.empty_like(u, memory_format=torch.contiguous_format)
+    if last_state is None:
+        last_state = torch.empty(Bsz, Dch, A.shape[1], dtype=torch.float32, device=u.device)
+    if ckpt is None:
+        ckpt = torch.empty(Bsz, Dch, (L + 7) // 8, 16, dtype=torch.float32, device=u.device)
+    ts = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    rc = load().ss_selective_scan_fwd_ckpt(*[_ref(t) for t in ts], int(bool(softplus)),
+                                           _ref(describe(y)), _ref(describe(last_state)),
+                                           _ref(describe(ckpt)), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_fwd_ckpt")
+    return y, last_state, ckpt
+
+
+def selective_scan_bwd_ckpt(u, delta, A, B, C, D, z, delta_bias, dout, ckpt, softplus=True,
+                            stream=None):
+    """Backward of a training step (ss_selective_scan_bwd_ckpt) from the
+    forward's checkpoints; returns the same dict as selective_scan_bwd."""
+    f32 = dict(dtype=torch.float32, device=u.device)
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    g = dict(du=torch.empty_like(u, memory_format=torch.contiguous_format),
+             ddelta=torch.empty_like(u, memory_format=torch.contiguous_format),
+             dz=None if z is None else torch.empty_like(u, memory_format=torch.contiguous_format),
+             dA=torch.empty(Dch, N, **f32), dB=torch.empty(Bsz, N, L, **f32),
+             dC=torch.empty(Bsz, N, L, **f32),
+             dD=None if D is None else torch.empty(Dch, **f32),
+             ddelta_bias=None if delta_bias is None else torch.empty(Dch, **f32))
+    ins = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    outs = [describe(g[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")]
+    rc = load().ss_selective_scan_bwd_ckpt(*[_ref(t) for t in ins], int(bool(softplus)),
+                                           _ref(describe(dout)), _ref(describe(ckpt)),
+                                           *[_ref(t) for t in outs], _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_selective_scan_bwd_ckpt")
     return g
 
 

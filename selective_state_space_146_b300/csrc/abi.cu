@@ -379,6 +379,41 @@ int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
                                       last_state, stream);
 }
 
+static bool is_contiguous(const ss_tensor* t);
+
+// The checkpoint tensor of the forward-for-training / backward pair: fp32,
+// (batch, channels, ceil(L / 8), 16), contiguous, 16-byte aligned.
+static int check_ckpt(const ss_tensor* ck, const ss_tensor* u) {
+    SS_TRY(check_tensor(ck, 4));
+    if (ck->dtype != SS_F32) return SS_ERR_DTYPE;
+    const int64_t L = u->shape[2];
+    if (ck->shape[0] != u->shape[0] || ck->shape[1] != u->shape[1] || ck->shape[2] != (L + 7) / 8 ||
+        ck->shape[3] != 16)
+        return SS_ERR_SHAPE;
+    if (!is_contiguous(ck)) return SS_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(ck->data) % 16) return SS_ERR_ALIGNMENT;
+    return SS_OK;
+}
+
+int ss_selective_scan_fwd_ckpt(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               ss_tensor* y, ss_tensor* last_state, ss_tensor* ckpt,
+                               void* stream) {
+    ScanArgs a{};
+    bool nothing = false;
+    if (B && B->ndim == 4) return SS_ERR_UNSUPPORTED;  // B, C shared per batch row only
+    SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, y, last_state,
+                          &a, &nothing));
+    SS_TRY(check_ckpt(ckpt, u));
+    if (nothing) return SS_OK;
+    a.ckpt = static_cast<float*>(ckpt->data);
+    a.err = device_error_ptr();
+    if (!a.err) return SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
+}
+
 int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                                   const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                                   const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
@@ -420,12 +455,12 @@ static int check_grad_f32(const ss_tensor* t, int ndim, const int64_t* shape) {
     return SS_OK;
 }
 
-int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
-                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
-                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
-                          const ss_tensor* dout, ss_tensor* du, ss_tensor* ddelta, ss_tensor* dA,
-                          ss_tensor* dB, ss_tensor* dC, ss_tensor* dD, ss_tensor* dz,
-                          ss_tensor* ddelta_bias, void* stream) {
+static int selective_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                         const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                         const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                         const ss_tensor* dout, const ss_tensor* ckpt, ss_tensor* du,
+                         ss_tensor* ddelta, ss_tensor* dA, ss_tensor* dB, ss_tensor* dC,
+                         ss_tensor* dD, ss_tensor* dz, ss_tensor* ddelta_bias, void* stream) {
     ScanArgs f{};
     bool nothing = false;
     if (B && B->ndim == 4) return SS_ERR_UNSUPPORTED;  // B, C shared per batch row only
@@ -450,6 +485,7 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
     if (dD) SS_TRY(check_grad_f32(dD, 1, sD1));
     if (ddelta_bias) SS_TRY(check_grad_f32(ddelta_bias, 1, sD1));
     if (N > 16) return SS_ERR_UNSUPPORTED;
+    if (ckpt) SS_TRY(check_ckpt(ckpt, u));
 
     BwdArgs a{};
     a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = u->dtype;
@@ -474,10 +510,32 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
         a.sddl_b = ddelta->stride[0]; a.sddl_d = ddelta->stride[1]; a.sddl_t = ddelta->stride[2];
         if (dz) { a.dz = dz->data; a.sdz_b = dz->stride[0]; a.sdz_d = dz->stride[1]; a.sdz_t = dz->stride[2]; }
     }
+    a.ckpt_in = ckpt ? static_cast<const float*>(ckpt->data) : nullptr;
     a.err = device_error_ptr();
     if (!a.err) return SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_selective_bwd(a, static_cast<cudaStream_t>(stream), sc);
+}
+
+int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                          const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                          const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                          const ss_tensor* dout, ss_tensor* du, ss_tensor* ddelta, ss_tensor* dA,
+                          ss_tensor* dB, ss_tensor* dC, ss_tensor* dD, ss_tensor* dz,
+                          ss_tensor* ddelta_bias, void* stream) {
+    return selective_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, nullptr, du, ddelta,
+                         dA, dB, dC, dD, dz, ddelta_bias, stream);
+}
+
+int ss_selective_scan_bwd_ckpt(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
+                               const ss_tensor* dout, const ss_tensor* ckpt, ss_tensor* du,
+                               ss_tensor* ddelta, ss_tensor* dA, ss_tensor* dB, ss_tensor* dC,
+                               ss_tensor* dD, ss_tensor* dz, ss_tensor* ddelta_bias, void* stream) {
+    if (!ckpt) return SS_ERR_INVALID_ARG;
+    return selective_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, ckpt, du, ddelta,
+                         dA, dB, dC, dD, dz, ddelta_bias, stream);
 }
 
 // ---------------------------------------------------------------------------

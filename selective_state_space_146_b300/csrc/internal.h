@@ -31,6 +31,9 @@ struct ScanArgs {
     int cwidth;
     int softplus;
     unsigned* err;  // device error word
+    // state at the start of every 8-step sub-chunk, [b][d][ceil(L/8)][16]
+    // fp32, written by the forward when non-null (the backward's layout)
+    float* ckpt = nullptr;
 };
 
 // Host view of one SSD call, element strides.
@@ -98,6 +101,9 @@ struct BwdArgs {
     float *dA, *dB, *dC, *dD, *dbias;
     float* ckpt;  // chunk-start states, filled by the kernel
     unsigned* err;
+    // the forward's states at every 8-step sub-chunk start, [b][d][ceil(L/8)][16]
+    // (ss_selective_scan_fwd_ckpt); when given the backward skips its forward pass
+    const float* ckpt_in = nullptr;
 };
 
 // Scratch provider: either stream-ordered allocation or a fixed buffer.

@@ -140,6 +140,8 @@ struct FastParams {
     int bc_dpg;     // channels per group, a multiple of the channel tile
     int softplus;
     unsigned* err;
+    float* ckpt;    // CKPT kernels: [Bsz*D][nkc][16] states at every 8-step sub-chunk start
+    int nkc;
 };
 
 template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY>
@@ -271,7 +273,8 @@ __device__ __forceinline__ void stg_elems(T* p, const float* v, int limit) {
     }
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV,
+          bool CKPT = false>
 __global__ void __launch_bounds__(FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>::NTHREADS, 3)
 scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -468,7 +471,17 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
         for (int j = 0; j < VEC; ++j)
             dd[j] = NSPLIT == 1 ? dv[j % K] : __shfl_sync(0xffffffffu, dv[j % K], gbase + j / K);
     };
+    // CKPT: the state at the start of every 8-step sub-chunk goes to p.ckpt
+    // (lane `part` holds states 4 part .. 4 part + 3), for the backward
+    static_assert(!CKPT || (NSPLIT == 4 && !SUMMARY && !CONV), "checkpoints: 4 lanes per channel");
+    int ck_t0 = 0;  // first step of the tile being scanned
     auto core = [&](uint32_t bcp, int c, const float* dd, const float* uf, float* yv) {
+        if constexpr (CKPT) {
+            const int tg = ck_t0 + c * VEC;
+            if (valid && tg % 8 == 0)
+                *reinterpret_cast<float4*>(p.ckpt + ((int64_t)bd * p.nkc + tg / 8) * 16 + part * NS) =
+                    make_float4(h2[0].x, h2[0].y, h2[1].x, h2[1].y);
+        }
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
             if (SUMMARY) dsum += dd[i];
@@ -589,6 +602,7 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
         const int tile_t0 = tbeg + k * TT;
         const int tcount = min(TT, tend - tile_t0);
         const uint32_t su = smem_u32(stage(s));
+        ck_t0 = tile_t0;
         if (tcount == TT) full_tile(su, tile_t0);
         else tail_tile(su, tile_t0, tcount);
         if constexpr (CONV) {
@@ -670,11 +684,12 @@ static bool fast_layout_ok(const ScanArgs& a) {
            a.L < (1 << 30);
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV,
+          bool CKPT = false>
 static cudaError_t launch_fast_kernel(const CUtensorMap* maps, const FastParams& fp, dim3 grid,
                                       cudaStream_t st) {
     using Cfg = FastCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY>;
-    auto kern = scan_fast<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY, CONV>;
+    auto kern = scan_fast<T, NSPLIT, CWARPS, STAGES, HAS_Z, SUMMARY, CONV, CKPT>;
     static bool attr_set[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -698,7 +713,7 @@ static cudaError_t launch_fast_kernel(const CUtensorMap* maps, const FastParams&
 // channels; three stages fit three CTAs in one SM's shared memory.
 constexpr int kStages = 3;
 
-template <typename T, int NSPLIT, int kCWarps, bool CONV>
+template <typename T, int NSPLIT, int kCWarps, bool CONV, bool CKPT = false>
 static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
     using CfgM = FastCfg<T, NSPLIT, kCWarps, kStages, true, false>;
     constexpr int TT = CfgM::TT, DT = CfgM::DT;
@@ -714,6 +729,7 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
     fp.cw = a.cw; fp.scw_d = a.scw_d; fp.scw_k = a.scw_k; fp.cb = a.cb; fp.scb = a.scb;
     fp.cwidth = a.cwidth;
     fp.softplus = a.softplus; fp.err = a.err;
+    fp.ckpt = a.ckpt; fp.nkc = (a.L + 7) / 8;
     const bool grouped = a.G > 1;
     fp.bc_groups = grouped ? a.G : 1;
     fp.bc_dpg = grouped ? a.D / a.G : a.D;
@@ -780,9 +796,9 @@ static int run_fast(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) 
             return SS_ERR_LAUNCH;
         }
     }
-    cudaError_t e = a.z ? launch_fast_kernel<T, NSPLIT, kCWarps, kStages, true, false, CONV>(
+    cudaError_t e = a.z ? launch_fast_kernel<T, NSPLIT, kCWarps, kStages, true, false, CONV, CKPT>(
                               maps, fp, dim3((unsigned)ctas, nseg), st)
-                        : launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, false, CONV>(
+                        : launch_fast_kernel<T, NSPLIT, kCWarps, kStages, false, false, CONV, CKPT>(
                               maps, fp, dim3((unsigned)ctas, nseg), st);
     if (summ) scratch.release(summ, st, scratch.ctx);
     return e == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
@@ -817,6 +833,13 @@ static int forced_path() {
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
     const int force = forced_path();
     const bool bf = a.dtype == SS_BF16;
+    if (a.ckpt) {
+        // checkpoints for the backward come from the fast kernel with four
+        // lanes per channel (the backward's layout of states across lanes)
+        if (a.L <= 0 || a.cw || a.G > 1 || !fast_layout_ok(a)) return SS_ERR_UNSUPPORTED;
+        return bf ? run_fast<__nv_bfloat16, 4, 4, false, true>(a, st, scratch)
+                  : run_fast<float, 4, 4, false, true>(a, st, scratch);
+    }
     if (force != 0 && a.L > 0 && fast_layout_ok(a)) {
         // The fewest lanes per channel (at most 4) that give every SM 16
         // consumer warps.  Eight lanes per channel gives more warps but costs

@@ -239,7 +239,8 @@ struct Params {
     const float* A; int64_t sA_d, sA_n;
     const float* Dv; int64_t sD;
     const float* bias; int64_t sbias;
-    float* ckpt;      // [b][d][L/16 rounded up][16]: the state before each sub-chunk
+    float* ckpt;      // [b][d][L/8 rounded up][16]: the state before each sub-chunk
+    int ck_given;     // ckpt holds the forward's states: no forward pass here
     float* part;      // [dgroup][b][t][32]: dB (n) then dC (n), summed over a CTA
     float* partA;     // [b][d][16]
     float* partD;     // [b][d]
@@ -323,11 +324,14 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     }
     __syncthreads();
 
-    // load q of 2 ntiles: pass 1 tile q, then pass 2 tile 2 ntiles - 1 - q
+    // load q of 2 ntiles: pass 1 tile q, then pass 2 tile 2 ntiles - 1 - q.
+    // With the forward's states given, pass 1 is skipped and the loads start
+    // at q0 = ntiles; stages and barrier phases count from q0.
+    const int q0 = p.ck_given ? ntiles : 0;
     auto issue = [&](int q) {
         if (q >= 2 * ntiles) return;
-        const uint32_t st = C::STAGE * (q & 1);
-        uint64_t* bar = &full[q & 1];
+        const uint32_t st = C::STAGE * ((q - q0) & 1);
+        uint64_t* bar = &full[(q - q0) & 1];
         uint8_t* base = smem + st;
         if (q < ntiles) {
             const int t0 = q * TT;
@@ -353,8 +357,8 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         tma_prefetch_desc(&tm_B);
         tma_prefetch_desc(&tm_C);
         if (HAS_Z) tma_prefetch_desc(&tm_z);
-        issue(0);
-        issue(1);
+        issue(q0);
+        issue(q0 + 1);
     }
 
     const uint32_t tab = s0 + C::OFF_TAB;
@@ -366,18 +370,18 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     // kind (lane bit 4: 0 = dB, 1 = dC) of state 4 sub + (lane bits 3..2)
     const int vidx = ((lane >> 4) & 1) * 16 + 4 * sub + ((lane >> 2) & 3);
 
-    int consumed = 0;  // loads waited for
+    int consumed = q0;  // loads waited for
     // start of load q: wait for it (and, in pass 2, for the previous tile's
     // output stores to have left the out tiles), then build the B|C table
     auto begin = [&](int q) -> bool {
         bool ok = true;
         if (tid == 0) {
-            ok = mbar_wait(&full[q & 1], (q >> 1) & 1, p.err);
+            ok = mbar_wait(&full[(q - q0) & 1], ((q - q0) >> 1) & 1, p.err);
             if (q >= ntiles + 1) bulk_wait_read<0>();
         }
         if (!__syncthreads_and(ok)) return false;
         consumed = q + 1;
-        const uint32_t st = s0 + C::STAGE * (q & 1);
+        const uint32_t st = s0 + C::STAGE * ((q - q0) & 1);
         convert_table<T, C::NWARPS>(st + C::OFF_B, st + C::OFF_C, tab, q >= ntiles, warp, lane);
         __syncthreads();
         return true;
@@ -445,7 +449,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     {
         // ---- pass 1: forward, store the state before every sub-chunk
         float2 h2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        for (int q = 0; q < ntiles && ok; ++q) {
+        for (int q = 0; q < ntiles && ok && !p.ck_given; ++q) {
             if (!(ok = begin(q))) break;
             const uint32_t st = s0 + C::STAGE * (q & 1);
             const int t0 = q * TT, tn = min(TT, L - t0);
@@ -488,7 +492,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     float4 ck_next = load_ck(nkc - 1), ck_next2 = load_ck(nkc - 2);
     for (int q = ntiles; q < 2 * ntiles && ok; ++q) {
         if (!(ok = begin(q))) break;
-        const uint32_t st = s0 + C::STAGE * (q & 1);
+        const uint32_t st = s0 + C::STAGE * ((q - q0) & 1);
         const int tile = 2 * ntiles - 1 - q;
         const int t0 = tile * TT, tn = min(TT, L - t0);
         // ---- pass 2: backward over the tile's sub-chunks, last first
@@ -639,7 +643,7 @@ scan_bwd_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         // a load never arrived: wait (bounded) for the ones still in flight
         if (tid == 0)
             for (int k = consumed; k < min(consumed + 2, 2 * ntiles); ++k)
-                mbar_wait(&full[k & 1], (k >> 1) & 1, p.err);
+                mbar_wait(&full[(k - q0) & 1], ((k - q0) >> 1) & 1, p.err);
         return;
     }
     if (!valid) return;
@@ -729,7 +733,7 @@ static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratc
     }
     const int dgroups = (a.D + C::CH - 1) / C::CH;
     const int nkc = (a.L + C::KS - 1) / C::KS;
-    const size_t n_ck = (size_t)a.Bsz * a.D * nkc * 16;
+    const size_t n_ck = a.ckpt_in ? 0 : (size_t)a.Bsz * a.D * nkc * 16;
     const size_t n_part = (size_t)dgroups * a.Bsz * a.L * 32;
     const size_t n_pa = (size_t)a.Bsz * a.D * 16, n_pd = (size_t)a.Bsz * a.D;
     const size_t bytes = sizeof(float) * (n_ck + n_part + n_pa + 2 * n_pd);
@@ -741,7 +745,8 @@ static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratc
     p.A = a.A; p.sA_d = a.sA_d; p.sA_n = a.sA_n;
     p.Dv = a.Dv; p.sD = a.sD;
     p.bias = a.bias; p.sbias = a.sbias;
-    p.ckpt = base;
+    p.ckpt = a.ckpt_in ? const_cast<float*>(a.ckpt_in) : base;  // given: only read
+    p.ck_given = a.ckpt_in ? 1 : 0;
     p.part = base + n_ck;
     p.partA = p.part + n_part;
     p.partD = p.partA + n_pa;
@@ -777,6 +782,13 @@ int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& sc
     BwdArgs a = args;
     const bool empty = a.L == 0 || a.Bsz == 0 || a.D == 0;
     const char* force = getenv("SS_BWD_PATH");
+    if (a.ckpt_in && !empty) {
+        // the forward's states come in the fast kernel's layout only
+        if (a.N != 16 || !bwd_fast_ok(a)) return SS_ERR_UNSUPPORTED;
+        const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
+                                          : run_bwd_fast<float>(a, st, scratch);
+        return rc == -1 ? SS_ERR_UNSUPPORTED : rc;
+    }
     if (!empty && !(force && !strcmp(force, "general")) && bwd_fast_ok(a)) {
         const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
                                           : run_bwd_fast<float>(a, st, scratch);
