@@ -31,7 +31,9 @@
 //    When the channels alone cannot fill the GPU the sequence is split into
 //    segments: a summary pass records, per segment, prod_t exp(dl A) =
 //    exp(A sum_t dl) and the end state from zero; the main pass seeds each
-//    segment with the fold of its predecessors' summaries.
+//    segment with the fold of its predecessors' summaries.  For a training
+//    step (CKPT) each lane also stores its four states at every 8-step
+//    sub-chunk start, in the backward kernel's layout.
 //
 //  * scan_step: one recurrent step (decode), four lanes per (b, d).
 #include <cuda.h>

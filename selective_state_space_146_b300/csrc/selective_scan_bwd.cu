@@ -17,10 +17,12 @@
 //    32 channels of a batch row, four lanes per channel, each lane keeping four
 //    states.  Activations arrive as 128-byte-swizzled TMA tiles (64 bf16 or 32
 //    fp32 steps), double buffered.  Pass 1 runs the recurrence forward over the
-//    tiles and stores the state every 8 steps (stream-ordered scratch).
-//    Pass 2 walks the tiles backwards; for each 8-step sub-chunk it recomputes
-//    the states into registers from the stored one (loaded one sub-chunk
-//    ahead), then steps t down with the adjoint.  Sums over the four lanes of a channel are two xor-shuffles; dB
+//    tiles and stores the state every 8 steps (stream-ordered scratch); given
+//    those states from the forward (ss_selective_scan_bwd_ckpt) it skips this
+//    pass.  Pass 2 walks the tiles backwards; for each 8-step sub-chunk it
+//    recomputes the states into registers from the stored one (loaded two
+//    sub-chunks ahead), then steps t down with the adjoint.  Sums over the
+//    four lanes of a channel are two xor-shuffles; dB
 //    and dC are reduce-scattered over the eight channels of a warp, summed over
 //    the CTA's warps in shared memory and written as per-CTA partial sums;
 //    du / ddelta / dz leave through TMA stores.  scan_bwd_finish then adds the
