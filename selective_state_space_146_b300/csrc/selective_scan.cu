@@ -835,10 +835,10 @@ static int forced_path() {
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
     const int force = forced_path();
     const bool bf = a.dtype == SS_BF16;
-    if (a.ckpt) {
+    if (a.ckpt && a.L > 0) {  // (with L = 0 there are no checkpoints to write)
         // checkpoints for the backward come from the fast kernel with four
         // lanes per channel (the backward's layout of states across lanes)
-        if (a.L <= 0 || a.cw || a.G > 1 || !fast_layout_ok(a)) return SS_ERR_UNSUPPORTED;
+        if (a.cw || a.G > 1 || !fast_layout_ok(a)) return SS_ERR_UNSUPPORTED;
         return bf ? run_fast<__nv_bfloat16, 4, 4, false, true>(a, st, scratch)
                   : run_fast<float, 4, 4, false, true>(a, st, scratch);
     }

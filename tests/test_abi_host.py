@@ -256,3 +256,40 @@ def test_host_buffer_entry_point_rejects_strided_tensors(lib):
     r = {k: v.ref for k, v in b.items()}
     assert lib.ss_selective_scan_fwd_host(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
                                           r["z"], r["bias"], 3, r["y"], r["last"], None) == -1
+
+
+def _call_fwd_ckpt(lib, a, ck):
+    r = {k: (None if v is None else v.ref) for k, v in a.items()}
+    return lib.ss_selective_scan_fwd_ckpt(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 1, r["y"], r["last"],
+                                          None if ck is None else ck.ref, None)
+
+
+def _call_bwd_ckpt(lib, a, g, ck):
+    r = {k: (None if v is None else v.ref) for k, v in a.items()}
+    o = {k: (None if v is None else v.ref) for k, v in g.items()}
+    return lib.ss_selective_scan_bwd_ckpt(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"],
+                                          r["z"], r["bias"], 1, r["y"],
+                                          None if ck is None else ck.ref, o["du"], o["ddelta"],
+                                          o["dA"], o["dB"], o["dC"], o["dD"], o["dz"], o["dbias"],
+                                          None)
+
+
+def test_checkpoint_pair_argument_errors(lib):
+    f = _abi.SS_F32
+    a = _sel_args()  # L = 64: 8 checkpoints per channel
+    assert _call_fwd_ckpt(lib, a, None) == -1
+    assert _call_fwd_ckpt(lib, a, FakeT((2, 8, 9, 16), f)) == -2          # count of checkpoints
+    assert _call_fwd_ckpt(lib, a, FakeT((2, 8, 8, 8), f)) == -2           # 16 states each
+    assert _call_fwd_ckpt(lib, a, FakeT((2, 8, 8, 16))) == -3             # fp32 only
+    assert _call_fwd_ckpt(lib, a, FakeT((2, 8, 8, 16), f, stride=[2048, 256, 32, 1])) == -5
+    assert _call_fwd_ckpt(lib, a, FakeT((2, 8, 8, 16), f, data=0x10004)) == -4  # 16-byte rows
+    g = _sel_args()
+    g["B"], g["C"] = FakeT((2, 2, 16, 64)), FakeT((2, 2, 16, 64))
+    assert _call_fwd_ckpt(lib, g, FakeT((2, 8, 8, 16), f)) == -5          # shared B, C only
+    assert _call_bwd_ckpt(lib, a, _bwd_grads(), None) == -1
+    assert _call_bwd_ckpt(lib, a, _bwd_grads(), FakeT((2, 8, 7, 16), f)) == -2
+    # nothing to scan and no final state asked for: accepted, no device touched
+    e = _sel_args(L=0)
+    e["last"] = None
+    assert _call_fwd_ckpt(lib, e, FakeT((2, 8, 0, 16), f)) == 0

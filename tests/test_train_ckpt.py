@@ -113,3 +113,15 @@ def test_checkpoint_calls_reject_what_they_do_not_take(cuda_device):
     odd = cuda_inputs(inputs.selective_inputs(1, 32, 16, 77, "f32", seed=1), cuda_device)
     with pytest.raises(_abi.SSError, match="UNSUPPORTED"):  # rows not 16-byte multiples
         _abi.selective_scan_fwd_ckpt(*_args(odd))
+
+
+def test_empty_sequence_writes_the_zero_state(cuda_device):
+    """L = 0: no checkpoints, and the final state is the zero state, as from
+    the plain forward."""
+    inp = inputs.selective_inputs(2, 32, 16, 0, "bf16", seed=2)
+    g = cuda_inputs(inp, cuda_device)
+    last = torch.full((2, 32, 16), float("nan"), device=cuda_device)
+    ck = torch.empty(2, 32, 0, 16, device=cuda_device)
+    _abi.selective_scan_fwd_ckpt(*_args(g), last_state=last, ckpt=ck)
+    torch.cuda.synchronize()
+    assert not last.any() and not last.isnan().any()
