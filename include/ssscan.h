@@ -1,11 +1,23 @@
 /*
  * ssscan.h -- C ABI of the B300 (sm_103a) selective-scan library.
  *
- * Two operations, both forward only, both asynchronous on the caller's CUDA
- * stream:
+ * The two scans and what sits around them, all asynchronous on the caller's
+ * CUDA stream:
  *
- *   ss_selective_scan_fwd   the Mamba (Mamba-1) selective scan
- *   ss_ssd_chunk_scan_fwd   the Mamba-2 SSD scan in chunked form
+ *   ss_selective_scan_fwd        the Mamba (Mamba-1) selective scan
+ *   ss_ssd_chunk_scan_fwd        the Mamba-2 SSD scan in chunked form
+ *   ss_selective_scan_fwd_init,  the same, continuing from a given state
+ *   ss_ssd_chunk_scan_fwd_init
+ *   ss_conv_selective_scan_fwd   the causal conv1d + SiLU fused in front
+ *   ss_selective_scan_bwd        the selective scan's gradients
+ *   ss_selective_scan_fwd_ckpt,  a training step's forward / backward that
+ *   ss_selective_scan_bwd_ckpt   share the states every 8 steps
+ *   ss_selective_state_update,   one decode step of either model
+ *   ss_ssd_state_update
+ *   ss_selective_scan_fwd_host   the selective scan from host buffers
+ *   ss_selective_scan_fwd_noalloc the selective scan with no allocation
+ *   ss_status_string, ss_get_device_error, ss_launch_count, ss_version,
+ *   ss_selftest_timeout          status, errors and diagnostics
  *
  * Every buffer is caller-owned device memory described by an ss_tensor
  * (pointer, dtype, shape, strides in elements).  The library keeps no pointer

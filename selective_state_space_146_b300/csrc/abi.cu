@@ -867,6 +867,6 @@ int ss_selftest_timeout(unsigned limit_us, void* stream) {
 
 uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int ss_version(void) { return 200; }
+int ss_version(void) { return 300; }
 
 }  // extern "C"
