@@ -183,3 +183,38 @@ def test_fuzz_decode_steps(cuda_device, c):
                                    inp["z"], inp["delta_bias"], h0=h0)
     check_close(to_np(torch.stack(ys, -1)), yo, _tdt(c["dt"]), f"y {c}")
     check_close(to_np(state), so, _tdt(c["dt"]), f"state {c}")
+
+
+@SETTINGS
+@given(c=st.fixed_dictionaries({
+    "Bsz": st.integers(1, 2), "D": st.integers(1, 70), "L": st.integers(1, 260),
+    "dt": st.sampled_from(["f32", "bf16"]), "gate": st.booleans(), "skip": st.booleans(),
+    "bias": st.booleans(), "seed": st.integers(0, 10_000)}))
+def test_fuzz_training_step_pair(cuda_device, c):
+    """The forward that keeps the states and the backward that reads them:
+    every gradient against the oracle where the rows are 16-byte multiples
+    (the layouts these calls take), SS_ERR_UNSUPPORTED elsewhere."""
+    inp = inputs.selective_inputs(c["Bsz"], c["D"], 16, c["L"], c["dt"], gate=c["gate"],
+                                  skip=c["skip"], bias=c["bias"], seed=c["seed"])
+    dout = inputs.grad_output((c["Bsz"], c["D"], c["L"]), c["dt"], seed=c["seed"])
+    dev = cuda_device
+    args = [_dev(inp[k], dev) for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")]
+    row_bytes = c["L"] * (4 if c["dt"] == "f32" else 2)
+    if row_bytes % 16:
+        with pytest.raises(_abi.SSError, match="UNSUPPORTED"):
+            _abi.selective_scan_fwd_ckpt(*args)
+        return
+    y, _, ck = _abi.selective_scan_fwd_ckpt(*args)
+    out = _abi.selective_scan_bwd_ckpt(*args, dout.to(dev), ck)
+    torch.cuda.synchronize()
+    assert _abi.device_error() == 0
+    yo, _ = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["delta_bias"], nthreads=8)
+    check_close(to_np(y), yo, _tdt(c["dt"]), f"y {c}")
+    ref = oracle.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                    inp["D"], inp["z"], inp["delta_bias"], dout)
+    for k, v in ref.items():
+        if v is None:
+            assert out[k] is None
+        else:
+            check_close(to_np(out[k]), v, _tdt(c["dt"]), f"{k} {c}")
