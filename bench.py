@@ -79,7 +79,7 @@ def selective_bytes(cfg):
     steps = cfg.batch * cfg.d_inner * cfg.seqlen
     per_step = es * (3 + (1 if cfg.gate else 0))           # u, delta, (z) in; y out
     bc = 2 * cfg.batch * cfg.d_state * cfg.seqlen * es       # B and C, read once
-    params = 4 * cfg.d_inner * (cfg.d_state + 2)             # A, D, delta_bias
+    params = 4 * cfg.d_inner * (cfg.d_state + int(cfg.skip) + int(cfg.bias))  # A, D, delta_bias
     state = 4 * cfg.batch * cfg.d_inner * cfg.d_state if cfg.last_state else 0
     return steps * per_step + bc + params + state
 
@@ -90,7 +90,7 @@ def ssd_bytes(cfg):
     dt = cfg.batch * cfg.seqlen * cfg.nheads * es
     bc = 2 * cfg.batch * cfg.seqlen * cfg.ngroups * cfg.d_state * es
     state = 4 * cfg.batch * cfg.nheads * cfg.headdim * cfg.d_state if cfg.last_state else 0
-    return xy + dt + bc + 8 * cfg.nheads + state
+    return xy + dt + bc + 4 * cfg.nheads * (1 + int(cfg.skip)) + state  # + A_head, D
 
 
 def ssd_flops(cfg):
