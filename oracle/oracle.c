@@ -33,6 +33,24 @@
  * consecutive channels; G = D is one B, C per channel); the SSD dt is
  * already positive.
  *
+ * What pins each function to something other than itself (CPU tests of the
+ * oracle; no function here is left unpinned):
+ *  - the selective scan: answers worked out by hand; the LTI special case
+ *    against a directly evaluated causal convolution; the zero-step limit;
+ *    brute-force unrolled products on short sequences; split invariance with
+ *    the state carried; linearity and the zero cases.
+ *  - its grouped form: brute-force sums per channel with the group's B and C,
+ *    and equality with the shared form when all groups hold the same B, C.
+ *  - the SSD scan: a hand-worked two-head case; equality with the selective
+ *    scan given a scalar A per head; the dense quadratic (dual) form.
+ *  - the causal convolution with SiLU: identity, delay and bias-only kernels
+ *    and numpy's convolution.
+ *  - the backward: central finite differences of the forward along random
+ *    directions for every input.
+ * A set of deliberately broken copies of this file (a dropped term, a wrong
+ * sign, index or operand) is compiled by the tests, and each must fail one
+ * of these pins.
+ *
  * Parallelism: the optional OpenMP loop runs over independent (batch,
  * channel) or (batch, head) units only; every unit is computed by the same
  * sequential loop, so the result does not depend on the thread count.
