@@ -63,3 +63,22 @@ def test_library_arm_line(cuda_device):
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert k in c, k
     assert set(d["step_ms"]) >= {"median", "min", "max"}
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the multi-GPU runs are (one process per rank), rank 0
+    alone times the oracle and prints the line; the other rank exits 0."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "1"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
