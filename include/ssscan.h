@@ -17,7 +17,8 @@
  *   ss_selective_scan_fwd_host   the selective scan from host buffers
  *   ss_selective_scan_fwd_noalloc the selective scan with no allocation
  *   ss_status_string, ss_get_device_error, ss_launch_count, ss_version,
- *   ss_selftest_timeout          status, errors and diagnostics
+ *   ss_selftest_timeout,         status, errors and diagnostics
+ *   ss_debug_set_path
  *
  * Every buffer is caller-owned device memory described by an ss_tensor
  * (pointer, dtype, shape, strides in elements).  The library keeps no pointer
@@ -359,12 +360,50 @@ int ss_get_device_error(void* stream);
  * whose wait ran out.  The next ss_get_device_error on that stream returns
  * SS_ERR_TIMEOUT and clears it; the CUDA context stays usable.  Nothing
  * faults, traps or hangs.
- *
- * Host-side fault injection for tests: with the environment variable
- * SS_FAULT_ALLOC=1 every stream-ordered scratch allocation of the library
- * fails, so calls that need scratch return SS_ERR_ALLOC before launching.
  */
 int ss_selftest_timeout(unsigned limit_us, void* stream);
+
+/*
+ * Diagnostic switches (no counterpart on the pages): which kernel a call
+ * takes, for tests that must reach one kernel on purpose and for
+ * measurements.  The library reads no environment variable; these switches
+ * change only when this function is called.  The setting is process-wide (all
+ * devices, all threads), read at the start of each call: change it only
+ * while no call of this library is in flight on another host thread.
+ * `value` -1 restores the library's own choice (the default of every switch).
+ *
+ *   SS_DEBUG_SCAN_PATH      selective scan: 0 the general kernel (any layout),
+ *                           1 scan_fast (lanes per channel from
+ *                           SS_DEBUG_SCAN_SPLIT), 2 scan_seq
+ *   SS_DEBUG_SCAN_SPLIT     scan_fast lanes per channel: 1, 2, 4 or 8
+ *   SS_DEBUG_SCAN_SHAPE     scan_seq launch shape 1 .. 4 (lanes per channel
+ *                           1, 1, 2, 4 over 128, 64, 64, 32 channels)
+ *   SS_DEBUG_SCAN_SEGMENTS  scan_seq time segments (1 .. 128)
+ *   SS_DEBUG_SSD_PATH       SSD scan: 0 the CUDA-core kernel, 1 the tensor-core
+ *                           kernels only, 2 the one-head tensor-core kernel
+ *                           only; with 1 or 2 a shape or layout those kernels
+ *                           do not take returns SS_ERR_UNSUPPORTED instead of
+ *                           falling back
+ *   SS_DEBUG_BWD_PATH       backward: 0 the general kernel
+ *   SS_DEBUG_GROUPED_PATH   B, C per small channel group: 0 the row kernel
+ *                           (scan_pc) instead of the TMA kernel
+ *   SS_DEBUG_FAULT_ALLOC    1: every stream-ordered scratch allocation fails,
+ *                           so calls that need scratch return SS_ERR_ALLOC
+ *                           before launching anything (host-side fault
+ *                           injection)
+ *
+ * Returns SS_OK, or SS_ERR_INVALID_ARG for an unknown switch.
+ */
+#define SS_DEBUG_SCAN_PATH 0
+#define SS_DEBUG_SCAN_SPLIT 1
+#define SS_DEBUG_SCAN_SHAPE 2
+#define SS_DEBUG_SCAN_SEGMENTS 3
+#define SS_DEBUG_SSD_PATH 4
+#define SS_DEBUG_BWD_PATH 5
+#define SS_DEBUG_GROUPED_PATH 6
+#define SS_DEBUG_FAULT_ALLOC 7
+#define SS_DEBUG_COUNT 8
+int ss_debug_set_path(int which, int value);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ss_launch_count(void);

@@ -8,6 +8,7 @@ call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -25,7 +26,10 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version", "ss_selftest_timeout", "ss_selective_scan_fwd_ckpt",
-           "ss_selective_scan_bwd_ckpt")
+           "ss_selective_scan_bwd_ckpt", "ss_debug_set_path")
+# Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
+DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
+             grouped_path=6, fault_alloc=7)
 
 
 class SSTensor(ctypes.Structure):
@@ -89,6 +93,8 @@ def load(path: str | None = None):
     lib.ss_launch_count.argtypes = []
     lib.ss_launch_count.restype = ctypes.c_uint64
     lib.ss_version.restype = i
+    lib.ss_debug_set_path.argtypes = [i, i]
+    lib.ss_debug_set_path.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -354,3 +360,25 @@ def selftest_timeout(limit_us=2000, stream=None) -> None:
 
 def launch_count() -> int:
     return int(load().ss_launch_count())
+
+
+def set_debug_path(name: str, value: int | None) -> None:
+    """ss_debug_set_path: force one kernel choice (value None or -1 restores
+    the library's own choice).  Names are the keys of DEBUG."""
+    rc = load().ss_debug_set_path(DEBUG[name], -1 if value is None else int(value))
+    if rc != 0:
+        raise SSError(rc, "ss_debug_set_path")
+
+
+@contextlib.contextmanager
+def debug_paths(**switches):
+    """Set diagnostic switches for the duration of a with-block, e.g.
+    ``with debug_paths(scan_path=1, scan_split=4): ...``; every switch given
+    is restored to the library's own choice afterwards."""
+    for k, v in switches.items():
+        set_debug_path(k, v)
+    try:
+        yield
+    finally:
+        for k in switches:
+            set_debug_path(k, None)

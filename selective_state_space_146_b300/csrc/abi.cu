@@ -72,12 +72,16 @@ void* tensor_map_encoder() {
     return fn;
 }
 
-// SS_FAULT_ALLOC=1 makes every stream-ordered scratch allocation report
-// failure (a host-side fault injection for the tests of SS_ERR_ALLOC).
-static bool fault_alloc() {
-    const char* f = getenv("SS_FAULT_ALLOC");
-    return f && f[0] == '1';
+// Diagnostic switches (ss_debug_set_path): -1 is the library's own choice.
+static std::atomic<int> g_debug[SS_DEBUG_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1};
+
+int debug_path(int which) {
+    return which >= 0 && which < SS_DEBUG_COUNT ? g_debug[which].load(std::memory_order_relaxed) : -1;
 }
+
+// SS_DEBUG_FAULT_ALLOC = 1 makes every stream-ordered scratch allocation
+// report failure (a host-side fault injection for the tests of SS_ERR_ALLOC).
+static bool fault_alloc() { return debug_path(SS_DEBUG_FAULT_ALLOC) == 1; }
 
 static void* scratch_alloc_async(size_t bytes, cudaStream_t st, void*) {
     if (fault_alloc()) return nullptr;
@@ -168,71 +172,6 @@ static void* fixed_scratch_alloc(size_t bytes, cudaStream_t, void* ctx) {
 }
 
 static void fixed_scratch_release(void*, cudaStream_t, void*) {}
-
-// Argument checks and ScanArgs assembly of the allocation-free entry point
-// (the same checks, in the same order, as ss_selective_scan_fwd).  Sets
-// *nothing_to_do for inputs with no work.
-static int noalloc_selective_args(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
-                                  const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
-                                  const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
-                                  ss_tensor* y, ss_tensor* last_state, ScanArgs* out,
-                                  bool* nothing_to_do) {
-    *nothing_to_do = false;
-    SS_TRY(check_tensor(u, 3));
-    SS_TRY(check_tensor(delta, 3));
-    SS_TRY(check_tensor(A, 2));
-    SS_TRY(check_tensor(B, 3));
-    SS_TRY(check_tensor(C, 3));
-    SS_TRY(check_tensor(y, 3));
-    if (D) SS_TRY(check_tensor(D, 1));
-    if (z) SS_TRY(check_tensor(z, 3));
-    if (delta_bias) SS_TRY(check_tensor(delta_bias, 1));
-    if (last_state) SS_TRY(check_tensor(last_state, 3));
-    if (softplus != 0 && softplus != 1) return SS_ERR_INVALID_ARG;
-    const int dt = u->dtype;
-    if (delta->dtype != dt || B->dtype != dt || C->dtype != dt || y->dtype != dt ||
-        (z && z->dtype != dt))
-        return SS_ERR_DTYPE;
-    if (A->dtype != SS_F32 || (D && D->dtype != SS_F32) ||
-        (delta_bias && delta_bias->dtype != SS_F32) || (last_state && last_state->dtype != SS_F32))
-        return SS_ERR_DTYPE;
-    const int64_t Bsz = u->shape[0], Dch = u->shape[1], L = u->shape[2], N = A->shape[1];
-    if (!same_shape(delta, u) || !same_shape(y, u) || (z && !same_shape(z, u)))
-        return SS_ERR_SHAPE;
-    if (A->shape[0] != Dch) return SS_ERR_SHAPE;
-    if (B->shape[0] != Bsz || B->shape[1] != N || B->shape[2] != L) return SS_ERR_SHAPE;
-    if (!same_shape(C, B)) return SS_ERR_SHAPE;
-    if (D && D->shape[0] != Dch) return SS_ERR_SHAPE;
-    if (delta_bias && delta_bias->shape[0] != Dch) return SS_ERR_SHAPE;
-    if (last_state && (last_state->shape[0] != Bsz || last_state->shape[1] != Dch ||
-                       last_state->shape[2] != N))
-        return SS_ERR_SHAPE;
-    if (N < 1) return SS_ERR_SHAPE;
-    if (N > 256) return SS_ERR_UNSUPPORTED;
-    if (Bsz * Dch >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
-    if (Bsz == 0 || Dch == 0 || (L == 0 && !last_state)) {
-        *nothing_to_do = true;
-        return SS_OK;
-    }
-    ScanArgs a{};
-    a.Bsz = (int)Bsz; a.D = (int)Dch; a.N = (int)N; a.L = (int)L; a.dtype = dt;
-    a.u = u->data; a.su_b = u->stride[0]; a.su_d = u->stride[1]; a.su_t = u->stride[2];
-    a.dl = delta->data; a.sdl_b = delta->stride[0]; a.sdl_d = delta->stride[1]; a.sdl_t = delta->stride[2];
-    if (z) { a.z = z->data; a.sz_b = z->stride[0]; a.sz_d = z->stride[1]; a.sz_t = z->stride[2]; }
-    a.y = y->data; a.sy_b = y->stride[0]; a.sy_d = y->stride[1]; a.sy_t = y->stride[2];
-    a.Bm = B->data; a.sB_b = B->stride[0]; a.sB_n = B->stride[1]; a.sB_t = B->stride[2];
-    a.Cm = C->data; a.sC_b = C->stride[0]; a.sC_n = C->stride[1]; a.sC_t = C->stride[2];
-    a.A = static_cast<const float*>(A->data); a.sA_d = A->stride[0]; a.sA_n = A->stride[1];
-    if (D) { a.Dv = static_cast<const float*>(D->data); a.sD = D->stride[0]; }
-    if (delta_bias) { a.bias = static_cast<const float*>(delta_bias->data); a.sbias = delta_bias->stride[0]; }
-    if (last_state) {
-        a.last = static_cast<float*>(last_state->data);
-        a.sl_b = last_state->stride[0]; a.sl_d = last_state->stride[1]; a.sl_n = last_state->stride[2];
-    }
-    a.softplus = softplus;
-    *out = a;
-    return SS_OK;
-}
 
 }  // namespace ss
 
@@ -371,6 +310,12 @@ int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
     return launch_selective(a, static_cast<cudaStream_t>(stream), sc);
 }
 
+int ss_debug_set_path(int which, int value) {
+    if (which < 0 || which >= SS_DEBUG_COUNT) return SS_ERR_INVALID_ARG;
+    g_debug[which].store(value < 0 ? -1 : value, std::memory_order_relaxed);
+    return SS_OK;
+}
+
 int ss_selective_scan_fwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                           const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
@@ -420,8 +365,8 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
                                   ss_tensor* y, ss_tensor* last_state, void* stream) {
     ScanArgs a{};
     bool nothing = false;
-    SS_TRY(noalloc_selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
-                                  &a, &nothing));
+    SS_TRY(selective_args(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, y, last_state,
+                          &a, &nothing));
     if (nothing) return SS_OK;
     a.err = device_error_ptr();
     if (!a.err) return SS_ERR_CUDA;

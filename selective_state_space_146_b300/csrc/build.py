@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libssscan.so")
-SOURCES = ["abi.cu", "selective_scan.cu", "selective_scan_grouped.cu", "selective_scan_wide.cu",
+SOURCES = ["abi.cu", "selective_scan.cu", "selective_scan_seq.cu", "selective_scan_grouped.cu", "selective_scan_wide.cu",
            "selective_scan_bwd.cu", "ssd.cu", "ssd_tc.cu", "selftest.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "ssscan.h"
+
 namespace ss {
 
 // Host view of one selective-scan call, element strides.
@@ -115,6 +117,13 @@ struct Scratch {
 };
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
+// scan_seq (N = 16, fast layouts, no conv, no checkpoints); *taken is false
+// when the call does not fit it.
+int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken);
+// Unit t-stride, 16-byte aligned rows and strides, N = 16: the TMA kernels' layout.
+bool fast_layout_ok(const ScanArgs& a);
+// A diagnostic switch set by ss_debug_set_path (SS_DEBUG_*), -1 when unset.
+int debug_path(int which);
 int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch);
 // B, C per small channel group (scan_pc / scan_pc_tma); *taken is false when
 // the layout suits neither and the caller should run the general kernel.

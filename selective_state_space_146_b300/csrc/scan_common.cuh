@@ -70,6 +70,77 @@ __device__ __forceinline__ void reduce_half(const float* v, float* out, bool upp
     }
 }
 
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 7)) << 4); }
+
+// Conversion of one tile's raw B / C ([n][t] as loaded by TMA) into the fp32
+// table bc[t][32]: 16-byte chunk j holds (B[2j], B[2j+1], C[2j], C[2j+1]), so
+// a lane keeping the state pairs [j0, j0 + m) reads m consecutive chunks, one
+// ld.shared.v4 per pair, at offsets known at compile time.  Lane l writes rows
+// 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by lane so the
+// lanes of one store hit distinct banks.  Without C (summary pass) the C slots
+// hold zeros.
+template <typename T, bool WITH_C>
+__device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int j = (it + lane) & 7;
+        const uint32_t rb = rawB + (2 * j) * 128, rc = rawC + (2 * j) * 128;
+        if constexpr (sizeof(T) == 2) {
+            // word `lane` of a 128-byte row holds the bf16 pair (t = 2 lane, 2 lane + 1)
+            const uint32_t b0 = lds32(rb + lane * 4), b1 = lds32(rb + 128 + lane * 4);
+            const uint32_t c0 = WITH_C ? lds32(rc + lane * 4) : 0u;
+            const uint32_t c1 = WITH_C ? lds32(rc + 128 + lane * 4) : 0u;
+            const float4 lo = make_float4(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16),
+                                          __uint_as_float(c0 << 16), __uint_as_float(c1 << 16));
+            const float4 hi = make_float4(__uint_as_float(b0 & 0xffff0000u),
+                                          __uint_as_float(b1 & 0xffff0000u),
+                                          __uint_as_float(c0 & 0xffff0000u),
+                                          __uint_as_float(c1 & 0xffff0000u));
+            sts128f(bc + (2 * lane) * 128 + j * 16, lo);
+            sts128f(bc + (2 * lane + 1) * 128 + j * 16, hi);
+        } else {
+            float4 v;
+            v.x = __uint_as_float(lds32(rb + lane * 4));
+            v.y = __uint_as_float(lds32(rb + 128 + lane * 4));
+            v.z = WITH_C ? __uint_as_float(lds32(rc + lane * 4)) : 0.f;
+            v.w = WITH_C ? __uint_as_float(lds32(rc + 128 + lane * 4)) : 0.f;
+            sts128f(bc + lane * 128 + j * 16, v);
+        }
+    }
+}
+
+// Store K floats as T to global memory: one aligned vector store, or (in the
+// last chunk of the sequence) element by element up to `limit` elements.
+template <typename T, int K>
+__device__ __forceinline__ void stg_elems(T* p, const float* v, int limit) {
+    constexpr int BYTES = K * (int)sizeof(T);
+    if constexpr (BYTES == 2) {
+        if (limit >= 1) p[0] = Elem<T>::from_f(v[0]);
+        return;
+    }
+    if (limit >= K) {
+        uint32_t w[4];
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < K / 2; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < K; ++i) w[i] = __float_as_uint(v[i]);
+        }
+        if constexpr (BYTES == 16) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        else if constexpr (BYTES == 8) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        else *reinterpret_cast<uint32_t*>(p) = w[0];
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            if (i < limit) p[i] = Elem<T>::from_f(v[i]);
+    }
+}
+
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                               CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,

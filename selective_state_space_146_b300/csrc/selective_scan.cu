@@ -180,46 +180,6 @@ struct FastCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 7)) << 4); }
-
-// Conversion of one tile's raw B / C ([n][t] as loaded by TMA) into the fp32
-// table bc[t][32]: 16-byte chunk j holds (B[2j], B[2j+1], C[2j], C[2j+1]), so
-// a lane keeping the state pairs [j0, j0 + m) reads m consecutive chunks, one
-// ld.shared.v4 per pair, at offsets known at compile time.  Lane l writes rows
-// 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by lane so the
-// lanes of one store hit distinct banks.  Without C (summary pass) the C slots
-// hold zeros.
-template <typename T, bool WITH_C>
-__device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int j = (it + lane) & 7;
-        const uint32_t rb = rawB + (2 * j) * 128, rc = rawC + (2 * j) * 128;
-        if constexpr (sizeof(T) == 2) {
-            // word `lane` of a 128-byte row holds the bf16 pair (t = 2 lane, 2 lane + 1)
-            const uint32_t b0 = lds32(rb + lane * 4), b1 = lds32(rb + 128 + lane * 4);
-            const uint32_t c0 = WITH_C ? lds32(rc + lane * 4) : 0u;
-            const uint32_t c1 = WITH_C ? lds32(rc + 128 + lane * 4) : 0u;
-            const float4 lo = make_float4(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16),
-                                          __uint_as_float(c0 << 16), __uint_as_float(c1 << 16));
-            const float4 hi = make_float4(__uint_as_float(b0 & 0xffff0000u),
-                                          __uint_as_float(b1 & 0xffff0000u),
-                                          __uint_as_float(c0 & 0xffff0000u),
-                                          __uint_as_float(c1 & 0xffff0000u));
-            sts128f(bc + (2 * lane) * 128 + j * 16, lo);
-            sts128f(bc + (2 * lane + 1) * 128 + j * 16, hi);
-        } else {
-            float4 v;
-            v.x = __uint_as_float(lds32(rb + lane * 4));
-            v.y = __uint_as_float(lds32(rb + 128 + lane * 4));
-            v.z = WITH_C ? __uint_as_float(lds32(rc + lane * 4)) : 0.f;
-            v.w = WITH_C ? __uint_as_float(lds32(rc + 128 + lane * 4)) : 0.f;
-            sts128f(bc + lane * 128 + j * 16, v);
-        }
-    }
-}
-
 // Store K floats as T (K * sizeof(T) in {4, 8, 16} bytes) to shared memory.
 template <typename T, int K>
 __device__ __forceinline__ void sts_elems(uint32_t a, const float* v) {
@@ -242,37 +202,6 @@ __device__ __forceinline__ void sts_elems(uint32_t a, const float* v) {
         asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(w[0]), "r"(w[1]) : "memory");
     else
         asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(w[0]) : "memory");
-}
-
-// Store K floats as T to global memory: one aligned vector store, or (in the
-// last chunk of the sequence) element by element up to `limit` elements.
-template <typename T, int K>
-__device__ __forceinline__ void stg_elems(T* p, const float* v, int limit) {
-    constexpr int BYTES = K * (int)sizeof(T);
-    if constexpr (BYTES == 2) {
-        if (limit >= 1) p[0] = Elem<T>::from_f(v[0]);
-        return;
-    }
-    if (limit >= K) {
-        uint32_t w[4];
-        if constexpr (sizeof(T) == 2) {
-#pragma unroll
-            for (int i = 0; i < K / 2; ++i) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                w[i] = *reinterpret_cast<uint32_t*>(&h);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < K; ++i) w[i] = __float_as_uint(v[i]);
-        }
-        if constexpr (BYTES == 16) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-        else if constexpr (BYTES == 8) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
-        else *reinterpret_cast<uint32_t*>(p) = w[0];
-    } else {
-#pragma unroll
-        for (int i = 0; i < K; ++i)
-            if (i < limit) p[i] = Elem<T>::from_f(v[i]);
-    }
 }
 
 template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMMARY, bool CONV,
@@ -660,7 +589,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t
     return r == CUDA_SUCCESS;
 }
 
-static bool fast_layout_ok(const ScanArgs& a) {
+bool fast_layout_ok(const ScanArgs& a) {
     if (a.N != 16) return false;
     const int es = a.dtype == SS_BF16 ? 2 : 4;
     auto row_ok = [&](const void* ptr, int64_t sb, int64_t sd, int64_t st) {
@@ -818,23 +747,21 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
-// Path selection for tests: SS_SCAN_PATH=general forces the general kernel;
-// split1 / split2 / split4 / split8 force the fast kernel with 1, 2, 4 or 8
-// lanes per channel (8 only for bf16; fp32 chunks hold 4 steps).
-static int forced_path() {
-    const char* s = getenv("SS_SCAN_PATH");
-    if (!s) return -1;
-    if (!strcmp(s, "general")) return 0;
-    if (!strcmp(s, "split1")) return 1;
-    if (!strcmp(s, "split2")) return 2;
-    if (!strcmp(s, "split4")) return 4;
-    if (!strcmp(s, "split8")) return 8;
-    return -1;
-}
-
+// Path selection (ss_debug_set_path): SS_DEBUG_SCAN_PATH 0 forces the general
+// kernel, 1 the fast kernel with SS_DEBUG_SCAN_SPLIT lanes per channel (1, 2,
+// 4 or 8; 8 only for bf16, fp32 chunks hold 4 steps), 2 scan_seq.
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
-    const int force = forced_path();
+    const int path = debug_path(SS_DEBUG_SCAN_PATH);
+    const int split_req = debug_path(SS_DEBUG_SCAN_SPLIT);
+    const int force = path == 0 ? 0 : (path == 1 ? split_req : -1);
     const bool bf = a.dtype == SS_BF16;
+    // scan_seq takes every d_state-16 call in the TMA layout except the fused
+    // conv and the checkpointing forward (scan_fast keeps those)
+    if ((path == 2 || path < 0) && !a.ckpt && !a.cw && a.L > 0) {
+        bool taken = false;
+        const int rc = launch_selective_seq(a, st, scratch, &taken);
+        if (taken) return rc;
+    }
     if (a.ckpt && a.L > 0) {  // (with L = 0 there are no checkpoints to write)
         // checkpoints for the backward come from the fast kernel with four
         // lanes per channel (the backward's layout of states across lanes)

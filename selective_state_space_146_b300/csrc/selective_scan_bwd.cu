@@ -783,7 +783,7 @@ static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratc
 int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& scratch) {
     BwdArgs a = args;
     const bool empty = a.L == 0 || a.Bsz == 0 || a.D == 0;
-    const char* force = getenv("SS_BWD_PATH");
+    const bool force_general = debug_path(SS_DEBUG_BWD_PATH) == 0;
     if (a.ckpt_in && !empty) {
         // the forward's states come in the fast kernel's layout only
         if (a.N != 16 || !bwd_fast_ok(a)) return SS_ERR_UNSUPPORTED;
@@ -791,7 +791,7 @@ int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& sc
                                           : run_bwd_fast<float>(a, st, scratch);
         return rc == -1 ? SS_ERR_UNSUPPORTED : rc;
     }
-    if (!empty && !(force && !strcmp(force, "general")) && bwd_fast_ok(a)) {
+    if (!empty && !force_general && bwd_fast_ok(a)) {
         const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
                                           : run_bwd_fast<float>(a, st, scratch);
         if (rc != -1) return rc;  // -1: no tensor map for this layout, take the general kernel

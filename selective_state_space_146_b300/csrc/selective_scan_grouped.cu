@@ -365,14 +365,14 @@ static int run_pc(const ScanArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
-// Groups of 1, 2, 4 or 8 channels: the TMA kernel (SS_PC_PATH=rows keeps the
+// Groups of 1, 2, 4 or 8 channels: the TMA kernel (SS_DEBUG_GROUPED_PATH 0 keeps the
 // row-load kernel, for tests); other small groups: the row-load kernel.  *taken says
 // whether a kernel was launched.
 int launch_selective_grouped(const ScanArgs& a, cudaStream_t st, bool* taken) {
     *taken = false;
     const bool bf = a.dtype == SS_BF16;
-    const char* rows = getenv("SS_PC_PATH");
-    if (pc_tma_ok(a) && !(rows && !strcmp(rows, "rows"))) {
+    const bool rows = debug_path(SS_DEBUG_GROUPED_PATH) == 0;
+    if (pc_tma_ok(a) && !rows) {
         const int rc = bf ? run_pc_tma<__nv_bfloat16>(a, st) : run_pc_tma<float>(a, st);
         if (rc != -1) {  // -1: no tensor map for this layout
             *taken = true;

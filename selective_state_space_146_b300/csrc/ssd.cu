@@ -79,12 +79,14 @@ static int run_ssd_general(const SSDArgs& a, cudaStream_t st) {
 int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken);
 
 int launch_ssd(const SSDArgs& a, cudaStream_t st, const Scratch& scratch) {
-    const char* force = getenv("SS_SSD_PATH");
-    const bool general_only = force && !strcmp(force, "general");
-    if (!general_only) {
+    // SS_DEBUG_SSD_PATH: 0 the CUDA-core kernel only; 1 / 2 the tensor-core
+    // kernels only (no fallback: SS_ERR_UNSUPPORTED where they do not apply)
+    const int path = debug_path(SS_DEBUG_SSD_PATH);
+    if (path != 0) {
         bool taken = false;
         int rc = launch_ssd_tc(a, st, scratch, &taken);
         if (taken) return rc;
+        if (path == 1 || path == 2) return SS_ERR_UNSUPPORTED;
     }
     return a.dtype == SS_BF16 ? run_ssd_general<__nv_bfloat16>(a, st) : run_ssd_general<float>(a, st);
 }

@@ -894,13 +894,12 @@ static bool tc_layout_ok(const SSDArgs& a) {
     return true;
 }
 
-// Path selection for tests: SS_SSD_PATH=general forces the CUDA-core kernel.
+// Path selection for tests: SS_DEBUG_SSD_PATH 0 forces the CUDA-core kernel.
 int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     (void)scratch;
     *taken = false;
-    const char* force = getenv("SS_SSD_PATH");
-    if (force && !strcmp(force, "general")) return SS_OK;
-    if (!tc_layout_ok(a) || a.L < 1) return SS_OK;
+    const int path = debug_path(SS_DEBUG_SSD_PATH);
+    if (path == 0 || !tc_layout_ok(a) || a.L < 1) return SS_OK;
     *taken = true;
 
     CUtensorMap mx, mb, mc, mdt;
@@ -940,8 +939,8 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
     p.err = a.err;
 
     // two heads per CTA when every group holds an even number of heads
-    // (SS_SSD_PATH=tc1 keeps one head per CTA, for tests)
-    const bool pair = (a.H / a.G) % 2 == 0 && !(force && !strcmp(force, "tc1"));
+    // (SS_DEBUG_SSD_PATH 2 keeps one head per CTA, for tests)
+    const bool pair = (a.H / a.G) % 2 == 0 && path != 2;
     static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

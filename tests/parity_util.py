@@ -86,3 +86,29 @@ def oracle_ssd_units(inp, units, nthreads=8):
         ys.append(y[0, :, 0])
         ss.append(s[0, 0])
     return np.stack(ys), np.stack(ss)
+
+
+def scan_switches(name):
+    """Diagnostic switches (ss_debug_set_path) that force one selective-scan
+    kernel: None (the library's choice), "general", "splitK" (scan_fast with K
+    lanes per channel), "seqK" or "seqKsN" (scan_seq launch shape K, N time
+    segments)."""
+    if name is None:
+        return {}
+    if name == "general":
+        return dict(scan_path=0)
+    if name.startswith("split"):
+        return dict(scan_path=1, scan_split=int(name[5:]))
+    if name.startswith("seq"):
+        shape, _, segs = name[3:].partition("s")
+        sw = dict(scan_path=2, scan_shape=int(shape))
+        if segs:
+            sw["scan_segments"] = int(segs)
+        return sw
+    raise ValueError(name)
+
+
+# SSD kernels: None (the library's choice), the CUDA-core kernel, the
+# tensor-core kernels with no fallback, the one-head tensor-core kernel.
+SSD_SWITCHES = {None: {}, "general": dict(ssd_path=0), "tc": dict(ssd_path=1),
+                "tc1": dict(ssd_path=2)}

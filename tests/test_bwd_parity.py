@@ -42,15 +42,12 @@ def _compare(out, ref, dt, tag):
 
 
 @pytest.fixture
-def bwd_path(request, monkeypatch):
+def bwd_path(request):
     """None: the library's choice (the TMA kernel where the layout allows);
     "general": the any-stride kernel."""
     val = getattr(request, "param", None)
-    if val:
-        monkeypatch.setenv("SS_BWD_PATH", val)
-    else:
-        monkeypatch.delenv("SS_BWD_PATH", raising=False)
-    return val
+    with _abi.debug_paths(**(dict(bwd_path=0) if val == "general" else {})):
+        yield val
 
 
 CASES = [

@@ -1,6 +1,5 @@
 """The fused causal conv1d + SiLU + selective scan against the fp64 oracle
 (GPU, C ABI).  The oracle composes its conv and scan functions."""
-import os
 
 import numpy as np
 import pytest
@@ -8,7 +7,7 @@ import torch
 
 import oracle
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, cuda_inputs, to_np
+from tests.parity_util import check_close, cuda_inputs, scan_switches, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -34,11 +33,12 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
 @pytest.mark.parametrize("path", [None, "general", "split1", "split2"])
-def test_conv_scan_small(cuda_device, case, path, monkeypatch):
-    if path:
-        monkeypatch.setenv("SS_SCAN_PATH", path)
-    else:
-        monkeypatch.delenv("SS_SCAN_PATH", raising=False)
+def test_conv_scan_small(cuda_device, case, path):
+    with _abi.debug_paths(**scan_switches(path)):
+        _conv_scan_small(cuda_device, case)
+
+
+def _conv_scan_small(cuda_device, case):
     Bsz, D, N, L, dt, W, bias = case
     inp = inputs.selective_inputs(Bsz, D, N, L, dt, seed=L + W)
     w, cb = _conv_params(D, W, L, bias)
@@ -82,10 +82,9 @@ def test_conv_scan_full_size_sampled(cuda_device):
     check_close(to_np(s.reshape(total, -1)[idx]), np.stack(ss), torch.bfloat16, "conv-scan state")
 
 
-def test_conv_scan_layer_shape_sampled(cuda_device, monkeypatch):
+def test_conv_scan_layer_shape_sampled(cuda_device):
     """The fused call the benchmark times (8 x 1536 x 2048 bf16, width 4),
     sampled channels against the oracle run on those channels alone."""
-    monkeypatch.delenv("SS_SCAN_PATH", raising=False)
     cfg = inputs.WORKLOADS["mamba130m_layer"]
     inp = inputs.workload_selective_inputs(cfg, seed=0)
     w, b = _conv_params(cfg.d_inner, 4, seed=7)

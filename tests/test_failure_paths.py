@@ -4,9 +4,10 @@
   mbarrier nothing arrives on, gives up after its limit and records the device
   error bit; the host reads SS_ERR_TIMEOUT, the word is cleared, and the next
   scan runs normally.
-* Allocation failure injected on the host (SS_FAULT_ALLOC=1): calls that need
-  stream-ordered scratch return SS_ERR_ALLOC without launching, calls that do
-  not need it still run, and everything works again once the hook is off.
+* Allocation failure injected on the host (ss_debug_set_path with
+  SS_DEBUG_FAULT_ALLOC): calls that need stream-ordered scratch return
+  SS_ERR_ALLOC without launching, calls that do not need it still run, and
+  everything works again once the switch is off.
 """
 import time
 
@@ -50,7 +51,7 @@ def test_selftest_rejects_bad_limits(cuda_device):
             _abi.selftest_timeout(limit_us=bad)
 
 
-def test_injected_allocation_failure(cuda_device, monkeypatch):
+def test_injected_allocation_failure(cuda_device):
     # few channels and a long sequence: the forward splits time into segments
     # and needs scratch for their summaries; the backward always needs scratch
     inp = inputs.selective_inputs(1, 32, 16, 8192, "bf16", seed=4)
@@ -59,23 +60,23 @@ def test_injected_allocation_failure(cuda_device, monkeypatch):
     ref = _scan(g)
     torch.cuda.synchronize()
     n0 = _abi.launch_count()
-    monkeypatch.setenv("SS_FAULT_ALLOC", "1")
-    with pytest.raises(_abi.SSError, match="ALLOC"):
-        _scan(g)
-    with pytest.raises(_abi.SSError, match="ALLOC"):
-        _abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
-                                g["delta_bias"], dout)
-    pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-    with pytest.raises(_abi.SSError, match="ALLOC"):
-        _abi.selective_scan_fwd_host(pinned["u"], pinned["delta"], pinned["A"], pinned["B"],
-                                     pinned["C"], pinned["D"], pinned["z"], pinned["delta_bias"])
-    assert _abi.launch_count() == n0  # nothing was launched
-    # the fixed-scratch entry point allocates nothing and still runs
-    y_fixed = torch.empty_like(g["u"])
-    _abi.selective_scan_fwd_noalloc(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
-                                    g["delta_bias"], y=y_fixed)
-    torch.cuda.synchronize()
-    monkeypatch.delenv("SS_FAULT_ALLOC")
+    with _abi.debug_paths(fault_alloc=1):
+        with pytest.raises(_abi.SSError, match="ALLOC"):
+            _scan(g)
+        with pytest.raises(_abi.SSError, match="ALLOC"):
+            _abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                    g["delta_bias"], dout)
+        pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+        with pytest.raises(_abi.SSError, match="ALLOC"):
+            _abi.selective_scan_fwd_host(pinned["u"], pinned["delta"], pinned["A"], pinned["B"],
+                                         pinned["C"], pinned["D"], pinned["z"],
+                                         pinned["delta_bias"])
+        assert _abi.launch_count() == n0  # nothing was launched
+        # the fixed-scratch entry point allocates nothing and still runs
+        y_fixed = torch.empty_like(g["u"])
+        _abi.selective_scan_fwd_noalloc(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"],
+                                        g["z"], g["delta_bias"], y=y_fixed)
+        torch.cuda.synchronize()
     y = _scan(g)
     torch.cuda.synchronize()
     assert _abi.device_error() == 0

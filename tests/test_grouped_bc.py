@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, cuda_inputs, to_np
+from tests.parity_util import check_close, cuda_inputs, scan_switches, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -22,17 +22,14 @@ def _tdt(dt):
 
 
 @pytest.fixture
-def scan_path(request, monkeypatch):
+def scan_path(request):
     """None: the library's choice; "general": the any-stride kernel; "rows":
-    per-channel B, C read row by row instead of through TMA tiles."""
+    per-channel B, C read row by row instead of through TMA tiles; "splitK" /
+    "seqK": scan_fast or scan_seq forced (groups that fit their channel tiles)."""
     val = getattr(request, "param", None)
-    monkeypatch.delenv("SS_SCAN_PATH", raising=False)
-    monkeypatch.delenv("SS_PC_PATH", raising=False)
-    if val == "rows":
-        monkeypatch.setenv("SS_PC_PATH", "rows")
-    elif val:
-        monkeypatch.setenv("SS_SCAN_PATH", val)
-    return val
+    sw = dict(grouped_path=0) if val == "rows" else scan_switches(val)
+    with _abi.debug_paths(**sw):
+        yield val
 
 
 CASES = [
@@ -54,7 +51,7 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:6])) +
                          ("" if c[6] else "-nogate"))
-@pytest.mark.parametrize("scan_path", [None, "general", "rows"], indirect=True)
+@pytest.mark.parametrize("scan_path", [None, "general", "rows", "seq3", "seq4"], indirect=True)
 def test_grouped_bc_matches_oracle(cuda_device, scan_path, case):
     Bsz, D, G, N, L, dt, on = case
     inp = inputs.selective_inputs(Bsz, D, N, L, dt, gate=on, skip=on, bias=on, groups=G,

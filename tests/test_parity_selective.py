@@ -5,32 +5,28 @@ compared element by element over the whole output; the full-size workloads
 (the same call the benchmark times) on sampled channels that the oracle
 computes one by one.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
 
 from selective_state_space_146_b300 import _abi, inputs
 from tests.parity_util import (check_close, cuda_inputs, oracle_selective,
-                               oracle_selective_channels, to_np)
+                               oracle_selective_channels, scan_switches, to_np)
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture
 def scan_path(request):
-    old = os.environ.get("SS_SCAN_PATH")
     val = getattr(request, "param", None)
-    if val:
-        os.environ["SS_SCAN_PATH"] = val
-    else:
-        os.environ.pop("SS_SCAN_PATH", None)
-    yield val
-    if old is None:
-        os.environ.pop("SS_SCAN_PATH", None)
-    else:
-        os.environ["SS_SCAN_PATH"] = old
+    with _abi.debug_paths(**scan_switches(val)):
+        yield val
+
+
+# every selective-scan kernel for N = 16: the general one, scan_fast with each
+# lane split, scan_seq with each launch shape (and forced time segments)
+PATHS = [None, "general", "split1", "split2", "split4", "split8", "seq1", "seq2", "seq3", "seq4",
+         "seq1s5", "seq3s7"]
 
 
 def _run(inp, dev, softplus=True, want_state=True):
@@ -43,8 +39,7 @@ def _run(inp, dev, softplus=True, want_state=True):
     return out
 
 
-@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4", "split8"],
-                         indirect=True)
+@pytest.mark.parametrize("scan_path", PATHS, indirect=True)
 def test_tiny_f32_workload(cuda_device, scan_path):
     cfg = inputs.WORKLOADS["tiny_f32"]
     inp = inputs.workload_selective_inputs(cfg)
@@ -74,8 +69,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])))
-@pytest.mark.parametrize("scan_path", [None, "general", "split1", "split2", "split4", "split8"],
-                         indirect=True)
+@pytest.mark.parametrize("scan_path", PATHS, indirect=True)
 def test_small_shapes(cuda_device, scan_path, case):
     Bsz, D, N, L, dt, gate, skip, bias, softplus = case
     inp = inputs.selective_inputs(Bsz, D, N, L, dt, gate=gate, skip=skip, bias=bias,
@@ -89,13 +83,12 @@ def test_small_shapes(cuda_device, scan_path, case):
     check_close(to_np(s), so, tdt if dt == "f32" else torch.bfloat16, "last_state")
 
 
-def test_paths_agree_with_each_other(cuda_device, scan_path):
+def test_paths_agree_with_each_other(cuda_device):
     inp = inputs.selective_inputs(2, 48, 16, 520, "bf16", seed=3)
     outs = []
-    for path in ("general", "split1", "split2", "split4", "split8"):
-        os.environ["SS_SCAN_PATH"] = path
-        outs.append([to_np(t) for t in _run(inp, cuda_device)])
-    os.environ.pop("SS_SCAN_PATH", None)
+    for path in PATHS[1:]:
+        with _abi.debug_paths(**scan_switches(path)):
+            outs.append([to_np(t) for t in _run(inp, cuda_device)])
     for o in outs[1:]:
         check_close(o[0], outs[0][0], torch.bfloat16, "y fast vs general")
         check_close(o[1], outs[0][1], torch.bfloat16, "state fast vs general")

@@ -1,60 +1,64 @@
-"""GPU parity of ss_ssd_chunk_scan_fwd against the fp64 oracle (C ABI, cuda:0)."""
-import os
+"""GPU parity of ss_ssd_chunk_scan_fwd against the fp64 oracle (C ABI, cuda:0).
 
+The tensor-core cases run with the SSD switch set to "tensor-core kernels
+only" (SS_DEBUG_SSD_PATH 1, or 2 for the one-head kernel): a shape or layout
+those kernels do not take fails with SS_ERR_UNSUPPORTED instead of silently
+running the CUDA-core kernel.  The tensor-core kernels read dt through a
+tensor map whose t-stride must be a multiple of 8 elements; cases with fewer
+heads pass dt as a view into a buffer padded to 8 heads.
+"""
 import numpy as np
 import pytest
 import torch
 
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, cuda_inputs, oracle_ssd, oracle_ssd_units, to_np
+from tests.parity_util import (SSD_SWITCHES, check_close, cuda_inputs, oracle_ssd,
+                               oracle_ssd_units, to_np)
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture
 def ssd_path(request):
-    old = os.environ.get("SS_SSD_PATH")
     val = getattr(request, "param", None)
-    if val:
-        os.environ["SS_SSD_PATH"] = val
-    else:
-        os.environ.pop("SS_SSD_PATH", None)
-    yield val
-    if old is None:
-        os.environ.pop("SS_SSD_PATH", None)
-    else:
-        os.environ["SS_SSD_PATH"] = old
+    with _abi.debug_paths(**SSD_SWITCHES[val]):
+        yield val
 
 
-def _run(inp, dev, chunk):
+def _padded_dt(dt, dev):
+    """dt (Bsz, L, H) as a view whose t-stride is H rounded up to 8."""
+    Bsz, L, H = dt.shape
+    Hp = (H + 7) // 8 * 8
+    buf = torch.zeros(Bsz, L, Hp, dtype=dt.dtype, device=dev)
+    buf[:, :, :H] = dt.to(dev)
+    return buf[:, :, :H]
+
+
+def _run(inp, dev, chunk, pad_dt=False):
     g = cuda_inputs(inp, dev)
-    y, s = _abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
+    dt = _padded_dt(inp["dt"], dev) if pad_dt else g["dt"]
+    y, s = _abi.ssd_chunk_scan_fwd(g["x"], dt, g["A_head"], g["B"], g["C"], g["D"],
                                    chunk=chunk, return_last_state=True)
     torch.cuda.synchronize()
     assert _abi.device_error() == 0
     return y, s
 
 
+# Shapes the tensor-core kernels do not take (fp32, other P or N): the
+# CUDA-core kernel, by the library's choice and forced.
 CASES = [
     # Bsz, L, H, P, N, G, dtype, chunk, skip
     (1, 64, 2, 4, 8, 1, "f32", 64, True),
     (2, 300, 4, 16, 32, 2, "f32", 128, True),
-    (2, 256, 4, 64, 128, 1, "bf16", 64, True),
-    (1, 1000, 8, 64, 128, 1, "bf16", 256, False),   # ragged last chunk
-    (2, 512, 4, 64, 128, 2, "bf16", 128, True),
     (1, 1, 2, 8, 16, 1, "f32", 64, True),            # L = 1
     (1, 130, 3, 5, 7, 3, "f32", 64, True),           # odd sizes
     (1, 384, 2, 64, 256, 1, "bf16", 64, True),       # N = 256
-    (1, 384, 3, 64, 128, 1, "bf16", 128, True),      # odd heads per group: one head per CTA
-    (2, 200, 8, 64, 128, 4, "bf16", 128, True),      # two heads per group, ragged tail
-    (1, 100, 2, 64, 128, 1, "bf16", 128, True),      # a single, partial 128-step block
-    (3, 128, 2, 64, 128, 1, "bf16", 64, False),      # exactly one block
-    (1, 129, 4, 64, 128, 2, "bf16", 128, True),      # a second block of one step
+    (2, 256, 4, 64, 128, 1, "bf16", 64, True),       # dt t-stride 4: not the tensor-core layout
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:8])))
-@pytest.mark.parametrize("ssd_path", [None, "general", "tc1"], indirect=True)
+@pytest.mark.parametrize("ssd_path", [None, "general"], indirect=True)
 def test_small_shapes(cuda_device, ssd_path, case):
     Bsz, L, H, P, N, G, dt, chunk, skip = case
     inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, skip=skip, seed=L + H)
@@ -65,16 +69,62 @@ def test_small_shapes(cuda_device, ssd_path, case):
     check_close(to_np(s), so, tdt, "last_state")
 
 
-def test_chunk_size_does_not_change_result(cuda_device):
-    inp = inputs.ssd_inputs(1, 768, 4, 64, 128, 1, "bf16", seed=9)
+# bf16, headdim 64, d_state 128: the tensor-core kernels.  The 128-step blocks
+# of those kernels meet: a single partial block, exactly one block, a second
+# block of one step, ragged tails, one step; heads per group odd (the one-head
+# kernel) and even (the two-head kernel).
+TC_CASES = [
+    # Bsz, L, H, G, chunk, skip
+    (2, 256, 8, 1, 64, True),
+    (1, 1000, 8, 1, 256, False),    # ragged last block
+    (2, 512, 8, 2, 128, True),
+    (1, 384, 3, 1, 128, True),      # odd heads per group: one head per CTA
+    (1, 384, 8, 8, 128, True),      # one head per group: one head per CTA
+    (2, 200, 8, 4, 128, True),      # two heads per group, ragged tail
+    (1, 100, 2, 1, 128, True),      # a single, partial 128-step block
+    (3, 128, 2, 1, 64, False),      # exactly one block
+    (1, 129, 4, 2, 128, True),      # a second block of one step
+    (1, 1, 8, 1, 64, True),         # L = 1
+    (1, 127, 8, 2, 256, True),      # one step short of a block
+    (2, 257, 2, 2, 64, False),      # two blocks and one step, one head per group
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "x".join(map(str, c[:5])))
+@pytest.mark.parametrize("ssd_path", ["tc", "tc1"], indirect=True)
+def test_tensor_core_shapes(cuda_device, ssd_path, case):
+    Bsz, L, H, G, chunk, skip = case
+    inp = inputs.ssd_inputs(Bsz, L, H, 64, 128, G, "bf16", skip=skip, seed=L + H + G)
+    y, s = _run(inp, cuda_device, chunk, pad_dt=H % 8 != 0)
+    yo, so = oracle_ssd(inp)
+    check_close(to_np(y), yo, torch.bfloat16, "y")
+    check_close(to_np(s), so, torch.bfloat16, "last_state")
+
+
+def test_no_fallback_switch_rejects_other_layouts(cuda_device):
+    """With the tensor-core-only switch a layout the tensor-core kernels do
+    not take (dt t-stride 4) is an error, not a silent CUDA-core run."""
+    inp = inputs.ssd_inputs(1, 128, 4, 64, 128, 1, "bf16", seed=1)
+    with _abi.debug_paths(ssd_path=1):
+        with pytest.raises(_abi.SSError, match="UNSUPPORTED"):
+            _run(inp, cuda_device, 128)
+        _run(inp, cuda_device, 128, pad_dt=True)  # the same call with a padded dt runs
+
+
+@pytest.mark.parametrize("ssd_path", ["tc", "general"], indirect=True)
+def test_chunk_size_does_not_change_result(cuda_device, ssd_path):
+    inp = inputs.ssd_inputs(1, 768, 8, 64, 128, 1, "bf16", seed=9)
     outs = [_run(inp, cuda_device, c) for c in (64, 128, 256)]
     for y, s in outs[1:]:
         check_close(to_np(y), to_np(outs[0][0]), torch.bfloat16, "y across chunk sizes")
         check_close(to_np(s), to_np(outs[0][1]), torch.bfloat16, "state across chunk sizes")
 
 
-@pytest.mark.parametrize("ssd_path", [None, "tc1"], indirect=True)
-def test_full_size_workload_sampled(cuda_device, ssd_path):
+@pytest.mark.parametrize("ssd_path", ["tc", "tc1"], indirect=True)
+def test_full_size_workload_sampled(cuda_device, ssd_path, record_property):
+    """The benchmark's call (B 4, L 8192, 64 heads x 64, N 128, bf16) on the
+    tensor-core kernels; sampled heads against the oracle.  The relative L2
+    errors are recorded (junit properties) and printed."""
     cfg = inputs.WORKLOADS["mamba2_ssd"]
     inp = inputs.workload_ssd_inputs(cfg)
     y, s = _run(inp, cuda_device, cfg.chunk)
@@ -82,6 +132,9 @@ def test_full_size_workload_sampled(cuda_device, ssd_path):
     yo, so = oracle_ssd_units(inp, units)
     yg = np.stack([to_np(y[u // cfg.nheads, :, u % cfg.nheads]) for u in units])
     sg = np.stack([to_np(s[u // cfg.nheads, u % cfg.nheads]) for u in units])
-    check_close(yg, yo, torch.bfloat16, "ssd y (sampled heads)")
-    check_close(sg, so, torch.bfloat16, "ssd last_state (sampled heads)")
+    ey = check_close(yg, yo, torch.bfloat16, "ssd y (sampled heads)")
+    es = check_close(sg, so, torch.bfloat16, "ssd last_state (sampled heads)")
+    record_property("rel_l2_y", float(ey))
+    record_property("rel_l2_state", float(es))
+    print(f"mamba2_ssd {ssd_path}: rel L2 y {ey:.3e}, last_state {es:.3e} (bar 3e-3)")
     assert bool(torch.isfinite(y).all())

@@ -4,7 +4,6 @@ The oracle already takes an initial state h0 (its split-invariance pin fixes
 what continuing from a state means); the decode step is one iteration of the
 oracle's time loop, so L steps in turn must reproduce the oracle's scan.
 """
-import os
 
 import numpy as np
 import pytest
@@ -12,24 +11,16 @@ import torch
 
 import oracle
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, cuda_inputs, to_np
+from tests.parity_util import SSD_SWITCHES, check_close, cuda_inputs, scan_switches, to_np
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture
 def scan_path(request):
-    old = os.environ.get("SS_SCAN_PATH")
     val = getattr(request, "param", None)
-    if val:
-        os.environ["SS_SCAN_PATH"] = val
-    else:
-        os.environ.pop("SS_SCAN_PATH", None)
-    yield val
-    if old is None:
-        os.environ.pop("SS_SCAN_PATH", None)
-    else:
-        os.environ["SS_SCAN_PATH"] = old
+    with _abi.debug_paths(**scan_switches(val)):
+        yield val
 
 
 def _tdt(dt):
@@ -108,11 +99,12 @@ def test_decode_steps_reproduce_the_scan(cuda_device, case):
                                   (1, 1000, 8, 64, 128, 2, "bf16")],
                          ids=lambda c: "x".join(map(str, c)))
 @pytest.mark.parametrize("ssd_path", [None, "general"])
-def test_ssd_with_initial_state(cuda_device, case, ssd_path, monkeypatch):
-    if ssd_path:
-        monkeypatch.setenv("SS_SSD_PATH", ssd_path)
-    else:
-        monkeypatch.delenv("SS_SSD_PATH", raising=False)
+def test_ssd_with_initial_state(cuda_device, case, ssd_path):
+    with _abi.debug_paths(**SSD_SWITCHES[ssd_path]):
+        _ssd_with_initial_state(cuda_device, case)
+
+
+def _ssd_with_initial_state(cuda_device, case):
     Bsz, L, H, P, N, G, dt = case
     inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, seed=L + 1)
     h0 = _h0((Bsz, H, P, N), 13)

@@ -6,7 +6,8 @@ import torch
 
 import oracle
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, cuda_inputs, oracle_selective_channels, to_np
+from tests.parity_util import (check_close, cuda_inputs, oracle_selective_channels,
+                               scan_switches, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -16,13 +17,10 @@ def _tdt(dt):
 
 
 @pytest.fixture
-def scan_path(request, monkeypatch):
+def scan_path(request):
     val = getattr(request, "param", None)
-    if val:
-        monkeypatch.setenv("SS_SCAN_PATH", val)
-    else:
-        monkeypatch.delenv("SS_SCAN_PATH", raising=False)
-    return val
+    with _abi.debug_paths(**scan_switches(val)):
+        yield val
 
 
 CASES = [
