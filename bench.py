@@ -2,15 +2,18 @@
 """Benchmark of the B300 selective scan (and the Mamba-2 SSD scan).
 
 One step = one full selective-scan call (discretise, recurrence, readout,
-skip, gate, final state) over the Mamba-130M-shaped layer workload: batch 8,
-d_inner 1536, d_state 16, L 2048, bf16 inputs, fp32 state.  Inputs are
+skip, gate, final state) over the long-context workload: batch 1, d_inner
+2048, d_state 16, L 262144, bf16 inputs, fp32 state, no z gate.  Inputs are
 resident in HBM when the timed region starts; L2 is flushed (a 256 MB write)
 before every timed step, outside the step's events.
 
 Prints ONE JSON line (rank 0): channel-steps/s, the HBM roofline of the scan
-kernel, the end-to-end number through the C ABI with host buffers, the fp64
-oracle timed on the host cores, clocks seen during the timed region, and
-secondary rows for the other workloads (timed only; parity is in tests/).
+kernel (with the MUFU exponential rate beside it, against the rate
+ss_probe_ex2_rate measures in the same run), the end-to-end number through
+the C ABI with host buffers, the fp64 oracle timed on the host cores, clocks
+seen during the timed region, a full record (the same fields) for each of the
+other benchmark workloads (the Mamba-130M and Mamba-2.8B layers and the
+Mamba-2 SSD layer), and timing rows for the rest.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun every rank runs its own replica of the workload (weak
@@ -33,24 +36,40 @@ sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan channel-steps/s (B·D·L/s) and achieved HBM GB/s vs B300 peak"
 UNIT = "channel-steps/s"
-HEADLINE = "mamba130m_layer"
+HEADLINE = "long_context"
+# the other benchmark workloads, each measured with the same fields as the headline
+FULL_ROWS = ("mamba130m_layer", "mamba2p8b_layer", "mamba2_ssd")
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
-# ALU roof of the selective scan.  Per channel-step the method needs N = 16
-# exponentials exp(delta*A), softplus log1p(exp(x)) (one ex2, one lg2) and the
-# gate's sigmoid 1/(1 + exp(-z)) (one ex2, one reciprocal): 18 ex2 and 2
-# half-rate MUFU operations, i.e. 22 ex2-equivalents.  The MUFU pipe bounds
-# the scan before the FP32 pipe does (64 + ~8 fp32 lane-operations per
-# channel-step at 128 lanes/SM/clock).  ex2.approx.f32 throughput measured on
-# the B300: 29.2 per SM per clock (lg2 and rcp at half that); 148 SMs at
-# 2032 MHz.
-MUFU_EQ_PER_CHANNEL_STEP = 22
 # nominal B300 HBM3e bandwidth, for the fraction next to the measured one
 NOMINAL_HBM_GBS = 7700.0
-MUFU_EX2_PER_SM_CLK = 29.2
 N_SM = 148
 SM_MHZ_MAX = 2032.0
+
+WORKLOAD_TEXT = {
+    "long_context": "long-context scan, batch 1, d_inner 2048, d_state 16, L 262144, bf16 "
+                    "inputs, fp32 state, no z gate, delta softplus with bias (dt log-uniform in "
+                    "[1e-4, 1e-1]), final state returned",
+    "mamba130m_layer": "Mamba-130M-shaped layer scan, batch 8, d_inner 1536, d_state 16, "
+                       "L 2048, bf16 inputs, fp32 state, z gate on, delta softplus with bias, "
+                       "final state returned",
+    "mamba2p8b_layer": "Mamba-2.8B-shaped layer scan, batch 4, d_inner 5120, d_state 16, "
+                       "L 8192, bf16 inputs, fp32 state, z gate on, delta softplus with bias, "
+                       "final state returned",
+    "mamba2_ssd": "Mamba-2 SSD chunked scan, batch 4, L 8192, 64 heads x headdim 64, d_state "
+                  "128, ngroups 1, chunk 256, bf16 inputs, fp32 state, D skip, final state "
+                  "returned",
+    "tiny_f32": "tiny selective scan, batch 1, d_inner 64, d_state 16, L 256, fp32, z gate on",
+}
+
+
+def mufu_ops_per_channel_step(cfg):
+    """MUFU operations the selective scan needs per channel-step, counted in
+    ex2-equivalents: the N exponentials exp(delta A), softplus's exponential
+    (its logarithm runs on the FMA pipe), and with a z gate the sigmoid's
+    exponential and reciprocal (a reciprocal takes two ex2 slots)."""
+    return cfg.d_state + (1 if cfg.softplus else 0) + (3 if cfg.gate else 0)
 
 
 def parse():
@@ -62,6 +81,8 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary workload rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--probe-mufu", action="store_true",
+                    help="print the measured ex2.approx rate (per SM per clock) and exit")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="run WORKLOAD's call warmup+steps times with no timing or output "
                          "(for ncu captures): a workload name, bwd_mamba130m_layer, "
@@ -115,6 +136,8 @@ def peaks():
 # kernels take their own parameter structs, so the host-side declarations in
 # internal.h do not enter).
 KERNEL_SOURCES = {
+    "scan_seq<bf16, 2 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
+    "scan_seq<bf16, 4 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "scan_common.cuh", "ptx.cuh"],
     "ssd_chunk_tc2": ["ssd_tc.cu", "tc.cuh", "ptx.cuh"],
     "scan_bwd_fast<bf16>": ["selective_scan_bwd.cu", "ptx.cuh"],
@@ -262,58 +285,105 @@ def run_selective_call(g, torch, abi, y, last):
                            g["delta_bias"], softplus=True, y=y, last_state=last)
 
 
-def headline(args, dev, rank, world, torch, abi, inputs, dist_helpers):
-    cfg = inputs.WORKLOADS[HEADLINE]
+def _selective_device_inputs(cfg, dev, rank, inputs):
     host = inputs.workload_selective_inputs(cfg, seed=rank)
     g = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
-    y = torch.empty_like(g["u"])
-    last = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, dtype=torch.float32, device=dev)
+    return host, g
+
+
+def measure_workload(name, args, dev, rank, torch, abi, inputs, dist_helpers, clocks=False):
+    """One benchmark workload measured in full: device-resident timing of
+    `args.steps` calls (L2 flushed before each), the library kernels they
+    launched, the end-to-end time with host buffers, and (optionally) the SM
+    clocks during the timed region."""
+    cfg = inputs.WORKLOADS[name]
+    ssd = name == "mamba2_ssd"
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if ssd:
+        host = inputs.workload_ssd_inputs(cfg, seed=rank)
+        g = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+        y = torch.empty_like(g["x"])
+        last = torch.empty(cfg.batch, cfg.nheads, cfg.headdim, cfg.d_state, device=dev)
 
-    def step():
-        run_selective_call(g, torch, abi, y, last)
+        def step():
+            abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
+                                   chunk=cfg.chunk, y=y, last_state=last)
+    else:
+        host, g = _selective_device_inputs(cfg, dev, rank, inputs)
+        y = torch.empty_like(g["u"])
+        last = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, dtype=torch.float32, device=dev)
 
-    # device-resident timing
+        def step():
+            run_selective_call(g, torch, abi, y, last)
+
     dist_helpers.barrier(dev)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    if clocks:
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+            times, launches = time_device(step, flush, args.steps, args.warmup, torch,
+                                          counter=abi.launch_count)
+        clk_summary = clk.summary()
+    else:
         times, launches = time_device(step, flush, args.steps, args.warmup, torch,
                                       counter=abi.launch_count)
+        clk_summary = None
     torch.cuda.synchronize()
     dist_helpers.barrier(dev)
     ms = statistics.mean(times)
     ms_max = dist_helpers.max_over_ranks(ms, dev)
 
-    # end to end through the C ABI with pinned host buffers
+    # end to end: inputs in pinned host memory, copied in and the results
+    # copied out inside every timed step
     pinned = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
     y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
     last_h = torch.empty(last.shape, dtype=last.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
     d2h = y_h.numel() * y_h.element_size() + last_h.numel() * last_h.element_size()
+    if ssd:
+        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev))
+                  for k, v in pinned.items()}
 
-    def e2e_step():
-        # host buffers in, host buffers out: the library chunks the batch and
-        # overlaps copies with the scan on two streams
-        abi.selective_scan_fwd_host(pinned["u"], pinned["delta"], pinned["A"], pinned["B"],
-                                    pinned["C"], pinned["D"], pinned["z"], pinned["delta_bias"],
-                                    softplus=True, y=y_h, last_state=last_h)
-
+        def e2e_step():
+            # the SSD call takes device buffers: copies in, the call, copies out,
+            # all on the current stream
+            for k, v in pinned.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            abi.ssd_chunk_scan_fwd(dev_in["x"], dev_in["dt"], dev_in["A_head"], dev_in["B"],
+                                   dev_in["C"], dev_in["D"], chunk=cfg.chunk, y=y,
+                                   last_state=last)
+            y_h.copy_(y, non_blocking=True)
+            last_h.copy_(last, non_blocking=True)
+        call = ("torch copies of pinned host tensors in, ss_ssd_chunk_scan_fwd, copies of y and "
+                "the final state out, on one stream")
+    else:
+        def e2e_step():
+            # host buffers in, host buffers out: the library chunks the rows and
+            # overlaps copies with the scan on two streams
+            abi.selective_scan_fwd_host(pinned["u"], pinned["delta"], pinned["A"], pinned["B"],
+                                        pinned["C"], pinned["D"], pinned["z"],
+                                        pinned["delta_bias"], softplus=True, y=y_h,
+                                        last_state=last_h)
+        call = "ss_selective_scan_fwd_host (pinned host tensors in and out)"
     e2e_times = time_device(e2e_step, flush, max(3, args.steps // 2), 2, torch)
     e2e_ms = dist_helpers.max_over_ranks(statistics.mean(e2e_times), dev)
 
     units = cfg.channel_steps
     total_units = dist_helpers.sum_over_ranks(units, dev)
-    return dict(cfg=cfg, host=host, ms=ms, ms_max=ms_max, times=times, launches=launches,
-                clocks=clk.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, units=units,
-                total_units=total_units)
+    out = dict(cfg=cfg, host=host, ms=ms, ms_max=ms_max, times=times, launches=launches,
+               clocks=clk_summary, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, units=units,
+               total_units=total_units, e2e_call=call)
+    del g, y, last, pinned, y_h, last_h
+    torch.cuda.empty_cache()
+    return out
 
 
-def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
-    """Timing of the other workloads (inputs drawn on the GPU with the same
-    recipe; parity for these shapes is covered by tests/)."""
+def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak, mufu_peak):
+    """Timing of the workloads outside the benchmark set (inputs drawn on the
+    GPU with the same recipe; parity for these shapes is covered by tests/)."""
     rows = {}
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    for name in ("tiny_f32", "mamba2p8b_layer", "long_context", "mamba2_ssd"):
+    for name in ("tiny_f32",):
         cfg = inputs.WORKLOADS[name]
         try:
             with inputs.on_device(dev):
@@ -386,7 +456,7 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak):
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
     rows.update(length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(grouped_rows(dev, torch, abi, inputs, hbm_peak, flush))
-    rows.update(wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush))
+    rows.update(wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush, mufu_peak))
     rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
     return rows
@@ -418,7 +488,7 @@ def length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush):
                                    "(summary pass + main pass)"}}
 
 
-def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush):
+def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush, mufu_peak):
     """d_state 64 and 128 at the Mamba-130M layer shape (bf16, gate on)."""
     rows = {}
     cfg = inputs.WORKLOADS["mamba130m_layer"]
@@ -438,7 +508,7 @@ def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush):
             rows[name] = {"ms_per_call": round(ms, 4),
                           "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
                           "state_steps_per_s": cfg.channel_steps * N / (ms * 1e-3),
-                          "mufu_frac": round(mufu / (MUFU_EX2_PER_SM_CLK * N_SM * SM_MHZ_MAX * 1e6), 4),
+                          "mufu_frac": round(mufu / mufu_peak, 4) if mufu_peak else None,
                           "launches_per_call": nl / 3}
             del g, yb, ls
             torch.cuda.empty_cache()
@@ -672,6 +742,50 @@ def oracle_throughput(host, cfg, seconds, oracle, threads=None):
     return done / t_used, nth, done, t_used
 
 
+def oracle_ssd_throughput(host, cfg, seconds, oracle, threads=None):
+    """The SSD oracle on a bounded sample: whole heads (full length, all
+    headdim channels) of one batch row at a time, until `seconds` have
+    passed.  Channel-steps count H*P channels."""
+    import numpy as np
+    nth = threads or oracle.max_threads()
+    H, G = cfg.nheads, cfg.ngroups
+    block = min(H, max(nth, 1))
+    f64 = {k: (None if v is None else v.double().numpy()) for k, v in host.items()}
+    done, t_used, rounds, b = 0, 0.0, 0, 0
+    while t_used < seconds and rounds < 100000:
+        h0 = (rounds * block) % H
+        h1 = min(H, h0 + block)
+        g0, g1 = h0 // (H // G), (h1 - 1) // (H // G) + 1
+        if g1 - g0 > 1:  # keep one group per block so the sub-call's head -> group map holds
+            h1 = (g0 + 1) * (H // G)
+            g1 = g0 + 1
+        sub = dict(x=f64["x"][b:b + 1, :, h0:h1], dt=f64["dt"][b:b + 1, :, h0:h1],
+                   A_head=f64["A_head"][h0:h1], B=f64["B"][b:b + 1, :, g0:g1],
+                   C=f64["C"][b:b + 1, :, g0:g1],
+                   D=None if f64["D"] is None else f64["D"][h0:h1])
+        sub = {k: (None if v is None else np.ascontiguousarray(v)) for k, v in sub.items()}
+        t0 = time.perf_counter()
+        oracle.ssd(sub["x"], sub["dt"], sub["A_head"], sub["B"], sub["C"], sub["D"],
+                   nthreads=nth)
+        t_used += time.perf_counter() - t0
+        done += (h1 - h0) * cfg.headdim * cfg.seqlen
+        rounds += 1
+        b = (b + 1) % cfg.batch
+    return done / t_used, nth, done, t_used
+
+
+def cpu_baseline(name, host, cfg, seconds, oracle):
+    """The oracle as it stands, timed on the host cores on a bounded sample of
+    the workload (whole channels or heads, full length)."""
+    ssd = name == "mamba2_ssd"
+    fn = oracle_ssd_throughput if ssd else oracle_throughput
+    v, nth, done, used = fn(host, cfg, seconds, oracle)
+    what = "whole heads (all headdim channels)" if ssd else "whole channels"
+    return {"value": v, "unit": UNIT, "cores": nth, "kind": "oracle",
+            "sample": f"{done} channel-steps ({what} of the workload, full length "
+                      f"{cfg.seqlen}) in {used:.1f} s on {cpu_model()}"}
+
+
 def cpu_model():
     try:
         for ln in open("/proc/cpuinfo"):
@@ -683,12 +797,17 @@ def cpu_model():
 
 
 def config_dict(cfg):
-    return {"workload": f"{cfg.name}: Mamba-130M-shaped layer scan, batch {cfg.batch}, d_inner "
-                        f"{cfg.d_inner}, d_state {cfg.d_state}, L {cfg.seqlen}, {cfg.dtype} inputs, "
-                        f"fp32 state, z gate on, delta softplus with bias, final state returned",
-            "batch": cfg.batch, "d_inner": cfg.d_inner, "d_state": cfg.d_state,
-            "seq_len": cfg.seqlen, "io_dtype": cfg.dtype, "parallelism": "replica per GPU",
-            "l2": "flushed (256 MB write) before every timed step, outside the step's events"}
+    """The workload as the JSON line names it (the same in both arms)."""
+    d = {"workload": f"{cfg.name}: {WORKLOAD_TEXT[cfg.name]}", "batch": cfg.batch}
+    if cfg.name == "mamba2_ssd":
+        d.update(seq_len=cfg.seqlen, nheads=cfg.nheads, headdim=cfg.headdim,
+                 d_state=cfg.d_state, ngroups=cfg.ngroups, chunk=cfg.chunk)
+    else:
+        d.update(d_inner=cfg.d_inner, d_state=cfg.d_state, seq_len=cfg.seqlen,
+                 z_gate=cfg.gate)
+    d.update(io_dtype=cfg.dtype, state_dtype="f32", parallelism="replica per GPU",
+             l2="flushed (256 MB write) before every timed step, outside the step's events")
+    return d
 
 
 # ---------------------------------------------------------------------------
@@ -809,6 +928,66 @@ def keep_pool_memory(dev_index, nbytes=1 << 30):
         return False
 
 
+def selective_kernel(cfg):
+    """Name of the kernel the library runs for a d_state-16 workload in the
+    TMA layout (the same rule as the library: two lanes per channel where its
+    64-channel tiles fill 60% of the 3 x 148 resident CTA slots or the sequence
+    is cut into segments, else four lanes per channel)."""
+    ch, slots = cfg.batch * cfg.d_inner, 3 * N_SM
+    lanes = 2 if (ch // 64) * 10 >= slots * 6 or (ch // 32) * 10 < slots * 6 else 4
+    return f"scan_seq<{cfg.dtype}, {lanes} lanes/channel>"
+
+
+def workload_record(name, m, pk, args, cpu=None):
+    """The fields of one measured workload (the headline's layout)."""
+    cfg, ms, ms_max = m["cfg"], m["ms"], m["ms_max"]
+    sec = ms * 1e-3
+    if name == "mamba2_ssd":
+        nbytes, flops = ssd_bytes(cfg), ssd_flops(cfg)
+        tf = flops / sec / 1e12
+        gbs = nbytes / sec / 1e9
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["tf_burst"],
+                "unit": "TFLOP/s", "frac": round(tf / pk["tf_burst"], 4),
+                "traffic": measured_traffic("ssd_chunk_tc2"), "kernel": "ssd_chunk_tc2",
+                "algorithmic_flops_per_launch": flops,
+                "peak_source": f"{pk['src']} bf16_tflops (burst: the kernel is timed alone)",
+                "frac_of_sustained": round(tf / pk["tf_sust"], 4),
+                "hbm_achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm"], 4),
+                "algorithmic_bytes_per_launch": nbytes}
+    else:
+        nbytes = selective_bytes(cfg)
+        gbs = nbytes / sec / 1e9
+        key = selective_kernel(cfg)
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm"], 4), "traffic": measured_traffic(key),
+                "kernel": key, "algorithmic_bytes_per_launch": nbytes,
+                "peak_source": f"{pk['src']} hbm_gbs",
+                "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                "nominal_gbs": NOMINAL_HBM_GBS}
+        if pk["mufu"]:
+            ops = mufu_ops_per_channel_step(cfg)
+            rate = cfg.channel_steps * ops / sec
+            roof["mufu"] = {
+                "achieved": round(rate / 1e9, 1), "peak": round(pk["mufu"] / 1e9, 1),
+                "unit": "Gop/s (ex2-equivalents)", "frac": round(rate / pk["mufu"], 4),
+                "ops_per_channel_step": ops,
+                "peak_source": f"ss_probe_ex2_rate in this run: {pk['ex2_rate']:.2f} ex2 per SM "
+                               f"per clock x {N_SM} SMs x {pk['sm_mhz']:.0f} MHz",
+                "note": "the method's exponentials per channel-step; segment summaries "
+                        "(long sequences over few channels) repeat them and are not counted"}
+    return {
+        "value": m["total_units"] / (ms_max * 1e-3), "unit": UNIT, "ms_per_step": ms_max,
+        "steps": args.steps, "warmup": args.warmup, "dtype": cfg.dtype,
+        "config": config_dict(cfg), "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": m["total_units"] / (m["e2e_ms"] * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                "ms_per_step": m["e2e_ms"], "call": m["e2e_call"]},
+        "gpu_launches": m["launches"],
+        "step_ms": {"median": statistics.median(m["times"]), "min": min(m["times"]),
+                    "max": max(m["times"])},
+    }
+
+
 def main_ours(args):
     import torch
     import torch.distributed as tdist
@@ -827,63 +1006,62 @@ def main_ours(args):
     abi.load()
     pool_kept = keep_pool_memory(local_rank)
     hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    try:
+        ex2_rate = abi.probe_ex2_rate()
+    except Exception:
+        ex2_rate = None
+    sm_mhz = SM_MHZ_MAX
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sm_mhz = float(json.load(f).get("sm_max_mhz", SM_MHZ_MAX))
+    except Exception:
+        pass
+    pk = {"hbm": hbm_peak, "tf_burst": tf_peak, "tf_sust": tf_sust, "src": peak_src,
+          "ex2_rate": ex2_rate, "sm_mhz": sm_mhz,
+          "mufu": ex2_rate * N_SM * sm_mhz * 1e6 if ex2_rate else None}
+    if args.probe_mufu:
+        if rank == 0:
+            print(json.dumps({"ex2_per_sm_per_clock": ex2_rate, "sms": N_SM, "sm_mhz": sm_mhz,
+                              "ex2_gop_s": pk["mufu"] / 1e9 if pk["mufu"] else None}))
+        return 0
 
-    h = headline(args, dev, rank, world, torch, abi, inputs, dh)
-    cfg = h["cfg"]
-    nbytes = selective_bytes(cfg)
-    kernel_ms = h["ms"]  # one kernel launch per call for this workload
-    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
-    value = h["total_units"] / (h["ms_max"] * 1e-3)
-    e2e_value = h["total_units"] / (h["e2e_ms"] * 1e-3)
-
-    rows = None
-    if rank == 0 and not args.no_rows:
-        rows = secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_sust)
+    h = measure_workload(HEADLINE, args, dev, rank, torch, abi, inputs, dh, clocks=True)
+    import oracle
     cpu = None
     if rank == 0 and not args.no_cpu:
-        import oracle
-        v, nth, done, used = oracle_throughput(h["host"], cfg, args.cpu_seconds, oracle)
-        v1, _, done1, used1 = oracle_throughput(h["host"], cfg, max(2.0, args.cpu_seconds / 5),
-                                                oracle, threads=1)
-        cpu = {"value": v, "unit": UNIT, "cores": nth, "kind": "oracle",
-               "sample": f"{done} channel-steps (whole channels of the workload, full length "
-                         f"{cfg.seqlen}) in {used:.1f} s on {cpu_model()}",
-               "single_thread_value": v1,
-               "single_thread_sample": f"{done1} channel-steps in {used1:.1f} s on one core"}
+        cpu = cpu_baseline(HEADLINE, h["host"], h["cfg"], args.cpu_seconds, oracle)
+    head = workload_record(HEADLINE, h, pk, args, cpu)
+    del h["host"]
+
+    rows = None
+    if not args.no_rows:
+        rows = {}
+        for name in FULL_ROWS:
+            try:
+                m = measure_workload(name, args, dev, rank, torch, abi, inputs, dh)
+                c = None
+                if rank == 0 and not args.no_cpu:
+                    c = cpu_baseline(name, m["host"], m["cfg"], max(2.0, args.cpu_seconds / 2),
+                                     oracle)
+                rows[name] = workload_record(name, m, pk, args, c)
+                del m
+            except Exception as e:  # a row failing must not hide the headline
+                rows[name] = {"error": str(e)[:200]}
+        if rank == 0:
+            rows.update(secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_sust, pk["mufu"]))
     if world > 1:
         dh.barrier(dev)
     if rank == 0:
-        key = "scan_fast<bf16, 4 lanes/channel>"
-        mufu_peak = MUFU_EX2_PER_SM_CLK * N_SM * SM_MHZ_MAX * 1e6
-        kernel_steps_per_s = cfg.channel_steps / (kernel_ms * 1e-3)
-        mufu_achieved = kernel_steps_per_s * MUFU_EQ_PER_CHANNEL_STEP
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": h["ms_max"], "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(config_dict(cfg), scratch_pool="default pool keeps up to 1 GiB"
-                           if pool_kept else "default pool at CUDA defaults"),
-            "roofline": {"bound": "alu", "achieved": round(mufu_achieved / 1e9, 1),
-                         "peak": round(mufu_peak / 1e9, 1),
-                         "unit": "Gop/s (MUFU ex2-equivalent)",
-                         "frac": round(mufu_achieved / mufu_peak, 4),
-                         "traffic": measured_traffic(key), "kernel": key,
-                         "ops_per_channel_step": MUFU_EQ_PER_CHANNEL_STEP,
-                         "peak_source": "measured ex2.approx rate x 148 SMs x 2032 MHz",
-                         "hbm_achieved_gbs": round(achieved, 1), "hbm_peak_gbs": hbm_peak,
-                         "hbm_frac": round(achieved / hbm_peak, 4),
-                         "hbm_peak_source": f"{peak_src} hbm_gbs",
-                         "hbm_frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "hbm_nominal_gbs": NOMINAL_HBM_GBS,
-                         "algorithmic_bytes_per_launch": nbytes},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h["h2d"],
-                    "d2h_bytes_per_step": h["d2h"], "ms_per_step": h["e2e_ms"],
-                    "call": "ss_selective_scan_fwd_host (pinned host tensors in and out)"},
-            "gpu_launches": h["launches"],
-            "clocks": h["clocks"],
-            "step_ms": {"median": statistics.median(h["times"]), "min": min(h["times"]),
-                        "max": max(h["times"])},
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+            "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "clocks": h["clocks"],
+            "step_ms": head["step_ms"],
+            "scratch_pool": "default pool keeps up to 1 GiB" if pool_kept
+                            else "default pool at CUDA defaults",
             "rows": rows,
         }
         print(json.dumps(line), flush=True)

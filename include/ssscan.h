@@ -18,7 +18,7 @@
  *   ss_selective_scan_fwd_noalloc the selective scan with no allocation
  *   ss_status_string, ss_get_device_error, ss_launch_count, ss_version,
  *   ss_selftest_timeout,         status, errors and diagnostics
- *   ss_debug_set_path
+ *   ss_debug_set_path, ss_probe_ex2_rate
  *
  * Every buffer is caller-owned device memory described by an ss_tensor
  * (pointer, dtype, shape, strides in elements).  The library keeps no pointer
@@ -404,6 +404,18 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
 #define SS_DEBUG_FAULT_ALLOC 7
 #define SS_DEBUG_COUNT 8
 int ss_debug_set_path(int which, int value);
+
+/*
+ * Throughput probe (no counterpart on the pages): measures how many
+ * ex2.approx.f32 operations (the MUFU exponential every state of the
+ * selective scan needs once per step) one SM completes per clock on the
+ * current device, with one 1024-thread CTA per SM running independent
+ * chains, timed by the SM's own clock.  Writes the rate to
+ * *ex2_per_sm_per_clock.  Synchronises `stream`; allocates nothing.
+ * Returns SS_OK, SS_ERR_INVALID_ARG (NULL output), SS_ERR_LAUNCH or
+ * SS_ERR_CUDA.
+ */
+int ss_probe_ex2_rate(double* ex2_per_sm_per_clock, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ss_launch_count(void);

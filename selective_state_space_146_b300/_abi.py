@@ -26,7 +26,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version", "ss_selftest_timeout", "ss_selective_scan_fwd_ckpt",
-           "ss_selective_scan_bwd_ckpt", "ss_debug_set_path")
+           "ss_selective_scan_bwd_ckpt", "ss_debug_set_path", "ss_probe_ex2_rate")
 # Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
 DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
              grouped_path=6, fault_alloc=7)
@@ -95,6 +95,8 @@ def load(path: str | None = None):
     lib.ss_version.restype = i
     lib.ss_debug_set_path.argtypes = [i, i]
     lib.ss_debug_set_path.restype = i
+    lib.ss_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+    lib.ss_probe_ex2_rate.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -382,3 +384,12 @@ def debug_paths(**switches):
     finally:
         for k in switches:
             set_debug_path(k, None)
+
+
+def probe_ex2_rate(stream=None) -> float:
+    """ss_probe_ex2_rate: measured ex2.approx.f32 operations per SM per clock."""
+    v = ctypes.c_double(0.0)
+    rc = load().ss_probe_ex2_rate(ctypes.byref(v), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_probe_ex2_rate")
+    return float(v.value)

@@ -810,6 +810,11 @@ int ss_selftest_timeout(unsigned limit_us, void* stream) {
     return launch_selftest_wait(limit_us, err, static_cast<cudaStream_t>(stream));
 }
 
+int ss_probe_ex2_rate(double* ex2_per_sm_per_clock, void* stream) {
+    if (!ex2_per_sm_per_clock) return SS_ERR_INVALID_ARG;
+    return probe_ex2_rate(ex2_per_sm_per_clock, static_cast<cudaStream_t>(stream));
+}
+
 uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int ss_version(void) { return 300; }

@@ -1,8 +1,8 @@
 """The JSON line `bench.py` prints: every key a reader of the benchmark relies
 on, with values of the right kind.  The CPU test runs the reference arm (the
 fp64 oracle timed on the host) for one short step; the GPU test runs the
-library's arm on the headline workload with the secondary rows and the CPU
-baseline left out."""
+library's arm on the headline workload (long context) with the other
+workloads and the CPU baseline left out."""
 import json
 import os
 import subprocess
@@ -37,8 +37,12 @@ def _common(d, steps, warmup):
 
 
 def test_reference_arm_line():
+    import bench
+    from selective_state_space_146_b300 import inputs
     d = _line(["--impl", "reference", "--steps", "1", "--warmup", "1"], timeout=600)
     _common(d, 1, 1)
+    # the same workload description as the library's arm prints
+    assert d["config"] == json.loads(json.dumps(bench.config_dict(inputs.WORKLOADS[bench.HEADLINE])))
     assert d["impl"] == "reference" and d["dtype"] == "f64"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
@@ -55,8 +59,11 @@ def test_library_arm_line(cuda_device):
     r = d["roofline"]
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in r, k
-    assert r["bound"] == "alu" and 0 < r["frac"] < 1.5
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert d["dtype"] == "bf16" and d["config"]["workload"].startswith("long_context")
+    m = r["mufu"]  # the exponential rate against the probe measured in the same run
+    assert 0 < m["frac"] < 1.5 and abs(m["frac"] - m["achieved"] / m["peak"]) < 1e-3
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0
     c = d["clocks"]
