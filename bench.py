@@ -136,6 +136,7 @@ def peaks():
 # kernels take their own parameter structs, so the host-side declarations in
 # internal.h do not enter).
 KERNEL_SOURCES = {
+    "scan_seq<bf16, 1 lane/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_seq<bf16, 2 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_seq<bf16, 4 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "scan_common.cuh", "ptx.cuh"],
@@ -930,12 +931,19 @@ def keep_pool_memory(dev_index, nbytes=1 << 30):
 
 def selective_kernel(cfg):
     """Name of the kernel the library runs for a d_state-16 workload in the
-    TMA layout (the same rule as the library: two lanes per channel where its
-    64-channel tiles fill 60% of the 3 x 148 resident CTA slots or the sequence
-    is cut into segments, else four lanes per channel)."""
+    TMA layout (the library's rule, with 3 x 148 resident CTA slots: two lanes
+    per channel where its 64-channel tiles fill 60% of the slots, four lanes
+    where its 32-channel tiles do, else the sequence is cut into segments and
+    one lane per channel runs from 512 tiles of 64 steps, two from 32)."""
     ch, slots = cfg.batch * cfg.d_inner, 3 * N_SM
-    lanes = 2 if (ch // 64) * 10 >= slots * 6 or (ch // 32) * 10 < slots * 6 else 4
-    return f"scan_seq<{cfg.dtype}, {lanes} lanes/channel>"
+    tiles64 = -(-cfg.seqlen // 64)
+    if (ch // 64) * 10 >= slots * 6:
+        lanes = 2
+    elif (ch // 32) * 10 >= slots * 6:
+        lanes = 4
+    else:
+        lanes = 1 if tiles64 >= 512 else 2 if tiles64 >= 32 else 4
+    return f"scan_seq<{cfg.dtype}, {lanes} lane{'s' if lanes > 1 else ''}/channel>"
 
 
 def workload_record(name, m, pk, args, cpu=None):

@@ -379,6 +379,7 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
  *   SS_DEBUG_SCAN_SHAPE     scan_seq launch shape 1 .. 4 (lanes per channel
  *                           1, 1, 2, 4 over 128, 64, 64, 32 channels)
  *   SS_DEBUG_SCAN_SEGMENTS  scan_seq time segments (1 .. 128)
+ *   SS_DEBUG_SCAN_SEG_TILES scan_seq shortest segment of its own choice, in tiles of t
  *   SS_DEBUG_SSD_PATH       SSD scan: 0 the CUDA-core kernel, 1 the tensor-core
  *                           kernels only, 2 the one-head tensor-core kernel
  *                           only; with 1 or 2 a shape or layout those kernels
@@ -402,7 +403,8 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
 #define SS_DEBUG_BWD_PATH 5
 #define SS_DEBUG_GROUPED_PATH 6
 #define SS_DEBUG_FAULT_ALLOC 7
-#define SS_DEBUG_COUNT 8
+#define SS_DEBUG_SCAN_SEG_TILES 8
+#define SS_DEBUG_COUNT 9
 int ss_debug_set_path(int which, int value);
 
 /*

@@ -29,7 +29,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_selective_scan_bwd_ckpt", "ss_debug_set_path", "ss_probe_ex2_rate")
 # Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
 DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
-             grouped_path=6, fault_alloc=7)
+             grouped_path=6, fault_alloc=7, scan_seg_tiles=8)
 
 
 class SSTensor(ctypes.Structure):

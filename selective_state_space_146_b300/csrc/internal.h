@@ -148,5 +148,8 @@ void* tensor_map_encoder();
 // t-stride: box of box_t steps x box_d rows, 128-byte swizzle if `swizzle`.
 bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
                  int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle = true);
+// The same with the swizzle span given in bytes (0, 64 or 128).
+bool make_map_3d_sw(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
+                    int64_t sd, int64_t sb, int box_t, int box_d, int swizzle_bytes);
 
 }  // namespace ss

@@ -110,6 +110,53 @@ __device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_
     }
 }
 
+// Byte offset of 16-byte chunk c of row r in a tile of ROWB-byte rows with
+// the ROWB-byte TMA swizzle: within each 1024-byte (128-byte rows) or
+// 512-byte (64-byte rows) atom, the chunk index is XORed with the row index
+// (128) or with half the row index (64), so the rows a quarter-warp reads
+// land on distinct banks.
+template <int ROWB>
+__device__ __forceinline__ int swz_rows(int r, int c) {
+    static_assert(ROWB == 128 || ROWB == 64, "row of 64 or 128 bytes");
+    if constexpr (ROWB == 128) return (r << 7) + ((c ^ (r & 7)) << 4);
+    return (r << 6) + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// convert_bc for raw tiles of 64-byte rows (32 bf16 or 16 fp32 steps): lanes
+// 0..15 write the state pairs 0..3 of their step pair (bf16) or step (fp32),
+// lanes 16..31 the pairs 4..7, chunk order rotated by lane.
+template <typename T, bool WITH_C>
+__device__ __forceinline__ void convert_bc64(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+    const int w = lane & 15, half = lane >> 4;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int j = 4 * half + ((it + w) & 3);
+        const uint32_t rb = rawB + (2 * j) * 64, rc = rawC + (2 * j) * 64;
+        if constexpr (sizeof(T) == 2) {
+            // word w of a 64-byte row holds the bf16 pair (t = 2 w, 2 w + 1)
+            const uint32_t b0 = lds32(rb + w * 4), b1 = lds32(rb + 64 + w * 4);
+            const uint32_t c0 = WITH_C ? lds32(rc + w * 4) : 0u;
+            const uint32_t c1 = WITH_C ? lds32(rc + 64 + w * 4) : 0u;
+            const float4 lo = make_float4(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16),
+                                          __uint_as_float(c0 << 16), __uint_as_float(c1 << 16));
+            const float4 hi = make_float4(__uint_as_float(b0 & 0xffff0000u),
+                                          __uint_as_float(b1 & 0xffff0000u),
+                                          __uint_as_float(c0 & 0xffff0000u),
+                                          __uint_as_float(c1 & 0xffff0000u));
+            sts128f(bc + (2 * w) * 128 + j * 16, lo);
+            sts128f(bc + (2 * w + 1) * 128 + j * 16, hi);
+        } else {
+            // word w of a 64-byte row holds step w
+            float4 v;
+            v.x = __uint_as_float(lds32(rb + w * 4));
+            v.y = __uint_as_float(lds32(rb + 64 + w * 4));
+            v.z = WITH_C ? __uint_as_float(lds32(rc + w * 4)) : 0.f;
+            v.w = WITH_C ? __uint_as_float(lds32(rc + 64 + w * 4)) : 0.f;
+            sts128f(bc + w * 128 + j * 16, v);
+        }
+    }
+}
+
 // Store K floats as T to global memory: one aligned vector store, or (in the
 // last chunk of the sequence) element by element up to `limit` elements.
 template <typename T, int K>

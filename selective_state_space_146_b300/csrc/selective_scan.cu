@@ -574,6 +574,11 @@ scan_fast(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUte
 
 bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
                  int64_t sd, int64_t sb, int box_t, int box_d, bool swizzle) {
+    return make_map_3d_sw(m, base, dtype, L, D, Bsz, sd, sb, box_t, box_d, swizzle ? 128 : 0);
+}
+
+bool make_map_3d_sw(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t D, int64_t Bsz,
+                    int64_t sd, int64_t sb, int box_t, int box_d, int swizzle_bytes) {
     auto enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
     if (!enc) return false;
     const int es = dtype == SS_BF16 ? 2 : 4;
@@ -584,7 +589,9 @@ bool make_map_3d(CUtensorMap* m, const void* base, int dtype, int64_t L, int64_t
     CUresult r = enc(m, dtype == SS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

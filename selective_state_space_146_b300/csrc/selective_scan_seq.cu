@@ -8,8 +8,8 @@
 //
 // scan_seq: one CTA = one work item over a tile of DT channels of one batch
 // row and one time segment.
-//   warp 0     lane 0 issues the TMA loads of the u / delta / z tiles (128
-//              bytes of t per channel row, 128-byte swizzle) and of the raw B,
+//   warp 0     lane 0 issues the TMA loads of the u / delta / z tiles (ROWB =
+//              64 or 128 bytes of t per channel row, swizzled over ROWB) and of the raw B,
 //              C tiles into a ring of stages; all lanes convert B and C of each
 //              landed tile into an fp32 table shared by all channels of the CTA;
 //   warps 1..  consumers: NSPLIT lanes per channel (1, 2 or 4), each keeping
@@ -71,21 +71,21 @@ struct SeqParams {
     unsigned* err;
 };
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB>
 struct SeqCfg {
     static constexpr int N = 16;
     static constexpr int ES = sizeof(T);
     static constexpr int VEC = 16 / ES;          // steps per 16-byte chunk
-    static constexpr int TT = 128 / ES;          // steps per tile (one 128-byte row)
-    static constexpr int CHUNKS = TT / VEC;      // = 8
+    static constexpr int TT = ROWB / ES;         // steps per tile (one ROWB-byte row)
+    static constexpr int CHUNKS = TT / VEC;      // 4 or 8
     static constexpr int CPW = 32 / NSPLIT;      // channels per consumer warp
     static constexpr int DT = CWARPS * CPW;      // channels per CTA
     static constexpr int NS = N / NSPLIT;        // states per lane
     static constexpr int K = VEC / NSPLIT;       // steps of a chunk whose y a lane owns
     static constexpr int NCONS = CWARPS * 32;
     static constexpr int NTHREADS = NCONS + 32;  // + the TMA / table warp
-    static constexpr int TILE_BYTES = DT * 128;  // one [DT][TT] tile of u, delta, z
-    static constexpr int RAW_BYTES = N * 128;    // one [N][TT] tile of B or C as loaded
+    static constexpr int TILE_BYTES = DT * ROWB;  // one [DT][TT] tile of u, delta, z
+    static constexpr int RAW_BYTES = N * ROWB;    // one [N][TT] tile of B or C as loaded
     static constexpr int BC_BYTES = TT * 2 * N * 4;
     // stage: u, delta, [z], raw B, raw C, fp32 B|C table
     static constexpr int OFF_DL = TILE_BYTES;
@@ -95,7 +95,6 @@ struct SeqCfg {
     static constexpr int OFF_BC = OFF_RAWC + RAW_BYTES;
     static constexpr int STAGE_BYTES = OFF_BC + BC_BYTES;
     static constexpr int SMEM_BYTES = STAGE_BYTES * STAGES + 128 /*barriers, item*/ + 1024 /*align*/;
-    static_assert(CHUNKS == 8, "the chunk pipeline below assumes 8 chunks per tile");
     static_assert(TILE_BYTES % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(NS % 2 == 0 && K >= 1, "states per lane come in pairs; each lane owns steps");
@@ -148,9 +147,12 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned* err) {
     };
     if (ld()) return true;
     const unsigned long long start = globaltimer();
+    unsigned sleep_ns = 64;
     for (uint32_t it = 1;; ++it) {
+        __nanosleep(sleep_ns);  // back off: the flag's L2 line is shared by many waiters
+        sleep_ns = sleep_ns < 1024 ? 2 * sleep_ns : sleep_ns;
         if (ld()) return true;
-        if ((it & 63u) == 0 && globaltimer() - start > kWaitLimitNs) {
+        if ((it & 15u) == 0 && globaltimer() - start > kWaitLimitNs) {
             atomicOr(err, ERR_WAIT_TIMEOUT);
             return false;
         }
@@ -164,12 +166,12 @@ __device__ __forceinline__ float2 lds64f(uint32_t a) {
 }
 
 // One work item: SUMM is a segment summary, otherwise the scan proper.
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, bool SUMM>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool SUMM>
 __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensorMap* tm_dl,
                                          const CUtensorMap* tm_z, const CUtensorMap* tm_B,
                                          const CUtensorMap* tm_C, const SeqParams& p,
                                          uint8_t* smem, uint64_t* bars, int seg, int tile) {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
     constexpr int N = Cfg::N, TT = Cfg::TT, VEC = Cfg::VEC, NS = Cfg::NS, DT = Cfg::DT;
     constexpr int ES = Cfg::ES, K = Cfg::K;
     constexpr bool LOAD_Z = HAS_Z && !SUMM;
@@ -207,7 +209,10 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
             const int s = k % STAGES;
             if (!__all_sync(0xffffffffu, mbar_wait(&raw[s], (k / STAGES) & 1, p.err))) break;
             const uint32_t st = smem_u32(stage(s));
-            convert_bc<T, !SUMM>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC, lane);
+            if constexpr (ROWB == 128)
+                convert_bc<T, !SUMM>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC, lane);
+            else
+                convert_bc64<T, !SUMM>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC, lane);
             mbar_arrive(&table[s]);
             const int kn = k - 1 + STAGES;
             bool ok = true;
@@ -249,9 +254,12 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
 
     const int64_t per = (int64_t)p.Bsz * p.D * 2 * N;  // floats per segment of summaries
     if (!SUMM && seg > 0) {
-        // the state entering this segment, stored by the tile's fold (the flag
-        // waited for with acquire; the state read from L2, not this SM's L1)
-        wait_flag(p.ready + tile, p.err);
+        // the state entering this segment, stored by the tile's fold: one
+        // thread waits for the flag (acquire), the consumers meet at a named
+        // barrier, and every lane reads its state from L2, not this SM's L1
+        if (threadIdx.x == 32) wait_flag(p.ready + tile, p.err);
+        named_sync(1, Cfg::NCONS);
+        __threadfence();
         if (valid) {
             const float* sm = p.summ + (seg - 1) * per + bd * 2 * N + N;
 #pragma unroll
@@ -268,10 +276,13 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     //           group; u of the chunk; du = delta * u;
     //   core:   the recurrence over the chunk's steps (partial readouts);
     //   finish: reduce-scatter of the readouts, skip and gate, store of y.
-    // Full tiles run prep(c+1) | core(c) | finish(c-1) in one block.
+    // A full tile runs the chunks in a short loop (unrolled by two with
+    // several lanes per channel): the loop body stays in the instruction
+    // cache, and with 16 states per lane a chunk alone has ample independent
+    // work.
     auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* du, float* uf, auto tail) {
         constexpr bool TAIL = decltype(tail)::value;
-        const int off = swz(ci, c);
+        const int off = swz_rows<ROWB>(ci, c);
         lds_elems<T, VEC>(su + off, uf);
         float dv[K];
         lds_elems<T, K>(su + Cfg::OFF_DL + off + part * K * ES, dv);
@@ -329,7 +340,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
                 reduce_half<VEC>(yv, w, (part >> 1) & 1, 2);
                 reduce_half<VEC / 2>(w, yo, part & 1, 1);
             }
-            const int own = swz(ci, c) + part * K * ES;
+            const int own = swz_rows<ROWB>(ci, c) + part * K * ES;
             float us[K];
             if constexpr (NSPLIT == 1) {
 #pragma unroll
@@ -367,22 +378,22 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     };
     auto full_tile = [&](uint32_t su, int tile_t0) {
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
-        float ddA[VEC], duA[VEC], ufA[VEC], yA[VEC], ddB[VEC], duB[VEC], ufB[VEC], yB[VEC];
-        prep(su, 0, TT, ddA, duA, ufA, std::false_type{});
-        core(bcp, 0, ddA, duA, yA);
-        prep(su, 1, TT, ddB, duB, ufB, std::false_type{});
+        float dd[VEC], du[VEC], uf[VEC], yv[VEC];
+        if constexpr (NSPLIT == 1) {
 #pragma unroll 1
-        for (int c = 1; c < 7; c += 2) {
-            core(bcp, c, ddB, duB, yB);
-            finish(su, tile_t0, c - 1, yA, ufA, std::false_type{});
-            prep(su, c + 1, TT, ddA, duA, ufA, std::false_type{});
-            core(bcp, c + 1, ddA, duA, yA);
-            finish(su, tile_t0, c, yB, ufB, std::false_type{});
-            prep(su, c + 2, TT, ddB, duB, ufB, std::false_type{});
+            for (int c = 0; c < Cfg::CHUNKS; ++c) {
+                prep(su, c, TT, dd, du, uf, std::false_type{});
+                core(bcp, c, dd, du, yv);
+                finish(su, tile_t0, c, yv, uf, std::false_type{});
+            }
+        } else {
+#pragma unroll 2
+            for (int c = 0; c < Cfg::CHUNKS; ++c) {
+                prep(su, c, TT, dd, du, uf, std::false_type{});
+                core(bcp, c, dd, du, yv);
+                finish(su, tile_t0, c, yv, uf, std::false_type{});
+            }
         }
-        core(bcp, 7, ddB, duB, yB);
-        finish(su, tile_t0, 6, yA, ufA, std::false_type{});
-        finish(su, tile_t0, 7, yB, ufB, std::false_type{});
     };
     auto tail_tile = [&](uint32_t su, int tile_t0, int tcount) {
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
@@ -435,28 +446,46 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
         named_sync(1, Cfg::NCONS);
         if (*s_last) {
             __threadfence();
-            if (valid) {
-                // h_{s+1} = P_s h_s + E_s from h_0; h_{s+1} replaces E_s
-                float2 hp[NS / 2];
+            // h_{s+1} = P_s h_s + E_s from h_0, h_{s+1} replacing E_s.  Spread over
+            // the consumer threads by (channel, state) so each warp access is two
+            // contiguous 64-byte runs: thread c of the consumers folds state
+            // c % 16 of channels c / 16 + i * CPP; the loads of BATCH segments
+            // are issued before their fold so that their L2 latencies overlap.
+            constexpr int CPP = Cfg::NCONS / 16;  // channels per pass
+            constexpr int PASSES = DT / CPP;      // (channel, state) pairs per thread
+            constexpr int BATCH = PASSES >= 16 ? 1 : 16 / PASSES;
+            const int tc = threadIdx.x - 32, n = tc & 15;
+            const int64_t bd0 = (int64_t)b * p.D + d0;
+            float hp[PASSES];
 #pragma unroll
-                for (int q = 0; q < NS / 2; ++q) {
-                    const int n = part * NS + 2 * q;
-                    hp[q] = p.h0 ? make_float2(p.h0[b * p.sh_b + d * p.sh_d + n * p.sh_n],
-                                               p.h0[b * p.sh_b + d * p.sh_d + (n + 1) * p.sh_n])
-                                 : make_float2(0.f, 0.f);
-                }
-                for (int j = 0; j < p.nseg - 1; ++j) {
-                    float* sm = p.summ + j * per + bd * 2 * N + part * NS;
-                    float2 P[NS / 2], E[NS / 2];
+            for (int k = 0; k < PASSES; ++k) {
+                const int dk = d0 + tc / 16 + k * CPP;
+                hp[k] = (p.h0 && dk < p.D) ? p.h0[b * p.sh_b + dk * p.sh_d + n * p.sh_n] : 0.f;
+            }
+            const int nsum = p.nseg - 1;
+            for (int j0 = 0; j0 < nsum; j0 += BATCH) {
+                float P[BATCH][PASSES], E[BATCH][PASSES];
 #pragma unroll
-                    for (int q = 0; q < NS / 2; ++q) {
-                        P[q] = __ldcg(reinterpret_cast<const float2*>(sm + 2 * q));
-                        E[q] = __ldcg(reinterpret_cast<const float2*>(sm + N + 2 * q));
+                for (int jb = 0; jb < BATCH; ++jb) {
+#pragma unroll
+                    for (int k = 0; k < PASSES; ++k) {
+                        const int ck = tc / 16 + k * CPP;
+                        if (j0 + jb < nsum && d0 + ck < p.D) {
+                            const float* sm = p.summ + (j0 + jb) * per + (bd0 + ck) * 2 * N + n;
+                            P[jb][k] = __ldcg(sm);
+                            E[jb][k] = __ldcg(sm + N);
+                        }
                     }
+                }
 #pragma unroll
-                    for (int q = 0; q < NS / 2; ++q) {
-                        hp[q] = __ffma2_rn(P[q], hp[q], E[q]);
-                        __stcg(reinterpret_cast<float2*>(sm + N + 2 * q), hp[q]);
+                for (int jb = 0; jb < BATCH; ++jb) {
+#pragma unroll
+                    for (int k = 0; k < PASSES; ++k) {
+                        const int ck = tc / 16 + k * CPP;
+                        if (j0 + jb < nsum && d0 + ck < p.D) {
+                            hp[k] = fmaf(P[jb][k], hp[k], E[jb][k]);
+                            __stcg(p.summ + (j0 + jb) * per + (bd0 + ck) * 2 * N + N + n, hp[k]);
+                        }
                     }
                 }
             }
@@ -480,12 +509,12 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     }
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int MINB>
-__global__ void __launch_bounds__(SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z>::NTHREADS, MINB)
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, int MINB>
+__global__ void __launch_bounds__(SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>::NTHREADS, MINB)
 scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
          const __grid_constant__ CUtensorMap tm_C, const SeqParams p) {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::STAGE_BYTES * STAGES);
@@ -510,11 +539,11 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const int item = *s_item;
     const int S = p.nseg;
     if (S > 1 && item < p.ntile * (S - 1)) {  // summaries, tile by tile
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                          bars, item % (S - 1), item / (S - 1));
     } else {                                  // mains, tile by tile
         const int m = S > 1 ? item - p.ntile * (S - 1) : item;
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                           bars, m % S, m / S);
     }
 }
@@ -524,16 +553,10 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
 
 namespace {
 
-// Launch shapes of scan_seq.  Each is (lanes per channel, consumer warps,
-// stages, CTAs per SM the launch bounds aim at).
-struct SeqShape {
-    int nsplit, cwarps, stages, minb;
-};
-
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int MINB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, int MINB>
 struct SeqKernel {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z>;
-    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, MINB>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
+    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, MINB>;
     // set the shared-memory attributes once per device; returns the resident
     // CTAs per SM (0 on failure)
     static int prepare() {
@@ -564,10 +587,11 @@ struct SeqKernel {
     }
 };
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, int MINB>
-static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
-    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, MINB>;
-    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, MINB>;
+template <typename T, int NSPLIT, int CWARPS, int STAGES, int ROWB, int MINB>
+static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch,
+                   int min_tiles_per_seg) {
+    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, ROWB, MINB>;
+    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, ROWB, MINB>;
     using Cfg = typename KZ::Cfg;
     constexpr int TT = Cfg::TT, DT = Cfg::DT;
     const int occ = a.z ? KZ::prepare() : KN::prepare();
@@ -587,17 +611,18 @@ static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
     sp.bc_groups = grouped ? a.G : 1;
     sp.bc_dpg = grouped ? a.D / a.G : a.D;
 
-    // Segments (measured on the B300 over 1536..20480 channels and 2048..262144
+    // Segments (measured on the B300 over 2048..20480 channels and 1024..262144
     // steps): none while the channel tiles fill at least 60% of the resident
-    // CTA slots; otherwise about 8 main items per slot (the dynamic order
-    // evens out the end of the launch), at least 8 tiles of t per segment, at
-    // most 128 segments, and no more than the scratch can hold.
+    // CTA slots; otherwise about three main items per slot (the dynamic order
+    // evens out the end of the launch), segments of at least
+    // `min_tiles_per_seg` tiles of t, at most 128 segments, and no more than
+    // the scratch can hold.
     const int64_t slots = (int64_t)sm_count_current() * occ;
     const int64_t tiles = (a.L + TT - 1) / TT;
     int64_t nseg = 1;
     if (sp.ntile * 10 < slots * 6) {
-        nseg = (8 * slots + sp.ntile - 1) / sp.ntile;
-        nseg = std::min<int64_t>(nseg, std::max<int64_t>(1, tiles / 8));
+        nseg = (3 * slots + sp.ntile - 1) / sp.ntile;
+        nseg = std::min<int64_t>(nseg, std::max<int64_t>(1, tiles / min_tiles_per_seg));
     }
     const int forced = debug_path(SS_DEBUG_SCAN_SEGMENTS);
     if (forced > 0) nseg = forced;
@@ -615,15 +640,15 @@ static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
 
     // maps: 0 u, 1 delta, 2 z, 3 B, 4 C
     CUtensorMap maps[5];
-    if (!make_map_3d(&maps[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, TT, DT) ||
-        !make_map_3d(&maps[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, TT, DT) ||
+    if (!make_map_3d_sw(&maps[0], a.u, a.dtype, a.L, a.D, a.Bsz, a.su_d, a.su_b, TT, DT, ROWB) ||
+        !make_map_3d_sw(&maps[1], a.dl, a.dtype, a.L, a.D, a.Bsz, a.sdl_d, a.sdl_b, TT, DT, ROWB) ||
         !make_map_3d(&maps[3], a.Bm, a.dtype, a.L, a.N, (int64_t)a.Bsz * sp.bc_groups, a.sB_n,
                      grouped ? a.sB_g : a.sB_b, TT, 16, false) ||
         !make_map_3d(&maps[4], a.Cm, a.dtype, a.L, a.N, (int64_t)a.Bsz * sp.bc_groups, a.sC_n,
                      grouped ? a.sC_g : a.sC_b, TT, 16, false))
         return SS_ERR_CUDA;
     if (a.z) {
-        if (!make_map_3d(&maps[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, TT, DT))
+        if (!make_map_3d_sw(&maps[2], a.z, a.dtype, a.L, a.D, a.Bsz, a.sz_d, a.sz_b, TT, DT, ROWB))
             return SS_ERR_CUDA;
     } else {
         maps[2] = maps[0];
@@ -656,38 +681,66 @@ static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch) {
 
 }  // namespace
 
-// Launch shapes by code (SS_DEBUG_SCAN_SHAPE): 1 = one lane per channel, four
-// consumer warps (128 channels), two stages; 2 = one lane, two warps (64
-// channels), two stages; 3 = two lanes per channel, four warps (64 channels),
-// two stages; 4 = four lanes per channel, four warps (32 channels), three stages.
+// Launch shapes by code (SS_DEBUG_SCAN_SHAPE): lanes per channel, consumer
+// warps (channels per CTA), stages, row bytes of t per tile, CTAs per SM the
+// launch bounds aim at.
+struct SeqShape {
+    int nsplit, dt;
+};
+static constexpr SeqShape kShapes[] = {
+    {0, 0},
+    {1, 128},  // 1: one lane, 4 warps (128 channels), 2 stages, 64-byte rows, 3 per SM
+    {1, 128},  // 2: one lane, 4 warps, 2 stages, 128-byte rows, 2 per SM
+    {2, 64},   // 3: two lanes, 4 warps (64 channels), 2 stages, 128-byte rows, 3 per SM
+    {4, 32},   // 4: four lanes, 4 warps (32 channels), 3 stages, 128-byte rows, 3 per SM
+    {2, 64},   // 5: two lanes, 4 warps, 2 stages, 64-byte rows, 4 per SM
+    {1, 128},  // 6: one lane, 4 warps, 3 stages, 64-byte rows, 3 per SM
+};
+constexpr int kNumShapes = 6;
+
 //
-// The library's choice (measured on the B300, d_state 16): two lanes per
-// channel (shape 3) wherever its 64-channel tiles fill 60% of the resident CTA
-// slots or the sequence has to be cut into segments anyway (few channels); four
-// lanes per channel (shape 4) in between, where its 32-channel tiles fill the
-// slots without segments (the Mamba-130M layer, 8 x 1536 channels).
+// The library's choice (measured on the B300, d_state 16):
+//   - enough channels for the 64-channel tiles of two lanes per channel
+//     (shape 3) to fill 60% of the 3 x SM CTA slots: shape 3, no segments
+//     (the Mamba-2.8B layer, 4 x 5120 channels);
+//   - enough for the 32-channel tiles of four lanes (shape 4): shape 4, no
+//     segments (the Mamba-130M layer, 8 x 1536 channels);
+//   - fewer channels, so the sequence is cut into segments: one lane per
+//     channel over 128 channels (shape 1) from 512 tiles of 64 steps (the
+//     long-context workload), two lanes (shape 3) from 32 tiles, four lanes
+//     below; segments of at least two tiles.
 int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
     if (a.N != 16 || a.cw || a.ckpt || a.L <= 0 || !fast_layout_ok(a)) return SS_OK;
     const bool bf = a.dtype == SS_BF16;
     int shape = debug_path(SS_DEBUG_SCAN_SHAPE);
-    if (shape < 1 || shape > 4) {
+    if (shape < 1 || shape > kNumShapes) {
         const int64_t ch = (int64_t)a.Bsz * a.D, slots = (int64_t)sm_count_current() * 3;
-        shape = (ch / 64) * 10 >= slots * 6 || (ch / 32) * 10 < slots * 6 ? 3 : 4;
-        if (a.G > 1 && (a.D / a.G) % 64 != 0) shape = 4;
+        const int64_t tiles64 = ((int64_t)a.L + 63) / 64;
+        if ((ch / 64) * 10 >= slots * 6) shape = 3;
+        else if ((ch / 32) * 10 >= slots * 6) shape = 4;
+        else shape = tiles64 >= 512 ? 1 : tiles64 >= 32 ? 3 : 4;
+        // B, C per channel group: the tile must lie within one group
+        while (a.G > 1 && (a.D / a.G) % kShapes[shape].dt != 0 && shape != 4)
+            shape = shape == 1 ? 3 : 4;
     }
-    const int dt = shape == 1 ? 128 : shape == 4 ? 32 : 64;
+    const int dt = kShapes[shape].dt;
     if (a.G > 1 && (a.D / a.G) % dt != 0) return SS_OK;
+    const int mtps = debug_path(SS_DEBUG_SCAN_SEG_TILES) > 0 ? debug_path(SS_DEBUG_SCAN_SEG_TILES) : 2;
     *taken = true;
     switch (shape) {
-        case 1: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 2>(a, st, scratch)
-                          : run_seq<float, 1, 4, 2, 2>(a, st, scratch);
-        case 2: return bf ? run_seq<__nv_bfloat16, 1, 2, 2, 3>(a, st, scratch)
-                          : run_seq<float, 1, 2, 2, 3>(a, st, scratch);
-        case 3: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 3>(a, st, scratch)
-                          : run_seq<float, 2, 4, 2, 3>(a, st, scratch);
-        default: return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 3>(a, st, scratch)
-                           : run_seq<float, 4, 4, 3, 3>(a, st, scratch);
+        case 1: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3>(a, st, scratch, mtps)
+                          : run_seq<float, 1, 4, 2, 64, 3>(a, st, scratch, mtps);
+        case 2: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 128, 2>(a, st, scratch, mtps)
+                          : run_seq<float, 1, 4, 2, 128, 2>(a, st, scratch, mtps);
+        case 3: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3>(a, st, scratch, mtps)
+                          : run_seq<float, 2, 4, 2, 128, 3>(a, st, scratch, mtps);
+        case 4: return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3>(a, st, scratch, mtps)
+                          : run_seq<float, 4, 4, 3, 128, 3>(a, st, scratch, mtps);
+        case 5: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 64, 4>(a, st, scratch, mtps)
+                          : run_seq<float, 2, 4, 2, 64, 4>(a, st, scratch, mtps);
+        default: return bf ? run_seq<__nv_bfloat16, 1, 4, 3, 64, 3>(a, st, scratch, mtps)
+                           : run_seq<float, 1, 4, 3, 64, 3>(a, st, scratch, mtps);
     }
 }
 
