@@ -168,10 +168,16 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
  *   A_head, D  : (H)               f32
  *   B, C       : (Bsz, L, G, N)    dtype T, H % G == 0
  *   last_state : (Bsz, H, P, N)    f32
- * chunk must be one of 64, 128, 256.  N <= 256, P <= 256.  The tensor-core
- * path is compiled for bf16 with P = 64, N = 128, unit inner strides and
- * 16-byte aligned rows; everything else runs a general CUDA-core kernel.
- * Zero-size inputs return SS_OK without a launch.
+ * chunk must be one of 64, 128, 256 (else SS_ERR_INVALID_ARG), but it does
+ * not change the computation: the tensor-core kernels always work in blocks
+ * of 128 steps (the largest diagonal block whose C B^T tile and decay matrix
+ * fit one SM's tensor memory next to the state), and the CUDA-core kernel
+ * steps through time one step at a time.  The chunked form's result does not
+ * depend on the chunk length beyond rounding, so every accepted value gives
+ * the same result.  N <= 256, P <= 256.  The tensor-core path is compiled for
+ * bf16 with P = 64, N = 128, unit inner strides and 16-byte aligned rows
+ * (dt's t-stride a multiple of 8 elements); everything else runs the general
+ * CUDA-core kernel.  Zero-size inputs return SS_OK without a launch.
  */
 int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
@@ -226,9 +232,11 @@ int ss_conv_selective_scan_fwd(const ss_tensor* x, const ss_tensor* conv_weight,
  *     lets the copies run asynchronously, pageable memory works but the
  *     copies then block the calling thread;
  *   - every tensor must be contiguous (else SS_ERR_UNSUPPORTED).
- * The batch is cut into chunks of about 32 MB of inputs; chunks alternate
- * between `stream` and one library-owned side stream per device, so copies in,
- * scans and copies out of neighbouring chunks overlap.  All work is joined back
+ * The batch is cut into chunks of about 32 MB of inputs: whole batch rows, or,
+ * when one row holds more, blocks of that row's channels (whole channel groups
+ * when B, C are grouped; the row's B and C are copied once per buffer set);
+ * chunks alternate between `stream` and one library-owned side stream per
+ * device, so copies in, scans and copies out of neighbouring chunks overlap.  All work is joined back
  * into `stream` before the call returns (asynchronously: y and last_state
  * are valid once `stream` has completed, and the host buffers must stay
  * valid until then).  Device memory for the chunks is taken stream-ordered

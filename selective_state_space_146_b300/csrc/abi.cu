@@ -485,9 +485,10 @@ int ss_selective_scan_bwd_ckpt(const ss_tensor* u, const ss_tensor* delta, const
 
 // ---------------------------------------------------------------------------
 // Host buffers in and out: ss_selective_scan_fwd_host.  The batch is cut into
-// chunks of rows; chunks alternate between the caller's stream and one side
-// stream per device, so the copy in of one chunk overlaps the scan of the one
-// before and the copy out of the one before that.
+// chunks of rows, or of one row's channels when a row is large; chunks
+// alternate between the caller's stream and one side stream per device, so the
+// copy in of one chunk overlaps the scan of the one before and the copy out of
+// the one before that.
 
 static cudaStream_t g_side[kMaxDevices];
 
@@ -534,23 +535,38 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
 
     const int es = elem_size(u->dtype);
     const int64_t Bsz = a.Bsz, Dch = a.D, L = a.L, N = a.N, G = a.G > 1 ? a.G : 1;
-    const size_t act_row = (size_t)Dch * L * es;        // one batch row of u / delta / z / y
+    const size_t act_ch = (size_t)L * es;               // one channel of u / delta / z / y
+    const size_t act_row = (size_t)Dch * act_ch;        // one batch row of them
     const size_t bc_row = (size_t)G * N * L * es;       // one batch row of B or C
-    const size_t st_row = (size_t)Dch * N * sizeof(float);
+    const size_t st_ch = (size_t)N * sizeof(float);
     const size_t in_row = act_row * (z ? 3 : 2) + 2 * bc_row;
-    // about 32 MB of inputs per chunk, and at least two chunks when there are two rows
-    int64_t rows = std::max<int64_t>(1, (int64_t)((size_t(32) << 20) / std::max<size_t>(in_row, 1)));
-    if (Bsz >= 2) rows = std::min<int64_t>(rows, (Bsz + 1) / 2);
-    rows = std::min<int64_t>(rows, Bsz);
-    const int64_t nchunk = (Bsz + rows - 1) / rows;
+    // Chunks of about 32 MB of inputs: whole batch rows while a row is
+    // smaller (at least two chunks when there are two rows), else blocks of
+    // channels of one row (whole channel groups when B, C are grouped), so
+    // that even one long row overlaps its copies with the scan.
+    constexpr size_t kChunkBytes = size_t(32) << 20;
+    int64_t rows = 1, cd = Dch;
+    if (in_row <= kChunkBytes) {
+        rows = std::max<int64_t>(1, (int64_t)(kChunkBytes / std::max<size_t>(in_row, 1)));
+        if (Bsz >= 2) rows = std::min<int64_t>(rows, (Bsz + 1) / 2);
+        rows = std::min<int64_t>(rows, Bsz);
+    } else {
+        const int64_t gsz = Dch / G;  // channels per group (all of them when shared)
+        const int64_t unit = G > 1 ? gsz : 1;
+        cd = (int64_t)(kChunkBytes / (act_ch * (z ? 3 : 2)));
+        cd = std::max<int64_t>(unit, cd / unit * unit);
+        cd = std::min<int64_t>(cd, Dch);
+    }
+    const int64_t cblocks = (Dch + cd - 1) / cd;  // channel blocks per batch row
+    const int64_t nchunk = cd < Dch ? Bsz * cblocks : (Bsz + rows - 1) / rows;
     const int nset = nchunk > 1 ? 2 : 1;
 
     // device layout: A, D, bias once; then `nset` sets of chunk buffers
     const size_t szA = round256(numel(A) * sizeof(float));
     const size_t szD = D ? round256(Dch * sizeof(float)) : 0;
     const size_t szb = delta_bias ? round256(Dch * sizeof(float)) : 0;
-    const size_t cact = round256(act_row * rows), cbc = round256(bc_row * rows);
-    const size_t cst = last_state ? round256(st_row * rows) : 0;
+    const size_t cact = round256(act_ch * cd * rows), cbc = round256(bc_row * rows);
+    const size_t cst = last_state ? round256(st_ch * cd * rows) : 0;
     const size_t per_set = cact * (z ? 4 : 3) + 2 * cbc + cst;
     const size_t total = szA + szD + szb + per_set * nset;
     uint8_t* base = nullptr;
@@ -581,31 +597,60 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
                         cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess))
         rc = SS_ERR_CUDA;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    int64_t set_row[2] = {-1, -1};  // batch row whose B, C a set holds (channel blocks)
     for (int64_t i = 0; i < nchunk && rc == SS_OK; ++i) {
-        const int64_t b0 = i * rows, nb = std::min(rows, Bsz - b0);
+        // rows [b0, b0 + nb) of channels [d0, d0 + nd)
+        int64_t b0, nb, d0, nd;
+        if (cd < Dch) {
+            b0 = i / cblocks; nb = 1;
+            d0 = (i % cblocks) * cd; nd = std::min(cd, Dch - d0);
+        } else {
+            b0 = i * rows; nb = std::min(rows, Bsz - b0);
+            d0 = 0; nd = Dch;
+        }
+        const int si = (int)(i % nset);
         cudaStream_t st = (i % 2 == 0) ? s0 : s1;
-        uint8_t* set = base + szA + szD + szb + per_set * (i % nset);
+        uint8_t* set = base + szA + szD + szb + per_set * si;
         uint8_t *du = set, *ddl = set + cact, *dy = set + 2 * cact;
         uint8_t* dz = z ? set + 3 * cact : nullptr;
         uint8_t* dB = set + cact * (z ? 4 : 3);
         uint8_t* dC = dB + cbc;
         float* dlast = last_state ? reinterpret_cast<float*>(dC + cbc) : nullptr;
-        const size_t off_act = (size_t)b0 * act_row, off_bc = (size_t)b0 * bc_row;
-        H2D(du, static_cast<const uint8_t*>(u->data) + off_act, act_row * nb, st);
-        H2D(ddl, static_cast<const uint8_t*>(delta->data) + off_act, act_row * nb, st);
-        if (z) H2D(dz, static_cast<const uint8_t*>(z->data) + off_act, act_row * nb, st);
-        H2D(dB, static_cast<const uint8_t*>(B->data) + off_bc, bc_row * nb, st);
-        H2D(dC, static_cast<const uint8_t*>(C->data) + off_bc, bc_row * nb, st);
+        // inputs: rows (or one row's channel block) are contiguous in every tensor
+        const size_t off_act = ((size_t)b0 * Dch + d0) * act_ch, n_act = (size_t)nb * nd * act_ch;
+        H2D(du, static_cast<const uint8_t*>(u->data) + off_act, n_act, st);
+        H2D(ddl, static_cast<const uint8_t*>(delta->data) + off_act, n_act, st);
+        if (z) H2D(dz, static_cast<const uint8_t*>(z->data) + off_act, n_act, st);
+        if (cd == Dch || set_row[si] != b0) {  // a channel block reuses its row's B, C
+            H2D(dB, static_cast<const uint8_t*>(B->data) + (size_t)b0 * bc_row, bc_row * nb, st);
+            H2D(dC, static_cast<const uint8_t*>(C->data) + (size_t)b0 * bc_row, bc_row * nb, st);
+            set_row[si] = b0;
+        }
         if (rc != SS_OK) break;
         ScanArgs c = a;  // contiguous rows: the strides stay, the pointers move
         c.Bsz = (int)nb;
-        c.u = du; c.dl = ddl; c.z = dz; c.y = dy; c.Bm = dB; c.Cm = dC;
-        c.A = dA; c.Dv = dD; c.bias = dbias; c.last = dlast;
+        c.D = (int)nd;
+        c.u = du; c.dl = ddl; c.z = dz; c.y = dy;
+        c.A = dA + d0 * a.sA_d; c.Dv = dD ? dD + d0 * a.sD : nullptr;
+        c.bias = dbias ? dbias + d0 * a.sbias : nullptr; c.last = dlast;
+        if (G > 1) {  // the block's groups only
+            const int64_t gsz = Dch / G;
+            c.G = (int)(nd / gsz);
+            c.Bm = dB + (size_t)(d0 / gsz) * a.sB_g * es;
+            c.Cm = dC + (size_t)(d0 / gsz) * a.sC_g * es;
+            if (nb == 1) {  // one row: its groups are evenly spaced, as the TMA map expects
+                c.sB_b = c.G * a.sB_g;
+                c.sC_b = c.G * a.sC_g;
+            }
+        } else {
+            c.Bm = dB; c.Cm = dC;
+        }
         rc = launch_selective(c, st, sc);
         if (rc != SS_OK) break;
-        D2H(static_cast<uint8_t*>(y->data) + off_act, dy, act_row * nb, st);
+        D2H(static_cast<uint8_t*>(y->data) + off_act, dy, n_act, st);
         if (last_state)
-            D2H(static_cast<uint8_t*>(last_state->data) + (size_t)b0 * st_row, dlast, st_row * nb, st);
+            D2H(static_cast<uint8_t*>(last_state->data) + ((size_t)b0 * Dch + d0) * st_ch, dlast,
+                (size_t)nb * nd * st_ch, st);
     }
     // join the side stream back into the caller's stream, then free
     if (ev_end && (cudaEventRecord(ev_end, s1) != cudaSuccess ||

@@ -1,6 +1,7 @@
 """ss_selective_scan_fwd_host: host tensors in, host tensors out, the batch
-cut into chunks that overlap on two streams.  Compared with the fp64 oracle
-on the same inputs (GPU)."""
+cut into chunks that overlap on two streams (rows, or blocks of one row's
+channels when a row holds more than 32 MB of inputs).  Compared with the fp64
+oracle on the same inputs (GPU)."""
 import pytest
 import torch
 
@@ -74,3 +75,44 @@ def test_host_api_layer_shape_sampled(cuda_device):
     idx = torch.as_tensor(chans)
     check_close(to_np(y.reshape(total, cfg.seqlen)[idx]), yo, torch.bfloat16, "y (sampled)")
     check_close(to_np(s.reshape(total, cfg.d_state)[idx]), so, torch.bfloat16, "state (sampled)")
+
+
+@pytest.mark.parametrize("case", [(1, 600, 16384, "bf16", None, True),
+                                  (1, 512, 20000, "bf16", 4, True),
+                                  (1, 96, 50000, "f32", None, False)],
+                         ids=lambda c: "x".join(map(str, c[:5])))
+def test_host_api_channel_blocks(cuda_device, case):
+    """Rows of more than 32 MB of inputs: the call cuts each row into blocks of
+    channels (whole groups when B, C are grouped; a ragged last block), the
+    row's B, C copied once per buffer set.  Sampled channels against the
+    oracle."""
+    from tests.parity_util import oracle_selective_channels
+    Bsz, D, L, dt, G, gate = case
+    inp = inputs.selective_inputs(Bsz, D, 16, L, dt, groups=G, gate=gate, seed=L)
+    h = _pin(inp)
+    y, s = _abi.selective_scan_fwd_host(h["u"], h["delta"], h["A"], h["B"], h["C"], h["D"],
+                                        h["z"], h["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    total = Bsz * D
+    chans = inputs.sample_units(total, 10, seed=L)
+    if G:
+        sel = [int(c) for c in chans]
+        ys, ss = [], []
+        for c in sel:  # one channel with its group's B, C
+            b, d = divmod(c, D)
+            g = d // (D // G)
+            sub = {"u": inp["u"][b:b + 1, d:d + 1], "delta": inp["delta"][b:b + 1, d:d + 1],
+                   "z": None if inp["z"] is None else inp["z"][b:b + 1, d:d + 1],
+                   "A": inp["A"][d:d + 1], "B": inp["B"][b:b + 1, g], "C": inp["C"][b:b + 1, g],
+                   "D": inp["D"][d:d + 1], "delta_bias": inp["delta_bias"][d:d + 1]}
+            yo1, so1 = oracle.selective_scan(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"],
+                                             sub["D"], sub["z"], sub["delta_bias"])
+            ys.append(yo1[0, 0])
+            ss.append(so1[0, 0])
+        import numpy as np
+        yo, so = np.stack(ys), np.stack(ss)
+    else:
+        yo, so = oracle_selective_channels(inp, chans)
+    idx = torch.as_tensor([int(c) for c in chans])
+    check_close(to_np(y.reshape(total, L)[idx]), yo, _tdt(dt), "y (sampled)")
+    check_close(to_np(s.reshape(total, 16)[idx]), so, _tdt(dt), "state (sampled)")
