@@ -83,6 +83,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--probe-mufu", action="store_true",
                     help="print the measured ex2.approx rate (per SM per clock) and exit")
+    ap.add_argument("--probe-scan-forms", action="store_true",
+                    help="print the channel-steps/s of the sequential and the warp-shuffle "
+                         "scan forms on synthetic tiles and exit")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="run WORKLOAD's call warmup+steps times with no timing or output "
                          "(for ncu captures): a workload name, bwd_mamba130m_layer, "
@@ -1027,6 +1030,12 @@ def main_ours(args):
     pk = {"hbm": hbm_peak, "tf_burst": tf_peak, "tf_sust": tf_sust, "src": peak_src,
           "ex2_rate": ex2_rate, "sm_mhz": sm_mhz,
           "mufu": ex2_rate * N_SM * sm_mhz * 1e6 if ex2_rate else None}
+    if args.probe_scan_forms:
+        if rank == 0:
+            seq, shfl = abi.probe_scan_forms()
+            print(json.dumps({"seq_channel_steps_per_s": seq, "shfl_channel_steps_per_s": shfl,
+                              "seq_over_shfl": seq / shfl}))
+        return 0
     if args.probe_mufu:
         if rank == 0:
             print(json.dumps({"ex2_per_sm_per_clock": ex2_rate, "sms": N_SM, "sm_mhz": sm_mhz,

@@ -18,7 +18,7 @@
  *   ss_selective_scan_fwd_noalloc the selective scan with no allocation
  *   ss_status_string, ss_get_device_error, ss_launch_count, ss_version,
  *   ss_selftest_timeout,         status, errors and diagnostics
- *   ss_debug_set_path, ss_probe_ex2_rate
+ *   ss_debug_set_path, ss_probe_ex2_rate, ss_probe_scan_forms
  *
  * Every buffer is caller-owned device memory described by an ss_tensor
  * (pointer, dtype, shape, strides in elements).  The library keeps no pointer
@@ -426,6 +426,19 @@ int ss_debug_set_path(int which, int value);
  * SS_ERR_CUDA.
  */
 int ss_probe_ex2_rate(double* ex2_per_sm_per_clock, void* stream);
+
+/*
+ * Throughput probe of the two forms of the recurrence (page "Mamba模型笔记"
+ * §4.5: the selective scan as a parallel scan over (A_bar, B_bar u) pairs):
+ * on synthetic 32-step tiles of one channel with 16 states and a shared B | C
+ * table, `seq` steps one lane per channel through t with the states in
+ * registers (the form the scan kernels use); `shfl` gives each lane one step
+ * and composes the tile's 32 pairs with a five-level warp-shuffle scan per
+ * state, then applies the previous tile's carry and takes the readout.  Writes
+ * the channel-steps per second of each form.  Synchronises `stream`;
+ * allocates nothing.  Returns SS_OK, SS_ERR_INVALID_ARG or SS_ERR_CUDA.
+ */
+int ss_probe_scan_forms(double* seq_steps_per_s, double* shfl_steps_per_s, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ss_launch_count(void);

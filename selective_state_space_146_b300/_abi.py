@@ -26,7 +26,8 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_conv_selective_scan_fwd", "ss_selective_scan_bwd", "ss_selective_scan_fwd_host",
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version", "ss_selftest_timeout", "ss_selective_scan_fwd_ckpt",
-           "ss_selective_scan_bwd_ckpt", "ss_debug_set_path", "ss_probe_ex2_rate")
+           "ss_selective_scan_bwd_ckpt", "ss_debug_set_path", "ss_probe_ex2_rate",
+           "ss_probe_scan_forms")
 # Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
 DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
              grouped_path=6, fault_alloc=7, scan_seg_tiles=8)
@@ -97,6 +98,9 @@ def load(path: str | None = None):
     lib.ss_debug_set_path.restype = i
     lib.ss_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
     lib.ss_probe_ex2_rate.restype = i
+    lib.ss_probe_scan_forms.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_double), vp]
+    lib.ss_probe_scan_forms.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -393,3 +397,13 @@ def probe_ex2_rate(stream=None) -> float:
     if rc != 0:
         raise SSError(rc, "ss_probe_ex2_rate")
     return float(v.value)
+
+
+def probe_scan_forms(stream=None) -> tuple[float, float]:
+    """ss_probe_scan_forms: channel-steps per second of the sequential and the
+    warp-shuffle (associative) scan forms on synthetic tiles."""
+    a, b = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    rc = load().ss_probe_scan_forms(ctypes.byref(a), ctypes.byref(b), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_probe_scan_forms")
+    return float(a.value), float(b.value)

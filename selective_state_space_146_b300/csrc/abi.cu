@@ -860,6 +860,11 @@ int ss_probe_ex2_rate(double* ex2_per_sm_per_clock, void* stream) {
     return probe_ex2_rate(ex2_per_sm_per_clock, static_cast<cudaStream_t>(stream));
 }
 
+int ss_probe_scan_forms(double* seq_steps_per_s, double* shfl_steps_per_s, void* stream) {
+    if (!seq_steps_per_s || !shfl_steps_per_s) return SS_ERR_INVALID_ARG;
+    return probe_scan_forms(seq_steps_per_s, shfl_steps_per_s, static_cast<cudaStream_t>(stream));
+}
+
 uint64_t ss_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int ss_version(void) { return 300; }

@@ -135,6 +135,9 @@ int launch_selective_wide(const ScanArgs& a, cudaStream_t st, bool* taken);
 int launch_selftest_wait(unsigned limit_us, unsigned* err, cudaStream_t st);
 // ex2.approx.f32 operations per SM per clock (ss_probe_ex2_rate); synchronises st.
 int probe_ex2_rate(double* per_sm_clk, cudaStream_t st);
+// channel-steps per second of the sequential and the warp-shuffle scan forms
+// (ss_probe_scan_forms); synchronises st.
+int probe_scan_forms(double* seq_steps_per_s, double* shfl_steps_per_s, cudaStream_t st);
 int launch_selective_bwd(const BwdArgs& a, cudaStream_t st, const Scratch& scratch);
 int launch_selective_step(const StepArgs& a, cudaStream_t st);
 int launch_ssd_step(const SSDStepArgs& a, cudaStream_t st);
