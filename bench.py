@@ -90,7 +90,8 @@ def parse():
                     help="run WORKLOAD's call warmup+steps times with no timing or output "
                          "(for ncu captures): a workload name, bwd_mamba130m_layer, "
                          "conv_mamba130m_layer, per_channel_bc_mamba130m_layer, "
-                         "mamba130m_layer_N64 or decode_mamba2_ssd")
+                         "mamba130m_layer_N64, decode_mamba2_ssd, or WORKLOAD:L (a "
+                         "benchmark workload with sequence length L)")
     return ap.parse_args()
 
 
@@ -899,12 +900,17 @@ def main_profile(args):
             abi.ssd_state_update(state, x, dt, g["A_head"], Bt, Ct, g["D"])
         torch.cuda.synchronize()
         return 0 if abi.device_error() == 0 else 1
-    cfg = inputs.WORKLOADS[args.profile]
+    if ":" in args.profile:  # a benchmark workload with another sequence length
+        import dataclasses
+        name, _, length = args.profile.partition(":")
+        cfg = dataclasses.replace(inputs.WORKLOADS[name], seqlen=int(length))
+    else:
+        cfg = inputs.WORKLOADS[args.profile]
     with inputs.on_device(dev):
-        g = (inputs.workload_ssd_inputs(cfg) if args.profile == "mamba2_ssd"
+        g = (inputs.workload_ssd_inputs(cfg) if cfg.name == "mamba2_ssd"
              else inputs.workload_selective_inputs(cfg))
     for _ in range(args.warmup + args.steps):
-        if args.profile == "mamba2_ssd":
+        if cfg.name == "mamba2_ssd":
             abi.ssd_chunk_scan_fwd(g["x"], g["dt"], g["A_head"], g["B"], g["C"], g["D"],
                                    chunk=cfg.chunk, return_last_state=True)
         else:
