@@ -3,7 +3,8 @@ states drawn by hypothesis (derandomised, so every run draws the same
 examples), each compared with the fp64 oracle on the same seeded inputs.
 
 Covers every compute entry point: the selective scan (shared and grouped
-B, C, with and without an initial state), the fused conv + scan, the
+B, C, with and without an initial state; also with scan_seq forced to each
+launch shape and to random segment counts), the fused conv + scan, the
 backward, the SSD scan and both decode steps.  The sizes stay small so the
 oracle answers in milliseconds; they still cross tile and chunk edges.
 """
@@ -81,6 +82,39 @@ def test_fuzz_selective_scan(cuda_device, c):
     assert _abi.device_error() == 0
     yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
                                    inp["z"], inp["delta_bias"], softplus=c["sp"], h0=h0, nthreads=8)
+    check_close(to_np(y), yo, _tdt(c["dt"]), f"y {c}")
+    check_close(to_np(s), so, _tdt(c["dt"]), f"state {c}")
+
+
+@SETTINGS
+@given(c=st.fixed_dictionaries({
+    "Bsz": st.integers(1, 2), "D": st.integers(1, 300), "L": st.integers(1, 3000),
+    "dt": st.sampled_from(["f32", "bf16"]), "gate": st.booleans(), "h0": st.booleans(),
+    "shape": st.integers(1, 6), "segs": st.sampled_from([None, 1, 2, 3, 7, 40]),
+    "groups": st.sampled_from([None, None, 2]), "seed": st.integers(0, 10_000)}))
+def test_fuzz_scan_seq_shapes(cuda_device, c):
+    """scan_seq forced to every launch shape and to random segment counts
+    (summaries, the per-tile carry fold, ragged segments and channel tiles),
+    with and without an initial state, against the oracle.  Calls the
+    kernel does not take (rows not 16-byte multiples, groups not a multiple
+    of the channel tile) run the library's other kernels."""
+    G = c["groups"] if c["groups"] and c["D"] % 2 == 0 else None
+    inp = inputs.selective_inputs(c["Bsz"], c["D"], 16, c["L"], c["dt"], gate=c["gate"],
+                                  groups=G, seed=c["seed"])
+    h0 = (torch.randn(c["Bsz"], c["D"], 16, generator=torch.Generator().manual_seed(c["seed"]))
+          if c["h0"] else None)
+    dev = cuda_device
+    sw = dict(scan_path=2, scan_shape=c["shape"])
+    if c["segs"]:
+        sw["scan_segments"] = c["segs"]
+    with _abi.debug_paths(**sw):
+        y, s = _abi.selective_scan_fwd(*(_dev(inp[k], dev) for k in
+                                         ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")),
+                                       return_last_state=True, initial_state=_dev(h0, dev))
+        torch.cuda.synchronize()
+    assert _abi.device_error() == 0
+    yo, so = oracle.selective_scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], h0=h0, nthreads=8)
     check_close(to_np(y), yo, _tdt(c["dt"]), f"y {c}")
     check_close(to_np(s), so, _tdt(c["dt"]), f"state {c}")
 
