@@ -117,8 +117,8 @@ struct Scratch {
 };
 
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
-// scan_seq (N = 16, fast layouts, no conv, no checkpoints); *taken is false
-// when the call does not fit it.
+// scan_seq (N = 16, fast layouts, with or without the conv in front, no
+// checkpoints); *taken is false when the call does not fit it.
 int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken);
 // Unit t-stride, 16-byte aligned rows and strides, N = 16: the TMA kernels' layout.
 bool fast_layout_ok(const ScanArgs& a);

@@ -65,6 +65,12 @@ struct SeqParams {
     unsigned* ready;    // [ntile]: the tile's states h_1 .. h_{nseg-1} are stored
     unsigned* done;     // [ntile]: summaries of the tile finished so far
     unsigned* counter;  // next item number
+    // causal conv1d + SiLU in front of the scan (CONV kernels): the u tiles
+    // hold x and u = silu(bias + sum_k w[k] x[t - W + 1 + k]) is computed in fp32
+    const void* x; int64_t sx_b, sx_d;       // x rows contiguous in t
+    const float* cw; int64_t scw_d, scw_k;   // taps (D, W), W <= 4
+    const float* cb; int64_t scb;            // bias (D), may be null
+    int cwidth;
     int bc_groups;      // B, C groups per batch row (1: shared)
     int bc_dpg;         // channels per group, a multiple of the channel tile
     int softplus;
@@ -166,7 +172,7 @@ __device__ __forceinline__ float2 lds64f(uint32_t a) {
 }
 
 // One work item: SUMM is a segment summary, otherwise the scan proper.
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool SUMM>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, bool SUMM>
 __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensorMap* tm_dl,
                                          const CUtensorMap* tm_z, const CUtensorMap* tm_B,
                                          const CUtensorMap* tm_C, const SeqParams& p,
@@ -271,19 +277,63 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     float dsum = 0.f;  // sum of delta over the segment (summary)
     T* yrow = static_cast<T*>(p.y) + (int64_t)b * p.sy_b + (int64_t)(valid ? d : 0) * p.sy_d;
 
+    // conv in front (CONV): taps right-aligned, wk[3] multiplies x[t] and
+    // wk[4-W] x[t-W+1]; xc holds x at the three steps before the current tile
+    // (read from global memory at the start of a segment)
+    [[maybe_unused]] float wk[4] = {0.f, 0.f, 0.f, 0.f}, xc[3] = {0.f, 0.f, 0.f};
+    [[maybe_unused]] float cbias = 0.f;
+    if constexpr (CONV) {
+        if (valid) {
+            for (int k = 0; k < p.cwidth; ++k)
+                wk[4 - p.cwidth + k] = p.cw[(int64_t)d * p.scw_d + k * p.scw_k];
+            cbias = p.cb ? p.cb[(int64_t)d * p.scb] : 0.f;
+            const T* xr = static_cast<const T*>(p.x) + (int64_t)b * p.sx_b + (int64_t)d * p.sx_d;
+            for (int j = 0; j < 3; ++j) {
+                const int t = tbeg - 3 + j;
+                xc[j] = t >= 0 ? Elem<T>::to_f(xr[t]) : 0.f;
+            }
+        }
+    }
+    // x at tile-local step j of this lane's row (j >= -3; the carry before 0)
+    [[maybe_unused]] auto x_at = [&](uint32_t su, int j) -> float {
+        if (j < 0) return j == -3 ? xc[0] : (j == -2 ? xc[1] : xc[2]);
+        const uint32_t a = su + swz_rows<ROWB>(ci, j / VEC) + (j % VEC) * ES;
+        return ES == 2 ? __uint_as_float(lds16(a) << 16) : __uint_as_float(lds32(a));
+    };
+
     // The three parts of one 16-byte chunk (VEC steps) of this lane's channel:
     //   prep:   delta of the own K-slot (softplus), all-gathered in the lane
-    //           group; u of the chunk; du = delta * u;
+    //           group; u of the chunk (with the conv in front: u of the own
+    //           K-slot computed from x, all-gathered like delta); du = delta * u;
     //   core:   the recurrence over the chunk's steps (partial readouts);
     //   finish: reduce-scatter of the readouts, skip and gate, store of y.
     // A full tile runs the chunks in a short loop (unrolled by two with
     // several lanes per channel): the loop body stays in the instruction
     // cache, and with 16 states per lane a chunk alone has ample independent
-    // work.
-    auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* du, float* uf, auto tail) {
+    // work.  With the conv in front, prep is a long chain (x loads, the taps,
+    // SiLU, the all-gather), so the chunks run prep(c+1) | core(c) |
+    // finish(c-1) instead.
+    auto prep = [&](uint32_t su, int c, int tcount, float* dd, float* du, float* uf, float* uo,
+                    auto tail) {
         constexpr bool TAIL = decltype(tail)::value;
         const int off = swz_rows<ROWB>(ci, c);
-        lds_elems<T, VEC>(su + off, uf);
+        if constexpr (CONV) {
+            const int j0 = c * VEC + part * K;
+            float xw[K + 3];
+#pragma unroll
+            for (int m = 0; m < K + 3; ++m) xw[m] = x_at(su, j0 - 3 + m);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const float pre = fmaf(wk[0], xw[k], fmaf(wk[1], xw[k + 1],
+                                       fmaf(wk[2], xw[k + 2], fmaf(wk[3], xw[k + 3], cbias))));
+                uo[k] = pre * sigmoid_accurate(pre);
+            }
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                uf[j] = NSPLIT == 1 ? uo[j % K] : __shfl_sync(0xffffffffu, uo[j % K], gbase + j / K);
+        } else {
+            lds_elems<T, VEC>(su + off, uf);
+        }
         float dv[K];
         lds_elems<T, K>(su + Cfg::OFF_DL + off + part * K * ES, dv);
         softplus_vals<K>(dv, biasd, sp);
@@ -326,7 +376,8 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
             if constexpr (!SUMM) yv[i] = acc.x + acc.y;
         }
     };
-    auto finish = [&](uint32_t su, int tile_t0, int c, const float* yv, const float* uf, auto tail) {
+    auto finish = [&](uint32_t su, int tile_t0, int c, const float* yv, const float* uf,
+                      const float* uo, auto tail) {
         [[maybe_unused]] constexpr bool TAIL = decltype(tail)::value;
         if constexpr (!SUMM) {
             float yo[K];
@@ -342,9 +393,9 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
             }
             const int own = swz_rows<ROWB>(ci, c) + part * K * ES;
             float us[K];
-            if constexpr (NSPLIT == 1) {
+            if constexpr (NSPLIT == 1 || CONV) {
 #pragma unroll
-                for (int k = 0; k < K; ++k) us[k] = uf[k];
+                for (int k = 0; k < K; ++k) us[k] = NSPLIT == 1 ? uf[k] : uo[k];
             } else {
                 lds_elems<T, K>(su + own, us);
             }
@@ -378,32 +429,54 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     };
     auto full_tile = [&](uint32_t su, int tile_t0) {
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
-        float dd[VEC], du[VEC], uf[VEC], yv[VEC];
+        if constexpr (CONV) {
+            // prep(c+1) | core(c) | finish(c-1): the conv's chain of loads,
+            // FMAs and SiLU hides behind the recurrence of the chunk before
+            float ddA[VEC], duA[VEC], ufA[VEC], yA[VEC], uoA[K];
+            float ddB[VEC], duB[VEC], ufB[VEC], yB[VEC], uoB[K];
+            prep(su, 0, TT, ddA, duA, ufA, uoA, std::false_type{});
+            core(bcp, 0, ddA, duA, yA);
+            prep(su, 1, TT, ddB, duB, ufB, uoB, std::false_type{});
+#pragma unroll 1
+            for (int c = 1; c < Cfg::CHUNKS - 1; c += 2) {
+                core(bcp, c, ddB, duB, yB);
+                finish(su, tile_t0, c - 1, yA, ufA, uoA, std::false_type{});
+                prep(su, c + 1, TT, ddA, duA, ufA, uoA, std::false_type{});
+                core(bcp, c + 1, ddA, duA, yA);
+                finish(su, tile_t0, c, yB, ufB, uoB, std::false_type{});
+                prep(su, c + 2, TT, ddB, duB, ufB, uoB, std::false_type{});
+            }
+            core(bcp, Cfg::CHUNKS - 1, ddB, duB, yB);
+            finish(su, tile_t0, Cfg::CHUNKS - 2, yA, ufA, uoA, std::false_type{});
+            finish(su, tile_t0, Cfg::CHUNKS - 1, yB, ufB, uoB, std::false_type{});
+            return;
+        }
+        float dd[VEC], du[VEC], uf[VEC], yv[VEC], uo[K];
         if constexpr (NSPLIT == 1) {
 #pragma unroll 1
             for (int c = 0; c < Cfg::CHUNKS; ++c) {
-                prep(su, c, TT, dd, du, uf, std::false_type{});
+                prep(su, c, TT, dd, du, uf, uo, std::false_type{});
                 core(bcp, c, dd, du, yv);
-                finish(su, tile_t0, c, yv, uf, std::false_type{});
+                finish(su, tile_t0, c, yv, uf, uo, std::false_type{});
             }
         } else {
 #pragma unroll 2
             for (int c = 0; c < Cfg::CHUNKS; ++c) {
-                prep(su, c, TT, dd, du, uf, std::false_type{});
+                prep(su, c, TT, dd, du, uf, uo, std::false_type{});
                 core(bcp, c, dd, du, yv);
-                finish(su, tile_t0, c, yv, uf, std::false_type{});
+                finish(su, tile_t0, c, yv, uf, uo, std::false_type{});
             }
         }
     };
     auto tail_tile = [&](uint32_t su, int tile_t0, int tcount) {
         const uint32_t bcp = su + Cfg::OFF_BC + part * (NS / 2) * 16;
         const int nch = (tcount + VEC - 1) / VEC;
-        float dd[VEC], du[VEC], uf[VEC], yv[VEC];
+        float dd[VEC], du[VEC], uf[VEC], yv[VEC], uo[K];
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
-            prep(su, c, tcount, dd, du, uf, std::true_type{});
+            prep(su, c, tcount, dd, du, uf, uo, std::true_type{});
             core(bcp, c, dd, du, yv);
-            finish(su, tile_t0, c, yv, uf, std::true_type{});
+            finish(su, tile_t0, c, yv, uf, uo, std::true_type{});
         }
     };
 
@@ -420,6 +493,11 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
         const uint32_t su = smem_u32(stage(s));
         if (tcount == TT) full_tile(su, tile_t0);
         else tail_tile(su, tile_t0, tcount);
+        if constexpr (CONV) {
+            // the next tile's first steps look back at the last three of this one
+            const float x0 = x_at(su, TT - 3), x1 = x_at(su, TT - 2), x2 = x_at(su, TT - 1);
+            xc[0] = x0; xc[1] = x1; xc[2] = x2;
+        }
         mbar_arrive(&empty[s]);
     }
 
@@ -509,7 +587,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     }
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, int MINB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, int MINB>
 __global__ void __launch_bounds__(SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>::NTHREADS, MINB)
 scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -539,11 +617,11 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const int item = *s_item;
     const int S = p.nseg;
     if (S > 1 && item < p.ntile * (S - 1)) {  // summaries, tile by tile
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                          bars, item % (S - 1), item / (S - 1));
     } else {                                  // mains, tile by tile
         const int m = S > 1 ? item - p.ntile * (S - 1) : item;
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                           bars, m % S, m / S);
     }
 }
@@ -553,10 +631,10 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
 
 namespace {
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, int MINB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, int MINB>
 struct SeqKernel {
     using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
-    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, MINB>;
+    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, MINB>;
     // set the shared-memory attributes once per device; returns the resident
     // CTAs per SM (0 on failure)
     static int prepare() {
@@ -587,11 +665,11 @@ struct SeqKernel {
     }
 };
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, int ROWB, int MINB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, int ROWB, int MINB, bool CONV = false>
 static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch,
                    int min_tiles_per_seg) {
-    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, ROWB, MINB>;
-    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, ROWB, MINB>;
+    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, ROWB, CONV, MINB>;
+    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, ROWB, CONV, MINB>;
     using Cfg = typename KZ::Cfg;
     constexpr int TT = Cfg::TT, DT = Cfg::DT;
     const int occ = a.z ? KZ::prepare() : KN::prepare();
@@ -607,6 +685,9 @@ static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch,
     sp.h0 = a.h0; sp.sh_b = a.sh_b; sp.sh_d = a.sh_d; sp.sh_n = a.sh_n;
     sp.y = a.y; sp.sy_b = a.sy_b; sp.sy_d = a.sy_d;
     sp.softplus = a.softplus; sp.err = a.err;
+    sp.x = a.u; sp.sx_b = a.su_b; sp.sx_d = a.su_d;
+    sp.cw = a.cw; sp.scw_d = a.scw_d; sp.scw_k = a.scw_k; sp.cb = a.cb; sp.scb = a.scb;
+    sp.cwidth = a.cwidth;
     const bool grouped = a.G > 1;
     sp.bc_groups = grouped ? a.G : 1;
     sp.bc_dpg = grouped ? a.D / a.G : a.D;
@@ -711,7 +792,7 @@ constexpr int kNumShapes = 6;
 //     below; segments of at least two tiles.
 int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
-    if (a.N != 16 || a.cw || a.ckpt || a.L <= 0 || !fast_layout_ok(a)) return SS_OK;
+    if (a.N != 16 || a.ckpt || a.L <= 0 || !fast_layout_ok(a)) return SS_OK;
     const bool bf = a.dtype == SS_BF16;
     int shape = debug_path(SS_DEBUG_SCAN_SHAPE);
     if (shape < 1 || shape > kNumShapes) {
@@ -727,6 +808,19 @@ int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scra
     const int dt = kShapes[shape].dt;
     if (a.G > 1 && (a.D / a.G) % dt != 0) return SS_OK;
     const int mtps = debug_path(SS_DEBUG_SCAN_SEG_TILES) > 0 ? debug_path(SS_DEBUG_SCAN_SEG_TILES) : 2;
+    if (a.cw) {
+        // the fused conv: the library's three shapes (others go to scan_fast)
+        if (shape != 1 && shape != 3 && shape != 4) return SS_OK;
+        *taken = true;
+        if (shape == 1)
+            return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3, true>(a, st, scratch, mtps)
+                      : run_seq<float, 1, 4, 2, 64, 3, true>(a, st, scratch, mtps);
+        if (shape == 3)
+            return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps)
+                      : run_seq<float, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps);
+        return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps)
+                  : run_seq<float, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps);
+    }
     *taken = true;
     switch (shape) {
         case 1: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3>(a, st, scratch, mtps)

@@ -32,7 +32,8 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
-@pytest.mark.parametrize("path", [None, "general", "split1", "split2"])
+@pytest.mark.parametrize("path", [None, "general", "split1", "split2", "split4", "seq1", "seq3",
+                                  "seq4", "seq1s5", "seq3s3"])
 def test_conv_scan_small(cuda_device, case, path):
     with _abi.debug_paths(**scan_switches(path)):
         _conv_scan_small(cuda_device, case)
