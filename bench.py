@@ -951,7 +951,7 @@ def selective_kernel(cfg):
     elif (ch // 32) * 10 >= slots * 6:
         lanes = 4
     else:
-        lanes = 1 if tiles64 >= 512 else 2 if tiles64 >= 32 else 4
+        lanes = 1 if tiles64 >= 512 and ch > 64 else 2 if tiles64 >= 32 and ch > 32 else 4
     return f"scan_seq<{cfg.dtype}, {lanes} lane{'s' if lanes > 1 else ''}/channel>"
 
 

@@ -789,7 +789,8 @@ constexpr int kNumShapes = 6;
 //   - fewer channels, so the sequence is cut into segments: one lane per
 //     channel over 128 channels (shape 1) from 512 tiles of 64 steps (the
 //     long-context workload), two lanes (shape 3) from 32 tiles, four lanes
-//     below; segments of at least two tiles.
+//     below; no tile much wider than the channels (64 or fewer channels: two
+//     lanes, 32 or fewer: four); segments of at least two tiles.
 int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
     if (a.N != 16 || a.ckpt || a.L <= 0 || !fast_layout_ok(a)) return SS_OK;
@@ -800,7 +801,8 @@ int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scra
         const int64_t tiles64 = ((int64_t)a.L + 63) / 64;
         if ((ch / 64) * 10 >= slots * 6) shape = 3;
         else if ((ch / 32) * 10 >= slots * 6) shape = 4;
-        else shape = tiles64 >= 512 ? 1 : tiles64 >= 32 ? 3 : 4;
+        else if (tiles64 >= 512 && ch > 64) shape = 1;  // no tile wider than the channels
+        else shape = tiles64 >= 32 && ch > 32 ? 3 : 4;
         // B, C per channel group: the tile must lie within one group
         while (a.G > 1 && (a.D / a.G) % kShapes[shape].dt != 0 && shape != 4)
             shape = shape == 1 ? 3 : 4;
