@@ -762,9 +762,10 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
     const int split_req = debug_path(SS_DEBUG_SCAN_SPLIT);
     const int force = path == 0 ? 0 : (path == 1 ? split_req : -1);
     const bool bf = a.dtype == SS_BF16;
-    // scan_seq takes every d_state-16 call in the TMA layout except the
-    // checkpointing forward (scan_fast keeps it: its states are the backward's
-    // own, bit for bit)
+    // scan_seq takes every d_state-16 call in the TMA layout except small
+    // calls that need time segments (scan_fast's two launches are faster
+    // there) and the checkpointing forward (scan_fast keeps it: its states
+    // are the backward's own, bit for bit)
     if ((path == 2 || path < 0) && !a.ckpt && a.L > 0) {
         bool taken = false;
         const int rc = launch_selective_seq(a, st, scratch, &taken);

@@ -799,6 +799,14 @@ int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scra
     if (shape < 1 || shape > kNumShapes) {
         const int64_t ch = (int64_t)a.Bsz * a.D, slots = (int64_t)sm_count_current() * 3;
         const int64_t tiles64 = ((int64_t)a.L + 63) / 64;
+        const bool segmented = (ch / 32) * 10 < slots * 6;
+        // a segmented call of under 2^22 channel-steps has items of a few
+        // thousand channel-steps, whose fixed costs (the flag clear, the
+        // per-tile fold on the critical path) outweigh the one launch: the
+        // two-launch scan_fast is faster there (measured 0.038 against 0.052
+        // ms at 1 x 512 x 4096); the caller takes it when *taken stays false
+        if (segmented && ch * a.L < (int64_t(1) << 22) && debug_path(SS_DEBUG_SCAN_PATH) != 2)
+            return SS_OK;
         if ((ch / 64) * 10 >= slots * 6) shape = 3;
         else if ((ch / 32) * 10 >= slots * 6) shape = 4;
         else if (tiles64 >= 512 && ch > 64) shape = 1;  // no tile wider than the channels
