@@ -384,8 +384,10 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
  *                           1 scan_fast (lanes per channel from
  *                           SS_DEBUG_SCAN_SPLIT), 2 scan_seq
  *   SS_DEBUG_SCAN_SPLIT     scan_fast lanes per channel: 1, 2, 4 or 8
- *   SS_DEBUG_SCAN_SHAPE     scan_seq launch shape 1 .. 4 (lanes per channel
- *                           1, 1, 2, 4 over 128, 64, 64, 32 channels)
+ *   SS_DEBUG_SCAN_SHAPE     scan_seq launch shape 1 .. 7: lanes per channel
+ *                           and channels per CTA 1/128, 1/128, 2/64, 4/32,
+ *                           2/64, 1/128, 2/64 (tile rows, stages, CTAs per SM
+ *                           and the helper warp differ)
  *   SS_DEBUG_SCAN_SEGMENTS  scan_seq time segments (1 .. 128)
  *   SS_DEBUG_SCAN_SEG_TILES scan_seq shortest segment of its own choice, in tiles of t
  *   SS_DEBUG_SSD_PATH       SSD scan: 0 the CUDA-core kernel, 1 the tensor-core

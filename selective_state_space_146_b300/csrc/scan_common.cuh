@@ -80,10 +80,11 @@ __device__ __forceinline__ int swz(int r, int c) { return (r << 7) + ((c ^ (r & 
 // 2l, 2l+1 (bf16) or row l (fp32); the chunk order is rotated by lane so the
 // lanes of one store hit distinct banks.  Without C (summary pass) the C slots
 // hold zeros.
+// convert_bc_part does pass `it` of 8 (one chunk column per lane), so that
+// the passes can be split over several warps.
 template <typename T, bool WITH_C>
-__device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
+__device__ __forceinline__ void convert_bc_part(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane, int it) {
+    {
         const int j = (it + lane) & 7;
         const uint32_t rb = rawB + (2 * j) * 128, rc = rawC + (2 * j) * 128;
         if constexpr (sizeof(T) == 2) {
@@ -110,6 +111,12 @@ __device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_
     }
 }
 
+template <typename T, bool WITH_C>
+__device__ __forceinline__ void convert_bc(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) convert_bc_part<T, WITH_C>(rawB, rawC, bc, lane, it);
+}
+
 // Byte offset of 16-byte chunk c of row r in a tile of ROWB-byte rows with
 // the ROWB-byte TMA swizzle: within each 1024-byte (128-byte rows) or
 // 512-byte (64-byte rows) atom, the chunk index is XORed with the row index
@@ -124,12 +131,11 @@ __device__ __forceinline__ int swz_rows(int r, int c) {
 
 // convert_bc for raw tiles of 64-byte rows (32 bf16 or 16 fp32 steps): lanes
 // 0..15 write the state pairs 0..3 of their step pair (bf16) or step (fp32),
-// lanes 16..31 the pairs 4..7, chunk order rotated by lane.
+// lanes 16..31 the pairs 4..7, chunk order rotated by lane; pass `it` of 4.
 template <typename T, bool WITH_C>
-__device__ __forceinline__ void convert_bc64(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+__device__ __forceinline__ void convert_bc64_part(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane, int it) {
     const int w = lane & 15, half = lane >> 4;
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    {
         const int j = 4 * half + ((it + w) & 3);
         const uint32_t rb = rawB + (2 * j) * 64, rc = rawC + (2 * j) * 64;
         if constexpr (sizeof(T) == 2) {
@@ -155,6 +161,12 @@ __device__ __forceinline__ void convert_bc64(uint32_t rawB, uint32_t rawC, uint3
             sts128f(bc + w * 128 + j * 16, v);
         }
     }
+}
+
+template <typename T, bool WITH_C>
+__device__ __forceinline__ void convert_bc64(uint32_t rawB, uint32_t rawC, uint32_t bc, int lane) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) convert_bc64_part<T, WITH_C>(rawB, rawC, bc, lane, it);
 }
 
 // Store K floats as T to global memory: one aligned vector store, or (in the

@@ -77,7 +77,7 @@ struct SeqParams {
     unsigned* err;
 };
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool HELPER>
 struct SeqCfg {
     static constexpr int N = 16;
     static constexpr int ES = sizeof(T);
@@ -89,7 +89,10 @@ struct SeqCfg {
     static constexpr int NS = N / NSPLIT;        // states per lane
     static constexpr int K = VEC / NSPLIT;       // steps of a chunk whose y a lane owns
     static constexpr int NCONS = CWARPS * 32;
-    static constexpr int NTHREADS = NCONS + 32;  // + the TMA / table warp
+    // + the TMA / table warp (HELPER), else the consumers take its work in turn
+    static constexpr int NTHREADS = NCONS + (HELPER ? 32 : 0);
+    static constexpr int WARP0 = HELPER ? 1 : 0;    // first consumer warp
+    static constexpr int LEAD = WARP0 * 32;         // the consumer thread that waits and signals
     static constexpr int TILE_BYTES = DT * ROWB;  // one [DT][TT] tile of u, delta, z
     static constexpr int RAW_BYTES = N * ROWB;    // one [N][TT] tile of B or C as loaded
     static constexpr int BC_BYTES = TT * 2 * N * 4;
@@ -172,19 +175,19 @@ __device__ __forceinline__ float2 lds64f(uint32_t a) {
 }
 
 // One work item: SUMM is a segment summary, otherwise the scan proper.
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, bool SUMM>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool HELPER, bool CONV, bool SUMM>
 __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensorMap* tm_dl,
                                          const CUtensorMap* tm_z, const CUtensorMap* tm_B,
                                          const CUtensorMap* tm_C, const SeqParams& p,
                                          uint8_t* smem, uint64_t* bars, int seg, int tile) {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER>;
     constexpr int N = Cfg::N, TT = Cfg::TT, VEC = Cfg::VEC, NS = Cfg::NS, DT = Cfg::DT;
     constexpr int ES = Cfg::ES, K = Cfg::K;
     constexpr bool LOAD_Z = HAS_Z && !SUMM;
     uint64_t* full = bars;                // u / delta / z landed
     uint64_t* raw = bars + STAGES;        // raw B / C landed
-    uint64_t* table = bars + 2 * STAGES;  // fp32 B|C table written
-    uint64_t* empty = bars + 3 * STAGES;  // consumers done with the stage
+    uint64_t* table = bars + 2 * STAGES;  // fp32 B|C table written (HELPER)
+    uint64_t* empty = bars + 3 * STAGES;  // consumers done with the stage (HELPER)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = tile / p.dtiles;
@@ -194,23 +197,25 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     const int ntiles = (tend - tbeg + TT - 1) / TT;
     auto stage = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
 
-    if (warp == 0) {
-        // ---------------- TMA loads (lane 0) and the B|C table (all lanes) ----------------
-        const int bc_row = b * p.bc_groups + d0 / p.bc_dpg;
-        auto issue = [&](int k) {
-            const int s = k % STAGES;
-            const int t0 = tbeg + k * TT;
-            uint8_t* st = stage(s);
-            mbar_arrive_expect_tx(&raw[s], Cfg::RAW_BYTES * (SUMM ? 1 : 2));
-            tma_load_3d(st + Cfg::OFF_RAWB, tm_B, &raw[s], t0, 0, bc_row);
-            if (!SUMM) tma_load_3d(st + Cfg::OFF_RAWC, tm_C, &raw[s], t0, 0, bc_row);
-            mbar_arrive_expect_tx(&full[s], Cfg::TILE_BYTES * (LOAD_Z ? 3 : 2));
-            tma_load_3d(st, tm_u, &full[s], t0, d0, b);
-            tma_load_3d(st + Cfg::OFF_DL, tm_dl, &full[s], t0, d0, b);
-            if (LOAD_Z) tma_load_3d(st + Cfg::OFF_Z, tm_z, &full[s], t0, d0, b);
-        };
-        if (lane == 0)
-            for (int k = 0; k < STAGES && k < ntiles; ++k) issue(k);
+    // TMA loads of tile k of the segment into stage k % STAGES (one thread)
+    const int bc_row = b * p.bc_groups + d0 / p.bc_dpg;
+    auto issue = [&](int k) {
+        const int s = k % STAGES;
+        const int t0 = tbeg + k * TT;
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx(&raw[s], Cfg::RAW_BYTES * (SUMM ? 1 : 2));
+        tma_load_3d(st + Cfg::OFF_RAWB, tm_B, &raw[s], t0, 0, bc_row);
+        if (!SUMM) tma_load_3d(st + Cfg::OFF_RAWC, tm_C, &raw[s], t0, 0, bc_row);
+        mbar_arrive_expect_tx(&full[s], Cfg::TILE_BYTES * (LOAD_Z ? 3 : 2));
+        tma_load_3d(st, tm_u, &full[s], t0, d0, b);
+        tma_load_3d(st + Cfg::OFF_DL, tm_dl, &full[s], t0, d0, b);
+        if (LOAD_Z) tma_load_3d(st + Cfg::OFF_Z, tm_z, &full[s], t0, d0, b);
+    };
+    if (threadIdx.x == 0)
+        for (int k = 0; k < STAGES && k < ntiles; ++k) issue(k);
+
+    if (HELPER && warp == 0) {
+        // ---------------- the B|C table (all lanes) and the later loads (lane 0) ----------------
         for (int k = 0; k < ntiles; ++k) {
             const int s = k % STAGES;
             if (!__all_sync(0xffffffffu, mbar_wait(&raw[s], (k / STAGES) & 1, p.err))) break;
@@ -235,7 +240,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     // NSPLIT consecutive lanes share one channel; lane `part` keeps states
     // [part*NS, part*NS + NS), computes delta for its K-slot of every chunk and
     // owns the outputs of that slot.
-    const int ci = (warp - 1) * Cfg::CPW + lane / NSPLIT;
+    const int ci = (warp - Cfg::WARP0) * Cfg::CPW + lane / NSPLIT;
     const int part = lane % NSPLIT;
     const int gbase = lane - part;
     const int d = d0 + ci;
@@ -263,7 +268,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
         // the state entering this segment, stored by the tile's fold: one
         // thread waits for the flag (acquire), the consumers meet at a named
         // barrier, and every lane reads its state from L2, not this SM's L1
-        if (threadIdx.x == 32) wait_flag(p.ready + tile, p.err);
+        if (threadIdx.x == Cfg::LEAD) wait_flag(p.ready + tile, p.err);
         named_sync(1, Cfg::NCONS);
         __threadfence();
         if (valid) {
@@ -483,10 +488,33 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     bool ok = true;
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % STAGES;
-        if (!mbar_wait(&full[s], (k / STAGES) & 1, p.err) ||
-            !mbar_wait(&table[s], (k / STAGES) & 1, p.err)) {
-            ok = false;
-            break;
+        if constexpr (HELPER) {
+            if (!mbar_wait(&full[s], (k / STAGES) & 1, p.err) ||
+                !mbar_wait(&table[s], (k / STAGES) & 1, p.err)) {
+                ok = false;
+                break;
+            }
+        } else {
+            // no helper warp: the consumers build the B|C table, a share of
+            // the passes per warp, and meet; past that barrier every thread
+            // is done with tile k - 1, whose stage then takes tile k - 1 + STAGES
+            const bool got = mbar_wait(&full[s], (k / STAGES) & 1, p.err) &&
+                             mbar_wait(&raw[s], (k / STAGES) & 1, p.err);
+            if (!__syncthreads_and(got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t st = smem_u32(stage(s));
+            constexpr int PASSES = ROWB == 128 ? 8 : 4;
+#pragma unroll
+            for (int it = warp; it < PASSES; it += CWARPS) {
+                if constexpr (ROWB == 128)
+                    convert_bc_part<T, !SUMM>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC, lane, it);
+                else
+                    convert_bc64_part<T, !SUMM>(st + Cfg::OFF_RAWB, st + Cfg::OFF_RAWC, st + Cfg::OFF_BC, lane, it);
+            }
+            __syncthreads();
+            if (threadIdx.x == 0 && k >= 1 && k - 1 + STAGES < ntiles) issue(k - 1 + STAGES);
         }
         const int tile_t0 = tbeg + k * TT;
         const int tcount = min(TT, tend - tile_t0);
@@ -498,7 +526,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
             const float x0 = x_at(su, TT - 3), x1 = x_at(su, TT - 2), x2 = x_at(su, TT - 1);
             xc[0] = x0; xc[1] = x1; xc[2] = x2;
         }
-        mbar_arrive(&empty[s]);
+        if constexpr (HELPER) mbar_arrive(&empty[s]);
     }
 
     if constexpr (SUMM) {
@@ -517,7 +545,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
         // summary in; the tile's last one folds them all
         int* s_last = reinterpret_cast<int*>(bars + 4 * STAGES) + 1;
         named_sync(1, Cfg::NCONS);
-        if (threadIdx.x == 32) {
+        if (threadIdx.x == Cfg::LEAD) {
             __threadfence();
             *s_last = atomicAdd(p.done + tile, 1u) == (unsigned)(p.nseg - 2);
         }
@@ -532,7 +560,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
             constexpr int CPP = Cfg::NCONS / 16;  // channels per pass
             constexpr int PASSES = DT / CPP;      // (channel, state) pairs per thread
             constexpr int BATCH = PASSES >= 16 ? 1 : 16 / PASSES;
-            const int tc = threadIdx.x - 32, n = tc & 15;
+            const int tc = threadIdx.x - Cfg::LEAD, n = tc & 15;
             const int64_t bd0 = (int64_t)b * p.D + d0;
             float hp[PASSES];
 #pragma unroll
@@ -568,7 +596,7 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
                 }
             }
             named_sync(1, Cfg::NCONS);
-            if (threadIdx.x == 32) {
+            if (threadIdx.x == Cfg::LEAD) {
                 __threadfence();
                 asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ready + tile), "r"(1u)
                              : "memory");
@@ -587,12 +615,12 @@ __device__ __forceinline__ void seq_item(const CUtensorMap* tm_u, const CUtensor
     }
 }
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, int MINB>
-__global__ void __launch_bounds__(SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>::NTHREADS, MINB)
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool HELPER, bool CONV, int MINB>
+__global__ void __launch_bounds__(SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER>::NTHREADS, MINB)
 scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
          const __grid_constant__ CUtensorMap tm_C, const SeqParams p) {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::STAGE_BYTES * STAGES);
@@ -617,11 +645,11 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const int item = *s_item;
     const int S = p.nseg;
     if (S > 1 && item < p.ntile * (S - 1)) {  // summaries, tile by tile
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER, CONV, true>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                          bars, item % (S - 1), item / (S - 1));
     } else {                                  // mains, tile by tile
         const int m = S > 1 ? item - p.ntile * (S - 1) : item;
-        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
+        seq_item<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER, CONV, false>(&tm_u, &tm_dl, &tm_z, &tm_B, &tm_C, p, smem,
                                                           bars, m % S, m / S);
     }
 }
@@ -631,10 +659,10 @@ scan_seq(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
 
 namespace {
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool CONV, int MINB>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, bool HAS_Z, int ROWB, bool HELPER, bool CONV, int MINB>
 struct SeqKernel {
-    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB>;
-    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, CONV, MINB>;
+    using Cfg = SeqCfg<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER>;
+    static constexpr auto fn = scan_seq<T, NSPLIT, CWARPS, STAGES, HAS_Z, ROWB, HELPER, CONV, MINB>;
     // set the shared-memory attributes once per device; returns the resident
     // CTAs per SM (0 on failure)
     static int prepare() {
@@ -665,11 +693,11 @@ struct SeqKernel {
     }
 };
 
-template <typename T, int NSPLIT, int CWARPS, int STAGES, int ROWB, int MINB, bool CONV = false>
+template <typename T, int NSPLIT, int CWARPS, int STAGES, int ROWB, int MINB, bool HELPER, bool CONV = false>
 static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch,
                    int min_tiles_per_seg) {
-    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, ROWB, CONV, MINB>;
-    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, ROWB, CONV, MINB>;
+    using KZ = SeqKernel<T, NSPLIT, CWARPS, STAGES, true, ROWB, HELPER, CONV, MINB>;
+    using KN = SeqKernel<T, NSPLIT, CWARPS, STAGES, false, ROWB, HELPER, CONV, MINB>;
     using Cfg = typename KZ::Cfg;
     constexpr int TT = Cfg::TT, DT = Cfg::DT;
     const int occ = a.z ? KZ::prepare() : KN::prepare();
@@ -764,33 +792,40 @@ static int run_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch,
 
 // Launch shapes by code (SS_DEBUG_SCAN_SHAPE): lanes per channel, consumer
 // warps (channels per CTA), stages, row bytes of t per tile, CTAs per SM the
-// launch bounds aim at.
+// launch bounds aim at, and whether a helper warp builds the B|C table and
+// issues the loads (else the consumers do, in step with each other).
 struct SeqShape {
     int nsplit, dt;
 };
 static constexpr SeqShape kShapes[] = {
     {0, 0},
-    {1, 128},  // 1: one lane, 4 warps (128 channels), 2 stages, 64-byte rows, 3 per SM
-    {1, 128},  // 2: one lane, 4 warps, 2 stages, 128-byte rows, 2 per SM
-    {2, 64},   // 3: two lanes, 4 warps (64 channels), 2 stages, 128-byte rows, 3 per SM
-    {4, 32},   // 4: four lanes, 4 warps (32 channels), 3 stages, 128-byte rows, 3 per SM
-    {2, 64},   // 5: two lanes, 4 warps, 2 stages, 64-byte rows, 4 per SM
-    {1, 128},  // 6: one lane, 4 warps, 3 stages, 64-byte rows, 3 per SM
+    {1, 128},  // 1: one lane, 4 warps (128 channels), 2 stages, 64-byte rows, 4 per SM, no helper
+    {1, 128},  // 2: one lane, 4 warps, 2 stages, 128-byte rows, 2 per SM, helper
+    {2, 64},   // 3: two lanes, 4 warps (64 channels), 2 stages, 128-byte rows, 3 per SM, no helper
+    {4, 32},   // 4: four lanes, 4 warps (32 channels), 3 stages, 128-byte rows, 3 per SM, helper
+    {2, 64},   // 5: two lanes, 4 warps, 2 stages, 64-byte rows, 4 per SM, helper
+    {1, 128},  // 6: one lane, 4 warps, 3 stages, 64-byte rows, 3 per SM, helper
+    {2, 64},   // 7: shape 3 with the helper warp
 };
-constexpr int kNumShapes = 6;
+constexpr int kNumShapes = 7;
 
 //
 // The library's choice (measured on the B300, d_state 16):
 //   - enough channels for the 64-channel tiles of two lanes per channel
 //     (shape 3) to fill 60% of the 3 x SM CTA slots: shape 3, no segments
-//     (the Mamba-2.8B layer, 4 x 5120 channels);
+//     (the Mamba-2.8B layer, 4 x 5120 channels; without the helper warp
+//     0.920 ms, with it 0.949 ms);
 //   - enough for the 32-channel tiles of four lanes (shape 4): shape 4, no
-//     segments (the Mamba-130M layer, 8 x 1536 channels);
+//     segments (the Mamba-130M layer, 8 x 1536 channels; here the helper
+//     warp's overlap of the table build with the scan wins by 1%);
 //   - fewer channels, so the sequence is cut into segments: one lane per
-//     channel over 128 channels (shape 1) from 512 tiles of 64 steps (the
-//     long-context workload), two lanes (shape 3) from 32 tiles, four lanes
-//     below; no tile much wider than the channels (64 or fewer channels: two
-//     lanes, 32 or fewer: four); segments of at least two tiles.
+//     channel over 128 channels (shape 1, 4 CTAs/SM without the helper warp:
+//     3.05 against 3.24 ms with it) from 512 tiles of 64 steps (the
+//     long-context workload), two lanes from 32 tiles (shape 7: the helper
+//     warp, whose overlap counts in items of a few tiles; without it
+//     1 x 2048 x 4096 took 0.099 against 0.078 ms), four lanes below; no tile
+//     much wider than the channels (64 or fewer channels: two lanes, 32 or
+//     fewer: four); segments of at least two tiles.
 int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
     if (a.N != 16 || a.ckpt || a.L <= 0 || !fast_layout_ok(a)) return SS_OK;
@@ -810,41 +845,45 @@ int launch_selective_seq(const ScanArgs& a, cudaStream_t st, const Scratch& scra
         if ((ch / 64) * 10 >= slots * 6) shape = 3;
         else if ((ch / 32) * 10 >= slots * 6) shape = 4;
         else if (tiles64 >= 512 && ch > 64) shape = 1;  // no tile wider than the channels
-        else shape = tiles64 >= 32 && ch > 32 ? 3 : 4;
+        else shape = tiles64 >= 32 && ch > 32 ? 7 : 4;
         // B, C per channel group: the tile must lie within one group
         while (a.G > 1 && (a.D / a.G) % kShapes[shape].dt != 0 && shape != 4)
-            shape = shape == 1 ? 3 : 4;
+            shape = shape == 1 ? 7 : 4;
     }
     const int dt = kShapes[shape].dt;
     if (a.G > 1 && (a.D / a.G) % dt != 0) return SS_OK;
     const int mtps = debug_path(SS_DEBUG_SCAN_SEG_TILES) > 0 ? debug_path(SS_DEBUG_SCAN_SEG_TILES) : 2;
     if (a.cw) {
-        // the fused conv: the library's three shapes (others go to scan_fast)
+        // the fused conv: the library's shapes, all with the helper warp
+        // (others go to scan_fast)
+        if (shape == 7) shape = 3;
         if (shape != 1 && shape != 3 && shape != 4) return SS_OK;
         *taken = true;
         if (shape == 1)
-            return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3, true>(a, st, scratch, mtps)
-                      : run_seq<float, 1, 4, 2, 64, 3, true>(a, st, scratch, mtps);
+            return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3, true, true>(a, st, scratch, mtps)
+                      : run_seq<float, 1, 4, 2, 64, 3, true, true>(a, st, scratch, mtps);
         if (shape == 3)
-            return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps)
-                      : run_seq<float, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps);
-        return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps)
-                  : run_seq<float, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps);
+            return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3, true, true>(a, st, scratch, mtps)
+                      : run_seq<float, 2, 4, 2, 128, 3, true, true>(a, st, scratch, mtps);
+        return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3, true, true>(a, st, scratch, mtps)
+                  : run_seq<float, 4, 4, 3, 128, 3, true, true>(a, st, scratch, mtps);
     }
     *taken = true;
     switch (shape) {
-        case 1: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 3>(a, st, scratch, mtps)
-                          : run_seq<float, 1, 4, 2, 64, 3>(a, st, scratch, mtps);
-        case 2: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 128, 2>(a, st, scratch, mtps)
-                          : run_seq<float, 1, 4, 2, 128, 2>(a, st, scratch, mtps);
-        case 3: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3>(a, st, scratch, mtps)
-                          : run_seq<float, 2, 4, 2, 128, 3>(a, st, scratch, mtps);
-        case 4: return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3>(a, st, scratch, mtps)
-                          : run_seq<float, 4, 4, 3, 128, 3>(a, st, scratch, mtps);
-        case 5: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 64, 4>(a, st, scratch, mtps)
-                          : run_seq<float, 2, 4, 2, 64, 4>(a, st, scratch, mtps);
-        default: return bf ? run_seq<__nv_bfloat16, 1, 4, 3, 64, 3>(a, st, scratch, mtps)
-                           : run_seq<float, 1, 4, 3, 64, 3>(a, st, scratch, mtps);
+        case 1: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 64, 4, false>(a, st, scratch, mtps)
+                          : run_seq<float, 1, 4, 2, 64, 4, false>(a, st, scratch, mtps);
+        case 2: return bf ? run_seq<__nv_bfloat16, 1, 4, 2, 128, 2, true>(a, st, scratch, mtps)
+                          : run_seq<float, 1, 4, 2, 128, 2, true>(a, st, scratch, mtps);
+        case 3: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3, false>(a, st, scratch, mtps)
+                          : run_seq<float, 2, 4, 2, 128, 3, false>(a, st, scratch, mtps);
+        case 4: return bf ? run_seq<__nv_bfloat16, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps)
+                          : run_seq<float, 4, 4, 3, 128, 3, true>(a, st, scratch, mtps);
+        case 5: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 64, 4, true>(a, st, scratch, mtps)
+                          : run_seq<float, 2, 4, 2, 64, 4, true>(a, st, scratch, mtps);
+        case 7: return bf ? run_seq<__nv_bfloat16, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps)
+                          : run_seq<float, 2, 4, 2, 128, 3, true>(a, st, scratch, mtps);
+        default: return bf ? run_seq<__nv_bfloat16, 1, 4, 3, 64, 3, true>(a, st, scratch, mtps)
+                           : run_seq<float, 1, 4, 3, 64, 3, true>(a, st, scratch, mtps);
     }
 }
 

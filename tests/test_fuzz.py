@@ -90,7 +90,7 @@ def test_fuzz_selective_scan(cuda_device, c):
 @given(c=st.fixed_dictionaries({
     "Bsz": st.integers(1, 2), "D": st.integers(1, 300), "L": st.integers(1, 3000),
     "dt": st.sampled_from(["f32", "bf16"]), "gate": st.booleans(), "h0": st.booleans(),
-    "shape": st.integers(1, 6), "segs": st.sampled_from([None, 1, 2, 3, 7, 40]),
+    "shape": st.integers(1, 7), "segs": st.sampled_from([None, 1, 2, 3, 7, 40]),
     "groups": st.sampled_from([None, None, 2]), "seed": st.integers(0, 10_000)}))
 def test_fuzz_scan_seq_shapes(cuda_device, c):
     """scan_seq forced to every launch shape and to random segment counts

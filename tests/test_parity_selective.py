@@ -26,7 +26,7 @@ def scan_path(request):
 # every selective-scan kernel for N = 16: the general one, scan_fast with each
 # lane split, scan_seq with each launch shape (and forced time segments)
 PATHS = [None, "general", "split1", "split2", "split4", "split8", "seq1", "seq2", "seq3", "seq4",
-         "seq5", "seq6", "seq1s5", "seq3s7", "seq4s3"]
+         "seq5", "seq6", "seq7", "seq1s5", "seq3s7", "seq7s5", "seq4s3"]
 
 
 def _run(inp, dev, softplus=True, want_state=True):
