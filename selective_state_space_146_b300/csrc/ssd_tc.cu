@@ -407,19 +407,45 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 // Two heads of one group per CTA (one CTA per SM, all 512 TMEM columns).
 //
 // Same algebra as ssd_chunk_tc.  C B^T is shared by the heads of a group, so
-// it is loaded and computed once for the pair; each head has its own Ydiag,
-// Yoff and dS^T columns, so C B^T of the next block can be issued as soon as
-// its B, C have landed, while both heads still finish the current block's
-// epilogue, and C S^T is issued per head as soon as that head's state copy is
-// written.  TMEM: C B^T [0, 128); head hh: Ydiag 128 + 192 hh, Yoff 192 + 192 hh,
-// dS^T 256 + 192 hh.  Warps 0-3 compute head 0, warps 4-7 head 1 (warp w
-// reads TMEM lanes 32 (w % 4) ..), warp 8 issues TMA loads and MMAs.
+// it is loaded and computed once for the pair.  Warps 0-3 compute head 0,
+// warps 4-7 head 1 (warp w reads TMEM lanes 32 (w % 4) ..), warp 8 issues TMA
+// loads and MMAs.  Differences from the one-head kernel:
+//  * M stays in tensor memory: each thread writes its row of M (bf16, two per
+//    32-bit column) into its head's dS^T columns, which are free from the
+//    head's state update of the previous block until this block's B^T X~, and
+//    M X reads its A operand from there (tcgen05.mma with A in TMEM).  B^T X~
+//    of both heads is issued once both M X are done.  Shared memory holds no
+//    M, which leaves room for two B buffers: B of block k+2 loads as soon as
+//    B^T X~ of block k has read its buffer, so C B^T of block k+1 never waits
+//    for B and runs under the epilogue.
+//  * B, C, dt and x of the next block are prefetched into L2 at the top of
+//    each block.
+//  * Every compute warp forms the head's whole cumulative decay itself, so
+//    the cumulative sum needs no barrier between the head's warps; it runs
+//    while M X and B^T X~ do if the next block's dt has landed, else after the
+//    state update.
 namespace ssdtc2 {
 
 // Prefetch a tile of a 4-D tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
                  ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return r != 0;
 }
 
 using ssdtc::N;
@@ -433,16 +459,14 @@ constexpr int NHEAD = 2;
 constexpr int NCOMP = 128 * NHEAD;
 constexpr int NTHREADS = NCOMP + 32;
 constexpr int OFF_X = 0;                  // NHEAD x [128 t][64 p] bf16            32 KB
-constexpr int OFF_B = OFF_X + 32768;      // 2 x [128 t][64 n]                     32 KB
-constexpr int OFF_C = OFF_B + 32768;      // 2 x [128 t][64 n]                     32 KB
-constexpr int OFF_M = OFF_C + 32768;      // NHEAD x M (K-major, two 64-col halves) 64 KB
-constexpr int OFF_S = OFF_M + 65536;      // NHEAD x (X~, then the S^T copy)       32 KB
+constexpr int OFF_B = OFF_X + 32768;      // 2 blocks x 2 x [128 t][64 n]          64 KB
+constexpr int OFF_C = OFF_B + 65536;      // 2 x [128 t][64 n]                     32 KB
+constexpr int OFF_S = OFF_C + 32768;      // NHEAD x (X~, then the S^T copy)       32 KB
 constexpr int OFF_DT = OFF_S + 32768;     // 2 x [128 t][8 h] bf16 (block parity)   4 KB
 constexpr int OFF_CUM = OFF_DT + 4096;    // [NHEAD][128] f32
 constexpr int OFF_DTF = OFF_CUM + 1024;
 constexpr int OFF_GF = OFF_DTF + 1024;
-constexpr int OFF_WS = OFF_GF + 1024;     // [NHEAD][4] f32
-constexpr int OFF_BAR = OFF_WS + 64;      // 15 mbarriers, then the TMEM address
+constexpr int OFF_BAR = OFF_GF + 1024;    // 16 mbarriers, then the TMEM address
 constexpr int SMEM_BYTES = OFF_BAR + 128 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -450,7 +474,8 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 // TMEM columns: C B^T 0..127, then per head pair M X, C S^T and B^T X~ with
 // the two heads side by side (C S^T and B^T X~ of both heads are one MMA of
 // N = 128 each: the heads' S buffers are 16 KB apart, the operand's stride
-// between its two 64-column halves)
+// between its two 64-column halves); a head's B^T X~ columns hold its M
+// (bf16) from its M build until its M X is done
 __device__ __forceinline__ uint32_t tm_ydg(int hh) { return 128u + 64u * hh; }
 __device__ __forceinline__ uint32_t tm_yoff(int hh) { return 256u + 64u * hh; }
 __device__ __forceinline__ uint32_t tm_ds(int hh) { return 384u + 64u * hh; }
@@ -466,12 +491,12 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     uint64_t* bar_x = bar + 1;       // [hh] x of the block landed
     uint64_t* bar_cb = bar + 3;      // C B^T done
     uint64_t* bar_yoff = bar + 4;    // [hh] C S^T done
-    uint64_t* bar_mma23 = bar + 6;   // [hh] M X and B^T X~ done
+    uint64_t* bar_mma23 = bar + 6;   // [hh] M X done
     uint64_t* bar_m = bar + 8;       // [hh] M and X~ written (compute -> control)
     uint64_t* bar_s = bar + 10;      // [hh] state copy written, x consumed
-    uint64_t* bar_b = bar + 12;      // B of the block landed
-    uint64_t* bar_cfree = bar + 13;  // C S^T of both heads done: C may be refilled
-    uint64_t* bar_bfree = bar + 14;  // B^T X~ of both heads done: B may be refilled
+    uint64_t* bar_b = bar + 12;      // [block parity] B of the block landed
+    uint64_t* bar_cfree = bar + 14;  // C S^T of both heads done: C may be refilled
+    uint64_t* bar_bfree = bar + 15;  // B^T X~ of both heads done: B may be refilled
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 128);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -483,7 +508,8 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
 
     if (tid == 0) {
         mbar_init(bar_c, 1);
-        mbar_init(bar_b, 1);
+        mbar_init(&bar_b[0], 1);
+        mbar_init(&bar_b[1], 1);
         mbar_init(bar_cb, 1);
         mbar_init(bar_cfree, 1);
         mbar_init(bar_bfree, 1);
@@ -516,10 +542,11 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tma_prefetch_desc(&tm_B);
             tma_prefetch_desc(&tm_C);
             tma_prefetch_desc(&tm_dt);
-            // C (with dt) and B have their own barriers and reload as soon as
-            // their last reader of block k is done: C after both heads' C S^T,
-            // B after both heads' B^T X~ (issued before M X for that reason),
-            // so block k+1's C B^T is ready when the compute warps reach it
+            // C (with dt) and B have their own barriers: C reloads (block
+            // k+1) once both heads' C S^T of block k are done; B has two
+            // buffers by block parity and reloads (block k+2) once both
+            // heads' B^T X~ of block k are done, so block k+1's C B^T only
+            // waits for C
             auto load_c = [&](int k) {
                 const int t0 = k * QB;
                 mbar_arrive_expect_tx(bar_c, 32768 + 2048);
@@ -529,9 +556,11 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             };
             auto load_b = [&](int k) {
                 const int t0 = k * QB;
-                mbar_arrive_expect_tx(bar_b, 32768);
-                tma_load_4d(sm + OFF_B, &tm_B, bar_b, 0, g, t0, b);
-                tma_load_4d(sm + OFF_B + 16384, &tm_B, bar_b, 64, g, t0, b);
+                uint64_t* bb = &bar_b[k & 1];
+                uint8_t* dst = sm + OFF_B + (k & 1) * 32768;
+                mbar_arrive_expect_tx(bb, 32768);
+                tma_load_4d(dst, &tm_B, bb, 0, g, t0, b);
+                tma_load_4d(dst + 16384, &tm_B, bb, 64, g, t0, b);
             };
             auto load_x = [&](int hh, int k) {
                 mbar_arrive_expect_tx(&bar_x[hh], 16384);
@@ -539,24 +568,29 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             };
             // the last block whose load was issued, per barrier (for draining
             // loads still in flight if a wait gives up)
-            int c_last = 0, b_last = 0, x_last[NHEAD] = {};
+            int c_last = 0, b_last[2] = {0, -1}, x_last[NHEAD] = {};
             // C B^T of block k into TMEM columns 0..127 (read by both heads'
             // M build of block k)
-            auto issue_cb = [&]() {
+            auto issue_cb = [&](int k) {
                 tc::fence_after_sync();
+                const uint32_t bbuf = sbase + OFF_B + (k & 1) * 32768;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
                     tc::mma_bf16(tmem + 0, tc::smem_desc_sw128(sbase + OFF_C + koff, 0, 1024),
-                                 tc::smem_desc_sw128(sbase + OFF_B + koff, 0, 1024), ID_CB, kk > 0);
+                                 tc::smem_desc_sw128(bbuf + koff, 0, 1024), ID_CB, kk > 0);
                 }
                 tc::mma_commit(bar_cb);
             };
             load_c(0);
             load_b(0);
+            if (nblk > 1) {
+                load_b(1);
+                b_last[1] = 1;
+            }
             for (int hh = 0; hh < NHEAD; ++hh) load_x(hh, 0);
-            bool go = mbar_wait(bar_c, 0, p.err) && mbar_wait(bar_b, 0, p.err);
-            if (go) issue_cb();
+            bool go = mbar_wait(bar_c, 0, p.err) && mbar_wait(&bar_b[0], 0, p.err);
+            if (go) issue_cb(0);
             for (int k = 0; k < nblk && go; ++k) {
                 // both heads' state copies S(k) written and x tiles free (y of
                 // block k-1 has left them): x of block k first, then C S^T
@@ -571,9 +605,19 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 // x of block k+1 into L2 now: its copy into shared memory (at
                 // the top of the next block, once y of this block has left the
                 // tile) then comes from L2 instead of DRAM
-                if (k + 1 < nblk)
+                if (k + 1 < nblk) {
                     for (int hh = 0; hh < NHEAD; ++hh)
                         tma_prefetch_l2_4d(&tm_x, 0, h0 + hh, (k + 1) * QB, b);
+                    // and its B, C and dt: their copies into shared memory
+                    // wait for this block's last reader of the buffer, and
+                    // then come from L2
+                    const int t1 = (k + 1) * QB;
+                    tma_prefetch_l2_4d(&tm_C, 0, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_C, 64, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_B, 0, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_B, 64, g, t1, b);
+                    tma_prefetch_l2_3d(&tm_dt, (h0 / 8) * 8, t1, b);
+                }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -589,53 +633,52 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                     load_c(k + 1);
                     c_last = k + 1;
                 }
-                // M X per head once the head's M and X~ are written; B^T X~ of
-                // both heads (one MMA of N = 128) once the last head's are,
-                // ahead of that head's M X so that B frees early
+                // M X per head as soon as the head's M (in its dS^T columns)
+                // and X~ are written
                 for (int hh = 0; hh < NHEAD && go; ++hh) {
                     if (!mbar_wait(&bar_m[hh], k & 1, p.err)) { go = false; break; }
                     tc::fence_after_sync();
-                    if (hh == NHEAD - 1) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            tc::mma_bf16(tmem + tm_ds(0),
-                                         tc::smem_desc_sw128(sbase + OFF_B + kk * 2048, 16384, 1024),
-                                         tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024),
-                                         ID_DS, kk > 0);
-                        tc::mma_commit(bar_bfree);
-                        // the earlier heads' results are complete with it
-                        for (int h2 = 0; h2 < NHEAD - 1; ++h2) tc::mma_commit(&bar_mma23[h2]);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + tm_ydg(hh),
-                                     tc::smem_desc_sw128(sbase + OFF_M + hh * 32768 + koff, 0, 1024),
-                                     tc::smem_desc_sw128(sbase + OFF_X + hh * 16384 + kk * 2048,
-                                                         16384, 1024),
-                                     ID_YDG, kk > 0);
-                    }
-                    if (hh == NHEAD - 1) tc::mma_commit(&bar_mma23[hh]);
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_bf16_ta(tmem + tm_ydg(hh), tmem + tm_ds(hh) + 8u * kk,
+                                    tc::smem_desc_sw128(sbase + OFF_X + hh * 16384 + kk * 2048, 16384, 1024),
+                                    ID_YDG, kk > 0);
+                    tc::mma_commit(&bar_mma23[hh]);
                 }
-                if (go && k + 1 < nblk) {
-                    // B of block k+1 once B^T X~ is done, then C B^T of block
-                    // k+1 right away (both heads' M of block k are built, so
-                    // the C B^T columns are free): it runs under the epilogue
-                    if (!mbar_wait(bar_bfree, k & 1, p.err)) { go = false; break; }
-                    load_b(k + 1);
-                    b_last = k + 1;
+                if (!go) break;
+                // B^T X~ of both heads (one MMA of N = 128) into the dS^T
+                // columns once both M X have read M there
+                if (!mbar_wait(&bar_mma23[NHEAD - 1], k & 1, p.err)) { go = false; break; }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_bf16(tmem + tm_ds(0),
+                                 tc::smem_desc_sw128(sbase + OFF_B + (k & 1) * 32768 + kk * 2048, 16384, 1024),
+                                 tc::smem_desc_sw128(sbase + OFF_S + kk * 2048, 16384, 1024), ID_DS, kk > 0);
+                tc::mma_commit(bar_bfree);
+                if (k + 1 < nblk) {
+                    // C B^T of block k+1 (both heads' M builds have read this
+                    // block's; its B landed a block ago): it runs under the
+                    // epilogue; then B of block k+2 into this block's B
+                    // buffer once B^T X~ has read it
                     if (!mbar_wait(bar_c, (k + 1) & 1, p.err) ||
-                        !mbar_wait(bar_b, (k + 1) & 1, p.err)) {
+                        !mbar_wait(&bar_b[(k + 1) & 1], ((k + 1) >> 1) & 1, p.err)) {
                         go = false;
                         break;
                     }
-                    issue_cb();
+                    issue_cb(k + 1);
+                    if (k + 2 < nblk) {
+                        if (!mbar_wait(bar_bfree, k & 1, p.err)) { go = false; break; }
+                        load_b(k + 2);
+                        b_last[k & 1] = k + 2;
+                    }
                 }
             }
             if (!go) {
                 // a wait gave up: let the loads still in flight land (bounded)
                 mbar_wait(bar_c, c_last & 1, p.err);
-                mbar_wait(bar_b, b_last & 1, p.err);
+                for (int j = 0; j < 2; ++j)
+                    if (b_last[j] >= 0) mbar_wait(&bar_b[j], (b_last[j] >> 1) & 1, p.err);
                 for (int hh = 0; hh < NHEAD; ++hh) mbar_wait(&bar_x[hh], x_last[hh] & 1, p.err);
             }
         }
@@ -651,10 +694,8 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         float* cum = reinterpret_cast<float*>(sm + OFF_CUM) + hh * 128;
         float* dtf = reinterpret_cast<float*>(sm + OFF_DTF) + hh * 128;
         float* gf = reinterpret_cast<float*>(sm + OFF_GF) + hh * 128;
-        float* wsum = reinterpret_cast<float*>(sm + OFF_WS) + hh * 4;
         uint8_t* xs = sm + OFF_X + hh * 16384;
         uint8_t* ss = sm + OFF_S + hh * 16384;
-        uint8_t* ms = sm + OFF_M + hh * 32768;
 
         float S[P];
         const float* h0row = p.h0 ? p.h0 + (int64_t)b * p.sh_b + (int64_t)h * p.sh_h +
@@ -674,41 +715,65 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         //      this row's step, cumulative decay and the block's total in
         //      registers, the head's columns in shared memory (read by the M
         //      build only, so the next block's may replace them once every
-        //      thread of the head has built its row of M)
-        auto cumsum = [&](int k, float& cum_t, float& dtv, float& cum_last) -> bool {
-            if (!named_sync_and(nb, 128, mbar_wait(bar_c, k & 1, p.err))) return false;
-            const uint16_t raw = *reinterpret_cast<const uint16_t*>(sm + OFF_DT + (k & 1) * 2048 +
-                                                                    row * 16 + (h & 7) * 2);
-            dtv = __uint_as_float((uint32_t)raw << 16);
-            float v = dtv * A2;
+        //      thread of the head has built its row of M).  Every warp of the
+        //      head forms all four 32-step chunks (lane l holds steps l,
+        //      l + 32, l + 64, l + 96), so no barrier between the warps is
+        //      needed: the same scan within each chunk, then the earlier
+        //      chunks' totals in order, and the same values written by all.
+        //      `landed`: the head already knows that dt of block k is here.
+        auto cumsum = [&](int k, bool landed, float& cum_t, float& dtv, float& cum_last) -> bool {
+            if (!landed && !named_sync_and(nb, 128, mbar_wait(bar_c, k & 1, p.err))) return false;
+            const uint8_t* dts = sm + OFF_DT + (k & 1) * 2048 + (h & 7) * 2;
+            float d[4], v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint16_t raw = *reinterpret_cast<const uint16_t*>(dts + (c * 32 + lane) * 16);
+                d[c] = __uint_as_float((uint32_t)raw << 16);
+                v[c] = d[c] * A2;
+            }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float u = __shfl_up_sync(0xffffffffu, v[c], o);
+                    if (lane >= o) v[c] += u;
+                }
             }
-            if (lane == 31) wsum[wq] = v;
-            named_sync(nb, 128);
-            for (int w = 0; w < wq; ++w) v += wsum[w];
-            cum_t = v;
-            cum[row] = cum_t;
-            dtf[row] = dtv;
-            const float cum_end = __shfl_sync(0xffffffffu, cum_t, 31);
-            gf[row] = ex2_approx(cum_end - cum_t) * dtv;  // <= dt when A <= 0
-            named_sync(nb, 128);
-            cum_last = cum[QB - 1];
+            float tot[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tot[c] = __shfl_sync(0xffffffffu, v[c], 31);
+#pragma unroll
+            for (int c = 1; c < 4; ++c)
+#pragma unroll
+                for (int w = 0; w < c; ++w) v[c] += tot[w];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float cend = __shfl_sync(0xffffffffu, v[c], 31);
+                const int r = c * 32 + lane;
+                cum[r] = v[c];
+                dtf[r] = d[c];
+                gf[r] = ex2_approx(cend - v[c]) * d[c];  // <= dt when A <= 0
+            }
+            __syncwarp();
+            cum_t = wq == 0 ? v[0] : wq == 1 ? v[1] : wq == 2 ? v[2] : v[3];
+            dtv = wq == 0 ? d[0] : wq == 1 ? d[1] : wq == 2 ? d[2] : d[3];
+            cum_last = __shfl_sync(0xffffffffu, v[3], 31);
             return true;
         };
 
         float cum_t = 0.f, dtv = 0.f, cum_last = 0.f;
-        bool ok = cumsum(0, cum_t, dtv, cum_last);
+        bool ok = cumsum(0, false, cum_t, dtv, cum_last);
         for (int k = 0; k < nblk && ok; ++k) {
             const int t0 = k * QB;
             if (!named_sync_and(nb, 128, mbar_wait(bar_cb, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-            // ---- row `row` of M = C B^T o decay o dt (lower triangle), bf16, K-major
+            // ---- row `row` of M = C B^T o decay o dt (lower triangle), bf16,
+            //      into this head's dS^T columns of TMEM (free from the last
+            //      state update to this block's B^T X~): chunk jc in columns
+            //      tm_ds(hh) + 16 jc .. + 16
 #pragma unroll 1
             for (int jc = 0; jc < 4; ++jc) {
-                uint8_t* mt = ms + (jc >> 1) * 16384;
+                uint32_t w[16];
                 if (jc <= wq) {
                     float cb[32];
                     tc::tmem_ld32(trow + jc * 32, cb);
@@ -740,28 +805,29 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                         }
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int c = (jc & 1) * 4 + q;
-                        *reinterpret_cast<uint4*>(mt + swz(row, c)) =
-                            make_uint4(pack_bf16(m[q * 8 + 0], m[q * 8 + 1]), pack_bf16(m[q * 8 + 2], m[q * 8 + 3]),
-                                       pack_bf16(m[q * 8 + 4], m[q * 8 + 5]), pack_bf16(m[q * 8 + 6], m[q * 8 + 7]));
-                    }
+                    for (int e = 0; e < 16; ++e) w[e] = pack_bf16(m[2 * e], m[2 * e + 1]);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(mt + swz(row, (jc & 1) * 4 + q)) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int e = 0; e < 16; ++e) w[e] = 0u;
                 }
+                tc::tmem_st16(trow + tm_ds(hh) + 16 * jc, w);
             }
+            tc::tmem_wait_st();
             // ---- X~ row = w_t x_t into the state-copy buffer, once C S^T has read it
             const bool got = mbar_wait(&bar_x[hh], k & 1, p.err) && mbar_wait(&bar_yoff[hh], k & 1, p.err);
             if (!named_sync_and(nb, 128, got)) { ok = false; break; }
             {
                 const float wt = ex2_approx(cum_last - cum_t) * dtv;
                 const float2 wt2 = make_float2(wt, wt);
+                // all eight chunks of the x row first: the stores below go to
+                // another buffer, but the compiler cannot tell
+                uint4 xr[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) xr[c] = *reinterpret_cast<const uint4*>(xs + swz(row, c));
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float x8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(xs + swz(row, c)), x8);
+                    unpack8(xr[c], x8);
                     uint32_t w[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -775,9 +841,12 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tc::fence_before_sync();
             mbar_arrive(&bar_m[hh]);
 
-            // ---- the next block's cumulative decay, while this block's MMAs run
+            // ---- the next block's cumulative decay while this block's MMAs
+            //      run if its dt has landed, else after the state update (a
+            //      late dt must not hold up this block's epilogue)
             float n_cum_t = 0.f, n_dtv = 0.f, n_cum_last = 0.f;
-            if (k + 1 < nblk && !cumsum(k + 1, n_cum_t, n_dtv, n_cum_last)) { ok = false; break; }
+            const bool early = k + 1 < nblk && named_sync_and(nb, 128, mbar_test(bar_c, (k + 1) & 1));
+            if (early && !cumsum(k + 1, true, n_cum_t, n_dtv, n_cum_last)) { ok = false; break; }
 
             if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
@@ -791,12 +860,15 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                     float yd[32], yo[32];
                     tc::tmem_ld32(trow + tm_ydg(hh) + half * 32, yd);
                     tc::tmem_ld32(trow + tm_yoff(hh) + half * 32, yo);
+                    uint4 xr[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xr[q] = *reinterpret_cast<const uint4*>(xs + swz(row, half * 4 + q));
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4* cell = reinterpret_cast<uint4*>(xs + swz(row, half * 4 + q));
                         float x8[8];
-                        unpack8(*cell, x8);
+                        unpack8(xr[q], x8);
                         uint32_t w[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -818,6 +890,8 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 }
             }
             // ---- S^T row <- exp(cum_last) S^T + dS^T; bf16 copy for block k+1
+            if (!named_sync_and(nb, 128, mbar_wait(bar_bfree, k & 1, p.err))) { ok = false; break; }
+            tc::fence_after_sync();
             {
                 const float ablk = ex2_approx(cum_last);
                 float ds[64];
@@ -841,6 +915,7 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tc::fence_before_sync();
             if (row == 0) bulk_wait_read<0>();  // y has left the x tile: it may be refilled
             mbar_arrive(&bar_s[hh]);
+            if (k + 1 < nblk && !early && !cumsum(k + 1, false, n_cum_t, n_dtv, n_cum_last)) { ok = false; break; }
             cum_t = n_cum_t;
             dtv = n_dtv;
             cum_last = n_cum_last;
