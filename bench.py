@@ -143,7 +143,6 @@ KERNEL_SOURCES = {
     "scan_seq<bf16, 1 lane/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_seq<bf16, 2 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
     "scan_seq<bf16, 4 lanes/channel>": ["selective_scan_seq.cu", "scan_common.cuh", "ptx.cuh"],
-    "scan_fast<bf16, 4 lanes/channel>": ["selective_scan.cu", "scan_common.cuh", "ptx.cuh"],
     "ssd_chunk_tc2": ["ssd_tc.cu", "tc.cuh", "ptx.cuh"],
     "scan_bwd_fast<bf16>": ["selective_scan_bwd.cu", "ptx.cuh"],
 }
