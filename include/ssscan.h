@@ -398,6 +398,11 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
  *   SS_DEBUG_BWD_PATH       backward: 0 the general kernel
  *   SS_DEBUG_GROUPED_PATH   B, C per small channel group: 0 the row kernel
  *                           (scan_pc) instead of the TMA kernel
+ *   SS_DEBUG_SSD_LATE_CUMSUM 1: the two-head tensor-core SSD kernel forms
+ *                           every next block's cumulative decay after the
+ *                           state update, never early while the MMAs run
+ *                           (which of the two it takes otherwise depends on
+ *                           when dt lands; the results are the same)
  *   SS_DEBUG_FAULT_ALLOC    1: every stream-ordered scratch allocation fails,
  *                           so calls that need scratch return SS_ERR_ALLOC
  *                           before launching anything (host-side fault
@@ -414,7 +419,8 @@ int ss_selftest_timeout(unsigned limit_us, void* stream);
 #define SS_DEBUG_GROUPED_PATH 6
 #define SS_DEBUG_FAULT_ALLOC 7
 #define SS_DEBUG_SCAN_SEG_TILES 8
-#define SS_DEBUG_COUNT 9
+#define SS_DEBUG_SSD_LATE_CUMSUM 9
+#define SS_DEBUG_COUNT 10
 int ss_debug_set_path(int which, int value);
 
 /*

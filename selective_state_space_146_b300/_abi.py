@@ -30,7 +30,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_probe_scan_forms")
 # Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
 DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
-             grouped_path=6, fault_alloc=7, scan_seg_tiles=8)
+             grouped_path=6, fault_alloc=7, scan_seg_tiles=8, ssd_late_cumsum=9)
 
 
 class SSTensor(ctypes.Structure):

@@ -73,7 +73,8 @@ void* tensor_map_encoder() {
 }
 
 // Diagnostic switches (ss_debug_set_path): -1 is the library's own choice.
-static std::atomic<int> g_debug[SS_DEBUG_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+static std::atomic<int> g_debug[SS_DEBUG_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+static_assert(SS_DEBUG_COUNT == 10, "one initial -1 per switch");
 
 int debug_path(int which) {
     return which >= 0 && which < SS_DEBUG_COUNT ? g_debug[which].load(std::memory_order_relaxed) : -1;

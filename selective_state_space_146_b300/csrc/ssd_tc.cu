@@ -79,6 +79,7 @@ struct Params {
     __nv_bfloat16* y; int64_t sy_b, sy_l, sy_h;
     float* last; int64_t sl_b, sl_h, sl_p, sl_n;
     const float* h0; int64_t sh_b, sh_h, sh_p, sh_n;  // initial state, may be null
+    int late_cumsum;  // two-head kernel: never form the next cumulative decay early
     unsigned* err;
 };
 
@@ -845,7 +846,8 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             //      run if its dt has landed, else after the state update (a
             //      late dt must not hold up this block's epilogue)
             float n_cum_t = 0.f, n_dtv = 0.f, n_cum_last = 0.f;
-            const bool early = k + 1 < nblk && named_sync_and(nb, 128, mbar_test(bar_c, (k + 1) & 1));
+            const bool early = k + 1 < nblk && !p.late_cumsum &&
+                               named_sync_and(nb, 128, mbar_test(bar_c, (k + 1) & 1));
             if (early && !cumsum(k + 1, true, n_cum_t, n_dtv, n_cum_last)) { ok = false; break; }
 
             if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
@@ -1007,6 +1009,7 @@ int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, boo
     }
     ssdtc::Params p{};
     p.Bsz = a.Bsz; p.L = a.L; p.H = a.H; p.G = a.G;
+    p.late_cumsum = debug_path(SS_DEBUG_SSD_LATE_CUMSUM) == 1;
     p.A = a.A; p.sA = a.sA; p.Dv = a.Dv; p.sD = a.sD;
     p.y = static_cast<__nv_bfloat16*>(a.y); p.sy_b = a.sy_b; p.sy_l = a.sy_l; p.sy_h = a.sy_h;
     p.last = a.last; p.sl_b = a.sl_b; p.sl_h = a.sl_h; p.sl_p = a.sl_p; p.sl_n = a.sl_n;

@@ -138,3 +138,29 @@ def test_full_size_workload_sampled(cuda_device, ssd_path, record_property):
     record_property("rel_l2_state", float(es))
     print(f"mamba2_ssd {ssd_path}: rel L2 y {ey:.3e}, last_state {es:.3e} (bar 3e-3)")
     assert bool(torch.isfinite(y).all())
+
+
+@pytest.mark.parametrize("case", [(2, 256, 8, 1, 64, True), (1, 1000, 8, 1, 256, False),
+                                  (1, 129, 4, 2, 128, True), (4, 8192, 64, 1, 256, True)],
+                         ids=lambda c: "x".join(map(str, c[:5])))
+def test_late_cumulative_sum_is_bit_identical(cuda_device, case):
+    """The two-head kernel forms the next block's cumulative decay early
+    (while the MMAs run) when its dt has landed, else after the state update;
+    the switch forces the second way everywhere.  Both must give the same
+    bits, and the oracle's values (on sampled heads at the full size)."""
+    Bsz, L, H, G, chunk, skip = case
+    inp = inputs.ssd_inputs(Bsz, L, H, 64, 128, G, "bf16", skip=skip, seed=L + H + G + 1)
+    with _abi.debug_paths(ssd_path=1):
+        y0, s0 = _run(inp, cuda_device, chunk, pad_dt=H % 8 != 0)
+        with _abi.debug_paths(ssd_late_cumsum=1):
+            y1, s1 = _run(inp, cuda_device, chunk, pad_dt=H % 8 != 0)
+    assert torch.equal(y0, y1) and torch.equal(s0, s1)
+    if L * H * Bsz <= 8192:
+        yo, so = oracle_ssd(inp)
+        check_close(to_np(y1), yo, torch.bfloat16, "y")
+        check_close(to_np(s1), so, torch.bfloat16, "last_state")
+    else:
+        units = inputs.sample_units(Bsz * H, 4, seed=5)
+        yo, so = oracle_ssd_units(inp, units)
+        check_close(np.stack([to_np(y1[u // H, :, u % H]) for u in units]), yo, torch.bfloat16, "y")
+        check_close(np.stack([to_np(s1[u // H, u % H]) for u in units]), so, torch.bfloat16, "state")
