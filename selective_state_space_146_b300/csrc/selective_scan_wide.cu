@@ -26,12 +26,15 @@ namespace ss {
 
 namespace wide {
 
-// Threads per CTA, measured at the Mamba-130M layer shape (8 x 1536 x 2048).
-// N = 64: 256-thread CTAs made 192 CTAs, two on 44 SMs and one on the rest;
-// 128-thread CTAs (four per SM) ran 14% faster.  N = 128: the fp32 B, C tables
-// (64 KB double-buffered) leave room for only three 128-thread CTAs per SM, and
-// 256-thread CTAs ran 13% faster.  N = 32: 256 threads, 1% ahead.
-__host__ __device__ constexpr int threads_for(int N) { return N == 64 ? 128 : 256; }
+// Threads per CTA and CTAs per SM (the register budget), measured at the
+// Mamba-130M layer shape (8 x 1536 x 2048, bf16).  N = 32 and 64: 128-thread
+// CTAs, three per SM (up to 168 registers, no spills): 0.450 and 0.595 ms,
+// against 0.583 ms (256 threads, two per SM, 128 registers and spills) and
+// 0.643 ms (128 threads, four per SM, spills).  N = 128: 256-thread CTAs, two
+// per SM: 1.20 ms, against 1.29 ms with three 128-thread CTAs (the fp32 B, C
+// tables, 64 KB double-buffered, leave room for no more).
+__host__ __device__ constexpr int threads_for(int N) { return N == 128 ? 256 : 128; }
+__host__ __device__ constexpr int ctas_per_sm_for(int N) { return N == 128 ? 2 : 3; }
 constexpr int TC = 32;  // steps per chunk
 constexpr int VEC = 8;  // steps per sub-chunk
 
@@ -196,7 +199,7 @@ struct ChunkLoader {
 };
 
 template <typename T, int N, bool HAS_Z>
-__global__ void __launch_bounds__(Cfg<N>::NT, Cfg<N>::NT == 128 ? 4 : 2) scan_wide(ScanArgs a) {
+__global__ void __launch_bounds__(Cfg<N>::NT, ctas_per_sm_for(N)) scan_wide(ScanArgs a) {
     using C = Cfg<N>;
     using AC = ActCfg<T, N>;
     constexpr int NL = C::NL, K = C::K, ES = (int)sizeof(T);
