@@ -493,10 +493,10 @@ def length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush):
 
 
 def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush, mufu_peak):
-    """d_state 64 and 128 at the Mamba-130M layer shape (bf16, gate on)."""
+    """d_state 32, 64 and 128 at the Mamba-130M layer shape (bf16, gate on)."""
     rows = {}
     cfg = inputs.WORKLOADS["mamba130m_layer"]
-    for N in (64, 128):
+    for N in (32, 64, 128):
         name = f"mamba130m_layer_N{N}"
         try:
             with inputs.on_device(dev):
