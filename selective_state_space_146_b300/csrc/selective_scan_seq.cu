@@ -8,11 +8,16 @@
 //
 // scan_seq: one CTA = one work item over a tile of DT channels of one batch
 // row and one time segment.
-//   warp 0     lane 0 issues the TMA loads of the u / delta / z tiles (ROWB =
-//              64 or 128 bytes of t per channel row, swizzled over ROWB) and of the raw B,
-//              C tiles into a ring of stages; all lanes convert B and C of each
-//              landed tile into an fp32 table shared by all channels of the CTA;
-//   warps 1..  consumers: NSPLIT lanes per channel (1, 2 or 4), each keeping
+//   loads      one thread issues the TMA loads of the u / delta / z tiles (ROWB =
+//              64 or 128 bytes of t per channel row, swizzled over ROWB) and of
+//              the raw B, C tiles into a ring of stages; B and C of each landed
+//              tile are converted into an fp32 table shared by all channels of
+//              the CTA.  With HELPER, warp 0 does both and the consumers follow
+//              it through mbarriers; without it the consumer warps share the
+//              conversion of each tile between two block barriers and thread
+//              0 refills the stage they have all left (a smaller CTA, one
+//              more per SM);
+//   consumers  NSPLIT lanes per channel (1, 2 or 4), each keeping
 //              16 / NSPLIT states in registers and stepping through t with
 //              packed f32x2 arithmetic; exp on the MUFU pipe, softplus with one
 //              MUFU exponential and a polynomial for log1p on the FMA pipe.
