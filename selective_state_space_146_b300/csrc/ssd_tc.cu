@@ -99,6 +99,16 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* o) {
     }
 }
 
+// Prefetch a tile of a 3-D / 4-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
 __global__ void __launch_bounds__(NTHREADS, 2)
 ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_dt,
@@ -173,6 +183,18 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             load_bc(0);
             load_x(0);
             for (int k = 0; k < nblk; ++k) {
+                // B, C, dt and x of the next block into L2 now: their copies
+                // into shared memory wait for this block's last reader, and
+                // then come from L2
+                if (k + 1 < nblk) {
+                    const int t1 = (k + 1) * QB;
+                    tma_prefetch_l2_4d(&tm_B, 0, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_B, 64, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_C, 0, g, t1, b);
+                    tma_prefetch_l2_4d(&tm_C, 64, g, t1, b);
+                    tma_prefetch_l2_3d(&tm_dt, (h / 8) * 8, t1, b);
+                    tma_prefetch_l2_4d(&tm_x, 0, h, t1, b);
+                }
                 // C B^T and C S^T: needs B, C of block k and the state copy S(k)
                 if (!mbar_wait(bar_bc, k & 1, p.err) || !mbar_wait(bar_s, k & 1, p.err)) break;
                 tc::fence_after_sync();
@@ -310,10 +332,13 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             {
                 const float wt = ex2_approx(cum_last - cum_t) * dtv;
                 const float2 wt2 = make_float2(wt, wt);
+                uint4 xr[8];  // all of the row first: the stores go to another buffer
+#pragma unroll
+                for (int c = 0; c < 8; ++c) xr[c] = *reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c));
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float x8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_X + swz(tid, c)), x8);
+                    unpack8(xr[c], x8);
                     uint32_t w[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -427,16 +452,8 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 //    state update.
 namespace ssdtc2 {
 
-// Prefetch a tile of a 4-D tensor map into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
-                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2) : "memory");
-}
+using ssdtc::tma_prefetch_l2_3d;
+using ssdtc::tma_prefetch_l2_4d;
 
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
