@@ -194,6 +194,44 @@ def test_fuzz_ssd(cuda_device, c):
 
 @SETTINGS
 @given(c=st.fixed_dictionaries({
+    "Bsz": st.integers(1, 2), "L": st.integers(1, 1500), "H": st.sampled_from([1, 2, 3, 4, 6, 8, 16]),
+    "G": st.sampled_from([1, 2, 4]), "skip": st.booleans(), "h0": st.booleans(),
+    "late": st.booleans(), "seed": st.integers(0, 10_000)}))
+def test_fuzz_ssd_tensor_core(cuda_device, c):
+    """The tensor-core SSD kernels (bf16, headdim 64, d_state 128) with no
+    fallback (a layout they do not take fails the test): random lengths over
+    one to a dozen 128-step blocks with ragged tails, heads per group even
+    (two-head kernel: the B buffers by block parity, M in TMEM) or odd
+    (one-head kernel), initial state on or off, and the next block's
+    cumulative sum forced late or left to timing; against the oracle."""
+    H = c["H"]
+    G = c["G"] if H % c["G"] == 0 else 1
+    inp = inputs.ssd_inputs(c["Bsz"], c["L"], H, 64, 128, G, "bf16", skip=c["skip"], seed=c["seed"])
+    h0 = (torch.randn(c["Bsz"], H, 64, 128, generator=torch.Generator().manual_seed(c["seed"]))
+          if c["h0"] else None)
+    dev = cuda_device
+    # dt as a view into a buffer whose t-stride is a multiple of 8 (the
+    # tensor map's rule for the tensor-core kernels)
+    Hp = (H + 7) // 8 * 8
+    dtb = torch.zeros(c["Bsz"], c["L"], Hp, dtype=inp["dt"].dtype, device=dev)
+    dtb[:, :, :H] = inp["dt"].to(dev)
+    sw = dict(ssd_path=1)
+    if c["late"]:
+        sw["ssd_late_cumsum"] = 1
+    with _abi.debug_paths(**sw):
+        y, s = _abi.ssd_chunk_scan_fwd(_dev(inp["x"], dev), dtb[:, :, :H],
+                                       *[_dev(inp[k], dev) for k in ("A_head", "B", "C", "D")],
+                                       chunk=256, return_last_state=True, initial_state=_dev(h0, dev))
+        torch.cuda.synchronize()
+    assert _abi.device_error() == 0
+    yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"], h0=h0,
+                        nthreads=8)
+    check_close(to_np(y), yo, torch.bfloat16, f"y {c}")
+    check_close(to_np(s), so, torch.bfloat16, f"state {c}")
+
+
+@SETTINGS
+@given(c=st.fixed_dictionaries({
     "Bsz": st.integers(1, 3), "D": st.integers(1, 40), "N": st.sampled_from([1, 16, 33]),
     "steps": st.integers(1, 6), "dt": st.sampled_from(["f32", "bf16"]), "gate": st.booleans(),
     "seed": st.integers(0, 10_000)}))
