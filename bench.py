@@ -344,22 +344,14 @@ def measure_workload(name, args, dev, rank, torch, abi, inputs, dist_helpers, cl
     h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
     d2h = y_h.numel() * y_h.element_size() + last_h.numel() * last_h.element_size()
     if ssd:
-        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev))
-                  for k, v in pinned.items()}
-
         def e2e_step():
-            # the SSD call takes device buffers: copies in, the call, copies out,
-            # all on the current stream
-            for k, v in pinned.items():
-                if v is not None:
-                    dev_in[k].copy_(v, non_blocking=True)
-            abi.ssd_chunk_scan_fwd(dev_in["x"], dev_in["dt"], dev_in["A_head"], dev_in["B"],
-                                   dev_in["C"], dev_in["D"], chunk=cfg.chunk, y=y,
-                                   last_state=last)
-            y_h.copy_(y, non_blocking=True)
-            last_h.copy_(last, non_blocking=True)
-        call = ("torch copies of pinned host tensors in, ss_ssd_chunk_scan_fwd, copies of y and "
-                "the final state out, on one stream")
+            # host buffers in, host buffers out: the library chunks the batch
+            # rows (or a row's heads) and overlaps copies with the scan on two
+            # streams
+            abi.ssd_chunk_scan_fwd_host(pinned["x"], pinned["dt"], pinned["A_head"], pinned["B"],
+                                        pinned["C"], pinned["D"], chunk=cfg.chunk, y=y_h,
+                                        last_state=last_h)
+        call = "ss_ssd_chunk_scan_fwd_host (pinned host tensors in and out)"
     else:
         def e2e_step():
             # host buffers in, host buffers out: the library chunks the rows and

@@ -15,6 +15,7 @@
  *   ss_selective_state_update,   one decode step of either model
  *   ss_ssd_state_update
  *   ss_selective_scan_fwd_host   the selective scan from host buffers
+ *   ss_ssd_chunk_scan_fwd_host   the SSD scan from host buffers
  *   ss_selective_scan_fwd_noalloc the selective scan with no allocation
  *   ss_status_string, ss_get_device_error, ss_launch_count, ss_version,
  *   ss_selftest_timeout,         status, errors and diagnostics
@@ -247,6 +248,30 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
                                const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
                                const ss_tensor* z, const ss_tensor* delta_bias, int softplus,
                                ss_tensor* y, ss_tensor* last_state, void* stream);
+
+/*
+ * The SSD scan of ss_ssd_chunk_scan_fwd with every tensor in HOST memory (no
+ * counterpart on the pages: the path of a caller whose data lives on the
+ * host, copies included).  Same arguments, shapes, dtypes and results as
+ * ss_ssd_chunk_scan_fwd, except:
+ *   - every ss_tensor.data is a host pointer; page-locked (pinned) memory
+ *     lets the copies run asynchronously, pageable memory works but the
+ *     copies then block the calling thread;
+ *   - every tensor must be contiguous (else SS_ERR_UNSUPPORTED).
+ * The batch is cut into chunks of about 32 MB of x: whole batch rows, or,
+ * when one row holds more, blocks of that row's heads (whole channel groups;
+ * x and y move as 2-D copies, dt to a device pitch of a multiple of 8 heads,
+ * the row's B and C once per buffer set); chunks alternate between `stream`
+ * and the library-owned side stream of ss_selective_scan_fwd_host, so copies
+ * in, scans and copies out of neighbouring chunks overlap.  All work is
+ * joined back into `stream` before the call returns (asynchronously: y and
+ * last_state are valid once `stream` has completed, and the host buffers must
+ * stay valid until then).  Device memory for the chunks is taken
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+int ss_ssd_chunk_scan_fwd_host(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               int chunk, ss_tensor* y, ss_tensor* last_state, void* stream);
 
 /*
  * Backward of the selective scan (training): given dout, the gradient of a

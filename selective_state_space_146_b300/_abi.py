@@ -27,7 +27,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_noalloc", "ss_ssd_chu
            "ss_ssd_state_update", "ss_status_string", "ss_get_device_error", "ss_launch_count",
            "ss_version", "ss_selftest_timeout", "ss_selective_scan_fwd_ckpt",
            "ss_selective_scan_bwd_ckpt", "ss_debug_set_path", "ss_probe_ex2_rate",
-           "ss_probe_scan_forms")
+           "ss_probe_scan_forms", "ss_ssd_chunk_scan_fwd_host")
 # Diagnostic switches of ss_debug_set_path (include/ssscan.h, SS_DEBUG_*).
 DEBUG = dict(scan_path=0, scan_split=1, scan_shape=2, scan_segments=3, ssd_path=4, bwd_path=5,
              grouped_path=6, fault_alloc=7, scan_seg_tiles=8, ssd_late_cumsum=9)
@@ -65,6 +65,8 @@ def load(path: str | None = None):
     lib.ss_selective_scan_fwd_noalloc.restype = i
     lib.ss_ssd_chunk_scan_fwd.argtypes = [T, T, T, T, T, T, i, T, T, vp]
     lib.ss_ssd_chunk_scan_fwd.restype = i
+    lib.ss_ssd_chunk_scan_fwd_host.argtypes = [T, T, T, T, T, T, i, T, T, vp]
+    lib.ss_ssd_chunk_scan_fwd_host.restype = i
     lib.ss_selective_scan_fwd_init.argtypes = [T, T, T, T, T, T, T, T, i, T, T, T, vp]
     lib.ss_selective_scan_fwd_init.restype = i
     lib.ss_ssd_chunk_scan_fwd_init.argtypes = [T, T, T, T, T, T, i, T, T, T, vp]
@@ -186,6 +188,25 @@ def selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, 
                                            _stream_ptr(stream))
     if rc != 0:
         raise SSError(rc, "ss_selective_scan_fwd_host")
+    return (y, last_state) if (return_last_state or last_state is not None) else y
+
+
+def ssd_chunk_scan_fwd_host(x, dt, A_head, B, C, D=None, chunk=256, y=None, last_state=None,
+                            return_last_state=False, stream=None):
+    """ss_ssd_chunk_scan_fwd_host: the SSD scan with every tensor in host
+    memory (contiguous CPU tensors, pinned for asynchronous copies).  The
+    results are valid once `stream` (default: the current CUDA stream) has
+    completed."""
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    if last_state is None and return_last_state:
+        last_state = torch.empty(x.shape[0], x.shape[2], x.shape[3], B.shape[3],
+                                 dtype=torch.float32, pin_memory=True)
+    ts = [describe(t) for t in (x, dt, A_head, B, C, D)]
+    rc = load().ss_ssd_chunk_scan_fwd_host(*[_ref(t) for t in ts], int(chunk), _ref(describe(y)),
+                                           _ref(describe(last_state)), _stream_ptr(stream))
+    if rc != 0:
+        raise SSError(rc, "ss_ssd_chunk_scan_fwd_host")
     return (y, last_state) if (return_last_state or last_state is not None) else y
 
 

@@ -663,11 +663,14 @@ int ss_selective_scan_fwd_host(const ss_tensor* u, const ss_tensor* delta, const
     return rc;
 }
 
-int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
-                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
-                               int chunk, const ss_tensor* initial_state, ss_tensor* y,
-                               ss_tensor* last_state, void* stream) {
-    const ss_tensor* h0 = initial_state;
+// Checks the arguments of an SSD call and fills `a` (pointers as given: the
+// host-buffer entry point uses it for the shapes and strides only); *nothing
+// is set when the call has no work.
+static int ssd_args(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                    const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
+                    const ss_tensor* h0, ss_tensor* y, ss_tensor* last_state, SSDArgs* out,
+                    bool* nothing) {
+    *nothing = false;
     SS_TRY(check_tensor(x, 4));
     SS_TRY(check_tensor(dt, 3));
     SS_TRY(check_tensor(A_head, 1));
@@ -697,10 +700,13 @@ int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss
         return SS_ERR_SHAPE;
     if (N > 256 || P > 1024) return SS_ERR_UNSUPPORTED;
     if (Bsz * H * P >= (int64_t(1) << 31) || L >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
-    if (Bsz == 0 || H == 0 || P == 0) return SS_OK;
-    if (L == 0 && !last_state) return SS_OK;
+    if (Bsz == 0 || H == 0 || P == 0 || (L == 0 && !last_state)) {
+        *nothing = true;
+        return SS_OK;
+    }
 
-    SSDArgs a{};
+    SSDArgs& a = *out;
+    a = SSDArgs{};
     a.Bsz = (int)Bsz; a.L = (int)L; a.H = (int)H; a.P = (int)P; a.G = (int)G; a.N = (int)N;
     a.chunk = chunk; a.dtype = ty;
     a.x = x->data; a.sx_b = x->stride[0]; a.sx_l = x->stride[1]; a.sx_h = x->stride[2]; a.sx_p = x->stride[3];
@@ -721,6 +727,17 @@ int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss
     }
     a.err = device_error_ptr();
     if (!a.err) return SS_ERR_CUDA;
+    return SS_OK;
+}
+
+int ss_ssd_chunk_scan_fwd_init(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               int chunk, const ss_tensor* initial_state, ss_tensor* y,
+                               ss_tensor* last_state, void* stream) {
+    SSDArgs a{};
+    bool nothing = false;
+    SS_TRY(ssd_args(x, dt, A_head, B, C, D, chunk, initial_state, y, last_state, &a, &nothing));
+    if (nothing) return SS_OK;
     Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
     return launch_ssd(a, static_cast<cudaStream_t>(stream), sc);
 }
@@ -730,6 +747,165 @@ int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tens
                           ss_tensor* y, ss_tensor* last_state, void* stream) {
     return ss_ssd_chunk_scan_fwd_init(x, dt, A_head, B, C, D, chunk, nullptr, y, last_state,
                                       stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host buffers in and out: ss_ssd_chunk_scan_fwd_host.  The batch is cut into
+// chunks of batch rows, or of one row's heads (whole channel groups) when a
+// row is large; chunks alternate between the caller's stream and the side
+// stream as in ss_selective_scan_fwd_host.
+
+int ss_ssd_chunk_scan_fwd_host(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
+                               const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
+                               int chunk, ss_tensor* y, ss_tensor* last_state, void* stream) {
+    SSDArgs a{};
+    bool nothing = false;
+    SS_TRY(ssd_args(x, dt, A_head, B, C, D, chunk, nullptr, y, last_state, &a, &nothing));
+    if (nothing) return SS_OK;
+    for (const ss_tensor* t : {x, dt, A_head, B, C, D, static_cast<const ss_tensor*>(y),
+                               static_cast<const ss_tensor*>(last_state)})
+        if (t && !is_contiguous(t)) return SS_ERR_UNSUPPORTED;
+    cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+    cudaStream_t s1 = side_stream();
+    if (!s1) return SS_ERR_CUDA;
+
+    const int es = elem_size(x->dtype);
+    const int64_t Bsz = a.Bsz, L = a.L, H = a.H, P = a.P, G = a.G, N = a.N;
+    const int64_t hpg = H / G;                       // heads per group
+    const size_t head_bytes = (size_t)L * P * es;    // one head of one batch row of x or y
+    const size_t row_bytes = head_bytes * H;
+    const size_t bc_row = (size_t)L * G * N * es;    // one batch row of B or C
+    // Chunks of about 32 MB of x: whole batch rows while a row is smaller (at
+    // least two chunks when there are two rows), else blocks of one row's
+    // heads, so that the copies overlap the scan: whole groups, or, when a
+    // group alone is larger, the largest divisor of the heads per group that
+    // fits (the block's heads then share one group's B, C).
+    constexpr size_t kChunkBytes = size_t(32) << 20;
+    int64_t rows = 1, nh = H;
+    if (row_bytes <= kChunkBytes) {
+        rows = std::max<int64_t>(1, (int64_t)(kChunkBytes / std::max<size_t>(row_bytes, 1)));
+        if (Bsz >= 2) rows = std::min<int64_t>(rows, (Bsz + 1) / 2);
+        rows = std::min<int64_t>(rows, Bsz);
+    } else {
+        const int64_t want = std::max<int64_t>(1, (int64_t)(kChunkBytes / std::max<size_t>(head_bytes, 1)));
+        if (want >= hpg) {
+            nh = std::min<int64_t>(H, want / hpg * hpg);
+        } else {
+            nh = 1;
+            for (int64_t d = want; d > 1; --d)
+                if (hpg % d == 0) {
+                    nh = d;
+                    break;
+                }
+        }
+    }
+    const int64_t hblocks = (H + nh - 1) / nh;       // head blocks per batch row (whole groups each)
+    const int64_t nchunk = nh < H ? Bsz * hblocks : (Bsz + rows - 1) / rows;
+    const int nset = nchunk > 1 ? 2 : 1;
+    const int64_t dtp = (nh + 7) / 8 * 8;            // dt's t-pitch on the device: a multiple of 8
+
+    // device layout: A_head, D once; then `nset` sets of chunk buffers
+    const size_t szA = round256(H * sizeof(float)), szD = D ? round256(H * sizeof(float)) : 0;
+    const size_t cx = round256((size_t)rows * L * nh * P * es);
+    const size_t cdt = round256((size_t)rows * L * dtp * es);
+    const size_t cbc = round256(bc_row * rows);
+    const size_t cst = last_state ? round256((size_t)rows * nh * P * N * sizeof(float)) : 0;
+    const size_t per_set = 2 * cx + cdt + 2 * cbc + cst;
+    const size_t total = szA + szD + per_set * nset;
+    uint8_t* base = nullptr;
+    if (fault_alloc() ||
+        cudaMallocAsync(reinterpret_cast<void**>(&base), total, s0) != cudaSuccess) {
+        cudaGetLastError();
+        return SS_ERR_ALLOC;
+    }
+    int rc = SS_OK;
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    auto copy = [&](void* dst, const void* src, size_t n, cudaMemcpyKind kind, cudaStream_t st) {
+        if (n && rc == SS_OK && cudaMemcpyAsync(dst, src, n, kind, st) != cudaSuccess) rc = SS_ERR_CUDA;
+    };
+    auto copy2d = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                      size_t height, cudaMemcpyKind kind, cudaStream_t st) {
+        if (width && height && rc == SS_OK &&
+            cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, st) != cudaSuccess)
+            rc = SS_ERR_CUDA;
+    };
+    float* dA = reinterpret_cast<float*>(base);
+    float* dD = D ? reinterpret_cast<float*>(base + szA) : nullptr;
+    copy(dA, A_head->data, H * sizeof(float), cudaMemcpyHostToDevice, s0);
+    if (D) copy(dD, D->data, H * sizeof(float), cudaMemcpyHostToDevice, s0);
+    if (rc == SS_OK && (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
+                        cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming) != cudaSuccess ||
+                        cudaEventRecord(ev_start, s0) != cudaSuccess ||
+                        cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess))
+        rc = SS_ERR_CUDA;
+    Scratch sc{scratch_alloc_async, scratch_free_async, nullptr};
+    int64_t set_row[2] = {-1, -1};  // batch row whose B, C a set holds (head blocks)
+    const uint8_t* xh = static_cast<const uint8_t*>(x->data);
+    const uint8_t* dth = static_cast<const uint8_t*>(dt->data);
+    for (int64_t i = 0; i < nchunk && rc == SS_OK; ++i) {
+        // rows [b0, b0 + nb) of heads [hb, hb + nhc)
+        int64_t b0, nb, hb, nhc;
+        if (nh < H) {
+            b0 = i / hblocks; nb = 1;
+            hb = (i % hblocks) * nh; nhc = std::min(nh, H - hb);
+        } else {
+            b0 = i * rows; nb = std::min(rows, Bsz - b0);
+            hb = 0; nhc = H;
+        }
+        const int si = (int)(i % nset);
+        cudaStream_t st = (i % 2 == 0) ? s0 : s1;
+        uint8_t* set = base + szA + szD + per_set * si;
+        uint8_t *dx = set, *dy = set + cx, *ddt = set + 2 * cx;
+        uint8_t* dB = ddt + cdt;
+        uint8_t* dC = dB + cbc;
+        float* dlast = last_state ? reinterpret_cast<float*>(dC + cbc) : nullptr;
+        // x: (nb * L) rows of nhc heads, pitch H heads on the host
+        const size_t hw = (size_t)nhc * P * es, hp = (size_t)H * P * es;
+        const size_t off_x = ((size_t)b0 * L * H + hb) * P * es;
+        if (nhc == H) copy(dx, xh + off_x, (size_t)nb * row_bytes, cudaMemcpyHostToDevice, st);
+        else copy2d(dx, hw, xh + off_x, hp, hw, (size_t)nb * L, cudaMemcpyHostToDevice, st);
+        // dt: (nb * L) rows of nhc values, to a pitch of dtp values
+        copy2d(ddt, (size_t)dtp * es, dth + ((size_t)b0 * L * H + hb) * es, (size_t)H * es,
+               (size_t)nhc * es, (size_t)nb * L, cudaMemcpyHostToDevice, st);
+        if (nh == H || set_row[si] != b0) {  // a head block reuses its row's B, C
+            copy(dB, static_cast<const uint8_t*>(B->data) + (size_t)b0 * bc_row, bc_row * nb,
+                 cudaMemcpyHostToDevice, st);
+            copy(dC, static_cast<const uint8_t*>(C->data) + (size_t)b0 * bc_row, bc_row * nb,
+                 cudaMemcpyHostToDevice, st);
+            set_row[si] = b0;
+        }
+        if (rc != SS_OK) break;
+        SSDArgs c = a;  // the chunk's tensors are contiguous (dt padded)
+        c.Bsz = (int)nb;
+        c.H = (int)nhc;
+        c.G = (int)(nhc >= hpg ? nhc / hpg : 1);  // whole groups, or part of one
+        c.x = dx; c.sx_b = L * nhc * P; c.sx_l = nhc * P; c.sx_h = P; c.sx_p = 1;
+        c.y = dy; c.sy_b = L * nhc * P; c.sy_l = nhc * P; c.sy_h = P; c.sy_p = 1;
+        c.dt = ddt; c.sdt_b = L * dtp; c.sdt_l = dtp; c.sdt_h = 1;
+        const int64_t g0 = hb / hpg;  // the block's first group
+        c.Bm = dB + (size_t)g0 * N * es; c.sB_b = L * G * N; c.sB_l = G * N; c.sB_g = N; c.sB_n = 1;
+        c.Cm = dC + (size_t)g0 * N * es; c.sC_b = L * G * N; c.sC_l = G * N; c.sC_g = N; c.sC_n = 1;
+        c.A = dA + hb; c.sA = 1;
+        c.Dv = dD ? dD + hb : nullptr; c.sD = 1;
+        c.last = dlast; c.sl_b = nhc * P * N; c.sl_h = P * N; c.sl_p = N; c.sl_n = 1;
+        c.h0 = nullptr;
+        rc = launch_ssd(c, st, sc);
+        if (rc != SS_OK) break;
+        uint8_t* yh = static_cast<uint8_t*>(y->data);
+        if (nhc == H) copy(yh + off_x, dy, (size_t)nb * row_bytes, cudaMemcpyDeviceToHost, st);
+        else copy2d(yh + off_x, hp, dy, hw, hw, (size_t)nb * L, cudaMemcpyDeviceToHost, st);
+        if (last_state)
+            copy(static_cast<uint8_t*>(last_state->data) + ((size_t)b0 * H + hb) * P * N * sizeof(float),
+                 dlast, (size_t)nb * nhc * P * N * sizeof(float), cudaMemcpyDeviceToHost, st);
+    }
+    // join the side stream back into the caller's stream, then free
+    if (ev_end && (cudaEventRecord(ev_end, s1) != cudaSuccess ||
+                   cudaStreamWaitEvent(s0, ev_end, 0) != cudaSuccess) && rc == SS_OK)
+        rc = SS_ERR_CUDA;
+    cudaFreeAsync(base, s0);
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (ev_end) cudaEventDestroy(ev_end);
+    return rc;
 }
 
 int ss_selective_state_update(ss_tensor* state, const ss_tensor* u, const ss_tensor* delta,

@@ -1,13 +1,13 @@
-"""ss_selective_scan_fwd_host: host tensors in, host tensors out, the batch
-cut into chunks that overlap on two streams (rows, or blocks of one row's
-channels when a row holds more than 32 MB of inputs).  Compared with the fp64
-oracle on the same inputs (GPU)."""
+"""ss_selective_scan_fwd_host and ss_ssd_chunk_scan_fwd_host: host tensors
+in, host tensors out, the batch cut into chunks that overlap on two streams
+(rows, or blocks of one row's channels or heads when a row holds more than 32
+MB).  Compared with the fp64 oracle on the same inputs (GPU)."""
 import pytest
 import torch
 
 import oracle
 from selective_state_space_146_b300 import _abi, inputs
-from tests.parity_util import check_close, to_np
+from tests.parity_util import check_close, oracle_ssd_units, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -116,3 +116,57 @@ def test_host_api_channel_blocks(cuda_device, case):
     idx = torch.as_tensor([int(c) for c in chans])
     check_close(to_np(y.reshape(total, L)[idx]), yo, _tdt(dt), "y (sampled)")
     check_close(to_np(s.reshape(total, 16)[idx]), so, _tdt(dt), "state (sampled)")
+
+
+# ss_ssd_chunk_scan_fwd_host: (batch, L, heads, headdim, N, groups, dtype);
+# the first three are small (whole batch rows per chunk), the others hold more
+# than 32 MB of x per row, so a row is cut into blocks of heads: half of one
+# group (G 1), whole groups (G 4), and an fp32 row on the CUDA-core kernel.
+SSD_HOST_CASES = [
+    (2, 256, 8, 64, 128, 1, "bf16"),
+    (3, 130, 4, 16, 32, 2, "f32"),
+    (1, 1, 2, 8, 16, 1, "f32"),
+    (1, 8192, 64, 64, 128, 1, "bf16"),
+    (2, 8192, 64, 64, 128, 4, "bf16"),
+    (1, 4100, 32, 64, 16, 1, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", SSD_HOST_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_ssd_host_api_matches_oracle(cuda_device, case):
+    Bsz, L, H, P, N, G, dt = case
+    inp = inputs.ssd_inputs(Bsz, L, H, P, N, G, dt, seed=L + H)
+    h = _pin(inp)
+    y, s = _abi.ssd_chunk_scan_fwd_host(h["x"], h["dt"], h["A_head"], h["B"], h["C"], h["D"],
+                                        return_last_state=True)
+    torch.cuda.synchronize()
+    assert y.device.type == "cpu" and s.device.type == "cpu"
+    assert _abi.device_error() == 0
+    if Bsz * L * H <= 1 << 16:
+        yo, so = oracle.ssd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"],
+                            nthreads=8)
+        check_close(to_np(y), yo, _tdt(dt), "y")
+        check_close(to_np(s), so, _tdt(dt), "last_state")
+    else:
+        # sampled heads, one from every head block and batch row at least
+        units = sorted(set(int(u) for u in inputs.sample_units(Bsz * H, 6, seed=L)) | {0, H // 2, Bsz * H - 1})
+        yo, so = oracle_ssd_units(inp, units)
+        yg = torch.stack([y[u // H, :, u % H] for u in units])
+        sg = torch.stack([s[u // H, u % H] for u in units])
+        check_close(to_np(yg), yo, _tdt(dt), "y (sampled heads)")
+        check_close(to_np(sg), so, _tdt(dt), "last_state (sampled heads)")
+        # the device call on the same inputs gives the same bits
+        dev = cuda_device
+        yd, sd = _abi.ssd_chunk_scan_fwd(*[(None if inp[k] is None else inp[k].to(dev))
+                                           for k in ("x", "dt", "A_head", "B", "C", "D")],
+                                         return_last_state=True)
+        torch.cuda.synchronize()
+        if dt == "bf16":  # the tensor-core kernels: per head pair, whatever the blocking
+            assert torch.equal(yd.cpu(), y) and torch.equal(sd.cpu(), s)
+
+
+def test_ssd_host_api_rejects_strided(cuda_device):
+    inp = inputs.ssd_inputs(1, 64, 4, 16, 16, 1, "f32", seed=3)
+    x = inp["x"].transpose(1, 2).contiguous().transpose(1, 2)  # same shape, not contiguous
+    with pytest.raises(_abi.SSError, match="UNSUPPORTED"):
+        _abi.ssd_chunk_scan_fwd_host(x, inp["dt"], inp["A_head"], inp["B"], inp["C"], inp["D"])
