@@ -24,7 +24,8 @@ Calls:
 * ``selective_scan_bwd`` -- all eight gradients for an incoming dy;
   ``selective_scan_fwd_ckpt`` / ``selective_scan_bwd_ckpt`` -- a training
   step's pair, the forward keeping the state every 8 steps for the backward.
-* ``ssd_chunk_scan_fwd`` -- the Mamba-2 SSD scan in chunked form.
+* ``ssd_chunk_scan_fwd`` -- the Mamba-2 SSD scan in chunked form;
+  ``ssd_chunk_scan_fwd_host`` -- the same with pinned host tensors in and out.
 * ``selective_state_update`` / ``ssd_state_update`` -- one decoding step,
   the state updated in place.
 * ``device_error`` -- the device error word (a bounded wait that ran out);
@@ -34,10 +35,10 @@ from ._abi import (SSError, conv_selective_scan_fwd, device_error,  # noqa: F401
                    launch_count, selective_scan_bwd, selective_scan_bwd_ckpt,
                    selective_scan_fwd, selective_scan_fwd_ckpt, selective_scan_fwd_host,
                    selective_scan_fwd_noalloc, selective_state_update, ssd_chunk_scan_fwd,
-                   ssd_state_update, status_string)
+                   ssd_chunk_scan_fwd_host, ssd_state_update, status_string)
 
 __all__ = ["selective_scan_fwd", "selective_scan_fwd_host", "conv_selective_scan_fwd", "selective_scan_fwd_noalloc",
-           "ssd_chunk_scan_fwd", "selective_scan_bwd", "selective_scan_fwd_ckpt",
+           "ssd_chunk_scan_fwd", "ssd_chunk_scan_fwd_host", "selective_scan_bwd", "selective_scan_fwd_ckpt",
            "selective_scan_bwd_ckpt",
            "selective_state_update", "ssd_state_update", "SSError", "device_error",
            "launch_count", "status_string"]
