@@ -754,6 +754,177 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
+// Up to eight row copies in one launch (blockIdx.y picks the copy): copy q
+// moves rows[q] rows of L elements, row r = i * n1[q] + j at i * s0 + j * s1
+// on either side.  A block copies one row at a time with eight loads in
+// flight per thread before the stores, so every warp access is contiguous
+// whatever the alignment of the rows.
+constexpr int kMaxRowCopies = 8;
+template <typename T>
+struct RowCopies {
+    const T* src[kMaxRowCopies];
+    T* dst[kMaxRowCopies];
+    int64_t ss0[kMaxRowCopies], ss1[kMaxRowCopies], ds0[kMaxRowCopies], ds1[kMaxRowCopies];
+    int64_t rows[kMaxRowCopies];
+    int n1[kMaxRowCopies];
+    int count, L;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopies<T> p) {
+    const int q = blockIdx.y;
+    const T* __restrict__ src = p.src[q];
+    T* __restrict__ dst = p.dst[q];
+    const int n1 = p.n1[q], L = p.L;
+    for (int64_t r = blockIdx.x; r < p.rows[q]; r += gridDim.x) {
+        const int64_t i = r / n1, j = r % n1;
+        const T* sp = src + i * p.ss0[q] + j * p.ss1[q];
+        T* dp = dst + i * p.ds0[q] + j * p.ds1[q];
+        for (int t0 = 0; t0 < L; t0 += 8 * 256) {
+            T v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = t0 + e * 256 + (int)threadIdx.x;
+                if (t < L) v[e] = sp[t];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = t0 + e * 256 + (int)threadIdx.x;
+                if (t < L) dp[t] = v[e];
+            }
+        }
+    }
+}
+
+// A call whose rows the fast kernels cannot map although every t-stride is 1
+// (a row pitch or base that is not a multiple of 16 bytes: odd sequence
+// lengths in bf16, for one) runs them on padded copies: u, delta, z and B, C
+// go into stream-ordered scratch with rows padded to 16 bytes (row copies on
+// the stream), the scan writes a padded y, which is copied back into the
+// caller's y.  That moves about twice the bytes of the scan itself, against
+// the general kernel's 19x (8 x 1536 x 2047) to 80x (1 x 2048 x 16383) of its
+// time.  *taken stays false when the call needs no repacking, when a stride
+// does not allow it, or with a fixed (size-limited) scratch.
+static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
+    *taken = false;
+    if (a.L < 2 || a.ckpt || scratch.limit != ~size_t(0)) return SS_OK;
+    if (a.N != 16 && a.N != 32 && a.N != 64 && a.N != 128) return SS_OK;
+    const int64_t es = a.dtype == SS_BF16 ? 2 : 4;
+    const int64_t G = a.G > 1 ? a.G : 1;
+    auto unit_t = [](const void* p, int64_t stt) { return !p || stt == 1; };
+    if (!unit_t(a.u, a.su_t) || !unit_t(a.dl, a.sdl_t) || !unit_t(a.z, a.sz_t) ||
+        !unit_t(a.y, a.sy_t) || !unit_t(a.Bm, a.sB_t) || !unit_t(a.Cm, a.sC_t))
+        return SS_OK;
+    auto aligned = [&](const void* p, int64_t s0, int64_t s1) {
+        return !p || (reinterpret_cast<uintptr_t>(p) % 16 == 0 && (s0 * es) % 16 == 0 &&
+                      (s1 * es) % 16 == 0);
+    };
+    const bool bc_ok = aligned(a.Bm, a.sB_b, a.sB_n) && aligned(a.Cm, a.sC_b, a.sC_n) &&
+                       (G == 1 || ((a.sB_g * es) % 16 == 0 && (a.sC_g * es) % 16 == 0));
+    if (aligned(a.u, a.su_b, a.su_d) && aligned(a.dl, a.sdl_b, a.sdl_d) &&
+        aligned(a.z, a.sz_b, a.sz_d) && aligned(a.y, a.sy_b, a.sy_d) && bc_ok)
+        return SS_OK;  // already the fast kernels' layout: nothing to gain
+    // every source row must be a full row of L elements (no overlap)
+    const int64_t L = a.L, Lp = (L * es + 15) / 16 * 16 / es;
+    if ((a.D > 1 && (a.su_d < L || a.sdl_d < L || (a.z && a.sz_d < L) || a.sy_d < L)) ||
+        (a.N > 1 && (a.sB_n < L || a.sC_n < L)))
+        return SS_OK;
+
+    // the padded call's layout (pointers stand in until the scratch exists):
+    // repack only when a fast kernel takes it
+    ScanArgs c = a;
+    void* const fake = reinterpret_cast<void*>(uintptr_t(256));
+    c.u = fake; c.su_b = (int64_t)a.D * Lp; c.su_d = Lp;
+    c.dl = fake; c.sdl_b = (int64_t)a.D * Lp; c.sdl_d = Lp;
+    if (a.z) { c.z = fake; c.sz_b = (int64_t)a.D * Lp; c.sz_d = Lp; }
+    c.y = fake; c.sy_b = (int64_t)a.D * Lp; c.sy_d = Lp;
+    c.Bm = fake; c.sB_b = G * a.N * Lp; c.sB_n = Lp; c.sB_g = a.N * Lp;
+    c.Cm = fake; c.sC_b = G * a.N * Lp; c.sC_n = Lp; c.sC_g = a.N * Lp;
+    const bool fast = a.N == 16 ? fast_layout_ok(c)
+                                : (G == 1 && !a.cw && !(a.N == 32 && a.dtype != SS_BF16));
+    if (!fast) return SS_OK;
+
+    const size_t act = (size_t)a.Bsz * a.D * Lp * es, bc = (size_t)a.Bsz * G * a.N * Lp * es;
+    auto r256 = [](size_t n) { return (n + 255) & ~size_t(255); };
+    const size_t bytes = r256(act) * (a.z ? 4 : 3) + 2 * r256(bc);
+    uint8_t* base = static_cast<uint8_t*>(scratch.alloc(bytes, st, scratch.ctx));
+    if (!base) return SS_OK;  // no room: the general kernel, as before
+    *taken = true;
+    uint8_t* pu = base;
+    uint8_t* pdl = pu + r256(act);
+    uint8_t* py = pdl + r256(act);
+    uint8_t* pz = a.z ? py + r256(act) : nullptr;
+    uint8_t* pB = py + r256(act) * (a.z ? 2 : 1);
+    uint8_t* pC = pB + r256(bc);
+    const size_t dp = (size_t)Lp * es;
+    int rc = SS_OK;
+    // rows (i, j) of L elements, i < n0 at stride s0, j < n1 at stride s1, into
+    // the padded layout (row i * n1 + j at pitch Lp) or back out of it; the
+    // copies gather in `batch` and go out in as few launches as they fit
+    RowCopies<uint8_t> batch{};
+    batch.L = (int)L;
+    int64_t max_rows = 0;
+    auto flush = [&]() {
+        if (rc != SS_OK || batch.count == 0 || max_rows == 0) return;
+        const dim3 grid((unsigned)std::min<int64_t>(max_rows, (int64_t)sm_count_current() * 4),
+                        (unsigned)batch.count);
+        if (a.dtype == SS_BF16)
+            copy_rows<<<grid, 256, 0, st>>>(reinterpret_cast<const RowCopies<__nv_bfloat16>&>(batch));
+        else
+            copy_rows<<<grid, 256, 0, st>>>(reinterpret_cast<const RowCopies<float>&>(batch));
+        count_launch(1);
+        if (cudaGetLastError() != cudaSuccess) rc = SS_ERR_LAUNCH;
+        batch.count = 0;
+        max_rows = 0;
+    };
+    auto rows_copy = [&](uint8_t* padded, const void* other, int64_t n0, int64_t s0, int64_t n1,
+                         int64_t s1, bool in) {
+        if (!other) return;
+        if (batch.count == kMaxRowCopies) flush();
+        const int q = batch.count++;
+        uint8_t* o = const_cast<uint8_t*>(static_cast<const uint8_t*>(other));
+        batch.src[q] = in ? o : padded;
+        batch.dst[q] = in ? padded : o;
+        batch.ss0[q] = in ? s0 : n1 * Lp;
+        batch.ss1[q] = in ? s1 : Lp;
+        batch.ds0[q] = in ? n1 * Lp : s0;
+        batch.ds1[q] = in ? Lp : s1;
+        batch.rows[q] = n0 * n1;
+        batch.n1[q] = (int)n1;
+        max_rows = std::max(max_rows, n0 * n1);
+    };
+    auto pack = [&](uint8_t* dst, const void* src, int64_t sb, int64_t sd, bool in) {
+        rows_copy(dst, src, a.Bsz, sb, a.D, sd, in);
+    };
+    // (b, g, n) rows of B or C: one copy when the (b, g) rows are evenly
+    // spaced, else one per batch row
+    auto pack_bc = [&](uint8_t* dst, const void* src, int64_t sb, int64_t sg, int64_t sn) {
+        if (G == 1 || sb == G * sg) {
+            rows_copy(dst, src, a.Bsz * G, G == 1 ? sb : sg, a.N, sn, true);
+        } else {
+            for (int64_t b = 0; b < a.Bsz; ++b)
+                rows_copy(dst + (size_t)b * G * a.N * dp,
+                          static_cast<const uint8_t*>(src) + (size_t)(b * sb * es), G, sg, a.N, sn, true);
+        }
+    };
+    pack(pu, a.u, a.su_b, a.su_d, true);
+    pack(pdl, a.dl, a.sdl_b, a.sdl_d, true);
+    if (a.z) pack(pz, a.z, a.sz_b, a.sz_d, true);
+    pack_bc(pB, a.Bm, a.sB_b, G > 1 ? a.sB_g : 0, a.sB_n);
+    pack_bc(pC, a.Cm, a.sC_b, G > 1 ? a.sC_g : 0, a.sC_n);
+    flush();
+    if (rc == SS_OK) {
+        c.u = pu; c.dl = pdl; c.z = pz; c.y = py; c.Bm = pB; c.Cm = pC;
+        rc = launch_selective(c, st, scratch);
+        if (rc == SS_OK) {  // y back to the caller's rows
+            pack(py, a.y, a.sy_b, a.sy_d, false);
+            flush();
+        }
+    }
+    scratch.release(base, st, scratch.ctx);
+    return rc;
+}
+
 // Path selection (ss_debug_set_path): SS_DEBUG_SCAN_PATH 0 forces the general
 // kernel, 1 the fast kernel with SS_DEBUG_SCAN_SPLIT lanes per channel (1, 2,
 // 4 or 8; 8 only for bf16, fp32 chunks hold 4 steps), 2 scan_seq.
@@ -820,6 +991,11 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
     if (force != 0 && a.L > 0) {
         bool taken = false;
         const int rc = launch_selective_wide(a, st, &taken);
+        if (taken) return rc;
+    }
+    if (force != 0) {
+        bool taken = false;
+        const int rc = run_repacked(a, st, scratch, &taken);
         if (taken) return rc;
     }
     return bf ? run_general<__nv_bfloat16>(a, st) : run_general<float>(a, st);
