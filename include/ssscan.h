@@ -89,19 +89,28 @@ typedef struct ss_tensor {
  *   D, delta_bias  : (D)                f32
  *   last_state     : (Bsz, D, N)        f32
  * T is SS_F32 or SS_BF16.  N <= 256; the fast paths are compiled for N = 16
- * (other N run a slower general kernel).  They need unit stride in t and
- * 16-byte aligned rows for u/delta/z/y/B/C; grouped B, C with groups of at
- * least 64 channels (a multiple of 64) share the shared-B, C kernel, smaller
- * groups run a kernel that streams each channel's own B, C.  Other layouts
- * take the general kernel (same results up to rounding order).  y may not
- * alias an input.
+ * and, with B, C shared by a whole batch row, for N = 32, 64 and 128 (bf16;
+ * fp32 too for 64 and 128); other N run a slower general kernel.  The fast
+ * paths need unit stride in t and 16-byte aligned rows for u/delta/z/y/B/C;
+ * grouped B, C (N = 16) with groups of at least 64 channels (a multiple of
+ * 64) share the shared-B, C kernel, smaller groups run a kernel that streams
+ * each channel's own B, C.  A call with unit t-strides whose row pitch or
+ * base is not a multiple of 16 bytes (an odd L in bf16, L not a multiple of
+ * 4 in fp32) is run on padded copies: u, delta, z, B, C go into
+ * stream-ordered scratch with 16-byte row pitch (one copy launch), the fast
+ * path scans them and y is copied back (one more launch), about twice the
+ * scan's own DRAM traffic.  Other layouts, and padded copies that do not fit
+ * in device memory, take the general kernel (same results up to rounding
+ * order).  y may not alias an input.
  * Arithmetic: fp32 state and accumulation for both dtypes.
  *
  * Scratch: when the channel count is too small to fill the GPU, the
  * sequence is split into segments scanned in parallel (a summary pass, then
  * the main pass seeded with each segment's incoming state); the summaries
  * live in stream-ordered memory (cudaMallocAsync / cudaFreeAsync on
- * `stream`), at most 2 * Bsz * D * N * 64 floats.
+ * `stream`), at most 2 * Bsz * D * N * 64 floats.  The padded copies above
+ * take the same kind of memory, (3 or 4) * Bsz * D + 2 * Bsz * G * N rows of
+ * the padded length.
  *
  * Zero-size inputs (Bsz, D or L = 0) return SS_OK without a launch.
  * `stream` is a cudaStream_t (NULL = legacy default stream).
