@@ -307,12 +307,17 @@ int ss_ssd_chunk_scan_fwd_host(const ss_tensor* x, const ss_tensor* dt, const ss
  *   SS_ERR_UNSUPPORTED).
  * N <= 16 (else SS_ERR_UNSUPPORTED).  With N = 16, unit t-stride and 16-byte
  * aligned rows the sums over channels, batch rows and steps are added in a
- * fixed order (bitwise reproducible); other layouts use f32 atomics, whose
- * order, and so the last bits, can differ from call to call.  Scratch is taken
- * stream-ordered from the device's default pool: the state every 8 steps
- * (Bsz*D*ceil(L/8)*64 bytes) and per-block partial sums of dB, dC
- * (ceil(D/32)*Bsz*L*128 bytes) on the fast path; SS_ERR_ALLOC if it cannot
- * be had.
+ * fixed order (bitwise reproducible).  With N = 16 and unit t-strides but rows
+ * whose pitch or base is not a multiple of 16 bytes (an odd L in bf16), u,
+ * delta, z, dout, B and C are copied into padded rows, the same kernel runs
+ * there and du, ddelta, dz are copied back (one copy launch each way; same
+ * fixed order).  Other layouts use f32 atomics, whose order, and so the last
+ * bits, can differ from call to call.  Scratch is taken stream-ordered from
+ * the device's default pool: the state every 8 steps (Bsz*D*ceil(L/8)*64
+ * bytes) and per-block partial sums of dB, dC (ceil(D/32)*Bsz*L*128 bytes) on
+ * the fast path, plus the padded copies (5 or 7 activations and B, C) where
+ * taken; SS_ERR_ALLOC if the fast path's own scratch cannot be had (padded
+ * copies that do not fit fall back to the atomics kernel).
  */
 int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_tensor* A,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D,
@@ -333,13 +338,16 @@ int ss_selective_scan_bwd(const ss_tensor* u, const ss_tensor* delta, const ss_t
  *   checks, y and last_state) that also writes `ckpt`, f32 (Bsz, D,
  *   ceil(L/8), 16), contiguous, 16-byte aligned: ckpt[b,d,k,:] = the state
  *   h before step 8k (h after steps 0 .. 8k-1; zero at k = 0).  N = 16, B, C
- *   (Bsz, N, L) shared per batch row, unit t-stride and 16-byte aligned rows
- *   only (the layouts the fast kernels take); else SS_ERR_UNSUPPORTED.
+ *   (Bsz, N, L) shared per batch row and unit t-strides only; else
+ *   SS_ERR_UNSUPPORTED.  Rows whose pitch or base is not a multiple of 16
+ *   bytes (an odd L in bf16) run on padded copies as in ss_selective_scan_fwd
+ *   (the checkpoints are written in place); SS_ERR_UNSUPPORTED when those
+ *   copies do not fit in device memory.
  * ss_selective_scan_bwd_ckpt: ss_selective_scan_bwd (same arguments, checks
  *   and gradients) given that checkpoint tensor from the forward of the same
  *   inputs; it reads the states from it instead of recomputing them (the
- *   scratch of the states is not taken).  Same layout limits, else
- *   SS_ERR_UNSUPPORTED; a null ckpt is SS_ERR_INVALID_ARG.  Gradients equal
+ *   scratch of the states is not taken).  Same layout limits and padded
+ *   copies, else SS_ERR_UNSUPPORTED; a null ckpt is SS_ERR_INVALID_ARG.  Gradients equal
  *   ss_selective_scan_bwd's up to rounding (bit for bit when the forward did
  *   not split the sequence into segments).
  */

@@ -116,6 +116,42 @@ struct Scratch {
     size_t limit = ~size_t(0);  // largest request alloc can meet (kernels size to fit)
 };
 
+// Row copies between a caller's strided rows of L elements and a padded
+// layout (row pitch Lp elements, Lp * element size a multiple of 16 bytes) in
+// scratch, for calls whose rows the TMA kernels cannot map.  Copies are
+// gathered and go out together, up to kMaxRowCopies per launch (one block
+// row copy at a time, coalesced whatever the rows' alignment).
+constexpr int kMaxRowCopies = 8;
+struct RowCopyList {
+    const void* src[kMaxRowCopies];
+    void* dst[kMaxRowCopies];
+    int64_t ss0[kMaxRowCopies], ss1[kMaxRowCopies], ds0[kMaxRowCopies], ds1[kMaxRowCopies];
+    int64_t rows[kMaxRowCopies];
+    int n1[kMaxRowCopies];
+    int count, L;
+};
+class RowPacker {
+  public:
+    RowPacker(int dtype, int64_t L, int64_t Lp, cudaStream_t st);
+    // rows (i, j), i < n0 at element stride s0 and j < n1 at stride s1, of
+    // `other`, into `padded` (row i * n1 + j at pitch Lp) when `in`, else from
+    // `padded` back into `other`; a null `other` is skipped
+    void add(void* padded, const void* other, int64_t n0, int64_t s0, int64_t n1, int64_t s1,
+             bool in);
+    // launches what was added; SS_OK or SS_ERR_LAUNCH (which sticks)
+    int flush();
+    int status() const { return rc_; }
+
+  private:
+    RowCopyList list_{};
+    int dtype_;
+    int64_t Lp_, max_rows_ = 0;
+    cudaStream_t st_;
+    int rc_ = 0;
+};
+// Padded length for rows of L elements: the row pitch rounded up to 16 bytes.
+inline int64_t padded_len(int64_t L, int es) { return (L * es + 15) / 16 * 16 / es; }
+
 int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch);
 // scan_seq (N = 16, fast layouts, with or without the conv in front, no
 // checkpoints); *taken is false when the call does not fit it.

@@ -754,27 +754,16 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
-// Up to eight row copies in one launch (blockIdx.y picks the copy): copy q
-// moves rows[q] rows of L elements, row r = i * n1[q] + j at i * s0 + j * s1
-// on either side.  A block copies one row at a time with eight loads in
-// flight per thread before the stores, so every warp access is contiguous
-// whatever the alignment of the rows.
-constexpr int kMaxRowCopies = 8;
+// Up to kMaxRowCopies row copies in one launch (blockIdx.y picks the copy):
+// copy q moves rows[q] rows of L elements, row r = i * n1[q] + j at
+// i * s0 + j * s1 on either side.  A block copies one row at a time with
+// eight loads in flight per thread before the stores, so every warp access is
+// contiguous whatever the alignment of the rows.
 template <typename T>
-struct RowCopies {
-    const T* src[kMaxRowCopies];
-    T* dst[kMaxRowCopies];
-    int64_t ss0[kMaxRowCopies], ss1[kMaxRowCopies], ds0[kMaxRowCopies], ds1[kMaxRowCopies];
-    int64_t rows[kMaxRowCopies];
-    int n1[kMaxRowCopies];
-    int count, L;
-};
-
-template <typename T>
-__global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopies<T> p) {
+__global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopyList p) {
     const int q = blockIdx.y;
-    const T* __restrict__ src = p.src[q];
-    T* __restrict__ dst = p.dst[q];
+    const T* __restrict__ src = static_cast<const T*>(p.src[q]);
+    T* __restrict__ dst = static_cast<T*>(p.dst[q]);
     const int n1 = p.n1[q], L = p.L;
     for (int64_t r = blockIdx.x; r < p.rows[q]; r += gridDim.x) {
         const int64_t i = r / n1, j = r % n1;
@@ -796,6 +785,41 @@ __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopi
     }
 }
 
+RowPacker::RowPacker(int dtype, int64_t L, int64_t Lp, cudaStream_t st)
+    : dtype_(dtype), Lp_(Lp), st_(st) {
+    list_.L = (int)L;
+}
+
+void RowPacker::add(void* padded, const void* other, int64_t n0, int64_t s0, int64_t n1,
+                    int64_t s1, bool in) {
+    if (!other || rc_ != SS_OK) return;
+    if (list_.count == kMaxRowCopies) flush();
+    const int q = list_.count++;
+    list_.src[q] = in ? other : padded;
+    list_.dst[q] = in ? padded : const_cast<void*>(other);
+    list_.ss0[q] = in ? s0 : n1 * Lp_;
+    list_.ss1[q] = in ? s1 : Lp_;
+    list_.ds0[q] = in ? n1 * Lp_ : s0;
+    list_.ds1[q] = in ? Lp_ : s1;
+    list_.rows[q] = n0 * n1;
+    list_.n1[q] = (int)n1;
+    max_rows_ = std::max(max_rows_, n0 * n1);
+}
+
+int RowPacker::flush() {
+    if (rc_ == SS_OK && list_.count > 0 && max_rows_ > 0) {
+        const dim3 grid((unsigned)std::min<int64_t>(max_rows_, (int64_t)sm_count_current() * 4),
+                        (unsigned)list_.count);
+        if (dtype_ == SS_BF16) copy_rows<__nv_bfloat16><<<grid, 256, 0, st_>>>(list_);
+        else copy_rows<float><<<grid, 256, 0, st_>>>(list_);
+        count_launch(1);
+        if (cudaGetLastError() != cudaSuccess) rc_ = SS_ERR_LAUNCH;
+    }
+    list_.count = 0;
+    max_rows_ = 0;
+    return rc_;
+}
+
 // A call whose rows the fast kernels cannot map although every t-stride is 1
 // (a row pitch or base that is not a multiple of 16 bytes: odd sequence
 // lengths in bf16, for one) runs them on padded copies: u, delta, z and B, C
@@ -807,7 +831,7 @@ __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopi
 // does not allow it, or with a fixed (size-limited) scratch.
 static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
-    if (a.L < 2 || a.ckpt || scratch.limit != ~size_t(0)) return SS_OK;
+    if (a.L < 2 || scratch.limit != ~size_t(0)) return SS_OK;
     if (a.N != 16 && a.N != 32 && a.N != 64 && a.N != 128) return SS_OK;
     const int64_t es = a.dtype == SS_BF16 ? 2 : 4;
     const int64_t G = a.G > 1 ? a.G : 1;
@@ -825,7 +849,7 @@ static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scrat
         aligned(a.z, a.sz_b, a.sz_d) && aligned(a.y, a.sy_b, a.sy_d) && bc_ok)
         return SS_OK;  // already the fast kernels' layout: nothing to gain
     // every source row must be a full row of L elements (no overlap)
-    const int64_t L = a.L, Lp = (L * es + 15) / 16 * 16 / es;
+    const int64_t L = a.L, Lp = padded_len(L, (int)es);
     if ((a.D > 1 && (a.su_d < L || a.sdl_d < L || (a.z && a.sz_d < L) || a.sy_d < L)) ||
         (a.N > 1 && (a.sB_n < L || a.sC_n < L)))
         return SS_OK;
@@ -840,8 +864,10 @@ static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scrat
     c.y = fake; c.sy_b = (int64_t)a.D * Lp; c.sy_d = Lp;
     c.Bm = fake; c.sB_b = G * a.N * Lp; c.sB_n = Lp; c.sB_g = a.N * Lp;
     c.Cm = fake; c.sC_b = G * a.N * Lp; c.sC_n = Lp; c.sC_g = a.N * Lp;
-    const bool fast = a.N == 16 ? fast_layout_ok(c)
-                                : (G == 1 && !a.cw && !(a.N == 32 && a.dtype != SS_BF16));
+    // (the checkpointing forward runs scan_fast only: N = 16, B, C per row)
+    const bool fast = a.ckpt ? (a.N == 16 && G == 1 && !a.cw && fast_layout_ok(c))
+                             : a.N == 16 ? fast_layout_ok(c)
+                                         : (G == 1 && !a.cw && !(a.N == 32 && a.dtype != SS_BF16));
     if (!fast) return SS_OK;
 
     const size_t act = (size_t)a.Bsz * a.D * Lp * es, bc = (size_t)a.Bsz * G * a.N * Lp * es;
@@ -857,54 +883,19 @@ static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scrat
     uint8_t* pB = py + r256(act) * (a.z ? 2 : 1);
     uint8_t* pC = pB + r256(bc);
     const size_t dp = (size_t)Lp * es;
-    int rc = SS_OK;
-    // rows (i, j) of L elements, i < n0 at stride s0, j < n1 at stride s1, into
-    // the padded layout (row i * n1 + j at pitch Lp) or back out of it; the
-    // copies gather in `batch` and go out in as few launches as they fit
-    RowCopies<uint8_t> batch{};
-    batch.L = (int)L;
-    int64_t max_rows = 0;
-    auto flush = [&]() {
-        if (rc != SS_OK || batch.count == 0 || max_rows == 0) return;
-        const dim3 grid((unsigned)std::min<int64_t>(max_rows, (int64_t)sm_count_current() * 4),
-                        (unsigned)batch.count);
-        if (a.dtype == SS_BF16)
-            copy_rows<<<grid, 256, 0, st>>>(reinterpret_cast<const RowCopies<__nv_bfloat16>&>(batch));
-        else
-            copy_rows<<<grid, 256, 0, st>>>(reinterpret_cast<const RowCopies<float>&>(batch));
-        count_launch(1);
-        if (cudaGetLastError() != cudaSuccess) rc = SS_ERR_LAUNCH;
-        batch.count = 0;
-        max_rows = 0;
-    };
-    auto rows_copy = [&](uint8_t* padded, const void* other, int64_t n0, int64_t s0, int64_t n1,
-                         int64_t s1, bool in) {
-        if (!other) return;
-        if (batch.count == kMaxRowCopies) flush();
-        const int q = batch.count++;
-        uint8_t* o = const_cast<uint8_t*>(static_cast<const uint8_t*>(other));
-        batch.src[q] = in ? o : padded;
-        batch.dst[q] = in ? padded : o;
-        batch.ss0[q] = in ? s0 : n1 * Lp;
-        batch.ss1[q] = in ? s1 : Lp;
-        batch.ds0[q] = in ? n1 * Lp : s0;
-        batch.ds1[q] = in ? Lp : s1;
-        batch.rows[q] = n0 * n1;
-        batch.n1[q] = (int)n1;
-        max_rows = std::max(max_rows, n0 * n1);
-    };
+    RowPacker pk(a.dtype, L, Lp, st);
     auto pack = [&](uint8_t* dst, const void* src, int64_t sb, int64_t sd, bool in) {
-        rows_copy(dst, src, a.Bsz, sb, a.D, sd, in);
+        pk.add(dst, src, a.Bsz, sb, a.D, sd, in);
     };
     // (b, g, n) rows of B or C: one copy when the (b, g) rows are evenly
     // spaced, else one per batch row
     auto pack_bc = [&](uint8_t* dst, const void* src, int64_t sb, int64_t sg, int64_t sn) {
         if (G == 1 || sb == G * sg) {
-            rows_copy(dst, src, a.Bsz * G, G == 1 ? sb : sg, a.N, sn, true);
+            pk.add(dst, src, a.Bsz * G, G == 1 ? sb : sg, a.N, sn, true);
         } else {
             for (int64_t b = 0; b < a.Bsz; ++b)
-                rows_copy(dst + (size_t)b * G * a.N * dp,
-                          static_cast<const uint8_t*>(src) + (size_t)(b * sb * es), G, sg, a.N, sn, true);
+                pk.add(dst + (size_t)b * G * a.N * dp,
+                       static_cast<const uint8_t*>(src) + (size_t)(b * sb * es), G, sg, a.N, sn, true);
         }
     };
     pack(pu, a.u, a.su_b, a.su_d, true);
@@ -912,13 +903,13 @@ static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scrat
     if (a.z) pack(pz, a.z, a.sz_b, a.sz_d, true);
     pack_bc(pB, a.Bm, a.sB_b, G > 1 ? a.sB_g : 0, a.sB_n);
     pack_bc(pC, a.Cm, a.sC_b, G > 1 ? a.sC_g : 0, a.sC_n);
-    flush();
+    int rc = pk.flush();
     if (rc == SS_OK) {
         c.u = pu; c.dl = pdl; c.z = pz; c.y = py; c.Bm = pB; c.Cm = pC;
         rc = launch_selective(c, st, scratch);
         if (rc == SS_OK) {  // y back to the caller's rows
             pack(py, a.y, a.sy_b, a.sy_d, false);
-            flush();
+            rc = pk.flush();
         }
     }
     scratch.release(base, st, scratch.ctx);
@@ -945,7 +936,12 @@ int launch_selective(const ScanArgs& a, cudaStream_t st, const Scratch& scratch)
     if (a.ckpt && a.L > 0) {  // (with L = 0 there are no checkpoints to write)
         // checkpoints for the backward come from the fast kernel with four
         // lanes per channel (the backward's layout of states across lanes)
-        if (a.cw || a.G > 1 || !fast_layout_ok(a)) return SS_ERR_UNSUPPORTED;
+        if (a.cw || a.G > 1) return SS_ERR_UNSUPPORTED;
+        if (!fast_layout_ok(a)) {
+            bool taken = false;
+            const int rc = run_repacked(a, st, scratch, &taken);
+            return taken ? rc : SS_ERR_UNSUPPORTED;
+        }
         return bf ? run_fast<__nv_bfloat16, 4, 4, false, true>(a, st, scratch)
                   : run_fast<float, 4, 4, false, true>(a, st, scratch);
     }

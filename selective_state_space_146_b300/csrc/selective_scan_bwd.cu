@@ -780,13 +780,105 @@ static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratc
     return e == cudaSuccess ? SS_OK : SS_ERR_LAUNCH;
 }
 
+// A call with unit t-strides whose rows are not 16-byte aligned (an odd L in
+// bf16, for one) runs scan_bwd_fast on padded copies: u, delta, z, dout, B
+// and C go into stream-ordered scratch with the row pitch rounded up to 16
+// bytes, du, ddelta and dz come back from padded rows into the caller's (dA,
+// dB, dC, dD and ddelta_bias are written in place: their layout does not
+// depend on the row pitch).  The forward's checkpoints keep their layout.
+// *taken stays false when the rows need no padding, when a stride or the
+// scratch does not allow it, or when no tensor map fits the padded layout.
+template <typename T>
+static int run_bwd_repacked(const BwdArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
+    *taken = false;
+    if (a.N != 16 || a.L < 2 || a.L >= (1 << 30) || scratch.limit != ~size_t(0)) return SS_OK;
+    const int64_t es = sizeof(T), L = a.L, Lp = padded_len(L, (int)es);
+    auto unit_t = [](const void* p, int64_t stt) { return !p || stt == 1; };
+    if (!unit_t(a.u, a.su_t) || !unit_t(a.dl, a.sdl_t) || !unit_t(a.z, a.sz_t) ||
+        !unit_t(a.dout, a.sg_t) || !unit_t(a.Bm, a.sB_t) || !unit_t(a.Cm, a.sC_t) ||
+        !unit_t(a.du, a.sdu_t) || !unit_t(a.ddl, a.sddl_t) || !unit_t(a.dz, a.sdz_t))
+        return SS_OK;
+    if (bwd_fast_ok(a)) return SS_OK;  // already the fast kernel's layout
+    // every row must be a full row of L elements (no overlap)
+    auto rows_ok = [&](const void* p, int64_t sr) { return !p || a.D < 2 || sr >= L; };
+    if (!rows_ok(a.u, a.su_d) || !rows_ok(a.dl, a.sdl_d) || !rows_ok(a.z, a.sz_d) ||
+        !rows_ok(a.dout, a.sg_d) || !rows_ok(a.du, a.sdu_d) || !rows_ok(a.ddl, a.sddl_d) ||
+        !rows_ok(a.dz, a.sdz_d) || a.sB_n < L || a.sC_n < L)
+        return SS_OK;
+    const size_t act = (size_t)a.Bsz * a.D * Lp * es, bc = (size_t)a.Bsz * 16 * Lp * es;
+    auto r256 = [](size_t n) { return (n + 255) & ~size_t(255); };
+    const int nact = a.z ? 7 : 5;  // u, delta, dout, du, ddelta (+ z, dz)
+    uint8_t* base = static_cast<uint8_t*>(scratch.alloc(r256(act) * nact + 2 * r256(bc), st,
+                                                        scratch.ctx));
+    if (!base) return SS_OK;  // no room: the general kernel
+    uint8_t* pu = base;
+    uint8_t* pdl = pu + r256(act);
+    uint8_t* pg = pdl + r256(act);
+    uint8_t* pdu = pg + r256(act);
+    uint8_t* pddl = pdu + r256(act);
+    uint8_t* pz = a.z ? pddl + r256(act) : nullptr;
+    uint8_t* pdz = a.z ? pz + r256(act) : nullptr;
+    uint8_t* pB = pddl + r256(act) * (a.z ? 3 : 1);
+    uint8_t* pC = pB + r256(bc);
+    BwdArgs c = a;
+    const int64_t sb = (int64_t)a.D * Lp;
+    c.u = pu;     c.su_b = sb;   c.su_d = Lp;
+    c.dl = pdl;   c.sdl_b = sb;  c.sdl_d = Lp;
+    c.dout = pg;  c.sg_b = sb;   c.sg_d = Lp;
+    c.du = pdu;   c.sdu_b = sb;  c.sdu_d = Lp;
+    c.ddl = pddl; c.sddl_b = sb; c.sddl_d = Lp;
+    if (a.z) {
+        c.z = pz;   c.sz_b = sb;  c.sz_d = Lp;
+        c.dz = pdz; c.sdz_b = sb; c.sdz_d = Lp;
+    }
+    c.Bm = pB; c.sB_b = 16 * Lp; c.sB_n = Lp;
+    c.Cm = pC; c.sC_b = 16 * Lp; c.sC_n = Lp;
+    if (!bwd_fast_ok(c)) {
+        scratch.release(base, st, scratch.ctx);
+        return SS_OK;
+    }
+    RowPacker pk(a.dtype, L, Lp, st);
+    pk.add(pu, a.u, a.Bsz, a.su_b, a.D, a.su_d, true);
+    pk.add(pdl, a.dl, a.Bsz, a.sdl_b, a.D, a.sdl_d, true);
+    pk.add(pg, a.dout, a.Bsz, a.sg_b, a.D, a.sg_d, true);
+    if (a.z) pk.add(pz, a.z, a.Bsz, a.sz_b, a.D, a.sz_d, true);
+    pk.add(pB, a.Bm, a.Bsz, a.sB_b, 16, a.sB_n, true);
+    pk.add(pC, a.Cm, a.Bsz, a.sC_b, 16, a.sC_n, true);
+    int rc = pk.flush();
+    if (rc == SS_OK) {
+        rc = run_bwd_fast<T>(c, st, scratch);
+        if (rc == -1) {  // no tensor map for the padded layout: nothing was launched on it
+            scratch.release(base, st, scratch.ctx);
+            return SS_OK;
+        }
+    }
+    *taken = true;
+    if (rc == SS_OK) {
+        pk.add(pdu, a.du, a.Bsz, a.sdu_b, a.D, a.sdu_d, false);
+        pk.add(pddl, a.ddl, a.Bsz, a.sddl_b, a.D, a.sddl_d, false);
+        if (a.z) pk.add(pdz, a.dz, a.Bsz, a.sdz_b, a.D, a.sdz_d, false);
+        rc = pk.flush();
+    }
+    scratch.release(base, st, scratch.ctx);
+    return rc;
+}
+
 int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& scratch) {
     BwdArgs a = args;
     const bool empty = a.L == 0 || a.Bsz == 0 || a.D == 0;
     const bool force_general = debug_path(SS_DEBUG_BWD_PATH) == 0;
+    auto repacked = [&](bool* taken) {
+        return a.dtype == SS_BF16 ? run_bwd_repacked<__nv_bfloat16>(a, st, scratch, taken)
+                                  : run_bwd_repacked<float>(a, st, scratch, taken);
+    };
     if (a.ckpt_in && !empty) {
         // the forward's states come in the fast kernel's layout only
-        if (a.N != 16 || !bwd_fast_ok(a)) return SS_ERR_UNSUPPORTED;
+        if (a.N != 16) return SS_ERR_UNSUPPORTED;
+        if (!bwd_fast_ok(a)) {
+            bool taken = false;
+            const int rc = repacked(&taken);
+            return taken ? rc : SS_ERR_UNSUPPORTED;
+        }
         const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
                                           : run_bwd_fast<float>(a, st, scratch);
         return rc == -1 ? SS_ERR_UNSUPPORTED : rc;
@@ -795,6 +887,11 @@ int launch_selective_bwd(const BwdArgs& args, cudaStream_t st, const Scratch& sc
         const int rc = a.dtype == SS_BF16 ? run_bwd_fast<__nv_bfloat16>(a, st, scratch)
                                           : run_bwd_fast<float>(a, st, scratch);
         if (rc != -1) return rc;  // -1: no tensor map for this layout, take the general kernel
+    }
+    if (!empty && !force_general) {
+        bool taken = false;
+        const int rc = repacked(&taken);
+        if (taken) return rc;
     }
     // the general kernel adds into the fp32 sums; with nothing to scan they stay zero
     const size_t nA = (size_t)a.D * a.N, nBC = (size_t)a.Bsz * a.N * a.L;

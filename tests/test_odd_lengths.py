@@ -4,7 +4,9 @@ kernels' tensor maps; the library runs them on padded copies of the inputs
 (and copies y back).  These cases check that path against the fp64 oracle:
 the layer and long-sequence shapes at full size on sampled channels, B, C per
 group, wider states, the fused conv, strided batch rows and one channel per
-row (GPU, C ABI)."""
+row (GPU, C ABI).  The backward takes the same route: the odd-length layer
+shape against the oracle's backward, and the padded route against the
+any-stride backward kernel."""
 import pytest
 import torch
 
@@ -104,3 +106,52 @@ def test_odd_length_general_switch_agrees(cuda_device):
         y0, s0 = _run(g)
     check_close(to_np(y1), to_np(y0), torch.bfloat16, "y")
     check_close(to_np(s1), to_np(s0), torch.bfloat16, "last_state")
+
+
+BWD_GRADS = ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias")
+
+
+def _bwd(g, dout):
+    out = _abi.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                  g["delta_bias"], dout)
+    torch.cuda.synchronize()
+    assert _abi.device_error() == 0
+    return out
+
+
+def test_odd_length_backward_layer_shape(cuda_device):
+    """Every gradient at 8 x 1536 x 2047 (bf16, gate on) against the full
+    oracle backward; the call launches the row copies, scan_bwd_fast and its
+    finishing sums, not the any-stride kernel."""
+    Bsz, D, L = 8, 1536, 2047
+    inp = inputs.selective_inputs(Bsz, D, 16, L, "bf16", seed=L)
+    dout = inputs.grad_output((Bsz, D, L), "bf16", seed=L)
+    g = cuda_inputs(inp, cuda_device)
+    n0 = _abi.launch_count()
+    out = _bwd(g, dout.to(cuda_device))
+    assert _abi.launch_count() - n0 == 4  # pack, scan_bwd_fast, scan_bwd_finish, unpack
+    ref = oracle.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                    inp["D"], inp["z"], inp["delta_bias"], dout)
+    for k in BWD_GRADS:
+        check_close(to_np(out[k]), ref[k], torch.bfloat16, f"odd-length backward {k}")
+
+
+@pytest.mark.parametrize("case", [(2, 70, 999, "bf16", True), (3, 24, 301, "f32", False),
+                                  (1, 1, 515, "bf16", True)],
+                         ids=lambda c: "x".join(map(str, c[:4])))
+def test_odd_length_backward_matches_any_stride_kernel(cuda_device, case):
+    Bsz, D, L, dt, gate = case
+    inp = inputs.selective_inputs(Bsz, D, 16, L, dt, gate=gate, seed=L + D)
+    dout = inputs.grad_output((Bsz, D, L), dt, seed=L + D)
+    g = cuda_inputs(inp, cuda_device)
+    fast = _bwd(g, dout.to(cuda_device))
+    with _abi.debug_paths(bwd_path=0):
+        gen = _bwd(g, dout.to(cuda_device))
+    ref = oracle.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                    inp["D"], inp["z"], inp["delta_bias"], dout)
+    for k in BWD_GRADS:
+        if ref[k] is None:
+            assert fast[k] is None and gen[k] is None, k
+            continue
+        check_close(to_np(fast[k]), ref[k], _tdt(dt), f"padded backward {k}")
+        check_close(to_np(fast[k]), to_np(gen[k]), _tdt(dt), f"padded vs any-stride {k}")

@@ -35,6 +35,8 @@ CASES = [
     (1, 64, 76, "f32", True, True, True),      # fp32: 4-step chunks, every other one kept
     (2, 32, 8, "bf16", False, False, False),   # one sub-chunk, optional inputs off
     (1, 48, 1000, "bf16", True, True, True),   # few channels: the forward splits in segments
+    (2, 40, 203, "bf16", True, True, True),    # odd length: both calls on padded copies
+    (1, 64, 77, "f32", True, False, True),     # fp32 rows of 308 bytes: padded copies
 ]
 
 
@@ -116,9 +118,13 @@ def test_checkpoint_calls_reject_what_they_do_not_take(cuda_device):
     small = cuda_inputs(inputs.selective_inputs(1, 32, 8, 64, "bf16", seed=1), cuda_device)
     with pytest.raises(_abi.SSError, match="UNSUPPORTED"):  # N = 8
         _abi.selective_scan_fwd_ckpt(*_args(small))
-    odd = cuda_inputs(inputs.selective_inputs(1, 32, 16, 77, "f32", seed=1), cuda_device)
-    with pytest.raises(_abi.SSError, match="UNSUPPORTED"):  # rows not 16-byte multiples
-        _abi.selective_scan_fwd_ckpt(*_args(odd))
+    # a time stride other than 1 (rows whose pitch is not a multiple of 16 bytes
+    # are accepted: they run on padded copies, in CASES above)
+    tv = dict(g)
+    for k in ("u", "delta", "z"):
+        tv[k] = g[k].transpose(1, 2).contiguous().transpose(1, 2)
+    with pytest.raises(_abi.SSError, match="UNSUPPORTED"):
+        _abi.selective_scan_fwd_ckpt(*_args(tv))
 
 
 def test_empty_sequence_writes_the_zero_state(cuda_device):
