@@ -756,15 +756,28 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
 
 // Up to kMaxRowCopies row copies in one launch (blockIdx.y picks the copy):
 // copy q moves rows[q] rows of L elements, row r = i * n1[q] + j at
-// i * s0 + j * s1 on either side.  A block copies one row at a time with
-// eight loads in flight per thread before the stores, so every warp access is
-// contiguous whatever the alignment of the rows.
+// i * s0 + j * s1 on either side.  Rows of kShortRow elements or more: a block
+// copies one row at a time with eight loads in flight per thread before the
+// stores, so every warp access is contiguous whatever the alignment of the
+// rows.  Shorter rows: consecutive threads take consecutive elements of the
+// rows laid end to end.
+constexpr int kShortRow = 256;
 template <typename T>
 __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopyList p) {
     const int q = blockIdx.y;
     const T* __restrict__ src = static_cast<const T*>(p.src[q]);
     T* __restrict__ dst = static_cast<T*>(p.dst[q]);
     const int n1 = p.n1[q], L = p.L;
+    if (L < kShortRow) {
+        const int64_t total = p.rows[q] * L;
+        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+             e += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t r = e / L, i = r / n1, j = r % n1;
+            const int t = (int)(e - r * L);
+            dst[i * p.ds0[q] + j * p.ds1[q] + t] = src[i * p.ss0[q] + j * p.ss1[q] + t];
+        }
+        return;
+    }
     for (int64_t r = blockIdx.x; r < p.rows[q]; r += gridDim.x) {
         const int64_t i = r / n1, j = r % n1;
         const T* sp = src + i * p.ss0[q] + j * p.ss1[q];
@@ -808,8 +821,11 @@ void RowPacker::add(void* padded, const void* other, int64_t n0, int64_t s0, int
 
 int RowPacker::flush() {
     if (rc_ == SS_OK && list_.count > 0 && max_rows_ > 0) {
-        const dim3 grid((unsigned)std::min<int64_t>(max_rows_, (int64_t)sm_count_current() * 4),
-                        (unsigned)list_.count);
+        const int64_t sms = sm_count_current();
+        const int64_t blocks = list_.L < kShortRow
+                                   ? std::min<int64_t>((max_rows_ * list_.L + 255) / 256, sms * 8)
+                                   : std::min<int64_t>(max_rows_, sms * 4);
+        const dim3 grid((unsigned)blocks, (unsigned)list_.count);
         if (dtype_ == SS_BF16) copy_rows<__nv_bfloat16><<<grid, 256, 0, st_>>>(list_);
         else copy_rows<float><<<grid, 256, 0, st_>>>(list_);
         count_launch(1);
@@ -831,7 +847,9 @@ int RowPacker::flush() {
 // does not allow it, or with a fixed (size-limited) scratch.
 static int run_repacked(const ScanArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
-    if (a.L < 2 || scratch.limit != ~size_t(0)) return SS_OK;
+    // (one step: the general kernel is as fast, except for the checkpointing
+    // forward, which has no general kernel)
+    if (a.L < (a.ckpt ? 1 : 2) || scratch.limit != ~size_t(0)) return SS_OK;
     if (a.N != 16 && a.N != 32 && a.N != 64 && a.N != 128) return SS_OK;
     const int64_t es = a.dtype == SS_BF16 ? 2 : 4;
     const int64_t G = a.G > 1 ? a.G : 1;

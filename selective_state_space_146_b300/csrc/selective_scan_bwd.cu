@@ -791,7 +791,8 @@ static int run_bwd_fast(const BwdArgs& a, cudaStream_t st, const Scratch& scratc
 template <typename T>
 static int run_bwd_repacked(const BwdArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
     *taken = false;
-    if (a.N != 16 || a.L < 2 || a.L >= (1 << 30) || scratch.limit != ~size_t(0)) return SS_OK;
+    if (a.N != 16 || a.L < (a.ckpt_in ? 1 : 2) || a.L >= (1 << 30) || scratch.limit != ~size_t(0))
+        return SS_OK;
     const int64_t es = sizeof(T), L = a.L, Lp = padded_len(L, (int)es);
     auto unit_t = [](const void* p, int64_t stt) { return !p || stt == 1; };
     if (!unit_t(a.u, a.su_t) || !unit_t(a.dl, a.sdl_t) || !unit_t(a.z, a.sz_t) ||

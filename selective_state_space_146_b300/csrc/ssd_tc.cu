@@ -988,12 +988,44 @@ static bool tc_layout_ok(const SSDArgs& a) {
     return true;
 }
 
+// dt whose (b, l) rows of H values are not at a 16-byte pitch (H not a
+// multiple of 8, for one) while everything else suits the tensor-core
+// kernels: dt is copied into stream-ordered scratch with the pitch rounded up
+// to 8 heads (B * L * H values, small beside x) and the kernels read it from
+// there.  *taken stays false when that does not make the layout fit.
+int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken);
+
+static int run_dt_padded(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
+    *taken = false;
+    if (a.dtype != SS_BF16 || a.sdt_h != 1 || a.H < 1 || scratch.limit != ~size_t(0)) return SS_OK;
+    if (a.L > 1 && a.sdt_l < a.H) return SS_OK;  // rows overlap
+    const int64_t Hp = padded_len(a.H, 2);
+    SSDArgs c = a;
+    c.dt = reinterpret_cast<const void*>(uintptr_t(256));  // stands in until the scratch exists
+    c.sdt_l = Hp;
+    c.sdt_b = (int64_t)a.L * Hp;
+    if (!tc_layout_ok(c)) return SS_OK;
+    void* pdt = scratch.alloc((size_t)a.Bsz * a.L * Hp * 2, st, scratch.ctx);
+    if (!pdt) return SS_OK;
+    RowPacker pk(SS_BF16, a.H, Hp, st);
+    pk.add(pdt, a.dt, a.Bsz, a.sdt_b, a.L, a.sdt_l, true);
+    int rc = pk.flush();
+    *taken = true;
+    if (rc == SS_OK) {
+        c.dt = pdt;
+        bool t2 = false;
+        rc = launch_ssd_tc(c, st, scratch, &t2);
+    }
+    scratch.release(pdt, st, scratch.ctx);
+    return rc;
+}
+
 // Path selection for tests: SS_DEBUG_SSD_PATH 0 forces the CUDA-core kernel.
 int launch_ssd_tc(const SSDArgs& a, cudaStream_t st, const Scratch& scratch, bool* taken) {
-    (void)scratch;
     *taken = false;
     const int path = debug_path(SS_DEBUG_SSD_PATH);
-    if (path == 0 || !tc_layout_ok(a) || a.L < 1) return SS_OK;
+    if (path == 0 || a.L < 1) return SS_OK;
+    if (!tc_layout_ok(a)) return run_dt_padded(a, st, scratch, taken);
     *taken = true;
 
     CUtensorMap mx, mb, mc, mdt;

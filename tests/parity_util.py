@@ -4,7 +4,12 @@ against the fp64 oracle.
 Tolerances (the stated bar for this scan): fp32 inputs -> max |err| <=
 1e-4 * max |ref|; bf16 inputs -> relative L2 error <= 3e-3, against the
 oracle run on the same bf16-rounded inputs (fp32 state and accumulation on
-the GPU).
+the GPU).  An output stored in bf16 carries its own rounding inside that
+budget (about 1.7e-3 for normally distributed values); on an output of a few
+elements rounding alone can cost more than 3e-3 (half a bf16 ulp is up to
+2^-8 of the value), so there the bar is 1.5 times what rounding the oracle's
+own values to bf16 costs (a value within a hair of a rounding midpoint may
+round the other way), never less than 3e-3.
 """
 import numpy as np
 import torch
@@ -33,8 +38,18 @@ def check_close(got, want, dtype, what=""):
     num = np.linalg.norm((got - want).ravel())
     den = np.linalg.norm(want.ravel())
     rel = num / max(den, 1e-30)
-    assert rel <= TOL_BF16_RELL2, f"{what}: rel L2 {rel:.3e} > 3e-3"
+    bar = TOL_BF16_RELL2
+    if _bf16_valued(got):
+        rounded = torch.from_numpy(want).to(torch.bfloat16).double().numpy()
+        bar = max(bar, 1.5 * np.linalg.norm((rounded - want).ravel()) / max(den, 1e-30))
+    assert rel <= bar, f"{what}: rel L2 {rel:.3e} > {bar:.3e}"
     return rel
+
+
+def _bf16_valued(a):
+    """Every value exactly a bf16 number (an output stored in bf16)."""
+    bits = np.asarray(a, np.float32).view(np.uint32)
+    return bool(np.all((bits & 0xFFFF) == 0))
 
 
 def cuda_inputs(d, device):

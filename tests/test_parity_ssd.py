@@ -53,7 +53,7 @@ CASES = [
     (1, 1, 2, 8, 16, 1, "f32", 64, True),            # L = 1
     (1, 130, 3, 5, 7, 3, "f32", 64, True),           # odd sizes
     (1, 384, 2, 64, 256, 1, "bf16", 64, True),       # N = 256
-    (2, 256, 4, 64, 128, 1, "bf16", 64, True),       # dt t-stride 4: not the tensor-core layout
+    (2, 256, 4, 64, 128, 1, "bf16", 64, True),       # dt t-stride 4: the library pads dt (tensor cores)
 ]
 
 
@@ -99,16 +99,30 @@ def test_tensor_core_shapes(cuda_device, ssd_path, case):
     yo, so = oracle_ssd(inp)
     check_close(to_np(y), yo, torch.bfloat16, "y")
     check_close(to_np(s), so, torch.bfloat16, "last_state")
+    if H % 8:
+        # a contiguous dt (t-stride H): the library copies it to a padded pitch
+        # itself and runs the same kernel on the same values: the same bits
+        y2, s2 = _run(inp, cuda_device, chunk)
+        assert torch.equal(y, y2) and torch.equal(s, s2)
 
 
 def test_no_fallback_switch_rejects_other_layouts(cuda_device):
     """With the tensor-core-only switch a layout the tensor-core kernels do
-    not take (dt t-stride 4) is an error, not a silent CUDA-core run."""
+    not take (dt with a head stride other than 1) is an error, not a silent
+    CUDA-core run; a dt whose t-stride (4 heads) is the only misfit is padded
+    by the library and runs."""
     inp = inputs.ssd_inputs(1, 128, 4, 64, 128, 1, "bf16", seed=1)
+    g = cuda_inputs(inp, cuda_device)
+    dt_hl = g["dt"].transpose(1, 2).contiguous().transpose(1, 2)  # (B, L, H) over (B, H, L)
     with _abi.debug_paths(ssd_path=1):
         with pytest.raises(_abi.SSError, match="UNSUPPORTED"):
-            _run(inp, cuda_device, 128)
-        _run(inp, cuda_device, 128, pad_dt=True)  # the same call with a padded dt runs
+            _abi.ssd_chunk_scan_fwd(g["x"], dt_hl, g["A_head"], g["B"], g["C"], g["D"], chunk=128)
+        n0 = _abi.launch_count()
+        y, s = _run(inp, cuda_device, 128)
+        assert _abi.launch_count() - n0 == 2  # the dt copy and the tensor-core kernel
+    yo, so = oracle_ssd(inp)
+    check_close(to_np(y), yo, torch.bfloat16, "y")
+    check_close(to_np(s), so, torch.bfloat16, "last_state")
 
 
 @pytest.mark.parametrize("ssd_path", ["tc", "general"], indirect=True)
