@@ -20,9 +20,11 @@ def _pin(d):
     return {k: (None if v is None else v.pin_memory()) for k, v in d.items()}
 
 
+# (odd lengths: each chunk goes to the device as it is and is scanned on padded copies)
 @pytest.mark.parametrize("case", [(2, 64, 16, 512, "bf16", None), (5, 40, 16, 300, "f32", None),
                                   (3, 48, 16, 200, "bf16", 48), (4, 24, 8, 77, "f32", None),
-                                  (1, 32, 16, 64, "bf16", None)],
+                                  (1, 32, 16, 64, "bf16", None), (2, 64, 16, 511, "bf16", None),
+                                  (3, 48, 16, 201, "bf16", 48), (2, 40, 16, 301, "f32", None)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_host_api_matches_oracle(cuda_device, case):
     Bsz, D, N, L, dt, G = case
@@ -79,7 +81,8 @@ def test_host_api_layer_shape_sampled(cuda_device):
 
 @pytest.mark.parametrize("case", [(1, 600, 16384, "bf16", None, True),
                                   (1, 512, 20000, "bf16", 4, True),
-                                  (1, 96, 50000, "f32", None, False)],
+                                  (1, 96, 50000, "f32", None, False),
+                                  (1, 600, 16383, "bf16", None, True)],
                          ids=lambda c: "x".join(map(str, c[:5])))
 def test_host_api_channel_blocks(cuda_device, case):
     """Rows of more than 32 MB of inputs: the call cuts each row into blocks of
