@@ -186,8 +186,11 @@ int ss_selective_scan_fwd_noalloc(const ss_tensor* u, const ss_tensor* delta, co
  * depend on the chunk length beyond rounding, so every accepted value gives
  * the same result.  N <= 256, P <= 256.  The tensor-core path is compiled for
  * bf16 with P = 64, N = 128, unit inner strides and 16-byte aligned rows
- * (dt's t-stride a multiple of 8 elements); everything else runs the general
- * CUDA-core kernel.  Zero-size inputs return SS_OK without a launch.
+ * (dt's t-stride a multiple of 8 elements).  A dt whose head stride is 1 but
+ * whose t-stride is not a multiple of 8 (H not a multiple of 8, contiguous)
+ * is copied into stream-ordered scratch at a pitch of H rounded up to 8 (one
+ * small copy launch) and takes the tensor-core path; everything else runs the
+ * general CUDA-core kernel.  Zero-size inputs return SS_OK without a launch.
  */
 int ss_ssd_chunk_scan_fwd(const ss_tensor* x, const ss_tensor* dt, const ss_tensor* A_head,
                           const ss_tensor* B, const ss_tensor* C, const ss_tensor* D, int chunk,
