@@ -757,10 +757,11 @@ static int run_general(const ScanArgs& a, cudaStream_t st) {
 // Up to kMaxRowCopies row copies in one launch (blockIdx.y picks the copy):
 // copy q moves rows[q] rows of L elements, row r = i * n1[q] + j at
 // i * s0 + j * s1 on either side.  Rows of kShortRow elements or more: a block
-// copies one row at a time with eight loads in flight per thread before the
-// stores, so every warp access is contiguous whatever the alignment of the
-// rows.  Shorter rows: consecutive threads take consecutive elements of the
-// rows laid end to end.
+// copies two rows at a time, sixteen loads in flight per thread before the
+// stores (enough bytes in flight per SM to cover the DRAM latency with 2-byte
+// accesses), every warp access contiguous whatever the alignment of the rows.
+// Shorter rows: consecutive threads take consecutive elements of the rows
+// laid end to end.
 constexpr int kShortRow = 256;
 template <typename T>
 __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopyList p) {
@@ -768,8 +769,9 @@ __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopy
     const T* __restrict__ src = static_cast<const T*>(p.src[q]);
     T* __restrict__ dst = static_cast<T*>(p.dst[q]);
     const int n1 = p.n1[q], L = p.L;
+    const int64_t rows = p.rows[q];
     if (L < kShortRow) {
-        const int64_t total = p.rows[q] * L;
+        const int64_t total = rows * L;
         for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
              e += (int64_t)gridDim.x * blockDim.x) {
             const int64_t r = e / L, i = r / n1, j = r % n1;
@@ -778,21 +780,32 @@ __global__ void __launch_bounds__(256) copy_rows(const __grid_constant__ RowCopy
         }
         return;
     }
-    for (int64_t r = blockIdx.x; r < p.rows[q]; r += gridDim.x) {
-        const int64_t i = r / n1, j = r % n1;
+    for (int64_t r = blockIdx.x; r < rows; r += 2 * (int64_t)gridDim.x) {
+        // rows r and r + gridDim.x (when there is one)
+        const int64_t r2 = r + gridDim.x;
+        const bool two = r2 < rows;
+        const int64_t i = r / n1, j = r % n1, i2 = two ? r2 / n1 : i, j2 = two ? r2 % n1 : j;
         const T* sp = src + i * p.ss0[q] + j * p.ss1[q];
+        const T* sp2 = src + i2 * p.ss0[q] + j2 * p.ss1[q];
         T* dp = dst + i * p.ds0[q] + j * p.ds1[q];
+        T* dp2 = dst + i2 * p.ds0[q] + j2 * p.ds1[q];
         for (int t0 = 0; t0 < L; t0 += 8 * 256) {
-            T v[8];
+            T v[8], w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = t0 + e * 256 + (int)threadIdx.x;
-                if (t < L) v[e] = sp[t];
+                if (t < L) {
+                    v[e] = sp[t];
+                    if (two) w[e] = sp2[t];
+                }
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = t0 + e * 256 + (int)threadIdx.x;
-                if (t < L) dp[t] = v[e];
+                if (t < L) {
+                    dp[t] = v[e];
+                    if (two) dp2[t] = w[e];
+                }
             }
         }
     }
@@ -824,7 +837,7 @@ int RowPacker::flush() {
         const int64_t sms = sm_count_current();
         const int64_t blocks = list_.L < kShortRow
                                    ? std::min<int64_t>((max_rows_ * list_.L + 255) / 256, sms * 8)
-                                   : std::min<int64_t>(max_rows_, sms * 4);
+                                   : std::min<int64_t>((max_rows_ + 1) / 2, sms * 8);
         const dim3 grid((unsigned)blocks, (unsigned)list_.count);
         if (dtype_ == SS_BF16) copy_rows<__nv_bfloat16><<<grid, 256, 0, st_>>>(list_);
         else copy_rows<float><<<grid, 256, 0, st_>>>(list_);
