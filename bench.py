@@ -452,6 +452,7 @@ def secondary_rows(dev, torch, abi, inputs, hbm_peak, tf_peak, mufu_peak):
         rows["conv_scan_mamba130m_layer"] = {"error": str(e)[:200]}
     rows.update(length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(grouped_rows(dev, torch, abi, inputs, hbm_peak, flush))
+    rows.update(odd_length_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush, mufu_peak))
     rows.update(backward_rows(dev, torch, abi, inputs, hbm_peak, flush))
     rows.update(decode_rows(dev, torch, abi, inputs, hbm_peak))
@@ -482,6 +483,38 @@ def length_sweep_rows(dev, torch, abi, inputs, hbm_peak, flush):
     return {"length_sweep_d2048": {"by_L": out, "note": "batch 1, d_inner 2048, N 16, bf16; "
                                    "few channels, so the sequence is split into segments "
                                    "(summary pass + main pass)"}}
+
+
+def odd_length_rows(dev, torch, abi, inputs, hbm_peak, flush):
+    """The Mamba-130M layer one step short (8 x 1536 x 2047, bf16, gate on):
+    rows of 4094 bytes, not a multiple of 16, so the call runs the TMA kernels
+    on padded copies of its rows (the copies counted in the launches)."""
+    import dataclasses
+    base = inputs.WORKLOADS["mamba130m_layer"]
+    cfg = dataclasses.replace(base, seqlen=base.seqlen - 1)
+    name = "odd_length_mamba130m_layer"
+    try:
+        with inputs.on_device(dev):
+            g = inputs.workload_selective_inputs(cfg)
+        yb = torch.empty_like(g["u"])
+        ls = torch.empty(cfg.batch, cfg.d_inner, cfg.d_state, device=dev)
+
+        def fn():
+            run_selective_call(g, torch, abi, yb, ls)
+        times, nl = time_device(fn, flush, 5, 3, torch, counter=abi.launch_count)
+        ms = statistics.mean(times)
+        nbytes = selective_bytes(cfg)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        row = {"ms_per_call": round(ms, 4), "channel_steps_per_s": cfg.channel_steps / (ms * 1e-3),
+               "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+               "launches_per_call": nl / 5, "seqlen": cfg.seqlen,
+               "note": "algorithmic bytes of the scan only; the padded copies move about as "
+                       "many again"}
+        del g, yb, ls
+        torch.cuda.empty_cache()
+    except Exception as ex:
+        row = {"error": str(ex)[:200]}
+    return {name: row}
 
 
 def wide_state_rows(dev, torch, abi, inputs, hbm_peak, flush, mufu_peak):
