@@ -295,13 +295,20 @@ __global__ void __launch_bounds__(Cfg<N>::NT, ctas_per_sm_for(N)) scan_wide(Scan
                 const float du = dd[i] * uf[i];
                 const float2 du2 = make_float2(du, du);
                 float2 acc = make_float2(0.f, 0.f);
+                // the step's loads and exponentials first, then the state updates
+                // and the readout, so no result is needed right after it is asked for
+                float4 bc[8];
+                float2 ab[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float4 bc = lds128f(rowp + i * C::ROW + ((j ^ part) & 7) * 16);  // B, C pair
+                    bc[j] = lds128f(rowp + i * C::ROW + ((j ^ part) & 7) * 16);  // B, C pair
                     const float2 ar = __fmul2_rn(d2, A2[j]);
-                    const float2 ab = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
-                    h2[j] = __ffma2_rn(ab, h2[j], __fmul2_rn(du2, make_float2(bc.x, bc.y)));
-                    acc = __ffma2_rn(make_float2(bc.z, bc.w), h2[j], acc);
+                    ab[j] = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    h2[j] = __ffma2_rn(ab[j], h2[j], __fmul2_rn(du2, make_float2(bc[j].x, bc[j].y)));
+                    acc = __ffma2_rn(make_float2(bc[j].z, bc[j].w), h2[j], acc);
                 }
                 yv[i] = acc.x + acc.y;
             }
