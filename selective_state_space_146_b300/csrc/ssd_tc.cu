@@ -13,6 +13,11 @@
 //                                                     for everything before it)
 //   S     <- exp(cum_last) S + (diag(w) X)^T B        (state passed on)
 //
+// M X runs on the tensor cores with M rounded to bf16, except M's diagonal
+// (M_ii = CB_ii dt_i, the step's own input): that term stays in fp32 and joins
+// the skip term, y_i += (D_h + M_ii) x_i, since on a short sequence one bf16
+// M_ii can set the error of a whole row on its own.
+//
 // The dual form of a longer chunk splits into these 128-step diagonal blocks
 // plus low-rank off-diagonal blocks, and the off-diagonal part is exactly the
 // state term above, so every chunk length that is a multiple of 128 gives the
@@ -67,7 +72,8 @@ constexpr int OFF_CUM = OFF_DT + 2048;   // cum (log2 units) [128] f32
 constexpr int OFF_DTF = OFF_CUM + 512;   // dt [128] f32
 constexpr int OFF_GF = OFF_DTF + 512;    // column factors of the decay matrix [128] f32
 constexpr int OFF_WS = OFF_GF + 512;     // warp partial sums [4] f32
-constexpr int OFF_BAR = OFF_WS + 64;     // mbarriers + TMEM address
+constexpr int OFF_DIAG = OFF_WS + 64;    // the diagonal of M per row [128] f32
+constexpr int OFF_BAR = OFF_DIAG + 512;  // mbarriers + TMEM address
 constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int BAR_COMP = 1;  // named barrier of the compute warps
@@ -129,6 +135,9 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     float* wsum = reinterpret_cast<float*>(sm + OFF_WS);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // M_ii of the thread's row, from its M build to its epilogue (in shared
+    // memory rather than a register held across the block)
+    const uint32_t sdiag = smem_u32(sm + OFF_DIAG) + tid * 4;
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int g = h / (p.H / p.G);
     const float A2 = p.A[h * p.sA] * kLog2e;
@@ -278,8 +287,9 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_mma1, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
 
-            // ---- row tid of M = C B^T o decay o dt (lower triangle), bf16,
-            //      K-major over the C tiles
+            // ---- row tid of M = C B^T o decay o dt (strictly lower triangle),
+            //      bf16, K-major over the C tiles; the diagonal M_ii = (C B^T)_ii
+            //      dt_i in fp32 (in shared memory, sdiag)
 #pragma unroll 1
             for (int jc = 0; jc < 4; ++jc) {
                 uint8_t* mt = sm + OFF_C + (jc >> 1) * 16384;
@@ -304,15 +314,24 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                         const float2* c2 = reinterpret_cast<const float2*>(cum + jc * 32);
                         const float2* d2 = reinterpret_cast<const float2*>(dtf + jc * 32);
                         const float2 ct = make_float2(cum_t, cum_t);
+                        // the diagonal (j = i) stays out of the bf16 M: the pair
+                        // holding it lane / 2 is kept in fp32 and the epilogue
+                        // adds M_ii x_i with the skip term
+                        const int ed = lane >> 1;
+                        float2 pick = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int j = jc * 32 + 2 * e;
                             const float2 arg = __ffma2_rn(c2[e], make_float2(-1.f, -1.f), ct);  // ct - c, exact negation
                             const float2 dec = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));  // j > i: discarded
                             const float2 v = __fmul2_rn(__fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]), dec), d2[e]);
-                            m[2 * e] = j <= tid ? v.x : 0.f;
-                            m[2 * e + 1] = j + 1 <= tid ? v.y : 0.f;
+                            if (e == ed) pick = v;
+                            m[2 * e] = j < tid ? v.x : 0.f;
+                            m[2 * e + 1] = j + 1 < tid ? v.y : 0.f;
                         }
+                        if (jc == warp)
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sdiag), "f"((lane & 1) ? pick.y : pick.x)
+                                         : "memory");
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -355,9 +374,12 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             if (!named_sync_and(BAR_COMP, NCOMP, mbar_wait(bar_mma23, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
 
-            // ---- y row tid = Ydiag + exp(cum) Yoff + D x
+            // ---- y row tid = Ydiag + exp(cum) Yoff + (D + M_ii) x
             {
                 const float eoff = ex2_approx(cum_t);
+                float mii;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mii) : "r"(sdiag) : "memory");
+                const float dx = Dh + mii;
                 const int t = t0 + tid;
                 __nv_bfloat16* yrow = p.y + (int64_t)b * p.sy_b + (int64_t)t * p.sy_l + (int64_t)h * p.sy_h;
 #pragma unroll
@@ -375,7 +397,7 @@ ssd_chunk_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                         for (int i = 0; i < 4; ++i) {
                             const int e = q * 8 + 2 * i;
                             const float2 o = __ffma2_rn(
-                                make_float2(Dh, Dh), make_float2(x8[2 * i], x8[2 * i + 1]),
+                                make_float2(dx, dx), make_float2(x8[2 * i], x8[2 * i + 1]),
                                 __ffma2_rn(make_float2(eoff, eoff), make_float2(yo[e], yo[e + 1]),
                                            make_float2(yd[e], yd[e + 1])));
                             w[i] = pack_bf16(o.x, o.y);
@@ -484,7 +506,8 @@ constexpr int OFF_DT = OFF_S + 32768;     // 2 x [128 t][8 h] bf16 (block parity
 constexpr int OFF_CUM = OFF_DT + 4096;    // [NHEAD][128] f32
 constexpr int OFF_DTF = OFF_CUM + 1024;
 constexpr int OFF_GF = OFF_DTF + 1024;
-constexpr int OFF_BAR = OFF_GF + 1024;    // 16 mbarriers, then the TMEM address
+constexpr int OFF_DIAG = OFF_GF + 1024;   // [NHEAD][128] f32: the diagonal of M per row
+constexpr int OFF_BAR = OFF_DIAG + 1024;  // 16 mbarriers, then the TMEM address
 constexpr int SMEM_BYTES = OFF_BAR + 128 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -712,6 +735,9 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         float* cum = reinterpret_cast<float*>(sm + OFF_CUM) + hh * 128;
         float* dtf = reinterpret_cast<float*>(sm + OFF_DTF) + hh * 128;
         float* gf = reinterpret_cast<float*>(sm + OFF_GF) + hh * 128;
+        // M_ii of the thread's row, from its M build to its epilogue (in shared
+        // memory rather than a register held across the block)
+        const uint32_t sdiag = smem_u32(sm + OFF_DIAG) + (hh * 128 + row) * 4;
         uint8_t* xs = sm + OFF_X + hh * 16384;
         uint8_t* ss = sm + OFF_S + hh * 16384;
 
@@ -785,10 +811,11 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             const int t0 = k * QB;
             if (!named_sync_and(nb, 128, mbar_wait(bar_cb, k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-            // ---- row `row` of M = C B^T o decay o dt (lower triangle), bf16,
-            //      into this head's dS^T columns of TMEM (free from the last
-            //      state update to this block's B^T X~): chunk jc in columns
-            //      tm_ds(hh) + 16 jc .. + 16
+            // ---- row `row` of M = C B^T o decay o dt (strictly lower
+            //      triangle), bf16, into this head's dS^T columns of TMEM (free
+            //      from the last state update to this block's B^T X~): chunk jc
+            //      in columns tm_ds(hh) + 16 jc .. + 16; the diagonal
+            //      M_ii = (C B^T)_ii dt_i in fp32 (in shared memory, sdiag)
 #pragma unroll 1
             for (int jc = 0; jc < 4; ++jc) {
                 uint32_t w[16];
@@ -812,15 +839,24 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                         const float2* c2 = reinterpret_cast<const float2*>(cum + jc * 32);
                         const float2* d2 = reinterpret_cast<const float2*>(dtf + jc * 32);
                         const float2 ct = make_float2(cum_t, cum_t);
+                        // the diagonal (j = row) stays out of the bf16 M: the pair
+                        // holding it (row & 31) / 2 is kept in fp32 and the
+                        // epilogue adds M_ii x_i with the skip term
+                        const int ed = (row & 31) >> 1;
+                        float2 pick = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int j = jc * 32 + 2 * e;
                             const float2 arg = __ffma2_rn(c2[e], make_float2(-1.f, -1.f), ct);  // ct - c, exact negation
                             const float2 dec = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));  // j > row: discarded
                             const float2 v = __fmul2_rn(__fmul2_rn(make_float2(cb[2 * e], cb[2 * e + 1]), dec), d2[e]);
-                            m[2 * e] = j <= row ? v.x : 0.f;
-                            m[2 * e + 1] = j + 1 <= row ? v.y : 0.f;
+                            if (e == ed) pick = v;
+                            m[2 * e] = j < row ? v.x : 0.f;
+                            m[2 * e + 1] = j + 1 < row ? v.y : 0.f;
                         }
+                        if (jc == wq)
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sdiag), "f"((row & 1) ? pick.y : pick.x)
+                                         : "memory");
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e) w[e] = pack_bf16(m[2 * e], m[2 * e + 1]);
@@ -869,11 +905,14 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
 
             if (!named_sync_and(nb, 128, mbar_wait(&bar_mma23[hh], k & 1, p.err))) { ok = false; break; }
             tc::fence_after_sync();
-            // ---- y row = Ydiag + exp(cum) Yoff + D x, written over the row's x in
-            //      shared memory; the tile leaves with one TMA store (rows past
-            //      the end are clipped)
+            // ---- y row = Ydiag + exp(cum) Yoff + (D + M_ii) x, written over the
+            //      row's x in shared memory; the tile leaves with one TMA store
+            //      (rows past the end are clipped)
             {
                 const float eoff = ex2_approx(cum_t);
+                float mii;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mii) : "r"(sdiag) : "memory");
+                const float dx = Dh + mii;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float yd[32], yo[32];
@@ -893,7 +932,7 @@ ssd_chunk_tc2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                         for (int i = 0; i < 4; ++i) {
                             const int e = q * 8 + 2 * i;
                             const float2 o = __ffma2_rn(
-                                make_float2(Dh, Dh), make_float2(x8[2 * i], x8[2 * i + 1]),
+                                make_float2(dx, dx), make_float2(x8[2 * i], x8[2 * i + 1]),
                                 __ffma2_rn(make_float2(eoff, eoff), make_float2(yo[e], yo[e + 1]),
                                            make_float2(yd[e], yd[e + 1])));
                             w[i] = pack_bf16(o.x, o.y);

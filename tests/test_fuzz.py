@@ -8,6 +8,8 @@ launch shape and to random segment counts), the fused conv + scan, the
 backward, the SSD scan and both decode steps.  The sizes stay small so the
 oracle answers in milliseconds; they still cross tile and chunk edges.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -20,7 +22,10 @@ from tests.parity_util import check_close, to_np
 
 pytestmark = pytest.mark.gpu
 
-SETTINGS = settings(max_examples=30, deadline=None, derandomize=True, database=None,
+# SS_FUZZ_EXAMPLES raises the number of drawn cases for a longer run (the
+# default suite draws 30 per test, the same ones every run)
+SETTINGS = settings(max_examples=int(os.environ.get("SS_FUZZ_EXAMPLES", "30")), deadline=None,
+                    derandomize=True, database=None,
                     suppress_health_check=[HealthCheck.function_scoped_fixture])
 
 
